@@ -1,0 +1,428 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+No GPU.  Each test names the passage (page title + section/table) or the
+mathematical fact it relies on; stored values live in tests/golden/ with their
+citations.  None of these tests re-types an oracle formula and compares it
+with itself: they use page values, brute force over all codes, exact rational
+arithmetic, an independent formulation, or a library routine (torch's CPU
+casts) as the other side.
+"""
+
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import gemm as G
+from oracle import quant as Q
+from tests.conftest import read_golden
+
+
+# ----------------------------------------------------------------------------
+# formats: max-finite closed form and page values
+# ----------------------------------------------------------------------------
+
+def _golden_max():
+    return {r[0]: float(r[3]) for r in read_golden("max_finite.txt")}
+
+
+def test_max_finite_closed_form_matches_page_values():
+    g = _golden_max()
+    # (2 - 2**-m) * 2**(2**e - 2 - B) for the IEEE formats
+    assert F.ieee_max_finite(5, 10) == g["float16_e5m10"]
+    assert F.ieee_max_finite(8, 7) == g["float16_e8m7"]
+    assert F.ieee_max_finite(5, 2) == g["float8_e5m2"]
+    # E4M3 extended range: (1 + 6/8) * 2**(15 - 7)
+    assert (1 + 6 / 8) * 2.0 ** (15 - 7) == g["float8_e4m3fn"]
+
+
+def test_decoders_reach_the_page_maxima_by_brute_force():
+    g = _golden_max()
+    e4 = F.e4m3_decode(np.arange(256))
+    e5 = F.e5m2_decode(np.arange(256))
+    e2 = F.e2m1_decode(np.arange(16))
+    bf = F.bf16_decode(np.arange(65536, dtype=np.uint32))
+    fp = F.fp16_decode(np.arange(65536, dtype=np.uint32))
+    fin = lambda v: v[np.isfinite(v)]
+    assert fin(e4).max() == g["float8_e4m3fn"] and fin(e4).min() == -g["float8_e4m3fn"]
+    assert fin(e5).max() == g["float8_e5m2"]
+    assert fin(bf).max() == g["float16_e8m7"]
+    assert fin(fp).max() == g["float16_e5m10"]
+    assert e2.max() == g["float4_e2m1"]
+    i4 = F.int4_decode(np.arange(16))
+    assert i4.max() == g["int4"] and i4.min() == g["int4_min"]
+
+
+def test_e4m3_code_structure():
+    v = F.e4m3_decode(np.arange(256))
+    nan = np.isnan(v)
+    assert list(np.nonzero(nan)[0]) == [0x7F, 0xFF]          # only S.1111.111
+    assert not np.isinf(v).any()                               # 'fn': no infinities
+    pos = v[1:0x7F]
+    assert np.all(np.diff(pos) > 0) and len(pos) == 126        # monotone in the code
+    assert pos[0] == 2.0 ** -9                                 # smallest subnormal
+    assert np.signbit(v[0x80]) and v[0x80] == 0
+
+
+def test_e2m1_page_lists():
+    rows = {r[0]: [float(t) for t in r[1:]] for r in read_golden("e2m1_lists.txt")}
+    assert list(F.e2m1_decode(np.arange(8))) == rows["values"]
+    mids = (F.E2M1_MAGNITUDES[:-1] + F.E2M1_MAGNITUDES[1:]) / 2
+    assert list(mids) == rows["bounds"]
+    assert list(F.e2m1_decode(np.arange(8, 16))) == [-v for v in rows["values"]]
+
+
+# ----------------------------------------------------------------------------
+# brute force: every code round-trips; two formulations of RNE agree
+# ----------------------------------------------------------------------------
+
+def test_e4m3_all_256_codes_round_trip():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    assert np.array_equal(F.e4m3_encode(F.e4m3_decode(codes)), codes)
+
+
+def test_e2m1_all_16_codes_round_trip():
+    codes = np.arange(16)
+    assert np.array_equal(F.e2m1_encode(F.e2m1_decode(codes)), codes)
+
+
+def test_marlin_bit_trick_identity_pins_e4m3_decoder():
+    """3090 article section 4.1: (q & 0x80008000) | ((q & 0x7F007F00) >> 1)
+    turns an E4M3 byte (placed in the high byte of a 16-bit lane) into the fp16
+    pattern of value * 2**-8; the bf16 variant shifts by 4 and gives value *
+    2**-120.  numpy's float16 decoding is the independent side."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint32)
+    q = codes << 8
+    h16 = (q & 0x8000) | ((q & 0x7F00) >> 1)
+    b16 = (q & 0x8000) | ((q & 0x7F00) >> 4)
+    val = F.e4m3_decode(codes)
+    assert np.array_equal(h16.astype(np.uint16).view(np.float16).astype(np.float64), val * 2.0 ** -8)
+    bf = torch.from_numpy(b16.astype(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(bf, val * 2.0 ** -120)
+
+
+def _e4m3_sweep():
+    """FreeToken PR #805's sweep design: every grid value and midpoint, one fp32
+    ulp either side of each midpoint, uniform samples over the range and over
+    the subnormals, both signs."""
+    g = F.E4M3_GRID
+    mids = (g[:-1] + g[1:]) / 2
+    m32 = mids.astype(np.float32)
+    up = np.nextafter(m32, np.float32(np.inf))
+    dn = np.nextafter(m32, np.float32(-np.inf))
+    r = np.random.Generator(np.random.PCG64(7))
+    uni = r.uniform(0, 448, 200000).astype(np.float32)
+    sub = r.uniform(0, 2.0 ** -6, 100000).astype(np.float32)
+    big = r.uniform(448, 1e4, 1000).astype(np.float32)
+    x = np.concatenate([g, mids, up, dn, uni, sub, big, [0.0, 2.0 ** -10]]).astype(np.float32)
+    return np.concatenate([x, -x])
+
+
+def test_e4m3_grid_vs_binade_formulations_agree():
+    x = _e4m3_sweep()
+    a = F.e4m3_decode(F.e4m3_encode(x))
+    b = F.e4m3_round_binade(x)
+    assert np.array_equal(a, b)
+    assert np.array_equal(np.signbit(a), np.signbit(b))
+
+
+def test_e2m1_grid_vs_binade_formulations_agree():
+    g = F.E2M1_GRID
+    mids = (g[:-1] + g[1:]) / 2
+    m32 = mids.astype(np.float32)
+    r = np.random.Generator(np.random.PCG64(8))
+    x = np.concatenate([g, mids, np.nextafter(m32, np.float32(9)), np.nextafter(m32, np.float32(-9)),
+                        r.uniform(0, 8, 100000)]).astype(np.float32)
+    x = np.concatenate([x, -x])
+    assert np.array_equal(F.e2m1_decode(F.e2m1_encode(x)), F.e2m1_round_binade(x))
+
+
+def test_e2m1_ties_go_to_the_even_code():
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    assert list(F.e2m1_decode(F.e2m1_encode(ties))) == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0]
+    assert list(F.e2m1_decode(F.e2m1_encode([6.5, 7.0, 100.0]))) == [6.0, 6.0, 6.0]
+
+
+def test_e4m3_matches_torch_cpu_cast_in_range():
+    """Library routine as the other side: torch's float32 -> float8_e4m3fn."""
+    x = _e4m3_sweep()
+    x = x[np.abs(x) <= 448]
+    t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(F.e4m3_encode(x), t)
+
+
+def test_bf16_matches_torch_cpu_cast():
+    r = np.random.Generator(np.random.PCG64(9))
+    bits = r.integers(0, 2 ** 32, 500000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    x = np.concatenate([x, (np.arange(1, 2 ** 16, dtype=np.uint32) << 16 | 0x8000).view(np.float32)])
+    x = x[np.isfinite(x)]
+    t = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(F.bf16_encode(x), t)
+
+
+# ----------------------------------------------------------------------------
+# page values for the casts
+# ----------------------------------------------------------------------------
+
+def test_e4m3_cast_page_values():
+    for inp, exp in ((float(a), float(b)) for a, b in read_golden("e4m3_cast.txt")):
+        got = F.e4m3_decode(F.e4m3_encode(np.float32(inp)))
+        assert got == exp and np.signbit(got) == np.signbit(exp), (inp, got, exp)
+
+
+def test_double_rounding_bug_is_not_reproduced():
+    """FreeToken PR #805: fp32 -RTZ-> fp16 -RNE-> e4m3 gives 192 for 200.04."""
+    x = np.float32(200.04)
+    h = np.float16(x)
+    rtz = h if abs(float(h)) <= float(x) else np.nextafter(h, np.float16(0))
+    assert F.e4m3_decode(F.e4m3_encode(np.float32(rtz))) == 192.0
+    assert F.e4m3_decode(F.e4m3_encode(x)) == 208.0
+
+
+def test_bf16_serial_sum_of_4096_ones():
+    rows = {r[0]: float(r[1]) for r in read_golden("accumulation.txt")}
+    s_bf16, s_f32 = 0.0, np.float32(0)
+    for _ in range(int(rows["terms"])):
+        s_bf16 = float(F.bf16_round(s_bf16 + 1.0))
+        s_f32 = np.float32(s_f32 + np.float32(1))
+    assert s_bf16 == rows["bf16_serial_sum"]
+    assert float(s_f32) == rows["fp32_serial_sum"]
+
+
+def test_70000_survives_bf16_not_fp16():
+    v = float(dict(read_golden("overflow.txt"))["value"])
+    assert np.isfinite(F.bf16_round(v))
+    assert np.isinf(np.float16(v))
+    # the binade rounding with fp16's parameters overflows past 65504 too
+    assert F.round_binade(v, 11, -14) > F.ieee_max_finite(5, 10)
+
+
+def test_bytes_per_param():
+    rows = {r[0]: float(r[1]) for r in read_golden("bits_per_param.txt")}
+    assert round(0.5 + 16 / 128 / 8, 3) == rows["int4_g128_bytes"]
+    assert 4 + 8 / 32 == rows["mxfp4_bits"]
+
+
+# ----------------------------------------------------------------------------
+# E8M0 scale rule (vLLM PR #43557)
+# ----------------------------------------------------------------------------
+
+def test_e8m0_worked_table():
+    for row in read_golden("e8m0_table.txt"):
+        vmax, old_be, old_s, be, s, r_old, r_new = map(float, row)
+        v = np.float32(vmax)
+        se = int(Q.e8m0_scale_exp(v))
+        assert se == be and 2.0 ** (se - 127) == s
+        assert round(vmax / 2.0 ** (se - 127), 6) == r_new
+        so = int(Q.e8m0_scale_exp_old(v))
+        assert so == old_be and 2.0 ** (so - 127) == old_s
+        assert round(vmax / 2.0 ** (so - 127), 6) == r_old
+
+
+@pytest.mark.parametrize("k", [-20, -3, 0, 1, 5, 40])
+def test_e8m0_threshold_edges(k):
+    s = lambda m: int(Q.e8m0_scale_exp(np.float32(m * 2.0 ** k)))
+    assert s(1.75) == 127 + k + 1 - 2          # significand 0.75 rounds the exponent up
+    assert s(1.7421875) == 127 + k - 2         # the bf16 just below does not
+    # ratio 6.5 saturates to 6; ratio 6 lands exactly on 6
+    for m, code in ((1.625, 7), (1.5, 7)):
+        x = np.zeros(16, np.float32)
+        x[0] = m * 2.0 ** k
+        packed, se = Q.quant_mxfp4(x, 16)
+        assert int(se[0]) == 127 + k - 2
+        assert int(Q.unpack_nibbles(packed)[0]) == code
+
+
+def test_clip_zone_fractions():
+    rows = {r[0]: float(r[1]) for r in read_golden("clip_zones.txt")}
+    r = np.random.Generator(np.random.PCG64(11))
+    sig = 1.0 + r.integers(0, 2 ** 23, 200000) / 2.0 ** 23
+    vmax = (sig * 2.0 ** r.integers(-10, 10, sig.size)).astype(np.float32)
+
+    def clip_frac(se):
+        ratio = vmax / np.ldexp(1.0, se.astype(np.int64) - 127)
+        return np.mean(ratio > 6.0)
+
+    assert abs(clip_frac(Q.e8m0_scale_exp(vmax)) - rows["threshold_0.75"]) < 0.01
+    assert abs(clip_frac(Q.e8m0_scale_exp_ocp(vmax)) - rows["strict_ocp"]) < 0.01
+    assert clip_frac(Q.e8m0_scale_exp_ceil(vmax)) == rows["threshold_0.5"]
+    ratio = vmax / np.ldexp(1.0, Q.e8m0_scale_exp(vmax).astype(np.int64) - 127)
+    assert ratio.max() < 7.0 and ratio.min() >= 3.5
+
+
+def test_quant_mxfp4_brute_force_small():
+    """Each element's code is the nearest of all 16 codes to x / 2**(se-127),
+    ties to the even code, found by exhaustive search with exact fractions."""
+    r = np.random.Generator(np.random.PCG64(12))
+    x = (r.standard_normal((4, 64)) * 3).astype(np.float32)
+    x[0, 5] = 0.0
+    x[1, :16] = 0.0
+    packed, se = Q.quant_mxfp4(x, 16)
+    codes = Q.unpack_nibbles(packed)
+    vals = [Fraction(float(v)) for v in F.e2m1_decode(np.arange(16))]
+    for i in range(4):
+        for j in range(64):
+            blk = x[i, (j // 16) * 16:(j // 16) * 16 + 16]
+            vmax = float(np.max(np.abs(blk)))
+            e = int(se[i, j // 16])
+            assert e == int(Q.e8m0_scale_exp(np.float32(vmax)))
+            t = Fraction(float(x[i, j])) / Fraction(2) ** (e - 127)
+            t = max(min(t, Fraction(6)), Fraction(-6))
+            best = min(range(16), key=lambda c: (abs(vals[c] - t), c % 2, -c if t < 0 else c))
+            got = int(codes[i, j])
+            assert vals[got] == vals[best], (i, j, got, best)
+
+
+# ----------------------------------------------------------------------------
+# FP8 block quantizer
+# ----------------------------------------------------------------------------
+
+def test_fp8_scale_page_example():
+    rows = {r[0]: float(r[1]) for r in read_golden("scale_example.txt")}
+    x = np.zeros(128, np.float32)
+    x[3] = np.float32(rows["amax"])
+    x[7] = np.float32(-1.0)
+    codes, s = Q.quant_fp8_block(x, 128)
+    assert np.isclose(float(s[0]), rows["scale"], rtol=1e-6)
+    assert F.e4m3_decode(codes[3]) == rows["largest_lands_on"]
+
+
+def test_fp8_block_invariants():
+    r = np.random.Generator(np.random.PCG64(13))
+    x = r.standard_normal((16, 512)).astype(np.float32) * np.float32(3.0)
+    x[2, 128:256] = 0.0
+    codes, s = Q.quant_fp8_block(x, 128)
+    dec = F.e4m3_decode(codes).reshape(16, 4, 128)
+    xb = x.reshape(16, 4, 128).astype(np.float64)
+    assert s[2, 1] == 1.0 and np.all(codes.reshape(16, 4, 128)[2, 1] == 0)
+    for i in range(16):
+        for b in range(4):
+            if i == 2 and b == 1:
+                continue
+            j = np.argmax(np.abs(xb[i, b]))
+            assert abs(dec[i, b, j]) == 448.0
+            t = xb[i, b] / float(s[i, b])
+            # one rounding: relative error <= 2**-4 for normals, abs <= 2**-10 below
+            err = np.abs(dec[i, b] - t)
+            assert np.all(err <= np.maximum(np.abs(t) * 2.0 ** -4, 2.0 ** -10) * (1 + 1e-6))
+
+
+# ----------------------------------------------------------------------------
+# weight quantizers (invariants only: parity unpinned)
+# ----------------------------------------------------------------------------
+
+def test_int4_rtn_invariants():
+    r = np.random.Generator(np.random.PCG64(14))
+    w = (r.standard_normal((8, 512)) * 0.02).astype(np.float32)
+    w[3, 128:256] = 0
+    packed, sb = Q.quant_int4_rtn(w, 128)
+    q = F.int4_decode(Q.unpack_nibbles(packed)).reshape(8, 4, 128)
+    s = F.bf16_decode(sb)
+    assert sb[3, 1] == 0x3F80 and np.all(q[3, 1] == 0)
+    wb = w.reshape(8, 4, 128).astype(np.float64)
+    for i in range(8):
+        for g in range(4):
+            if i == 3 and g == 1:
+                continue
+            assert np.max(np.abs(q[i, g])) == 7
+            assert np.all(np.abs(q[i, g] * s[i, g] - wb[i, g]) <= s[i, g] / 2 * (1 + 2.0 ** -7))
+
+
+def test_nvfp4_invariants():
+    r = np.random.Generator(np.random.PCG64(15))
+    w = (r.standard_normal((8, 256)) * 0.02).astype(np.float32)
+    packed, sb, gs = Q.quant_nvfp4(w)
+    assert np.isclose(float(gs), np.abs(w).max() / 2688.0, rtol=1e-6)
+    i, j = np.unravel_index(np.argmax(np.abs(w)), w.shape)
+    assert F.e4m3_decode(sb[i, j // 16]) == 448.0
+    codes = Q.unpack_nibbles(packed)
+    assert abs(F.e2m1_decode(codes[i, j])) == 6.0
+    deq = F.e2m1_decode(codes) * np.repeat(F.e4m3_decode(sb), 16, axis=1) * float(gs)
+    scale = np.repeat(F.e4m3_decode(sb), 16, axis=1) * float(gs)
+    # one E2M1 rounding of w / scale (relative 2**-2 for normals) plus saturation at 6
+    assert np.all(np.abs(deq - w) <= np.maximum(np.abs(w) * 0.25, 0.25 * scale) * 1.001 + 1e-12)
+
+
+# ----------------------------------------------------------------------------
+# dequantization and products: exact arithmetic as the other side
+# ----------------------------------------------------------------------------
+
+def _nearest_bf16_fraction(v):
+    """Round an exact Fraction to bf16 by exhaustive search over the 2 neighbours."""
+    f = float(v)                                     # within 1 ulp of double
+    lo = F.bf16_decode(F.bf16_encode(np.float64(f)))
+    cands = set()
+    for base in (float(lo),):
+        b = int(F.bf16_encode(np.float64(base)))
+        for d in (-2, -1, 0, 1, 2):
+            c = (b + d) & 0xFFFF
+            cv = float(F.bf16_decode(np.uint16(c)))
+            if np.isfinite(cv):
+                cands.add((Fraction(cv), c))
+    best = min(cands, key=lambda fc: (abs(fc[0] - v), (fc[1] & 1)))
+    return best[0]
+
+
+def test_dequant_int4_is_one_rounding_of_the_exact_product():
+    r = np.random.Generator(np.random.PCG64(16))
+    s_bits = r.integers(0x3000, 0x4400, 64).astype(np.uint16)
+    q = np.arange(-8, 8)
+    packed = Q.pack_nibbles(np.tile(q & 0xF, 8).reshape(1, 128).repeat(64, 0))
+    deq = F.bf16_decode(G.dequant_int4(packed, s_bits.reshape(64, 1), 128))
+    for n in range(64):
+        s = Fraction(float(F.bf16_decode(s_bits[n])))
+        for k in range(16):
+            assert Fraction(float(deq[n, k])) == _nearest_bf16_fraction(int(q[k]) * s)
+
+
+def test_gemm_f64_matches_exact_brute_force():
+    """Dyadic x and w on tiny odd shapes: the fp64 product is exact, so it must
+    equal a pure-Python Fraction sum; a transposed operand or dropped scale
+    fails here (N != M != K)."""
+    r = np.random.Generator(np.random.PCG64(17))
+    M, N, K = 3, 5, 64
+    x = (r.integers(-16, 16, (M, K)) / 8.0).astype(np.float32)
+    w = (r.integers(-16, 16, (N, K)) / 4.0).astype(np.float32)
+    cs = (r.integers(1, 9, N) / 2.0)
+    xb = F.bf16_encode(x)
+    wb = F.bf16_encode(w)
+    y = G.gemm_bf16_f64(xb, wb, cs)
+    for m in range(M):
+        for n in range(N):
+            ref = sum(Fraction(float(x[m, k])) * Fraction(float(w[n, k])) for k in range(K))
+            assert Fraction(float(y[m, n])) == ref * Fraction(float(cs[n]))
+
+
+def test_w4a8_grouped_matches_exact_brute_force():
+    r = np.random.Generator(np.random.PCG64(18))
+    E, N, K, g = 3, 4, 256, 128
+    off = np.array([0, 2, 2, 5], dtype=np.int32)
+    a = r.integers(0, 256, (5, K)).astype(np.uint8)
+    a[(a & 0x7F) == 0x7F] = 0x10
+    a_s = (r.integers(1, 5, 5) / 4.0).astype(np.float32)
+    qn = r.integers(0, 16, (E, N, K)).astype(np.uint8)
+    packed = Q.pack_nibbles(qn)
+    s_bits = r.integers(0x3C00, 0x4000, (E, N, K // g)).astype(np.uint16)
+    y = G.w4a8_grouped_f64(a, a_s, off, packed, s_bits, g)
+    av = F.e4m3_decode(a)
+    qv = F.int4_decode(qn)
+    sv = F.bf16_decode(s_bits)
+    for row in range(5):
+        e = int(np.searchsorted(off, row, side="right") - 1)
+        for n in range(N):
+            ref = sum(Fraction(float(av[row, k])) * int(qv[e, n, k]) * Fraction(float(sv[e, n, k // g]))
+                      for k in range(K))
+            assert Fraction(float(y[row, n])) == ref * Fraction(float(a_s[row]))
+
+
+def test_output_narrowing_is_a_single_rounding():
+    """bf16(y64) must not go through fp32 (double rounding): y = 1 + 2**-8 +
+    2**-30 rounds up in one step but ties-to-even down via fp32."""
+    y = 1.0 + 2.0 ** -8 + 2.0 ** -30
+    assert F.bf16_decode(G.to_bf16(np.float64(y))) == 1.0 + 2.0 ** -7
+    y32 = np.float32(y)            # 1 + 2**-8 exactly (the 2**-30 is lost)
+    assert F.bf16_decode(G.to_bf16(np.float64(y32))) == 1.0
