@@ -1,0 +1,610 @@
+"""Benchmark of the quantized-weight GEMM/GEMV hot path on GB300.
+
+One step = one pass over every row of the hot path at its workload size:
+  decode sweep   W x A16 GEMV, M in {1, 4, 16} x (N,K) in {4096^2, 14336x4096,
+                 4096x14336} x {INT4-g128, FP8-channel, MXFP4, NVFP4}
+  prefill        W4A16 GEMM, M = 8192, same three (N, K), INT4 g128
+  quantizers     4096 x 7168 bf16 -> FP8 E4M3 per 1x128, MXFP4 (E8M0 per 16)
+  MoE            W4A8 layer, T = 4096, hidden 4096, inter 14336, E = 8, top-2
+Each row is one CUDA graph; CUDA events between the graphs time every row
+inside the timed region.  The headline value is the metric's first quantity:
+effective HBM GB/s of the M = 1 GEMVs (algorithmic bytes / time); the
+M = 8192 TFLOP/s is reported beside it.  Inputs are seeded synthetic data
+(weights N(0, 0.02), activations N(0, 1)), resident in HBM before timing; the
+step's working set is far larger than L2, and every weight matrix is read
+once per step.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (there is no other implementation to run).
+"""
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "M=1 effective HBM GB/s (% of peak); M=8192 TFLOP/s (% of bf16 dense peak)"
+SHAPES = [(4096, 4096), (14336, 4096), (4096, 14336)]
+FORMATS = ["int4", "fp8", "mxfp4", "nvfp4"]
+BYTES_PER_PARAM = {"int4": 0.5 + 2 / 128, "fp8": 1.0, "mxfp4": 0.5 + 1 / 32, "nvfp4": 0.5 + 1 / 16}
+
+
+def gemv_bytes(fmt, M, N, K):
+    """Algorithmic bytes: weights + scales, activations in, outputs out."""
+    b = N * K * BYTES_PER_PARAM[fmt] + 2 * M * K + 2 * M * N
+    if fmt == "fp8":
+        b += 4 * N
+    if fmt == "nvfp4":
+        b += 4
+    return b
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only: the path has no exchange step)
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(v, world, device="cpu"):
+    """Max of a float over ranks (timing: the slowest replica sets the time)."""
+    if world == 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_units, elapsed_s_max):
+    """Whole-job throughput: units processed by all ranks / slowest rank's time."""
+    return float(per_rank_units) / float(elapsed_s_max)
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the workload on the device
+# ----------------------------------------------------------------------------
+
+class Workload:
+    def __init__(self, torch, qg, dev, rows):
+        self.t, self.qg, self.dev = torch, qg, dev
+        self.rows = rows
+        self.launches = {}          # segment -> kernel launches per replay
+        self.bytes = {}             # segment -> algorithmic bytes per replay
+        self.flops = {}
+        self.detail = {}
+        self._build()
+
+    def _randn(self, shape, seed, std=1.0):
+        g = self.t.Generator(device=self.dev)
+        g.manual_seed(seed)
+        return self.t.randn(shape, generator=g, device=self.dev, dtype=self.t.float32) * std
+
+    def _bf16(self, x):
+        return x.to(self.t.bfloat16).view(self.t.int16).contiguous()
+
+    def _weights(self, fmt, w):
+        t, qg = self.t, self.qg
+        N, K = w.shape
+        if fmt == "int4":
+            q = t.empty((N, K // 2), dtype=t.uint8, device=self.dev)
+            s = t.empty((N, K // 128), dtype=t.int16, device=self.dev)
+            qg.qg_quantize_weights_int4(w, q, s, 128, N, K)
+            return dict(q=q, s=s)
+        if fmt == "fp8":
+            q = t.empty((N, K), dtype=t.uint8, device=self.dev)
+            s = t.empty((N,), dtype=t.float32, device=self.dev)
+            qg.qg_quantize_weights_fp8(w, q, s, N, K)
+            return dict(q=q, s=s)
+        if fmt == "mxfp4":
+            q = t.empty((N, K // 2), dtype=t.uint8, device=self.dev)
+            s = t.empty((N, K // 32), dtype=t.uint8, device=self.dev)
+            qg.qg_quantize_weights_mxfp4(w, q, s, 32, N, K)
+            return dict(q=q, s=s)
+        q = t.empty((N, K // 2), dtype=t.uint8, device=self.dev)
+        s = t.empty((N, K // 16), dtype=t.uint8, device=self.dev)
+        gs = t.empty((1,), dtype=t.float32, device=self.dev)
+        qg.qg_quantize_weights_nvfp4(w, q, s, gs, N, K)
+        return dict(q=q, s=s, gs=gs)
+
+    def gemv(self, fmt, W, x, y, M, N, K):
+        qg = self.qg
+        if fmt == "int4":
+            qg.qgemm_w4a16(W["q"], W["s"], 128, x, y, M, N, K)
+        elif fmt == "fp8":
+            qg.qgemm_w8a16(W["q"], W["s"], x, y, M, N, K)
+        elif fmt == "mxfp4":
+            qg.qgemm_fp4a16(W["q"], W["s"], qg.QG_SCALE_E8M0, 32, None, x, y, M, N, K)
+        else:
+            qg.qgemm_fp4a16(W["q"], W["s"], qg.QG_SCALE_E4M3, 16, W["gs"], x, y, M, N, K)
+
+    def _build(self):
+        t = self.t
+        from numerics_packed_int4_gb300 import inputs
+        self.W = {}
+        if any(r.startswith("decode") or r == "prefill" for r in self.rows):
+            for i, (N, K) in enumerate(SHAPES):
+                w = self._randn((N, K), seed=1000 + i, std=0.02)
+                for fmt in FORMATS:
+                    if fmt != "int4" and not any(r.startswith("decode") for r in self.rows):
+                        continue
+                    self.W[(fmt, N, K)] = self._weights(fmt, w)
+                del w
+        self.X, self.Y = {}, {}
+        for M in (1, 4, 16):
+            for K in sorted({k for _, k in SHAPES}):
+                self.X[(M, K)] = self._bf16(self._randn((M, K), seed=2000 + M * 7 + K))
+            for N in sorted({n for n, _ in SHAPES}):
+                self.Y[(M, N)] = t.empty((M, N), dtype=t.int16, device=self.dev)
+        if "prefill" in self.rows:
+            self.XP = {}
+            for K in sorted({k for _, k in SHAPES}):
+                x = self._randn((8192, K), seed=3000 + K)
+                g = np.random.Generator(np.random.PCG64(3001 + K))
+                ch = t.from_numpy(g.permutation(K)[: K // 100]).to(self.dev)
+                x[:, ch] *= 50.0                               # 1 % outlier channels x50
+                self.XP[K] = self._bf16(x)
+            self.YP = {N: t.empty((8192, N), dtype=t.int16, device=self.dev) for N, _ in SHAPES}
+        if "quant" in self.rows:
+            xq = inputs.quantizer_activations_bf16(4096, 7168, seed=0)
+            self.XQ = t.from_numpy(xq.view(np.int16)).to(self.dev)
+            self.QF = t.empty((4096, 7168), dtype=t.uint8, device=self.dev)
+            self.QFs = t.empty((4096, 56), dtype=t.float32, device=self.dev)
+            self.QM = t.empty((4096, 3584), dtype=t.uint8, device=self.dev)
+            self.QMs = t.empty((4096, 448), dtype=t.uint8, device=self.dev)
+        if "moe" in self.rows:
+            self._build_moe(inputs)
+
+    def _build_moe(self, inputs):
+        t, dev = self.t, self.dev
+        T, E, H, I, topk = 4096, 8, 4096, 14336, 2
+        rt = inputs.moe_routing(T, E, topk, seed=9)
+        R = int(rt["expert_off"][-1])
+        self.moe = dict(T=T, E=E, H=H, I=I, topk=topk, R=R)
+        row_of = np.full((T, topk), -1, np.int32)
+        wt = np.zeros((T, topk), np.float32)
+        fill = np.zeros(T, np.int64)
+        for r, tok in enumerate(rt["route_rows"]):
+            row_of[tok, fill[tok]] = r
+            wt[tok, fill[tok]] = rt["route_weight"][r]
+            fill[tok] += 1
+        m = self.moe
+        m["off"] = t.from_numpy(rt["expert_off"]).to(dev)
+        m["rows"] = t.from_numpy(rt["route_rows"]).to(dev)
+        m["row_of"] = t.from_numpy(row_of).to(dev)
+        m["wt"] = t.from_numpy(wt).to(dev)
+        m["x"] = self._bf16(self._randn((T, H), seed=4000))
+        w1q = t.empty((E, 2 * I, H // 2), dtype=t.uint8, device=dev)
+        w1s = t.empty((E, 2 * I, H // 128), dtype=t.int16, device=dev)
+        w2q = t.empty((E, H, I // 2), dtype=t.uint8, device=dev)
+        w2s = t.empty((E, H, I // 128), dtype=t.int16, device=dev)
+        for e in range(E):
+            w = self._randn((2 * I, H), seed=5000 + e, std=0.02)
+            self.qg.qg_quantize_weights_int4(w, w1q[e], w1s[e], 128, 2 * I, H)
+            w = self._randn((H, I), seed=6000 + e, std=0.02)
+            self.qg.qg_quantize_weights_int4(w, w2q[e], w2s[e], 128, H, I)
+            del w
+        m.update(w1q=w1q, w1s=w1s, w2q=w2q, w2s=w2s)
+        m["xq"] = t.empty((T, H), dtype=t.uint8, device=dev)
+        m["xs"] = t.empty((T,), dtype=t.float32, device=dev)
+        m["aq"] = t.empty((R, H), dtype=t.uint8, device=dev)
+        m["as"] = t.empty((R,), dtype=t.float32, device=dev)
+        m["gu"] = t.empty((R, 2 * I), dtype=t.int16, device=dev)
+        m["hq"] = t.empty((R, I), dtype=t.uint8, device=dev)
+        m["hs"] = t.empty((R,), dtype=t.float32, device=dev)
+        m["down"] = t.empty((R, H), dtype=t.int16, device=dev)
+        m["out"] = t.empty((T, H), dtype=t.int16, device=dev)
+
+    # ---- segments -----------------------------------------------------------
+    def run_segment(self, name):
+        qg = self.qg
+        if name.startswith("decode_m"):
+            M = int(name[len("decode_m"):])
+            for fmt in FORMATS:
+                for N, K in SHAPES:
+                    self.gemv(fmt, self.W[(fmt, N, K)], self.X[(M, K)], self.Y[(M, N)], M, N, K)
+        elif name == "prefill":
+            for N, K in SHAPES:
+                W = self.W[("int4", N, K)]
+                qg.qgemm_w4a16(W["q"], W["s"], 128, self.XP[K], self.YP[N], 8192, N, K)
+        elif name == "quant":
+            qg.quant_act_fp8_block(self.XQ, self.QF, self.QFs, 128, 4096, 7168)
+            qg.quant_act_mxfp4(self.XQ, self.QM, self.QMs, 16, 4096, 7168)
+        elif name == "moe":
+            m = self.moe
+            T, E, H, I, R, topk = m["T"], m["E"], m["H"], m["I"], m["R"], m["topk"]
+            qg.quant_act_fp8_block(m["x"], m["xq"], m["xs"], H, T, H)
+            qg.qg_moe_gather_fp8(m["xq"], m["xs"], m["rows"], m["aq"], m["as"], R, T, H)
+            qg.qgemm_w4a8_grouped(m["aq"], m["as"], m["off"], m["w1q"], m["w1s"], 128, m["gu"], R, E, 2 * I, H)
+            qg.qg_swiglu_quant_fp8(m["gu"], m["hq"], m["hs"], R, I)
+            qg.qgemm_w4a8_grouped(m["hq"], m["hs"], m["off"], m["w2q"], m["w2s"], 128, m["down"], R, E, H, I)
+            qg.qg_moe_combine(m["down"], m["row_of"], m["wt"], m["out"], T, topk, R, H)
+
+    def accounting(self):
+        for M in (1, 4, 16):
+            name = "decode_m%d" % M
+            if name in self.rows:
+                self.bytes[name] = sum(gemv_bytes(f, M, N, K) for f in FORMATS for N, K in SHAPES)
+                self.launches[name] = None
+        if "prefill" in self.rows:
+            self.flops["prefill"] = sum(2.0 * 8192 * N * K for N, K in SHAPES)
+        if "quant" in self.rows:
+            M, K = 4096, 7168
+            self.bytes["quant"] = M * K * (2 + 1) + M * K // 128 * 4 + M * K * 2 + M * K // 2 + M * K // 16
+        if "moe" in self.rows:
+            m = self.moe
+            self.flops["moe"] = 2.0 * m["R"] * (2 * m["I"] * m["H"] + m["H"] * m["I"])
+
+
+def count_launches(torch, fn):
+    """Kernel launches of one segment: count them with the profiler once."""
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    n = 0
+    for ev in prof.events():
+        if ev.device_type.name == "CUDA" and "memcpy" not in ev.name.lower() and "memset" not in ev.name.lower():
+            n += 1
+    return n
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and cpu_baseline)
+# ----------------------------------------------------------------------------
+
+def oracle_gemv_sample(seconds_budget=15.0, max_items=None):
+    """Time the oracle on M=1 GEMVs of the decode workload (a bounded sample).
+
+    Returns (GB/s in the metric's unit, seconds, description)."""
+    from numerics_packed_int4_gb300 import inputs
+    from oracle import gemm as OG
+    from oracle import quant as OQ
+    done_bytes, spent, items = 0.0, 0.0, []
+    plan = [(f, N, K) for N, K in SHAPES for f in FORMATS]
+    for i, (fmt, N, K) in enumerate(plan):
+        if spent > seconds_budget or (max_items and i >= max_items):
+            break
+        w = inputs.weights_f32(N, K, seed=1000 + i)
+        x = inputs.activations_bf16(1, K, seed=2000 + K)
+        t0 = time.perf_counter()
+        if fmt == "int4":
+            q, s = OQ.quant_int4_rtn(w, 128)
+            t0 = time.perf_counter()
+            OG.to_bf16(OG.qgemm_w4a16(x, q, s, 128))
+        elif fmt == "fp8":
+            q, cs = OQ.quant_fp8_channel(w)
+            t0 = time.perf_counter()
+            OG.to_bf16(OG.qgemm_w8a16(x, q, cs))
+        elif fmt == "mxfp4":
+            q, se = OQ.quant_mxfp4_weights(w)
+            t0 = time.perf_counter()
+            OG.to_bf16(OG.qgemm_mxfp4a16(x, q, se))
+        else:
+            q, sb, gs = OQ.quant_nvfp4(w)
+            t0 = time.perf_counter()
+            OG.to_bf16(OG.qgemm_nvfp4a16(x, q, sb, gs))
+        dt = time.perf_counter() - t0
+        spent += dt
+        done_bytes += gemv_bytes(fmt, 1, N, K)
+        items.append("%s %dx%d" % (fmt, N, K))
+    return done_bytes / spent / 1e9, spent, ", ".join(items)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1:
+        dist_init(world, "gloo")
+        if rank != 0:
+            dist_barrier(world)
+            return 0
+    vals = []
+    for _ in range(args.warmup):
+        oracle_gemv_sample(max_items=1)
+    t0 = time.perf_counter()
+    desc = ""
+    for _ in range(args.steps):
+        v, _, desc = oracle_gemv_sample(max_items=1)
+        vals.append(v)
+    el = time.perf_counter() - t0
+    value = float(np.mean(vals))
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * el / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": "decode sweep M=1 (oracle sample: %s)" % desc},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": "one M=1 GEMV per step: %s" % desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist_barrier(world)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        dist_init(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from numerics_packed_int4_gb300 import qgemm as qg
+    qg.load()
+    peaks = load_peaks()
+
+    rows = args.rows.split(",")
+    wl = Workload(torch, qg, dev, rows)
+    wl.accounting()
+    torch.cuda.synchronize()
+
+    # eager warm-up of every segment (sets kernel attributes), then capture graphs
+    for r in rows:
+        wl.run_segment(r)
+    qg.qg_check_device_error()
+    for r in rows:
+        wl.launches[r] = count_launches(torch, lambda r=r: wl.run_segment(r))
+    graphs = {}
+    cap = torch.cuda.Stream(device=dev)
+    for r in rows:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            wl.run_segment(r)
+        graphs[r] = g
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        for r in rows:
+            graphs[r].replay()
+    qg.qg_check_device_error()
+
+    ev = {r: [] for r in rows}
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        t_wall = time.perf_counter()
+        start.record(stream)
+        for _ in range(args.steps):
+            for r in rows:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                graphs[r].replay()
+                b.record(stream)
+                ev[r].append((a, b))
+        end.record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    dist_barrier(world)
+    qg.qg_check_device_error()
+    total_ms = dist_max(start.elapsed_time(end), world, dev)
+    seg_ms = {r: sum(a.elapsed_time(b) for a, b in ev[r]) / args.steps for r in rows}
+    seg_ms_max = {r: dist_max(seg_ms[r], world, dev) for r in rows}
+
+    # ---- per-row throughput and rooflines ----------------------------------------
+    row_out = {}
+    for r in rows:
+        ms = seg_ms_max[r]
+        if r in wl.bytes:
+            gbs = wl.bytes[r] / (ms * 1e-3) / 1e9
+            row_out[r] = {"ms": ms, "GB/s": gbs, "launches": wl.launches[r],
+                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                                       "frac": gbs / peaks["hbm"],
+                                       "traffic": None}}
+        else:
+            tf = wl.flops[r] / (ms * 1e-3) / 1e12
+            peak = peaks["bf16"]
+            row_out[r] = {"ms": ms, "TFLOP/s": tf, "launches": wl.launches[r],
+                          "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                                       "frac": tf / peak, "traffic": None}}
+    dominant = max(rows, key=lambda r: seg_ms_max[r])
+    value = aggregate(world * wl.bytes.get("decode_m1", 0.0), seg_ms_max.get("decode_m1", 1.0) * 1e-3) / 1e9
+
+    e2e = e2e_decode_m1(torch, qg, wl, dev, steps=max(2, min(args.steps, 5))) if "decode_m1" in rows else None
+    clocks = clk.summary()
+    launches_per_step = sum((wl.launches[r] or 0) for r in rows)
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded: weights N(0,0.02), activations N(0,1))",
+        "config": {"workload": "decode sweep M in {1,4,16} x {4096^2, 14336x4096, 4096x14336} x "
+                               "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill W4A16 M=8192 + "
+                               "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2",
+                   "rows": rows, "l2": "inputs larger than L2: every weight matrix read once per step; "
+                                       "step working set > 1 GB vs 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "secondary": None,
+        "roofline": dict(row_out[dominant]["roofline"], kernel=dominant),
+        "roofline_value": dict(row_out["decode_m1"]["roofline"], kernel="decode_m1") if "decode_m1" in row_out else None,
+        "rows": row_out, "peaks_source": peaks["src"], "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps, "e2e": e2e,
+        "wall_s": t_wall,
+    }
+    if "prefill" in row_out:
+        p = row_out["prefill"]
+        line["secondary"] = {"metric": "M=8192 TFLOP/s", "value": p["TFLOP/s"], "unit": "TFLOP/s",
+                             "frac_of_bf16_peak": p["TFLOP/s"] / peaks["bf16"],
+                             "frac_of_bf16_sustained": p["TFLOP/s"] / peaks["bf16_sus"]}
+    if not args.no_cpu_baseline and world == 1:
+        v, spent, desc = oracle_gemv_sample(seconds_budget=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": "M=1 GEMVs (oracle dequant + fp64 product): %s; %.1f s" % (desc, spent)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def e2e_decode_m1(torch, qg, wl, dev, steps):
+    """M=1 GB/s through the C ABI with host buffers: every step copies each
+    GEMV's weights, scales and activation from pinned host memory, runs the
+    12 GEMVs and copies the outputs back."""
+    host = {}
+    h2d = 0
+    for fmt in FORMATS:
+        for N, K in SHAPES:
+            W = wl.W[(fmt, N, K)]
+            hw = {k: v.cpu().pin_memory() for k, v in W.items()}
+            dw = {k: torch.empty_like(v) for k, v in W.items()}
+            host[(fmt, N, K)] = (hw, dw)
+            h2d += sum(v.numel() * v.element_size() for v in hw.values())
+    hx = {K: wl.X[(1, K)].cpu().pin_memory() for _, K in SHAPES}
+    h2d += len(FORMATS) * sum(hx[K].numel() * 2 for _, K in SHAPES)
+    hy = {N: torch.empty((1, N), dtype=torch.int16).pin_memory() for N, _ in SHAPES}
+    d2h = len(FORMATS) * sum(hy[N].numel() * 2 for N, _ in SHAPES)
+    dx = {K: torch.empty_like(wl.X[(1, K)]) for _, K in SHAPES}
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        for fmt in FORMATS:
+            for N, K in SHAPES:
+                hw, dw = host[(fmt, N, K)]
+                for k in hw:
+                    dw[k].copy_(hw[k], non_blocking=True)
+                dx[K].copy_(hx[K], non_blocking=True)
+                wl.gemv(fmt, dw, dx[K], wl.Y[(1, N)], 1, N, K)
+                hy[N].copy_(wl.Y[(1, N)], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": wl.bytes["decode_m1"] / (ms * 1e-3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

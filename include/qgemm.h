@@ -1,0 +1,215 @@
+/*
+ * qgemm.h -- C ABI of the GB300 (sm_103a) quantized-weight GEMM/GEMV library.
+ *
+ * The problem is stated the way the pages state it: a packed weight buffer,
+ * a scale buffer, a group/block size, an activation pointer and M/N/K
+ * ("Numerics: FP32 to INT4, and why bf16 won", the block-scaled Triton GEMM
+ * and the dequantization kernel excerpt; "Production-Ready W4A8", section
+ * "High-Performance W4A8 GEMM Kernel").
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  Buffers are
+ *    contiguous and row-major; base addresses must be 16-byte aligned (the
+ *    vLLM MXFP4 fix PR added .contiguous() for exactly this class of bug).
+ *  - bf16 tensors are passed as uint16_t bit patterns.
+ *  - W is [N][K] (output channel major, K contiguous); X is [M][K]; Y is [M][N].
+ *  - Packed 4-bit codes hold two elements per byte along K, the even k in the
+ *    low nibble.  INT4 nibbles are two's complement in [-8, 7]; E2M1 nibbles
+ *    are sign-magnitude (bit 3 = sign).
+ *  - All work is enqueued on the caller's stream; the library never allocates,
+ *    frees or synchronizes (except qg_check_device_error, which syncs).
+ *  - Every call returns a qg_status and never aborts; qg_last_error_string()
+ *    gives a message for the last failing call on the calling thread.
+ *  - Results are deterministic: the same inputs give the same output bits.
+ *  - Arithmetic: dequantized weights are formed in registers exactly as the
+ *    canonical dequantization below; products accumulate in fp32; the output
+ *    is rounded to bf16 once (round to nearest even) at the store.
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QG_API __attribute__((visibility("default")))
+#else
+#define QG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* qg_stream_t;
+
+typedef enum qg_status {
+  QG_OK = 0,
+  QG_ERR_INVALID_ARG = 1,        /* NULL pointer, bad enum value, negative size */
+  QG_ERR_UNSUPPORTED_SHAPE = 2,  /* sizes outside the documented rules */
+  QG_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
+  QG_ERR_CUDA = 4,               /* a CUDA runtime call or kernel launch failed */
+  QG_ERR_TIMEOUT = 5             /* a device-side wait hit its iteration cap */
+} qg_status;
+
+/* scale formats of qgemm_fp4a16 */
+enum { QG_SCALE_E8M0 = 0, QG_SCALE_E4M3 = 1 };
+/* weight formats of qg_dequant_weights */
+enum { QG_FMT_INT4 = 0, QG_FMT_FP8 = 1, QG_FMT_MXFP4 = 2, QG_FMT_NVFP4 = 3 };
+
+/* ------------------------------------------------------------------------ *
+ * Weight-only GEMM/GEMV (W x A16): Y = X . dequant(W)^T, fp32 accumulate.
+ * M <= 16 runs the HBM-streaming decode kernel; larger M the prefill kernel.
+ * Shape rules: M >= 1, N >= 1, N % 8 == 0, K % 128 == 0.
+ * ------------------------------------------------------------------------ */
+
+/* INT4 weights with one bf16 scale per group of g along K.
+ * Canonical weight: bf16_RNE(q * s) (one rounding of the exact product):
+ * "Dequantize INT4 weights to BF16 using CUDA cores ... run the matrix
+ * multiplication in BF16" (Production-Ready W4A8, "High-Performance W4A8
+ * GEMM Kernel"); symmetric affine map with zero-point 0 ("Numerics", integer
+ * formats paragraph).
+ *   w_q [N][K/2]  packed INT4        w_s [N][K/g] bf16
+ *   x   [M][K]    bf16               y   [M][N]   bf16 (written)
+ *   g in {32, 64, 128, 256, ...}, g % 32 == 0, K % g == 0.               */
+QG_API qg_status qgemm_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g,
+                      const uint16_t* x, uint16_t* y, int M, int N, int K,
+                      qg_stream_t stream);
+
+/* FP8 E4M3 weights with one fp32 scale per output channel.
+ * y[m,n] = w_cs[n] * sum_k x[m,k] * e4m3(w[n,k]); the E4M3 -> bf16 decode is
+ * exact ("Every E4M3 and E2M1 value is exactly representable in FP16/BF16",
+ * "Your 3090 Isn't Missing Anything...", section 4.1).
+ *   w_e4m3 [N][K] u8    w_cs [N] fp32                                      */
+QG_API qg_status qgemm_w8a16(const uint8_t* w_e4m3, const float* w_cs,
+                      const uint16_t* x, uint16_t* y, int M, int N, int K,
+                      qg_stream_t stream);
+
+/* FP4 E2M1 weights with block scales.
+ *  scale_fmt QG_SCALE_E8M0: MXFP4, g == 32, w_bs [N][K/32] E8M0 codes,
+ *     canonical weight e2m1 * 2^(c-127) (exact); global_scale must be NULL.
+ *     ("Numerics", "MXFP4 and the block-scaled family": block of 32, bare
+ *     power-of-two scale.)
+ *  scale_fmt QG_SCALE_E4M3: NVFP4, g == 16, w_bs [N][K/16] E4M3 codes,
+ *     canonical weight e2m1 * e4m3(sb) (exact); global_scale is a DEVICE
+ *     pointer to one fp32 applied to the accumulated row ("decodes each
+ *     16-value E2M1 weight block and its E4M3 scale to BF16", 3090 article
+ *     section 2.1).
+ *   w_e2m1 [N][K/2] packed E2M1                                            */
+QG_API qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt,
+                       int g, const float* global_scale, const uint16_t* x,
+                       uint16_t* y, int M, int N, int K, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Online activation quantizers.  Rules: M >= 1, K % g == 0, K % 8 == 0.
+ * ------------------------------------------------------------------------ */
+
+/* MXFP4 per block of g in {16, 32}: vecMax = max|x|; scale code from the
+ * exponent-first 0.75-threshold rule (bits(vecMax) + (1<<21)) & 0xFF800000,
+ * biased exponent - 2, clamped at 0; element code E2M1_RNE_satfinite(
+ * x * 2^(127-se)) (vLLM PR #43557, "Fix: Exponent-First with 0.75-Threshold
+ * Rounding").
+ *   x [M][K] bf16 -> q [M][K/2] packed E2M1, s_e8m0 [M][K/g] E8M0 codes.    */
+QG_API qg_status quant_act_mxfp4(const uint16_t* x, uint8_t* q, uint8_t* s_e8m0, int g,
+                          int M, int K, qg_stream_t stream);
+
+/* FP8 E4M3 per 1 x g block (g == K gives per-token): s = amax/448 in fp32
+ * (all-zero block: s = 1), q = E4M3_RNE_satfinite(x / s) with IEEE fp32
+ * division and a single rounding ("Numerics", fp8 linear walk-through;
+ * FreeToken PR #805).  g % 8 == 0.
+ *   x [M][K] bf16 -> q [M][K] E4M3 codes, s [M][K/g] fp32.                  */
+QG_API qg_status quant_act_fp8_block(const uint16_t* x, uint8_t* q, float* s, int g,
+                              int M, int K, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * W4A8 grouped (MoE) GEMM.
+ * Rows of A are grouped by expert: rows expert_off[e] .. expert_off[e+1]-1
+ * use expert e.  y[r,n] = a_s[r] * sum_k e4m3(a[r,k]) * q_e[n,k] * s_e[n,k/g]
+ * with the group scale applied in fp32 per K-group (INT4 x FP8 activations,
+ * per-token x group scales: Production-Ready W4A8).
+ *   a_e4m3 [R][K] E4M3   a_s [R] fp32   expert_off [E+1] int32 (DEVICE,
+ *   non-decreasing, expert_off[0] == 0, expert_off[E] == R)
+ *   w_q [E][N][K/2] packed INT4   w_s [E][N][K/g] bf16   y [R][N] bf16.
+ * Rules: g == 128, K % 128 == 0, N % 16 == 0, R >= 0, E >= 1.               */
+QG_API qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,
+                             const int32_t* expert_off, const uint8_t* w_q,
+                             const uint16_t* w_s, int g, uint16_t* y, int R,
+                             int E, int N, int K, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Load-time weight quantizers (fp32 weights -> the formats above).
+ * ------------------------------------------------------------------------ */
+
+/* INT4 round-to-nearest, s = bf16_RNE(absmax/7) per group (fp32 division),
+ * q = clamp(rint(w/s), -8, 7); an all-zero group (or a scale that rounds to
+ * zero) gets s = 1, q = 0 ("Numerics": symmetric scale from a live amax,
+ * "Define an all-zero-group policy such as s=1").  K % g == 0, g % 8 == 0. */
+QG_API qg_status qg_quantize_weights_int4(const float* w, uint8_t* w_q, uint16_t* w_s, int g,
+                                   int N, int K, qg_stream_t stream);
+/* FP8 E4M3 per output channel: cs = absmax/448 (zero row: 1), code =
+ * E4M3_RNE_satfinite(w / cs).  K % 8 == 0.                                  */
+QG_API qg_status qg_quantize_weights_fp8(const float* w, uint8_t* w_e4m3, float* w_cs,
+                                  int N, int K, qg_stream_t stream);
+/* MXFP4 weights: the quant_act_mxfp4 rule on fp32 rows, g == 32.            */
+QG_API qg_status qg_quantize_weights_mxfp4(const float* w, uint8_t* w_e2m1, uint8_t* w_e8m0,
+                                    int g, int N, int K, qg_stream_t stream);
+/* NVFP4 weights: gs = amax(W)/(448*6) (zero W: 1), sb = E4M3_RNE_sat(
+ * amax_block / (6*gs)), code = E2M1_RNE_sat(w / (e4m3(sb)*gs)); sb == 0 gives
+ * zero codes.  Elements are divided by the dequantized block scale (vLLM PR
+ * #43557 review).  global_scale is a DEVICE fp32 written by the call.
+ * K % 16 == 0.                                                              */
+QG_API qg_status qg_quantize_weights_nvfp4(const float* w, uint8_t* w_e2m1, uint8_t* w_e4m3,
+                                    float* global_scale, int N, int K, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * MoE harness kernels (outside the GEMM, used between the two projections).
+ * ------------------------------------------------------------------------ */
+
+/* rows[r] <- src[route_rows[r]] for E4M3 codes and their per-row scale.
+ *   src_q [T][K] u8, src_s [T] fp32, route_rows [R] int32 (DEVICE)
+ *   dst_q [R][K] u8, dst_s [R] fp32.  K % 16 == 0.                          */
+QG_API qg_status qg_moe_gather_fp8(const uint8_t* src_q, const float* src_s,
+                            const int32_t* route_rows, uint8_t* dst_q, float* dst_s,
+                            int R, int T, int K, qg_stream_t stream);
+/* h = SiLU(gate) * up in fp32 from the bf16 projection output [R][2I] (gate
+ * columns first), then the per-row FP8 quantizer (block = I).
+ *   gate_up [R][2I] bf16 -> q [R][I] E4M3, s [R] fp32.  I % 8 == 0.          */
+QG_API qg_status qg_swiglu_quant_fp8(const uint16_t* gate_up, uint8_t* q, float* s,
+                              int R, int I, qg_stream_t stream);
+/* out[t] = bf16( sum_j weight[t,j] * down[row_of[t,j]] ), j < topk, fp32 sum.
+ *   down [R][H] bf16, row_of [T][topk] int32, weight [T][topk] fp32 (DEVICE)
+ *   out [T][H] bf16.  H % 8 == 0.                                           */
+QG_API qg_status qg_moe_combine(const uint16_t* down, const int32_t* row_of,
+                         const float* weight, uint16_t* out, int T, int topk,
+                         int R, int H, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Test and diagnostics entry points.
+ * ------------------------------------------------------------------------ */
+
+/* Canonical dequantized weights as bf16 [N][K], through the same in-register
+ * decode the GEMM kernels use (epilogue scales excluded: FP8 channel scale,
+ * NVFP4 global scale).  scales: INT4 -> bf16 [N][K/g]; FP8 -> ignored (may be
+ * NULL); MXFP4 -> E8M0 [N][K/32]; NVFP4 -> E4M3 [N][K/16].  K % 128 == 0.    */
+QG_API qg_status qg_dequant_weights(int fmt, const uint8_t* w, const void* scales, int g,
+                             uint16_t* w_out, int N, int K, qg_stream_t stream);
+
+/* Synchronizes the stream, then reads and clears this device's error word.
+ * Returns QG_ERR_TIMEOUT if a kernel gave up on a wait, QG_ERR_CUDA on an
+ * asynchronous CUDA error, QG_OK otherwise.                                  */
+QG_API qg_status qg_check_device_error(qg_stream_t stream);
+
+/* Message for the last failing call on the calling thread ("" if none).     */
+QG_API const char* qg_last_error_string(void);
+
+/* Iteration cap of every device-side spin wait (0 restores the default).
+ * Intended for tests that exercise the timeout path.                        */
+QG_API void qg_set_wait_limit(uint32_t iterations);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_H */

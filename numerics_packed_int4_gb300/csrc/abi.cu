@@ -1,0 +1,119 @@
+// Status, error reporting and device error word shared by every entry point.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "qg_common.cuh"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+// One 32-bit error word per device.  Kernels with spin waits receive its
+// address; on a timeout they store DEV_ERR_TIMEOUT and return early.
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::mutex g_mu;
+
+constexpr uint32_t kDefaultWaitLimit = 1u << 26;   // ~ seconds of try_wait polling
+uint32_t g_wait_limit = kDefaultWaitLimit;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+}  // namespace
+
+namespace qg {
+
+qg_status set_error(qg_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+qg_status check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return set_error(QG_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  return QG_OK;
+}
+
+unsigned int* device_error_word() {
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = static_cast<unsigned int*>(p);
+  }
+  return g_err_ptr[d];
+}
+
+int sm_count() {
+  const int d = current_device();
+  if (d < 0) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[d]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0)
+      n = 148;
+    g_sms[d] = n;
+  }
+  return g_sms[d];
+}
+
+uint32_t wait_limit() { return g_wait_limit; }
+
+bool ensure_smem_attr(const void* kernel, int bytes) {
+  static std::unordered_map<const void*, int> done[kMaxDevices];
+  const int d = current_device();
+  if (d < 0) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = done[d].find(kernel);
+  if (it != done[d].end() && it->second >= bytes) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return false;
+  done[d][kernel] = bytes;
+  return true;
+}
+
+}  // namespace qg
+
+extern "C" {
+
+const char* qg_last_error_string(void) { return g_msg; }
+
+void qg_set_wait_limit(uint32_t iterations) {
+  g_wait_limit = iterations ? iterations : kDefaultWaitLimit;
+}
+
+qg_status qg_check_device_error(qg_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return qg::set_error(QG_ERR_CUDA, "qg_check_device_error: %s", cudaGetErrorString(e));
+  unsigned int* p = qg::device_error_word();
+  if (!p) return qg::set_error(QG_ERR_CUDA, "qg_check_device_error: no error word");
+  unsigned int v = 0;
+  e = cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess)
+    return qg::set_error(QG_ERR_CUDA, "qg_check_device_error: %s", cudaGetErrorString(e));
+  if (v != qg::DEV_ERR_NONE) {
+    const unsigned int zero = 0;
+    cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    return qg::set_error(QG_ERR_TIMEOUT, "a device-side wait exceeded its iteration cap (code %u)", v);
+  }
+  return QG_OK;
+}
+
+}  // extern "C"

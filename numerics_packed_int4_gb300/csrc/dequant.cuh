@@ -1,0 +1,92 @@
+// In-register weight decode: packed low-bit codes -> bf16x2 pairs.
+//
+// Every routine produces the canonical dequantized weight bit for bit:
+//   INT4   bf16_RNE(q * s): the nibble becomes the exact bf16 integer q with
+//          the magic-number trick ((u | 0x4300) - 136 with u = q + 8), then one
+//          bf16 multiply by the group scale rounds the exact product once;
+//   E4M3   exact: sign and the 7 exponent/mantissa bits move into bf16
+//          position with shift/and/or (the FP8 -> FP16 bit trick described in
+//          "Your 3090 Isn't Missing Anything...", section 4.1, with the bf16
+//          shift of 4) and one exact multiply by 2^120 restores the bias;
+//   E2M1   exact: the three magnitude bits land in the bf16 exponent/mantissa
+//          field (value * 2^-126, subnormal code included) and one exact
+//          multiply by 2^126 restores the bias; the block scale (a power of
+//          two for MXFP4, an E4M3 value for NVFP4) is one more exact multiply.
+// No table lookups; shifts, lop3 and packed bf16 arithmetic only.
+//
+// Pair order: the "kperm" forms return, for the 8 k-values k0..k7 held by one
+// 32-bit word (4-bit formats) or two words (E4M3), the pairs used directly as
+// mma.sync A fragments.  Callers that need natural k order use the
+// *_natural helpers (one prmt per pair).
+#pragma once
+
+#include "qg_common.cuh"
+
+namespace qg {
+
+constexpr uint32_t kBf16x2_136 = 0x43084308u;     // 136.0 in both lanes
+constexpr uint32_t kBf16x2_2p120 = 0x7B807B80u;   // 2^120
+constexpr uint32_t kBf16x2_2p126 = 0x7E807E80u;   // 2^126
+
+// lop3 truth tables: a = 0xF0, b = 0xCC, c = 0xAA
+constexpr int kLutAndXor = 0x6A;   // (a & b) ^ c
+constexpr int kLutAndOr = 0xEA;    // (a & b) | c
+
+// ---- INT4 -------------------------------------------------------------------
+// p[i] = (k_i, k_{i+4}) for i = 0..3
+QG_DEVICE void int4x8_kperm(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {
+  p[0] = lop3<kLutAndXor>(v, 0x000F000Fu, 0x43084308u);   // 0x4300 | (nibble ^ 8)
+  p[1] = lop3<kLutAndXor>(v >> 4, 0x000F000Fu, 0x43084308u);
+  p[2] = lop3<kLutAndXor>(v >> 8, 0x000F000Fu, 0x43084308u);
+  p[3] = lop3<kLutAndXor>(v >> 12, 0x000F000Fu, 0x43084308u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = bf16x2_mul(bf16x2_sub(p[i], kBf16x2_136), s2);
+}
+
+// ---- E2M1 -------------------------------------------------------------------
+// p[i] = (k_i, k_{i+4}) for i = 0..3, each e2m1 * scale (exact)
+QG_DEVICE void e2m1x8_kperm(uint32_t v, uint32_t scale2, uint32_t (&p)[4]) {
+  const uint32_t MAG = 0x01C001C0u, SGN = 0x80008000u;
+  p[0] = lop3<kLutAndOr>(v << 6, MAG, (v << 12) & SGN);
+  p[1] = lop3<kLutAndOr>(v << 2, MAG, (v << 8) & SGN);
+  p[2] = lop3<kLutAndOr>(v >> 2, MAG, (v << 4) & SGN);
+  p[3] = lop3<kLutAndOr>(v >> 6, MAG, v & SGN);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = bf16x2_mul(bf16x2_mul(p[i], kBf16x2_2p126), scale2);
+}
+
+// ---- E4M3 -------------------------------------------------------------------
+// w holds bytes k0..k3: p02 = (k0, k2), p13 = (k1, k3), exact values
+QG_DEVICE void e4m3x4_kperm(uint32_t w, uint32_t& p02, uint32_t& p13) {
+  const uint32_t SGN = 0x80008000u, EM = 0x07F007F0u;
+  p13 = lop3<kLutAndOr>(w, SGN, (w >> 4) & EM);
+  const uint32_t w8 = w << 8;
+  p02 = lop3<kLutAndOr>(w8, SGN, (w8 >> 4) & EM);
+  p13 = bf16x2_mul(p13, kBf16x2_2p120);
+  p02 = bf16x2_mul(p02, kBf16x2_2p120);
+}
+
+// ---- scales -> bf16x2 ----------------------------------------------------------
+QG_DEVICE uint32_t bf16x2_splat(uint32_t b) { return (b & 0xFFFFu) * 0x00010001u; }
+
+// E8M0 code c -> bf16 2^(c-127) (c = 0 is the subnormal 2^-127; 255 is NaN)
+QG_DEVICE uint32_t e8m0_to_bf16x2(uint32_t c) {
+  const uint32_t b = c == 0 ? 0x0040u : (c == 255 ? 0x7FC0u : (c << 7));
+  return bf16x2_splat(b);
+}
+
+// E4M3 code -> bf16 (exact)
+QG_DEVICE uint32_t e4m3_to_bf16x2(uint32_t c) {
+  return bf16x2_splat(__float_as_uint(e4m3_to_f32(c & 0xFFu)) >> 16);
+}
+
+// ---- natural order ---------------------------------------------------------
+// (k0,k1),(k2,k3),(k4,k5),(k6,k7) from the (k_i, k_{i+4}) pairs
+QG_DEVICE void kperm4_to_natural(const uint32_t (&p)[4], uint32_t (&o)[4]) {
+  o[0] = prmt(p[0], p[1], 0x5410u);
+  o[1] = prmt(p[2], p[3], 0x5410u);
+  o[2] = prmt(p[0], p[1], 0x7632u);
+  o[3] = prmt(p[2], p[3], 0x7632u);
+}
+
+}  // namespace qg

@@ -1,0 +1,468 @@
+// Decode (M <= 16) weight-only GEMV for the four weight formats, plus the
+// test-only canonical dequantization export.
+//
+// Design ("Your 3090 Isn't Missing Anything...", section 4.3: at M = 1 DRAM
+// bandwidth sets the time; the dequant must stay off the critical path):
+//   * A CTA owns 128 output channels (8 warps x one 16-row mma group) and a
+//     slice of K; the K slices of one row block form a thread-block cluster
+//     (1..8 CTAs) whose partial sums are reduced through distributed shared
+//     memory, so no global scratch and no atomics are needed.
+//   * Each lane streams 16-byte weight words of two rows (g and g+8 of its
+//     mma group) straight from HBM with L1-bypassing loads, keeping a ring of
+//     PF segments in flight, and decodes them in registers into mma.sync
+//     m16n8k16 A fragments (weights are the M=16 side, activations the N=8
+//     side, so one mma covers 256 weights).
+//   * The activation slice is staged once per CTA in shared memory with the k
+//     order permuted to match the decode's pair order and a bank swizzle.
+//   * fp32 accumulation; the FP8 channel scale / NVFP4 global scale is
+//     applied to the reduced row; one bf16 rounding at the store.
+#include <algorithm>
+
+#include "dequant.cuh"
+
+#define QG_REQUIRE(cond, st, ...) \
+  do { if (!(cond)) return qg::set_error(st, __VA_ARGS__); } while (0)
+
+namespace qg {
+namespace {
+
+enum Fmt { F_INT4 = 0, F_FP8 = 1, F_MXFP4 = 2, F_NVFP4 = 3 };
+
+constexpr int kWarps = 8;
+constexpr int kRowsPerCta = 16 * kWarps;
+constexpr int kPF = 4;                 // segments in flight per lane
+
+template <int FMT> struct FmtTraits;
+template <> struct FmtTraits<F_INT4>  { static constexpr int KSEG = 128, CPL = 4; };
+template <> struct FmtTraits<F_MXFP4> { static constexpr int KSEG = 128, CPL = 4; };
+template <> struct FmtTraits<F_NVFP4> { static constexpr int KSEG = 128, CPL = 4; };
+template <> struct FmtTraits<F_FP8>   { static constexpr int KSEG = 64,  CPL = 2; };
+
+struct GemvArgs {
+  const uint8_t* w;        // packed weights [N][row_bytes]
+  const void* scales;      // per-format scale array (or channel scales for FP8)
+  const float* gscale;     // NVFP4 global scale (device scalar) or nullptr
+  const uint16_t* x;       // [M][K] bf16
+  uint16_t* y;             // [M][N] bf16
+  int M, N, K, g;
+  int nseg;                // K / KSEG
+  int ncp;                 // X smem row pitch in 16-byte chunks
+};
+
+QG_DEVICE int swz(int c) { return c ^ ((c >> 3) & 1); }
+
+QG_DEVICE void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Per-lane scale state for one segment of one row.
+struct Scale { uint32_t a, b; };
+
+template <int FMT>
+QG_DEVICE Scale load_scale(const GemvArgs& p, int n, int seg, int t) {
+  Scale s{0u, 0u};
+  if constexpr (FMT == F_INT4) {
+    const uint16_t* ws = static_cast<const uint16_t*>(p.scales);
+    const int grp = (seg * 128 + 32 * t) / p.g;
+    s.a = bf16x2_splat(__ldg(ws + (size_t)n * (p.K / p.g) + grp));
+  } else if constexpr (FMT == F_MXFP4) {
+    const uint8_t* ws = static_cast<const uint8_t*>(p.scales);
+    s.a = __ldg(ws + (size_t)n * (p.K / 32) + seg * 4 + t);
+  } else if constexpr (FMT == F_NVFP4) {
+    const uint8_t* ws = static_cast<const uint8_t*>(p.scales);
+    s.a = __ldg(reinterpret_cast<const uint16_t*>(ws + (size_t)n * (p.K / 16) + seg * 8 + 2 * t));
+  }
+  return s;
+}
+
+// Decode chunk j (8 k-values) of the lane's 16-byte word into A pairs:
+// a[0], a[1] for the first mma (lo / hi k-slots), a[2], a[3] for the second.
+template <int FMT>
+QG_DEVICE void decode_chunk(const uint4& w, const Scale& s, int j, uint32_t (&a)[4]) {
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  if constexpr (FMT == F_INT4) {
+    int4x8_kperm(ww[j], s.a, a);
+  } else if constexpr (FMT == F_MXFP4) {
+    e2m1x8_kperm(ww[j], e8m0_to_bf16x2(s.a), a);
+  } else if constexpr (FMT == F_NVFP4) {
+    e2m1x8_kperm(ww[j], e4m3_to_bf16x2(j < 2 ? (s.a & 0xFFu) : (s.a >> 8)), a);
+  } else {
+    e4m3x4_kperm(ww[2 * j], a[0], a[1]);
+    e4m3x4_kperm(ww[2 * j + 1], a[2], a[3]);
+  }
+}
+
+// X chunk permutation matching decode_chunk's pair order
+template <int FMT>
+QG_DEVICE uint4 perm_x(const uint4& u) {
+  if constexpr (FMT == F_FP8)   // (0,2,1,3,4,6,5,7)
+    return make_uint4(prmt(u.x, u.y, 0x5410u), prmt(u.x, u.y, 0x7632u),
+                      prmt(u.z, u.w, 0x5410u), prmt(u.z, u.w, 0x7632u));
+  else                          // (0,4,1,5,2,6,3,7)
+    return make_uint4(prmt(u.x, u.z, 0x5410u), prmt(u.x, u.z, 0x7632u),
+                      prmt(u.y, u.w, 0x5410u), prmt(u.y, u.w, 0x7632u));
+}
+
+QG_DEVICE uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+QG_DEVICE void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+QG_DEVICE float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+template <int FMT, int MT>
+__global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
+  using Tr = FmtTraits<FMT>;
+  extern __shared__ __align__(16) uint4 smem[];
+  const int M = p.M;
+  const int MP = MT * 8;
+  uint4* xs = smem;                                              // [M][ncp]
+  float* red = reinterpret_cast<float*>(smem + (size_t)M * p.ncp); // [128][MP]
+
+  const int ks = gridDim.x, kr = blockIdx.x;
+  const int seg_lo = (int)((long long)p.nseg * kr / ks);
+  const int seg_hi = (int)((long long)p.nseg * (kr + 1) / ks);
+  const int nseg = seg_hi - seg_lo;
+  const int k0 = seg_lo * Tr::KSEG;
+  const int nchunk = nseg * Tr::KSEG / 8;
+
+  // ---- stage the activation slice, permuted and swizzled -------------------
+  for (int i = threadIdx.x; i < M * nchunk; i += kWarps * 32) {
+    const int m = i / nchunk, c = i - m * nchunk;
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * p.K + k0 + 8 * c));
+    xs[m * p.ncp + swz(c)] = perm_x<FMT>(u);
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int nb = blockIdx.y * kRowsPerCta + warp * 16;
+  const int n0 = min(nb + g, p.N - 1), n1 = min(nb + g + 8, p.N - 1);
+  const size_t row_bytes = (FMT == F_FP8) ? (size_t)p.K : (size_t)p.K / 2;
+  const uint8_t* w0 = p.w + (size_t)n0 * row_bytes + (size_t)seg_lo * 64 + 16 * t;
+  const uint8_t* w1 = p.w + (size_t)n1 * row_bytes + (size_t)seg_lo * 64 + 16 * t;
+
+  const int col0 = min(g, M - 1), col1 = min(8 + g, M - 1);
+  const uint4* xr0 = xs + col0 * p.ncp;
+  const uint4* xr1 = xs + col1 * p.ncp;
+
+  float acc[MT][4];
+#pragma unroll
+  for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  uint4 wa[kPF], wb[kPF];
+  Scale sa[kPF], sb[kPF];
+#pragma unroll
+  for (int u = 0; u < kPF; ++u) {
+    if (u < nseg) {
+      wa[u] = ldg_stream(w0 + 64 * u);
+      wb[u] = ldg_stream(w1 + 64 * u);
+      sa[u] = load_scale<FMT>(p, n0, seg_lo + u, t);
+      sb[u] = load_scale<FMT>(p, n1, seg_lo + u, t);
+    }
+  }
+
+  for (int s0 = 0; s0 < nseg; s0 += kPF) {
+#pragma unroll
+    for (int u = 0; u < kPF; ++u) {
+      const int s = s0 + u;
+      if (s < nseg) {
+#pragma unroll
+        for (int j = 0; j < Tr::CPL; ++j) {
+          uint32_t ag[4], ah[4];
+          decode_chunk<FMT>(wa[u], sa[u], j, ag);
+          decode_chunk<FMT>(wb[u], sb[u], j, ah);
+          const int c = swz(s * (Tr::KSEG / 8) + t * Tr::CPL + j);
+          {
+            const uint4 xf = xr0[c];
+            mma_bf16(acc[0], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
+            mma_bf16(acc[0], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
+          }
+          if constexpr (MT == 2) {
+            const uint4 xf = xr1[c];
+            mma_bf16(acc[1], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
+            mma_bf16(acc[1], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
+          }
+        }
+        const int sn = s + kPF;
+        if (sn < nseg) {
+          wa[u] = ldg_stream(w0 + 64 * sn);
+          wb[u] = ldg_stream(w1 + 64 * sn);
+          sa[u] = load_scale<FMT>(p, n0, seg_lo + sn, t);
+          sb[u] = load_scale<FMT>(p, n1, seg_lo + sn, t);
+        }
+      }
+    }
+  }
+
+  // ---- partial sums -> shared memory [row][m] ---------------------------------
+#pragma unroll
+  for (int i = 0; i < MT; ++i) {
+    const int m = 8 * i + 2 * t;
+    const int r0 = warp * 16 + g, r1 = r0 + 8;
+    red[r0 * MP + m] = acc[i][0];
+    red[r0 * MP + m + 1] = acc[i][1];
+    red[r1 * MP + m] = acc[i][2];
+    red[r1 * MP + m + 1] = acc[i][3];
+  }
+  if (ks > 1) cluster_sync(); else __syncthreads();
+
+  // ---- cluster reduction of this CTA's share of rows, epilogue, store --------
+  const int rows_per = kRowsPerCta / ks;
+  const int rbeg = kr * rows_per;
+  for (int i = threadIdx.x; i < rows_per * M; i += kWarps * 32) {
+    const int m = i / rows_per, r = rbeg + (i - m * rows_per);
+    const int n = blockIdx.y * kRowsPerCta + r;
+    float v;
+    if (ks > 1) {
+      const uint32_t a = smem_u32(red + r * MP + m);
+      v = 0.f;
+      for (int q = 0; q < ks; ++q) v += ld_dsmem_f32(a, q);
+    } else {
+      v = red[r * MP + m];
+    }
+    if (n < p.N) {
+      if constexpr (FMT == F_FP8) v *= __ldg(static_cast<const float*>(p.scales) + n);
+      if constexpr (FMT == F_NVFP4) v *= __ldg(p.gscale);
+      p.y[(size_t)m * p.N + n] = f32_to_bf16_bits(v);
+    }
+  }
+  if (ks > 1) cluster_sync();
+}
+
+// ---------------------------------------------------------------------------
+// test-only canonical dequantization (same decode routines, natural order)
+// ---------------------------------------------------------------------------
+template <int FMT>
+__global__ void dequant_kernel(const uint8_t* __restrict__ w, const void* __restrict__ scales, int g,
+                               uint16_t* __restrict__ out, int N, int K) {
+  using Tr = FmtTraits<FMT>;
+  const int t = threadIdx.x & 3;              // position inside a 64-byte segment
+  const long long lane_id = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 2;
+  const int nseg = K / Tr::KSEG;
+  const long long total = (long long)N * nseg;
+  if (lane_id >= total) return;
+  const int n = int(lane_id / nseg), seg = int(lane_id % nseg);
+  const size_t row_bytes = (FMT == F_FP8) ? (size_t)K : (size_t)K / 2;
+  const uint4 wv = *reinterpret_cast<const uint4*>(w + (size_t)n * row_bytes + seg * 64 + 16 * t);
+  GemvArgs p{};
+  p.scales = scales; p.K = K; p.g = g;
+  const Scale s = load_scale<FMT>(p, n, seg, t);
+  uint16_t* o = out + (size_t)n * K + (size_t)seg * Tr::KSEG + t * Tr::CPL * 8;
+#pragma unroll
+  for (int j = 0; j < Tr::CPL; ++j) {
+    uint32_t a[4], nat[4];
+    decode_chunk<FMT>(wv, s, j, a);
+    if constexpr (FMT == F_FP8) {       // a = (0,2),(1,3),(4,6),(5,7)
+      nat[0] = prmt(a[0], a[1], 0x5410u); nat[1] = prmt(a[0], a[1], 0x7632u);
+      nat[2] = prmt(a[2], a[3], 0x5410u); nat[3] = prmt(a[2], a[3], 0x7632u);
+    } else {
+      kperm4_to_natural(a, nat);
+    }
+    *reinterpret_cast<uint4*>(o + 8 * j) = make_uint4(nat[0], nat[1], nat[2], nat[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+template <int FMT, int MT>
+qg_status launch_gemv_t(const GemvArgs& a0, cudaStream_t st, const char* name) {
+  using Tr = FmtTraits<FMT>;
+  GemvArgs a = a0;
+  a.nseg = a.K / Tr::KSEG;
+  const int rb = (a.N + kRowsPerCta - 1) / kRowsPerCta;
+  const int target = 2 * sm_count();
+  int ks = 1;
+  while (ks < 8 && rb * ks < target && a.nseg >= 2 * ks) ks *= 2;
+  // activation slice must fit in shared memory
+  auto smem_bytes = [&](int kk) {
+    const int nseg_max = (a.nseg + kk - 1) / kk;
+    int ncp = nseg_max * Tr::KSEG / 8;
+    const int want = (FMT == F_FP8) ? 1 : 2;
+    while ((ncp & 7) != want) ++ncp;
+    a.ncp = ncp;
+    return (size_t)a.M * ncp * 16 + (size_t)kRowsPerCta * MT * 8 * 4;
+  };
+  size_t smem = smem_bytes(ks);
+  while (smem > 200 * 1024 && ks < 8) { ks *= 2; smem = smem_bytes(ks); }
+  if (smem > 200 * 1024)
+    return set_error(QG_ERR_UNSUPPORTED_SHAPE, "%s: activation slice too large for one CTA", name);
+
+  auto kern = gemv_kernel<FMT, MT>;
+  if (!ensure_smem(kern, (int)smem))
+    return set_error(QG_ERR_CUDA, "%s: cannot set shared memory size", name);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ks, rb, 1);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return set_error(QG_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
+  return QG_OK;
+}
+
+template <int FMT>
+qg_status launch_gemv(const GemvArgs& a, cudaStream_t st, const char* name) {
+  // M <= 8: one 8-column activation tile; 9..16: two.  Larger M is processed
+  // in slices of 16 rows.
+  if (a.M <= 8) return launch_gemv_t<FMT, 1>(a, st, name);
+  return launch_gemv_t<FMT, 2>(a, st, name);
+}
+
+template <int FMT>
+qg_status run_weight_only(GemvArgs a, cudaStream_t st, const char* name) {
+  const int M = a.M;
+  for (int m0 = 0; m0 < M; m0 += 16) {
+    GemvArgs s = a;
+    s.M = std::min(16, M - m0);
+    s.x = a.x + (size_t)m0 * a.K;
+    s.y = a.y + (size_t)m0 * a.N;
+    const qg_status r = launch_gemv<FMT>(s, st, name);
+    if (r != QG_OK) return r;
+  }
+  return QG_OK;
+}
+
+qg_status check_common(const void* w, const void* x, const void* y, int M, int N, int K, const char* name) {
+  QG_REQUIRE(w && x && y, QG_ERR_INVALID_ARG, "%s: NULL pointer", name);
+  QG_REQUIRE(M >= 0 && N > 0 && K > 0, QG_ERR_INVALID_ARG, "%s: bad sizes M=%d N=%d K=%d", name, M, N, K);
+  QG_REQUIRE(N % 8 == 0 && K % 128 == 0, QG_ERR_UNSUPPORTED_SHAPE,
+             "%s: need N %% 8 == 0 and K %% 128 == 0 (N=%d K=%d)", name, N, K);
+  QG_REQUIRE(aligned16(w) && aligned16(x) && aligned16(y), QG_ERR_MISALIGNED, "%s: misaligned pointer", name);
+  return QG_OK;
+}
+
+}  // namespace
+
+// entry for the prefill path (gemm_tc.cu) when it declines a shape
+qg_status gemv_w4a16_any_m(const uint8_t* w_q, const uint16_t* w_s, int g, const uint16_t* x,
+                           uint16_t* y, int M, int N, int K, cudaStream_t st) {
+  GemvArgs a{};
+  a.w = w_q; a.scales = w_s; a.x = x; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
+  return run_weight_only<F_INT4>(a, st, "qgemm_w4a16");
+}
+
+}  // namespace qg
+
+using qg::aligned16;
+
+// prefill dispatcher lives in gemm_tc.cu
+namespace qg {
+qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint16_t* x, uint16_t* y,
+                        int M, int N, int K, cudaStream_t st, bool* handled);
+}
+
+extern "C" {
+
+qg_status qgemm_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint16_t* x, uint16_t* y,
+                      int M, int N, int K, qg_stream_t stream) {
+  qg_status r = qg::check_common(w_q, x, y, M, N, K, "qgemm_w4a16");
+  if (r != QG_OK) return r;
+  QG_REQUIRE(w_s, QG_ERR_INVALID_ARG, "qgemm_w4a16: NULL scales");
+  QG_REQUIRE(g >= 32 && g % 32 == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
+             "qgemm_w4a16: need g %% 32 == 0 and K %% g == 0 (g=%d)", g);
+  if (M == 0) return QG_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (M > 16) {
+    bool handled = false;
+    r = qg::prefill_w4a16(w_q, w_s, g, x, y, M, N, K, st, &handled);
+    if (handled) return r;
+  }
+  return qg::gemv_w4a16_any_m(w_q, w_s, g, x, y, M, N, K, st);
+}
+
+qg_status qgemm_w8a16(const uint8_t* w_e4m3, const float* w_cs, const uint16_t* x, uint16_t* y,
+                      int M, int N, int K, qg_stream_t stream) {
+  qg_status r = qg::check_common(w_e4m3, x, y, M, N, K, "qgemm_w8a16");
+  if (r != QG_OK) return r;
+  QG_REQUIRE(w_cs, QG_ERR_INVALID_ARG, "qgemm_w8a16: NULL channel scales");
+  if (M == 0) return QG_OK;
+  qg::GemvArgs a{};
+  a.w = w_e4m3; a.scales = w_cs; a.x = x; a.y = y; a.M = M; a.N = N; a.K = K; a.g = K;
+  return qg::run_weight_only<qg::F_FP8>(a, reinterpret_cast<cudaStream_t>(stream), "qgemm_w8a16");
+}
+
+qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt, int g,
+                       const float* global_scale, const uint16_t* x, uint16_t* y, int M, int N, int K,
+                       qg_stream_t stream) {
+  qg_status r = qg::check_common(w_e2m1, x, y, M, N, K, "qgemm_fp4a16");
+  if (r != QG_OK) return r;
+  QG_REQUIRE(w_bs, QG_ERR_INVALID_ARG, "qgemm_fp4a16: NULL block scales");
+  qg::GemvArgs a{};
+  a.w = w_e2m1; a.scales = w_bs; a.x = x; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (scale_fmt == QG_SCALE_E8M0) {
+    QG_REQUIRE(g == 32, QG_ERR_UNSUPPORTED_SHAPE, "qgemm_fp4a16: MXFP4 needs g == 32");
+    QG_REQUIRE(global_scale == nullptr, QG_ERR_INVALID_ARG, "qgemm_fp4a16: MXFP4 takes no global scale");
+    if (M == 0) return QG_OK;
+    return qg::run_weight_only<qg::F_MXFP4>(a, st, "qgemm_fp4a16");
+  }
+  if (scale_fmt == QG_SCALE_E4M3) {
+    QG_REQUIRE(g == 16, QG_ERR_UNSUPPORTED_SHAPE, "qgemm_fp4a16: NVFP4 needs g == 16");
+    QG_REQUIRE(global_scale != nullptr, QG_ERR_INVALID_ARG, "qgemm_fp4a16: NVFP4 needs a global scale");
+    QG_REQUIRE((reinterpret_cast<uintptr_t>(global_scale) & 3) == 0, QG_ERR_MISALIGNED,
+               "qgemm_fp4a16: misaligned global scale");
+    a.gscale = global_scale;
+    if (M == 0) return QG_OK;
+    return qg::run_weight_only<qg::F_NVFP4>(a, st, "qgemm_fp4a16");
+  }
+  return qg::set_error(QG_ERR_INVALID_ARG, "qgemm_fp4a16: unknown scale format %d", scale_fmt);
+}
+
+qg_status qg_dequant_weights(int fmt, const uint8_t* w, const void* scales, int g, uint16_t* w_out,
+                             int N, int K, qg_stream_t stream) {
+  QG_REQUIRE(w && w_out, QG_ERR_INVALID_ARG, "qg_dequant_weights: NULL pointer");
+  QG_REQUIRE(N >= 0 && K > 0, QG_ERR_INVALID_ARG, "qg_dequant_weights: bad sizes");
+  QG_REQUIRE(K % 128 == 0, QG_ERR_UNSUPPORTED_SHAPE, "qg_dequant_weights: K %% 128 != 0");
+  QG_REQUIRE(aligned16(w) && aligned16(w_out), QG_ERR_MISALIGNED, "qg_dequant_weights: misaligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int threads = 256;
+  auto grid = [&](int kseg) {
+    const long long lanes = (long long)N * (K / kseg) * 4;
+    return unsigned((lanes + threads - 1) / threads);
+  };
+  if (N == 0) return QG_OK;
+  switch (fmt) {
+    case QG_FMT_INT4:
+      QG_REQUIRE(scales && g >= 32 && g % 32 == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
+                 "qg_dequant_weights: INT4 needs scales and g %% 32 == 0");
+      qg::dequant_kernel<qg::F_INT4><<<grid(128), threads, 0, st>>>(w, scales, g, w_out, N, K);
+      break;
+    case QG_FMT_FP8:
+      qg::dequant_kernel<qg::F_FP8><<<grid(64), threads, 0, st>>>(w, scales, g, w_out, N, K);
+      break;
+    case QG_FMT_MXFP4:
+      QG_REQUIRE(scales, QG_ERR_INVALID_ARG, "qg_dequant_weights: NULL scales");
+      qg::dequant_kernel<qg::F_MXFP4><<<grid(128), threads, 0, st>>>(w, scales, 32, w_out, N, K);
+      break;
+    case QG_FMT_NVFP4:
+      QG_REQUIRE(scales, QG_ERR_INVALID_ARG, "qg_dequant_weights: NULL scales");
+      qg::dequant_kernel<qg::F_NVFP4><<<grid(128), threads, 0, st>>>(w, scales, 16, w_out, N, K);
+      break;
+    default:
+      return qg::set_error(QG_ERR_INVALID_ARG, "qg_dequant_weights: unknown format %d", fmt);
+  }
+  return qg::check_launch("qg_dequant_weights");
+}
+
+}  // extern "C"

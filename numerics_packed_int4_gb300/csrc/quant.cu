@@ -1,0 +1,455 @@
+// Online activation quantizers, load-time weight quantizers and the MoE
+// harness kernels.  All of them are HBM-streaming: each thread owns 8
+// consecutive elements (one 16-byte bf16 load or two 16-byte fp32 loads), the
+// quantization block is reduced with warp shuffles (blocks of <= 256) or a
+// CTA reduction (larger blocks, e.g. per-token), and codes leave as one
+// 4- or 8-byte store per thread.
+#include <cfloat>
+
+#include "qg_common.cuh"
+
+#define QG_REQUIRE(cond, st, ...) \
+  do { if (!(cond)) return qg::set_error(st, __VA_ARGS__); } while (0)
+
+namespace qg {
+namespace {
+
+constexpr int kThreads = 256;
+
+// ---- loading 8 consecutive elements as fp32 --------------------------------
+template <typename T> struct Load8;
+template <> struct Load8<uint16_t> {          // bf16 bit patterns
+  static QG_DEVICE void run(const uint16_t* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { v[2 * i] = bf16_lo_to_f32(w[i]); v[2 * i + 1] = bf16_hi_to_f32(w[i]); }
+  }
+};
+template <> struct Load8<float> {
+  static QG_DEVICE void run(const float* p, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+QG_DEVICE float absmax8(const float (&v)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
+// ---- E4M3 block step: s = amax/448 (zero -> 1), codes of x/s ---------------
+QG_DEVICE float fp8_scale(float amax) { return amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f); }
+
+QG_DEVICE uint2 fp8_codes8(const float (&v)[8], float s) {
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    c[i] = f32x2_to_e4m3x2(__fdiv_rn(v[2 * i + 1], s), __fdiv_rn(v[2 * i], s));
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// ---- MXFP4 block step -----------------------------------------------------------
+// Exponent-first 0.75-threshold rule (vLLM PR #43557, "Fix").
+QG_DEVICE uint32_t e8m0_scale_exp(float vecMax) {
+  const uint32_t max_bits = __float_as_uint(vecMax);
+  const uint32_t rounded_bits = (max_bits + (1u << 21)) & 0xFF800000u;
+  const uint32_t biased_exp = (rounded_bits >> 23) & 0xFFu;
+  return biased_exp > 2u ? biased_exp - 2u : 0u;
+}
+
+QG_DEVICE uint32_t e2m1_codes8(const float (&v)[8], float mul) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    r |= f32x2_to_e2m1x2(__fmul_rn(v[2 * i + 1], mul), __fmul_rn(v[2 * i], mul)) << (8 * i);
+  return r;
+}
+
+// ===========================================================================
+// block size <= 256: GT = g/8 lanes per block, shuffles only
+// ===========================================================================
+template <typename Tin, int GT>
+__global__ void __launch_bounds__(kThreads) fp8_block_small_kernel(
+    const Tin* __restrict__ x, uint8_t* __restrict__ q, float* __restrict__ s,
+    long long nchunks, int K) {
+  const long long c = blockIdx.x * (long long)kThreads + threadIdx.x;
+  const bool live = c < nchunks;
+  float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (live) Load8<Tin>::run(x + c * 8, v);
+  const float amax = group_max<GT>(absmax8(v));
+  const float sc = fp8_scale(amax);
+  if (!live) return;
+  *reinterpret_cast<uint2*>(q + c * 8) = fp8_codes8(v, sc);
+  if ((c % GT) == 0) s[c / GT] = sc;
+}
+
+template <typename Tin, int GT>
+__global__ void __launch_bounds__(kThreads) mxfp4_kernel(
+    const Tin* __restrict__ x, uint8_t* __restrict__ q, uint8_t* __restrict__ se_out,
+    long long nchunks) {
+  const long long c = blockIdx.x * (long long)kThreads + threadIdx.x;
+  const bool live = c < nchunks;
+  float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (live) Load8<Tin>::run(x + c * 8, v);
+  const float vecMax = group_max<GT>(absmax8(v));
+  const uint32_t se = e8m0_scale_exp(vecMax);
+  if (!live) return;
+  *reinterpret_cast<uint32_t*>(q + c * 4) = e2m1_codes8(v, pow2_127_minus(se));
+  if ((c % GT) == 0) se_out[c / GT] = uint8_t(se);
+}
+
+template <int GT>
+__global__ void __launch_bounds__(kThreads) int4_rtn_kernel(
+    const float* __restrict__ w, uint8_t* __restrict__ q, uint16_t* __restrict__ s,
+    long long nchunks) {
+  const long long c = blockIdx.x * (long long)kThreads + threadIdx.x;
+  const bool live = c < nchunks;
+  float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (live) Load8<float>::run(w + c * 8, v);
+  const float amax = group_max<GT>(absmax8(v));
+  if (!live) return;
+  uint16_t sb = f32_to_bf16_bits(__fdiv_rn(amax, 7.f));
+  float sf = bf16_bits_to_f32(sb);
+  uint32_t packed = 0;
+  if (sf == 0.f) {
+    sb = 0x3F80;                       // all-zero group policy: s = 1, q = 0
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float t = rintf(__fdiv_rn(v[i], sf));
+      t = fminf(fmaxf(t, -8.f), 7.f);
+      packed |= (uint32_t(int(t)) & 0xFu) << (4 * i);
+    }
+  }
+  *reinterpret_cast<uint32_t*>(q + c * 4) = packed;
+  if ((c % GT) == 0) s[c / GT] = sb;
+}
+
+// ===========================================================================
+// large blocks (g > 256, e.g. per-token / per-channel): one CTA per block
+// ===========================================================================
+QG_DEVICE float cta_max(float v, float* red) {
+  v = group_max<32>(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < kThreads / 32 ? red[lane] : 0.f;
+    v = group_max<32>(v);
+    if (lane == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float r = red[0];
+  __syncthreads();
+  return r;
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads) fp8_block_large_kernel(
+    const Tin* __restrict__ x, uint8_t* __restrict__ q, float* __restrict__ s, int g) {
+  __shared__ float red[kThreads / 32];
+  const long long base = (long long)blockIdx.x * g;
+  float m = 0.f;
+  for (int c = threadIdx.x; c < g / 8; c += kThreads) {
+    float v[8];
+    Load8<Tin>::run(x + base + c * 8, v);
+    m = fmaxf(m, absmax8(v));
+  }
+  const float sc = fp8_scale(cta_max(m, red));
+  for (int c = threadIdx.x; c < g / 8; c += kThreads) {
+    float v[8];
+    Load8<Tin>::run(x + base + c * 8, v);
+    *reinterpret_cast<uint2*>(q + base + c * 8) = fp8_codes8(v, sc);
+  }
+  if (threadIdx.x == 0) s[blockIdx.x] = sc;
+}
+
+// ===========================================================================
+// NVFP4 weights
+// ===========================================================================
+__global__ void __launch_bounds__(kThreads) amax_kernel(const float* __restrict__ w, long long nchunks,
+                                                        unsigned int* __restrict__ out) {
+  __shared__ float red[kThreads / 32];
+  float m = 0.f;
+  for (long long c = blockIdx.x * (long long)kThreads + threadIdx.x; c < nchunks;
+       c += (long long)gridDim.x * kThreads) {
+    float v[8];
+    Load8<float>::run(w + c * 8, v);
+    m = fmaxf(m, absmax8(v));
+  }
+  m = cta_max(m, red);
+  if (threadIdx.x == 0) atomicMax(out, __float_as_uint(m));   // m >= 0: bits are ordered
+}
+
+QG_DEVICE float nvfp4_global_scale(float amax) { return amax == 0.f ? 1.f : __fdiv_rn(amax, 2688.f); }
+
+__global__ void __launch_bounds__(kThreads) nvfp4_kernel(
+    const float* __restrict__ w, uint8_t* __restrict__ q, uint8_t* __restrict__ sb_out,
+    const float* __restrict__ amax_word, long long nchunks) {
+  const long long c = blockIdx.x * (long long)kThreads + threadIdx.x;
+  const bool live = c < nchunks;
+  float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (live) Load8<float>::run(w + c * 8, v);
+  const float amax_b = group_max<2>(absmax8(v));
+  if (!live) return;
+  const float gs = nvfp4_global_scale(*amax_word);
+  const float d = __fmul_rn(6.f, gs);
+  const uint32_t sb = f32x2_to_e4m3x2(0.f, __fdiv_rn(amax_b, d)) & 0xFFu;
+  const float den = __fmul_rn(e4m3_to_f32(sb), gs);
+  uint32_t packed = 0;
+  if (den != 0.f) {
+    float t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t[i] = __fdiv_rn(v[i], den);
+    packed = e2m1_codes8(t, 1.f);
+  }
+  *reinterpret_cast<uint32_t*>(q + c * 4) = packed;
+  if ((c & 1) == 0) sb_out[c / 2] = uint8_t(sb);
+}
+
+__global__ void nvfp4_finalize_kernel(float* gs_word) {
+  gs_word[0] = nvfp4_global_scale(gs_word[0]);
+}
+
+// ===========================================================================
+// MoE harness
+// ===========================================================================
+__global__ void __launch_bounds__(kThreads) gather_fp8_kernel(
+    const uint8_t* __restrict__ src_q, const float* __restrict__ src_s,
+    const int32_t* __restrict__ rows, uint8_t* __restrict__ dst_q, float* __restrict__ dst_s,
+    int T, int K) {
+  const int r = blockIdx.x;
+  int t = rows[r];
+  t = t < 0 ? 0 : (t >= T ? T - 1 : t);
+  const uint4* src = reinterpret_cast<const uint4*>(src_q + (long long)t * K);
+  uint4* dst = reinterpret_cast<uint4*>(dst_q + (long long)r * K);
+  for (int i = threadIdx.x; i < K / 16; i += kThreads) dst[i] = src[i];
+  if (threadIdx.x == 0) dst_s[r] = src_s[t];
+}
+
+QG_DEVICE void swiglu8(const uint16_t* gu, int I, int c, float (&h)[8]) {
+  float gv[8], uv[8];
+  Load8<uint16_t>::run(gu + c * 8, gv);
+  Load8<uint16_t>::run(gu + I + c * 8, uv);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = __fmul_rn(__fdiv_rn(gv[i], 1.f + expf(-gv[i])), uv[i]);
+}
+
+__global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(
+    const uint16_t* __restrict__ gate_up, uint8_t* __restrict__ q, float* __restrict__ s, int I) {
+  __shared__ float red[kThreads / 32];
+  const uint16_t* gu = gate_up + (long long)blockIdx.x * 2 * I;
+  float m = 0.f;
+  for (int c = threadIdx.x; c < I / 8; c += kThreads) {
+    float h[8];
+    swiglu8(gu, I, c, h);
+    m = fmaxf(m, absmax8(h));
+  }
+  const float sc = fp8_scale(cta_max(m, red));
+  for (int c = threadIdx.x; c < I / 8; c += kThreads) {
+    float h[8];
+    swiglu8(gu, I, c, h);
+    *reinterpret_cast<uint2*>(q + (long long)blockIdx.x * I + c * 8) = fp8_codes8(h, sc);
+  }
+  if (threadIdx.x == 0) s[blockIdx.x] = sc;
+}
+
+__global__ void __launch_bounds__(kThreads) combine_kernel(
+    const uint16_t* __restrict__ down, const int32_t* __restrict__ row_of,
+    const float* __restrict__ weight, uint16_t* __restrict__ out, int topk, int R, int H) {
+  const int t = blockIdx.y;
+  const int c = blockIdx.x * kThreads + threadIdx.x;
+  if (c >= H / 8) return;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int j = 0; j < topk; ++j) {
+    int r = row_of[t * topk + j];
+    if (r < 0 || r >= R) continue;
+    const float p = weight[t * topk + j];
+    float d[8];
+    Load8<uint16_t>::run(down + (long long)r * H + c * 8, d);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(p, d[i], acc[i]);
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = uint32_t(f32_to_bf16_bits(acc[2 * i])) | (uint32_t(f32_to_bf16_bits(acc[2 * i + 1])) << 16);
+  *reinterpret_cast<uint4*>(out + (long long)t * H + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ---- launch helpers ----------------------------------------------------------
+inline unsigned grid_for(long long nchunks) { return unsigned((nchunks + kThreads - 1) / kThreads); }
+
+template <typename Tin>
+qg_status launch_fp8_block(const Tin* x, uint8_t* q, float* s, int g, long long rows, int K,
+                           cudaStream_t st, const char* name) {
+  const long long nchunks = rows * (long long)K / 8;
+  if (nchunks == 0) return QG_OK;
+  const long long nblocks = rows * (long long)(K / g);
+  switch (g) {
+    case 8:   fp8_block_small_kernel<Tin, 1><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 16:  fp8_block_small_kernel<Tin, 2><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 32:  fp8_block_small_kernel<Tin, 4><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 64:  fp8_block_small_kernel<Tin, 8><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 128: fp8_block_small_kernel<Tin, 16><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 256: fp8_block_small_kernel<Tin, 32><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    default:
+      if (nblocks > 0x7FFFFFFFLL) return set_error(QG_ERR_UNSUPPORTED_SHAPE, "%s: too many blocks", name);
+      fp8_block_large_kernel<Tin><<<unsigned(nblocks), kThreads, 0, st>>>(x, q, s, g);
+  }
+  return check_launch(name);
+}
+
+template <typename Tin>
+qg_status launch_mxfp4(const Tin* x, uint8_t* q, uint8_t* se, int g, long long rows, int K,
+                       cudaStream_t st, const char* name) {
+  const long long nchunks = rows * (long long)K / 8;
+  if (nchunks == 0) return QG_OK;
+  if (g == 16) mxfp4_kernel<Tin, 2><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, se, nchunks);
+  else         mxfp4_kernel<Tin, 4><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, se, nchunks);
+  return check_launch(name);
+}
+
+bool is_pow2_block(int g) { return g == 8 || g == 16 || g == 32 || g == 64 || g == 128 || g == 256; }
+
+}  // namespace
+}  // namespace qg
+
+using qg::aligned16;
+
+extern "C" {
+
+qg_status quant_act_fp8_block(const uint16_t* x, uint8_t* q, float* s, int g, int M, int K,
+                              qg_stream_t stream) {
+  QG_REQUIRE(x && q && s, QG_ERR_INVALID_ARG, "quant_act_fp8_block: NULL pointer");
+  QG_REQUIRE(M >= 0 && K > 0 && g > 0, QG_ERR_INVALID_ARG, "quant_act_fp8_block: bad sizes");
+  QG_REQUIRE(K % g == 0 && g % 8 == 0, QG_ERR_UNSUPPORTED_SHAPE,
+             "quant_act_fp8_block: need K %% g == 0 and g %% 8 == 0 (K=%d g=%d)", K, g);
+  QG_REQUIRE(aligned16(x) && aligned16(q) && (reinterpret_cast<uintptr_t>(s) & 3) == 0,
+             QG_ERR_MISALIGNED, "quant_act_fp8_block: misaligned pointer");
+  return qg::launch_fp8_block(x, q, s, g, M, K, reinterpret_cast<cudaStream_t>(stream),
+                              "quant_act_fp8_block");
+}
+
+qg_status quant_act_mxfp4(const uint16_t* x, uint8_t* q, uint8_t* s_e8m0, int g, int M, int K,
+                          qg_stream_t stream) {
+  QG_REQUIRE(x && q && s_e8m0, QG_ERR_INVALID_ARG, "quant_act_mxfp4: NULL pointer");
+  QG_REQUIRE(M >= 0 && K > 0, QG_ERR_INVALID_ARG, "quant_act_mxfp4: bad sizes");
+  QG_REQUIRE(g == 16 || g == 32, QG_ERR_UNSUPPORTED_SHAPE, "quant_act_mxfp4: g must be 16 or 32");
+  QG_REQUIRE(K % g == 0, QG_ERR_UNSUPPORTED_SHAPE, "quant_act_mxfp4: K %% g != 0");
+  QG_REQUIRE(aligned16(x) && (reinterpret_cast<uintptr_t>(q) & 3) == 0, QG_ERR_MISALIGNED,
+             "quant_act_mxfp4: misaligned pointer");
+  return qg::launch_mxfp4(x, q, s_e8m0, g, M, K, reinterpret_cast<cudaStream_t>(stream),
+                          "quant_act_mxfp4");
+}
+
+qg_status qg_quantize_weights_int4(const float* w, uint8_t* w_q, uint16_t* w_s, int g, int N, int K,
+                                   qg_stream_t stream) {
+  QG_REQUIRE(w && w_q && w_s, QG_ERR_INVALID_ARG, "qg_quantize_weights_int4: NULL pointer");
+  QG_REQUIRE(N >= 0 && K > 0, QG_ERR_INVALID_ARG, "qg_quantize_weights_int4: bad sizes");
+  QG_REQUIRE(qg::is_pow2_block(g) && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
+             "qg_quantize_weights_int4: g must be a power of two in [8, 256] dividing K");
+  QG_REQUIRE(aligned16(w) && (reinterpret_cast<uintptr_t>(w_q) & 3) == 0, QG_ERR_MISALIGNED,
+             "qg_quantize_weights_int4: misaligned pointer");
+  const long long nchunks = (long long)N * K / 8;
+  if (nchunks == 0) return QG_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned grid = qg::grid_for(nchunks);
+  switch (g / 8) {
+    case 1:  qg::int4_rtn_kernel<1><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, nchunks); break;
+    case 2:  qg::int4_rtn_kernel<2><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, nchunks); break;
+    case 4:  qg::int4_rtn_kernel<4><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, nchunks); break;
+    case 8:  qg::int4_rtn_kernel<8><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, nchunks); break;
+    case 16: qg::int4_rtn_kernel<16><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, nchunks); break;
+    default: qg::int4_rtn_kernel<32><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, nchunks); break;
+  }
+  return qg::check_launch("qg_quantize_weights_int4");
+}
+
+qg_status qg_quantize_weights_fp8(const float* w, uint8_t* w_e4m3, float* w_cs, int N, int K,
+                                  qg_stream_t stream) {
+  QG_REQUIRE(w && w_e4m3 && w_cs, QG_ERR_INVALID_ARG, "qg_quantize_weights_fp8: NULL pointer");
+  QG_REQUIRE(N >= 0 && K > 0, QG_ERR_INVALID_ARG, "qg_quantize_weights_fp8: bad sizes");
+  QG_REQUIRE(K % 8 == 0, QG_ERR_UNSUPPORTED_SHAPE, "qg_quantize_weights_fp8: K %% 8 != 0");
+  QG_REQUIRE(aligned16(w) && aligned16(w_e4m3), QG_ERR_MISALIGNED,
+             "qg_quantize_weights_fp8: misaligned pointer");
+  return qg::launch_fp8_block(w, w_e4m3, w_cs, K, N, K, reinterpret_cast<cudaStream_t>(stream),
+                              "qg_quantize_weights_fp8");
+}
+
+qg_status qg_quantize_weights_mxfp4(const float* w, uint8_t* w_e2m1, uint8_t* w_e8m0, int g, int N,
+                                    int K, qg_stream_t stream) {
+  QG_REQUIRE(w && w_e2m1 && w_e8m0, QG_ERR_INVALID_ARG, "qg_quantize_weights_mxfp4: NULL pointer");
+  QG_REQUIRE(N >= 0 && K > 0, QG_ERR_INVALID_ARG, "qg_quantize_weights_mxfp4: bad sizes");
+  QG_REQUIRE(g == 32 && K % 32 == 0, QG_ERR_UNSUPPORTED_SHAPE,
+             "qg_quantize_weights_mxfp4: g must be 32 and divide K");
+  QG_REQUIRE(aligned16(w) && (reinterpret_cast<uintptr_t>(w_e2m1) & 3) == 0, QG_ERR_MISALIGNED,
+             "qg_quantize_weights_mxfp4: misaligned pointer");
+  return qg::launch_mxfp4(w, w_e2m1, w_e8m0, g, N, K, reinterpret_cast<cudaStream_t>(stream),
+                          "qg_quantize_weights_mxfp4");
+}
+
+qg_status qg_quantize_weights_nvfp4(const float* w, uint8_t* w_e2m1, uint8_t* w_e4m3,
+                                    float* global_scale, int N, int K, qg_stream_t stream) {
+  QG_REQUIRE(w && w_e2m1 && w_e4m3 && global_scale, QG_ERR_INVALID_ARG,
+             "qg_quantize_weights_nvfp4: NULL pointer");
+  QG_REQUIRE(N >= 0 && K > 0, QG_ERR_INVALID_ARG, "qg_quantize_weights_nvfp4: bad sizes");
+  QG_REQUIRE(K % 16 == 0, QG_ERR_UNSUPPORTED_SHAPE, "qg_quantize_weights_nvfp4: K %% 16 != 0");
+  QG_REQUIRE(aligned16(w) && (reinterpret_cast<uintptr_t>(w_e2m1) & 3) == 0 &&
+                 (reinterpret_cast<uintptr_t>(global_scale) & 3) == 0,
+             QG_ERR_MISALIGNED, "qg_quantize_weights_nvfp4: misaligned pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(global_scale, 0, sizeof(float), st) != cudaSuccess)
+    return qg::set_error(QG_ERR_CUDA, "qg_quantize_weights_nvfp4: memset failed");
+  const long long nchunks = (long long)N * K / 8;
+  if (nchunks > 0) {
+    const unsigned g1 = unsigned(std::min<long long>(qg::grid_for(nchunks), 4LL * qg::sm_count()));
+    qg::amax_kernel<<<g1, qg::kThreads, 0, st>>>(w, nchunks, reinterpret_cast<unsigned int*>(global_scale));
+    qg::nvfp4_kernel<<<qg::grid_for(nchunks), qg::kThreads, 0, st>>>(w, w_e2m1, w_e4m3, global_scale, nchunks);
+  }
+  qg::nvfp4_finalize_kernel<<<1, 1, 0, st>>>(global_scale);
+  return qg::check_launch("qg_quantize_weights_nvfp4");
+}
+
+qg_status qg_moe_gather_fp8(const uint8_t* src_q, const float* src_s, const int32_t* route_rows,
+                            uint8_t* dst_q, float* dst_s, int R, int T, int K, qg_stream_t stream) {
+  QG_REQUIRE(src_q && src_s && route_rows && dst_q && dst_s, QG_ERR_INVALID_ARG,
+             "qg_moe_gather_fp8: NULL pointer");
+  QG_REQUIRE(R >= 0 && T > 0 && K > 0, QG_ERR_INVALID_ARG, "qg_moe_gather_fp8: bad sizes");
+  QG_REQUIRE(K % 16 == 0, QG_ERR_UNSUPPORTED_SHAPE, "qg_moe_gather_fp8: K %% 16 != 0");
+  QG_REQUIRE(aligned16(src_q) && aligned16(dst_q), QG_ERR_MISALIGNED, "qg_moe_gather_fp8: misaligned");
+  if (R == 0) return QG_OK;
+  qg::gather_fp8_kernel<<<R, qg::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      src_q, src_s, route_rows, dst_q, dst_s, T, K);
+  return qg::check_launch("qg_moe_gather_fp8");
+}
+
+qg_status qg_swiglu_quant_fp8(const uint16_t* gate_up, uint8_t* q, float* s, int R, int I,
+                              qg_stream_t stream) {
+  QG_REQUIRE(gate_up && q && s, QG_ERR_INVALID_ARG, "qg_swiglu_quant_fp8: NULL pointer");
+  QG_REQUIRE(R >= 0 && I > 0, QG_ERR_INVALID_ARG, "qg_swiglu_quant_fp8: bad sizes");
+  QG_REQUIRE(I % 8 == 0, QG_ERR_UNSUPPORTED_SHAPE, "qg_swiglu_quant_fp8: I %% 8 != 0");
+  QG_REQUIRE(aligned16(gate_up) && aligned16(q), QG_ERR_MISALIGNED, "qg_swiglu_quant_fp8: misaligned");
+  if (R == 0) return QG_OK;
+  qg::swiglu_quant_kernel<<<R, qg::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(gate_up, q, s, I);
+  return qg::check_launch("qg_swiglu_quant_fp8");
+}
+
+qg_status qg_moe_combine(const uint16_t* down, const int32_t* row_of, const float* weight,
+                         uint16_t* out, int T, int topk, int R, int H, qg_stream_t stream) {
+  QG_REQUIRE(down && row_of && weight && out, QG_ERR_INVALID_ARG, "qg_moe_combine: NULL pointer");
+  QG_REQUIRE(T >= 0 && topk > 0 && R >= 0 && H > 0, QG_ERR_INVALID_ARG, "qg_moe_combine: bad sizes");
+  QG_REQUIRE(H % 8 == 0, QG_ERR_UNSUPPORTED_SHAPE, "qg_moe_combine: H %% 8 != 0");
+  QG_REQUIRE(aligned16(down) && aligned16(out), QG_ERR_MISALIGNED, "qg_moe_combine: misaligned");
+  if (T == 0) return QG_OK;
+  dim3 grid((H / 8 + qg::kThreads - 1) / qg::kThreads, T);
+  qg::combine_kernel<<<grid, qg::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      down, row_of, weight, out, topk, R, H);
+  return qg::check_launch("qg_moe_combine");
+}
+
+}  // extern "C"

@@ -114,8 +114,8 @@ def fp16_decode(bits):
 
 def int4_decode(nibbles):
     """Two's-complement 4-bit integer."""
-    n = np.asarray(nibbles).astype(np.int64) & 0xF
-    return np.where(n >= 8, n - 16, n)
+    n = (np.asarray(nibbles) & 0xF).astype(np.int8)
+    return np.where(n >= 8, n - 16, n).astype(np.int8)
 
 
 # ----------------------------------------------------------------------------
@@ -192,8 +192,29 @@ def bf16_round(x):
     return np.where(np.abs(r) > BF16_MAX, np.copysign(np.inf, r), r)
 
 
+def bf16_encode_f32(x):
+    """float32 -> bf16 bit pattern, round to nearest even, on the bit pattern.
+
+    Keep the upper 16 bits after adding 0x7FFF plus the lowest kept bit: a
+    discarded half above 0x8000 carries, below does not, and exactly 0x8000
+    carries only when the kept part is odd (ties to even).  A carry out of the
+    mantissa bumps the exponent, and past the largest finite value it yields
+    the infinity pattern, as IEEE overflow under round-to-nearest does.
+    Finite inputs only.
+    """
+    u = bits_from_f32(np.asarray(x, dtype=np.float32)).astype(np.uint32)
+    return ((u + np.uint32(0x7FFF) + ((u >> 16) & np.uint32(1))) >> 16).astype(np.uint16)
+
+
 def bf16_encode(x):
-    """Exact value -> bf16 bit pattern (uint16), round to nearest even once."""
+    """Exact value -> bf16 bit pattern (uint16), round to nearest even once.
+
+    float32 input uses the bit-pattern rounding above; any other input (the
+    float64 products) is rounded once from its exact value by ``bf16_round``.
+    """
+    x = np.asarray(x)
+    if x.dtype == np.float32:
+        return bf16_encode_f32(x)
     r = bf16_round(x).astype(np.float32)      # exact: r is a bf16 value
     return (bits_from_f32(r) >> 16).astype(np.uint16)
 

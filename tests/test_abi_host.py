@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads, every
+symbol declared in include/qgemm.h is exported and bound, and argument
+validation fails cleanly before any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "qgemm.h")
+
+
+def header_symbols():
+    src = open(HEADER).read()
+    return re.findall(r"QG_API\s+(?:const\s+char\s*\*|qg_status|void)\s+(\w+)\s*\(", src)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from numerics_packed_int4_gb300 import _build, qgemm
+    if not os.path.exists(qgemm.LIB_PATH):
+        _build.build()
+    return qgemm.load()
+
+
+def test_header_declares_the_six_path_entry_points():
+    names = set(header_symbols())
+    for n in ("qgemm_w4a16", "qgemm_w8a16", "qgemm_fp4a16", "quant_act_mxfp4",
+              "quant_act_fp8_block", "qgemm_w4a8_grouped"):
+        assert n in names
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in header_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_header_symbol():
+    from numerics_packed_int4_gb300 import qgemm
+    bound = set(qgemm.SIGNATURES) | {"qg_last_error_string", "qg_set_wait_limit"}
+    assert bound == set(header_symbols())
+    for name in qgemm.SIGNATURES:
+        if name != "qg_check_device_error":
+            assert callable(getattr(qgemm, name))
+
+
+P = ctypes.c_void_p
+FAKE = P(0x10000)            # aligned, never dereferenced: validation fails first
+FAKE_MIS = P(0x10001)
+
+
+def _rc(lib, name, *args):
+    return getattr(lib, name)(*args, P(0))
+
+
+def test_null_pointers_are_invalid_args(lib):
+    assert _rc(lib, "qgemm_w4a16", None, FAKE, 128, FAKE, FAKE, 1, 128, 128) == 1
+    assert _rc(lib, "qgemm_w8a16", FAKE, None, FAKE, FAKE, 1, 128, 128) == 1
+    assert _rc(lib, "quant_act_fp8_block", FAKE, None, FAKE, 128, 1, 128) == 1
+    assert _rc(lib, "qgemm_w4a8_grouped", None, FAKE, FAKE, FAKE, FAKE, 128, FAKE, 1, 1, 16, 128) == 1
+    assert "NULL" in lib.qg_last_error_string().decode()
+
+
+def test_shape_rules(lib):
+    assert _rc(lib, "qgemm_w4a16", FAKE, FAKE, 128, FAKE, FAKE, 1, 128, 100) == 2    # K % 128
+    assert _rc(lib, "qgemm_w4a16", FAKE, FAKE, 48, FAKE, FAKE, 1, 128, 384) == 2     # g % 32
+    assert _rc(lib, "qgemm_w8a16", FAKE, FAKE, FAKE, FAKE, 1, 12, 128) == 2          # N % 8
+    assert _rc(lib, "qgemm_fp4a16", FAKE, FAKE, 0, 16, None, FAKE, FAKE, 1, 128, 128) == 2
+    assert _rc(lib, "qgemm_fp4a16", FAKE, FAKE, 1, 16, None, FAKE, FAKE, 1, 128, 128) == 1
+    assert _rc(lib, "qgemm_fp4a16", FAKE, FAKE, 7, 16, FAKE, FAKE, FAKE, 1, 128, 128) == 1
+    assert _rc(lib, "quant_act_mxfp4", FAKE, FAKE, FAKE, 8, 1, 128) == 2
+    assert _rc(lib, "quant_act_fp8_block", FAKE, FAKE, FAKE, 12, 1, 96) == 2
+    assert _rc(lib, "qgemm_w4a8_grouped", FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, 1, 1, 16, 128) == 2
+    assert _rc(lib, "qg_dequant_weights", 9, FAKE, FAKE, 128, FAKE, 8, 128) == 1
+
+
+def test_misaligned_pointers(lib):
+    assert _rc(lib, "qgemm_w4a16", FAKE_MIS, FAKE, 128, FAKE, FAKE, 1, 128, 128) == 3
+    assert _rc(lib, "quant_act_fp8_block", FAKE, FAKE_MIS, FAKE, 128, 1, 128) == 3
+
+
+def test_wait_limit_setter_is_callable(lib):
+    lib.qg_set_wait_limit(5)
+    lib.qg_set_wait_limit(0)
+
+
+def test_input_generators_are_deterministic():
+    from numerics_packed_int4_gb300 import inputs
+    a = inputs.activations_bf16(4, 256, seed=3, outlier_frac=0.01, outlier_scale=50)
+    b = inputs.activations_bf16(4, 256, seed=3, outlier_frac=0.01, outlier_scale=50)
+    assert a.dtype == np.uint16 and np.array_equal(a, b)
+    w = inputs.weights_f32(8, 64, seed=1)
+    assert w.dtype == np.float32 and abs(float(w.std()) - 0.02) < 0.005
+    r = inputs.moe_routing(64, 8, 2, seed=4)
+    assert r["expert_off"][-1] == 128 and np.all(np.diff(r["expert_off"]) >= 0)
+    assert np.all(r["route_weight"] > 0)
+
+
+def test_quantizer_workload_injects_edges():
+    from numerics_packed_int4_gb300 import inputs
+    x = inputs.quantizer_activations_bf16(16, 1024, seed=0)
+    v = (x.astype(np.uint32) << 16).view(np.float32)
+    anchors = np.abs(v[0, ::128][::3])
+    assert np.all(np.log2(anchors / 448.0) == np.round(np.log2(anchors / 448.0)))

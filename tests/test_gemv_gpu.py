@@ -1,0 +1,103 @@
+"""GPU parity of the weight-only GEMM/GEMV entry points against the fp64 oracle.
+
+Tolerance (the path's contract): relative Frobenius <= 2e-3 and max |err| <=
+1e-2 * max |ref| against the oracle's bf16 output.  Inputs are the seeded
+synthetic workloads quantized by the oracle's own weight quantizers.
+"""
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+from numerics_packed_int4_gb300 import inputs, qgemm as Q
+from oracle import formats as OF
+from oracle import gemm as OG
+from oracle import quant as OQ
+from tests.gpu_util import check_gemm, dev, empty, host
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = ["int4", "fp8", "mxfp4", "nvfp4"]
+
+
+@functools.lru_cache(maxsize=16)
+def quantized(fmt, N, K, seed):
+    """Oracle-quantized weights for one format, plus its canonical dequant."""
+    w = inputs.weights_f32(N, K, seed=seed)
+    if fmt == "int4":
+        q, s = OQ.quant_int4_rtn(w, 128)
+        return dict(q=q, s=s, deq=OG.dequant_int4(q, s, 128), epi=None)
+    if fmt == "fp8":
+        q, cs = OQ.quant_fp8_channel(w)
+        return dict(q=q, s=cs, deq=OG.dequant_fp8(q), epi=cs.astype(np.float64))
+    if fmt == "mxfp4":
+        q, se = OQ.quant_mxfp4_weights(w)
+        return dict(q=q, s=se, deq=OG.dequant_mxfp4(q, se), epi=None)
+    q, sb, gs = OQ.quant_nvfp4(w)
+    return dict(q=q, s=sb, gs=gs, deq=OG.dequant_nvfp4(q, sb), epi=np.full(N, float(gs)))
+
+
+def run_gpu(qg, fmt, Wd, x, M, N, K):
+    y = empty((M, N), torch.int16)
+    dq, ds, dx = dev(Wd["q"]), dev(Wd["s"]), dev(x)
+    if fmt == "int4":
+        qg.qgemm_w4a16(dq, ds, 128, dx, y, M, N, K)
+    elif fmt == "fp8":
+        qg.qgemm_w8a16(dq, ds, dx, y, M, N, K)
+    elif fmt == "mxfp4":
+        qg.qgemm_fp4a16(dq, ds, Q.QG_SCALE_E8M0, 32, None, dx, y, M, N, K)
+    else:
+        gs = dev(np.array([Wd["gs"]], np.float32))
+        qg.qgemm_fp4a16(dq, ds, Q.QG_SCALE_E4M3, 16, gs, dx, y, M, N, K)
+    qg.qg_check_device_error()
+    return OF.bf16_decode(host(y))
+
+
+def reference(Wd, x, rows=None):
+    xs = x if rows is None else x[rows]
+    y64 = OG.gemm_bf16_f64(xs, Wd["deq"], Wd["epi"])
+    return OF.bf16_decode(OG.to_bf16(y64)), y64
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("M,N,K", [(1, 1024, 1024), (1, 1000, 384), (3, 136, 1280), (8, 512, 2048),
+                                   (9, 256, 896), (16, 392, 512), (17, 264, 256), (40, 128, 640)])
+def test_small_shapes(qg, fmt, M, N, K):
+    Wd = quantized(fmt, N, K, seed=11)
+    x = inputs.activations_bf16(M, K, seed=12 + M)
+    y = run_gpu(qg, fmt, Wd, x, M, N, K)
+    ref, y64 = reference(Wd, x)
+    check_gemm(y, ref, "%s M=%d N=%d K=%d" % (fmt, M, N, K))
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("N,K", [(4096, 4096), (14336, 4096), (4096, 14336)])
+def test_decode_sweep_config(qg, fmt, N, K):
+    """The decode sweep at full size: M in {1, 4, 16}, full parity (the oracle
+    handles M <= 16 at these sizes in seconds)."""
+    Wd = quantized(fmt, N, K, seed=100 + N // 1024 + K // 1024)
+    for M in (1, 4, 16):
+        x = inputs.activations_bf16(M, K, seed=200 + M)
+        y = run_gpu(qg, fmt, Wd, x, M, N, K)
+        ref, _ = reference(Wd, x)
+        check_gemm(y, ref, "%s M=%d N=%d K=%d" % (fmt, M, N, K))
+
+
+def test_gemv_is_deterministic(qg):
+    Wd = quantized("int4", 4096, 4096, seed=5)
+    x = inputs.activations_bf16(4, 4096, seed=6)
+    a = run_gpu(qg, "int4", Wd, x, 4, 4096, 4096)
+    b = run_gpu(qg, "int4", Wd, x, 4, 4096, 4096)
+    assert np.array_equal(a, b)
+
+
+def test_zero_rows_and_zero_m(qg):
+    N, K = 256, 512
+    Wd = quantized("int4", N, K, seed=7)
+    x = np.zeros((2, K), np.uint16)
+    y = run_gpu(qg, "int4", Wd, x, 2, N, K)
+    assert np.all(y == 0)
+    y0 = empty((1, N), torch.int16)
+    qg.qgemm_w4a16(dev(Wd["q"]), dev(Wd["s"]), 128, dev(x), y0, 0, N, K)   # M = 0 is a no-op

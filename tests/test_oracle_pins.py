@@ -164,6 +164,20 @@ def test_bf16_matches_torch_cpu_cast():
     assert np.array_equal(F.bf16_encode(x), t)
 
 
+def test_bf16_bit_rounding_agrees_with_binade_rounding():
+    """The two bf16 formulations (bit-pattern carry, significand rounding in
+    the binade) agree on random finite fp32 values, ties and near-ties."""
+    r = np.random.Generator(np.random.PCG64(10))
+    bits = r.integers(0, 2 ** 32, 400000, dtype=np.uint64).astype(np.uint32)
+    bits = np.concatenate([bits, (bits & 0xFFFF0000) | 0x8000, (bits & 0xFFFF0000) | 0x7FFF,
+                           (bits & 0xFFFF0000) | 0x8001])
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    a = F.bf16_encode_f32(x)
+    b = F.bf16_encode(x.astype(np.float64))
+    assert np.array_equal(a, b)
+
+
 # ----------------------------------------------------------------------------
 # page values for the casts
 # ----------------------------------------------------------------------------
