@@ -73,7 +73,7 @@ enum { QG_FMT_INT4 = 0, QG_FMT_FP8 = 1, QG_FMT_MXFP4 = 2, QG_FMT_NVFP4 = 3 };
  * formats paragraph).
  *   w_q [N][K/2]  packed INT4        w_s [N][K/g] bf16
  *   x   [M][K]    bf16               y   [M][N]   bf16 (written)
- *   g in {32, 64, 128, 256, ...}, g % 32 == 0, K % g == 0.               */
+ *   g a power of two >= 32 (32, 64, 128, 256, ...), K % g == 0.          */
 QG_API qg_status qgemm_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g,
                       const uint16_t* x, uint16_t* y, int M, int N, int K,
                       qg_stream_t stream);

@@ -20,7 +20,7 @@ unsigned int* g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::mutex g_mu;
 
-constexpr uint32_t kDefaultWaitLimit = 1u << 26;   // ~ seconds of try_wait polling
+constexpr uint32_t kDefaultWaitLimit = 1u << 20;   // polls of <= 1 us each: about a second
 uint32_t g_wait_limit = kDefaultWaitLimit;
 
 int current_device() {

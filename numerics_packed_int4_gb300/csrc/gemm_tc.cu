@@ -1,12 +1,267 @@
-// Prefill (M > 16) W4A16 GEMM on the 5th-generation tensor cores.
-#include "qg_common.cuh"
+// Prefill (M > 16) W4A16 GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// Orientation: the MMA computes Y^T tiles, D[n, m] = sum_k W[n,k] X[m,k].
+//   * A operand = dequantized weights, 128 output channels x 16 k per MMA,
+//     written straight from registers into tensor memory (tcgen05.st) by the
+//     dequant warps -- the canonical bf16_RNE(q*s) never touches shared
+//     memory.  ("Load INT4 weights and BF16 group scales from HBM into
+//     registers, dequantize to BF16 using CUDA cores, multiply in BF16 on the
+//     tensor cores", Production-Ready W4A8, "High-Performance W4A8 GEMM
+//     Kernel"; the same scheme as the tcgen05 BF16 x NVFP4 kernel the 3090
+//     article quotes in section 2.1.)
+//   * B operand = activations, 256 tokens x 64 k per stage, TMA-loaded into
+//     shared memory in the 128-byte swizzled K-major layout.
+//   * D = fp32 accumulator in tensor memory, 128 lanes x 256 columns.
+// One CTA computes a 256-token x 128-channel output tile:
+//   warp 0      TMA producer (one elected lane)
+//   warp 1      TMEM allocator + MMA issuer (one elected lane)
+//   warps 2..9  dequant producers during the K loop (lane quarter = warp % 4,
+//               k half = (warp - 2) / 4), then the epilogue
+// A 4-stage ring couples them: x_full (TMA bytes landed), a_full (256 dequant
+// threads stored their TMEM slice), empty (the MMAs that read the stage
+// completed, via tcgen05.commit).  Every wait is bounded; on expiry the CTA
+// records a timeout in the device error word, drains its in-flight copies and
+// MMAs, frees its tensor memory and returns.
+#include "dequant.cuh"
+#include "tc_common.cuh"
 
 namespace qg {
+namespace {
 
-qg_status prefill_w4a16(const uint8_t*, const uint16_t*, int, const uint16_t*, uint16_t*, int, int, int,
-                        cudaStream_t, bool* handled) {
+constexpr int kTileW = 128;            // weight rows (MMA M)
+constexpr int kTileT = 256;            // tokens (MMA N)
+constexpr int kBK = 64;                // k per stage (one 128-byte swizzle row of bf16)
+constexpr int kStages = 4;
+constexpr int kDeqWarps = 8;
+constexpr int kThreadsTc = (2 + kDeqWarps) * 32;
+constexpr int kXStageBytes = kTileT * kBK * 2;      // 32 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kACol0 = 256;                    // A slots follow the accumulator
+constexpr uint32_t kACols = kBK / 2;                // 32 columns (2 bf16 per column)
+constexpr uint32_t kDrainCap = 1u << 21;            // waits on work already issued (~2 s)
+
+struct TcArgs {
+  const uint8_t* wq;
+  const uint16_t* ws;
+  uint16_t* y;
+  int M, N, K, g;
+  int tiles_t, tiles_w, group_t;
+  unsigned int* err;
+  uint32_t cap;
+};
+
+struct __align__(8) TcSmemTail {
+  uint64_t x_full[kStages];
+  uint64_t a_full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__global__ void __launch_bounds__(kThreadsTc, 1)
+w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* xs = smem;                                                     // [kStages][32 KB]
+  TcSmemTail* tl = reinterpret_cast<TcSmemTail*>(smem + kStages * kXStageBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- tile of this CTA (grouped raster: group_t token tiles share a wave) --
+  const int per_group = p.group_t * p.tiles_w;
+  const int grp = blockIdx.x / per_group;
+  const int first_t = grp * p.group_t;
+  const int gsize = min(p.group_t, p.tiles_t - first_t);
+  const int within = blockIdx.x - grp * per_group;
+  const int tt = first_t + within % gsize;
+  const int wt = within / gsize;
+  const int m0 = tt * kTileT, n0 = wt * kTileW;
+  const int nslab = p.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&tl->x_full[s], 1);
+      mbar_init(&tl->a_full[s], kDeqWarps * 32);
+      mbar_init(&tl->empty[s], 1);
+    }
+    mbar_init(&tl->acc_full, 1);
+    mbar_init(&tl->drain, 1);
+    tl->abort = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmap_x);
+  }
+  if (warp == 1) tmem_alloc(&tl->tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tl->tmem_base;
+  volatile int* abort = &tl->abort;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int s = 0; s < nslab; ++s) {
+        const int st = s % kStages, r = s / kStages;
+        if (r > 0 && !mbar_wait(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+        mbar_arrive_expect_tx(&tl->x_full[st], kXStageBytes);
+        tma_load_2d(xs + st * kXStageBytes, &tmap_x, &tl->x_full[st], s * kBK, m0);
+        issued = s + 1;
+      }
+      if (*abort) {     // let every copy already issued land before the CTA exits
+        for (int s = max(0, issued - kStages); s < issued; ++s)
+          mbar_wait(&tl->x_full[s % kStages], (s / kStages) & 1, kDrainCap, abort, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kTileW, kTileT);
+      bool any = false;
+      for (int s = 0; s < nslab; ++s) {
+        const int st = s % kStages, r = s / kStages;
+        if (!mbar_wait(&tl->x_full[st], r & 1, p.cap, abort, p.err)) break;
+        if (!mbar_wait(&tl->a_full[st], r & 1, p.cap, abort, p.err)) break;
+        tc_fence_after();
+        const uint64_t bdesc = sw128_kmajor_desc(smem_addr(xs + st * kXStageBytes));
+#pragma unroll
+        for (int j = 0; j < kBK / 16; ++j)
+          tc_mma_ts(tmem, tmem + kACol0 + st * kACols + 8 * j, bdesc + 2 * j, idesc, (s | j) != 0);
+        tc_commit(&tl->empty[st]);
+        any = true;
+      }
+      if (!*abort) {
+        tc_commit(&tl->acc_full);
+      } else if (any) {
+        tc_commit(&tl->drain);                         // every MMA issued so far completes
+        mbar_wait(&tl->drain, 0, kDrainCap, abort, nullptr);
+      }
+    }
+  } else {
+    // ---------------- dequant producers ----------------
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int row = 32 * q + lane;
+    const int n = min(n0 + row, p.N - 1);
+    const uint8_t* wrow = p.wq + (size_t)n * (p.K / 2) + 16 * h;
+    const uint16_t* srow = p.ws + (size_t)n * (p.K / p.g);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + kACol0 + 16 * h;
+    constexpr int PF = 4;
+    uint4 pw[PF];
+#pragma unroll
+    for (int i = 0; i < PF; ++i)
+      if (i < nslab) pw[i] = ldg_stream(wrow + 32 * i);
+    for (int s0 = 0; s0 < nslab; s0 += PF) {
+#pragma unroll
+      for (int u = 0; u < PF; ++u) {
+        const int s = s0 + u;
+        if (s >= nslab || warp_aborted(abort)) break;
+        const uint32_t s2 = bf16x2_splat(__ldg(srow + (s * kBK + 32 * h) / p.g));
+        const uint32_t v[4] = {pw[u].x, pw[u].y, pw[u].z, pw[u].w};
+        if (s + PF < nslab) pw[u] = ldg_stream(wrow + 32 * (s + PF));
+        uint32_t out[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t pq[4], nat[4];
+          int4x8_kperm(v[j], s2, pq);
+          kperm4_to_natural(pq, nat);
+          out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
+          out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
+        }
+        const int st = s % kStages, r = s / kStages;
+        if (r > 0) {
+          if (!mbar_wait_warp(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+          tc_fence_after();
+        }
+        tmem_st16(lane_base + st * kACols, out);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&tl->a_full[st]);
+      }
+    }
+
+    // ---------------- epilogue: TMEM -> bf16 -> Y[m][n] ----------------
+    if (mbar_wait_warp(&tl->acc_full, 0, p.cap, abort, p.err)) {
+      tc_fence_after();
+      const int nn = n0 + row;
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 128 * h + 32 * i, v);
+        tmem_wait_ld();
+        const int mb = m0 + 128 * h + 32 * i;
+        if (nn < p.N) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (mb + c < p.M) p.y[(size_t)(mb + c) * p.N + nn] = f32_to_bf16_bits(__uint_as_float(v[c]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---- host: tensor map + launch -------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// bf16 [rows][cols] row-major -> TMA map with a (box_cols x box_rows) box, 128-byte swizzle
+bool make_bf16_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint16_t* x, uint16_t* y,
+                        int M, int N, int K, cudaStream_t st, bool* handled) {
   *handled = false;
-  return QG_OK;
+  if (M <= 16 || K % kBK != 0 || g % 32 != 0 || K % g != 0) return QG_OK;   // decode path instead
+  *handled = true;
+  CUtensorMap tmap;
+  if (!make_bf16_tmap(&tmap, x, M, K, kTileT, kBK))
+    return set_error(QG_ERR_CUDA, "qgemm_w4a16: cannot encode the activation tensor map");
+  unsigned int* err = device_error_word();
+  if (!err) return set_error(QG_ERR_CUDA, "qgemm_w4a16: no device error word");
+  TcArgs a{};
+  a.wq = w_q; a.ws = w_s; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
+  a.tiles_t = (M + kTileT - 1) / kTileT;
+  a.tiles_w = (N + kTileW - 1) / kTileW;
+  a.group_t = 8;
+  a.err = err;
+  a.cap = wait_limit();
+  const int smem = kStages * kXStageBytes + (int)sizeof(TcSmemTail) + 1024;
+  if (!ensure_smem(w4a16_tc_kernel, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a16: smem attribute");
+  const long long tiles = (long long)a.tiles_t * a.tiles_w;
+  w4a16_tc_kernel<<<(unsigned)tiles, kThreadsTc, smem, st>>>(tmap, a);
+  return check_launch("qgemm_w4a16 (prefill)");
 }
 
 }  // namespace qg

@@ -45,6 +45,7 @@ struct GemvArgs {
   const uint16_t* x;       // [M][K] bf16
   uint16_t* y;             // [M][N] bf16
   int M, N, K, g;
+  int lg;                  // log2(g) for INT4 (g is a power of two)
   int nseg;                // K / KSEG
   int ncp;                 // X smem row pitch in 16-byte chunks
 };
@@ -63,21 +64,37 @@ QG_DEVICE void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, ui
 // Per-lane scale state for one segment of one row.
 struct Scale { uint32_t a, b; };
 
+// Scale row of output channel n (bytes), and the scale of segment 'seg' for lane t.
 template <int FMT>
-QG_DEVICE Scale load_scale(const GemvArgs& p, int n, int seg, int t) {
+QG_DEVICE const uint8_t* scale_row(const GemvArgs& p, int n) {
+  const uint8_t* base = static_cast<const uint8_t*>(p.scales);
+  if constexpr (FMT == F_INT4) return base + (size_t)n * (size_t)(p.K >> p.lg) * 2;
+  if constexpr (FMT == F_MXFP4) return base + (size_t)n * (size_t)(p.K / 32);
+  if constexpr (FMT == F_NVFP4) return base + (size_t)n * (size_t)(p.K / 16);
+  return base;
+}
+
+template <int FMT>
+QG_DEVICE Scale load_scale(const GemvArgs& p, const uint8_t* srow, int seg, int t) {
   Scale s{0u, 0u};
   if constexpr (FMT == F_INT4) {
-    const uint16_t* ws = static_cast<const uint16_t*>(p.scales);
-    const int grp = (seg * 128 + 32 * t) / p.g;
-    s.a = bf16x2_splat(__ldg(ws + (size_t)n * (p.K / p.g) + grp));
+    const int grp = (seg * 128 + 32 * t) >> p.lg;
+    s.a = bf16x2_splat(__ldg(reinterpret_cast<const uint16_t*>(srow) + grp));
   } else if constexpr (FMT == F_MXFP4) {
-    const uint8_t* ws = static_cast<const uint8_t*>(p.scales);
-    s.a = __ldg(ws + (size_t)n * (p.K / 32) + seg * 4 + t);
+    s.a = __ldg(srow + seg * 4 + t);
   } else if constexpr (FMT == F_NVFP4) {
-    const uint8_t* ws = static_cast<const uint8_t*>(p.scales);
-    s.a = __ldg(reinterpret_cast<const uint16_t*>(ws + (size_t)n * (p.K / 16) + seg * 8 + 2 * t));
+    s.a = __ldg(reinterpret_cast<const uint16_t*>(srow + seg * 8 + 2 * t));
   }
   return s;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue now, and wait for the previous kernel's results before touching
+// any input.
+QG_DEVICE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+QG_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+QG_DEVICE void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
 }
 
 // Decode chunk j (8 k-values) of the lane's 16-byte word into A pairs:
@@ -137,6 +154,15 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   const int nseg = seg_hi - seg_lo;
   const int k0 = seg_lo * Tr::KSEG;
   const int nchunk = nseg * Tr::KSEG / 8;
+  const size_t row_bytes = (FMT == F_FP8) ? (size_t)p.K : (size_t)p.K / 2;
+
+  // ---- prologue that touches no input: start the next kernel, warm L2 ------
+  pdl_launch_dependents();
+  if (threadIdx.x < kRowsPerCta && nseg > 0) {
+    const int n = min(blockIdx.y * kRowsPerCta + (int)threadIdx.x, p.N - 1);
+    prefetch_l2(p.w + (size_t)n * row_bytes + (size_t)seg_lo * 64, (uint32_t)nseg * 64u);
+  }
+  pdl_wait();
 
   // ---- stage the activation slice, permuted and swizzled -------------------
   for (int i = threadIdx.x; i < M * nchunk; i += kWarps * 32) {
@@ -150,7 +176,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   const int g = lane >> 2, t = lane & 3;
   const int nb = blockIdx.y * kRowsPerCta + warp * 16;
   const int n0 = min(nb + g, p.N - 1), n1 = min(nb + g + 8, p.N - 1);
-  const size_t row_bytes = (FMT == F_FP8) ? (size_t)p.K : (size_t)p.K / 2;
+  const uint8_t* sr0 = scale_row<FMT>(p, n0);
+  const uint8_t* sr1 = scale_row<FMT>(p, n1);
   const uint8_t* w0 = p.w + (size_t)n0 * row_bytes + (size_t)seg_lo * 64 + 16 * t;
   const uint8_t* w1 = p.w + (size_t)n1 * row_bytes + (size_t)seg_lo * 64 + 16 * t;
 
@@ -169,8 +196,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
     if (u < nseg) {
       wa[u] = ldg_stream(w0 + 64 * u);
       wb[u] = ldg_stream(w1 + 64 * u);
-      sa[u] = load_scale<FMT>(p, n0, seg_lo + u, t);
-      sb[u] = load_scale<FMT>(p, n1, seg_lo + u, t);
+      sa[u] = load_scale<FMT>(p, sr0, seg_lo + u, t);
+      sb[u] = load_scale<FMT>(p, sr1, seg_lo + u, t);
     }
   }
 
@@ -200,8 +227,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
         if (sn < nseg) {
           wa[u] = ldg_stream(w0 + 64 * sn);
           wb[u] = ldg_stream(w1 + 64 * sn);
-          sa[u] = load_scale<FMT>(p, n0, seg_lo + sn, t);
-          sb[u] = load_scale<FMT>(p, n1, seg_lo + sn, t);
+          sa[u] = load_scale<FMT>(p, sr0, seg_lo + sn, t);
+          sb[u] = load_scale<FMT>(p, sr1, seg_lo + sn, t);
         }
       }
     }
@@ -258,8 +285,8 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ w, const void* __rest
   const size_t row_bytes = (FMT == F_FP8) ? (size_t)K : (size_t)K / 2;
   const uint4 wv = *reinterpret_cast<const uint4*>(w + (size_t)n * row_bytes + seg * 64 + 16 * t);
   GemvArgs p{};
-  p.scales = scales; p.K = K; p.g = g;
-  const Scale s = load_scale<FMT>(p, n, seg, t);
+  p.scales = scales; p.K = K; p.g = g; p.lg = 31 - __clz(g);
+  const Scale s = load_scale<FMT>(p, scale_row<FMT>(p, n), seg, t);
   uint16_t* o = out + (size_t)n * K + (size_t)seg * Tr::KSEG + t * Tr::CPL * 8;
 #pragma unroll
   for (int j = 0; j < Tr::CPL; ++j) {
@@ -309,13 +336,15 @@ qg_status launch_gemv_t(const GemvArgs& a0, cudaStream_t st, const char* name) {
   cfg.blockDim = dim3(kWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = ks;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) return set_error(QG_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
   return QG_OK;
@@ -359,6 +388,8 @@ qg_status gemv_w4a16_any_m(const uint8_t* w_q, const uint16_t* w_s, int g, const
                            uint16_t* y, int M, int N, int K, cudaStream_t st) {
   GemvArgs a{};
   a.w = w_q; a.scales = w_s; a.x = x; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
+  a.lg = 0;
+  while ((1 << a.lg) < g) ++a.lg;
   return run_weight_only<F_INT4>(a, st, "qgemm_w4a16");
 }
 
@@ -379,8 +410,8 @@ qg_status qgemm_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint
   qg_status r = qg::check_common(w_q, x, y, M, N, K, "qgemm_w4a16");
   if (r != QG_OK) return r;
   QG_REQUIRE(w_s, QG_ERR_INVALID_ARG, "qgemm_w4a16: NULL scales");
-  QG_REQUIRE(g >= 32 && g % 32 == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
-             "qgemm_w4a16: need g %% 32 == 0 and K %% g == 0 (g=%d)", g);
+  QG_REQUIRE(g >= 32 && (g & (g - 1)) == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
+             "qgemm_w4a16: need g a power of two >= 32 dividing K (g=%d)", g);
   if (M == 0) return QG_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (M > 16) {
@@ -444,8 +475,8 @@ qg_status qg_dequant_weights(int fmt, const uint8_t* w, const void* scales, int 
   if (N == 0) return QG_OK;
   switch (fmt) {
     case QG_FMT_INT4:
-      QG_REQUIRE(scales && g >= 32 && g % 32 == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
-                 "qg_dequant_weights: INT4 needs scales and g %% 32 == 0");
+      QG_REQUIRE(scales && g >= 32 && (g & (g - 1)) == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
+                 "qg_dequant_weights: INT4 needs scales and g a power of two >= 32");
       qg::dequant_kernel<qg::F_INT4><<<grid(128), threads, 0, st>>>(w, scales, g, w_out, N, K);
       break;
     case QG_FMT_FP8:

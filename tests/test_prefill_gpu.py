@@ -1,0 +1,65 @@
+"""GPU parity of the tcgen05 prefill W4A16 GEMM (M > 16) against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from numerics_packed_int4_gb300 import inputs
+from oracle import formats as OF
+from oracle import gemm as OG
+from oracle import quant as OQ
+from tests.gpu_util import check_gemm, dev, empty, host
+
+pytestmark = pytest.mark.gpu
+
+
+def run(qg, x, q, s, M, N, K, g=128):
+    y = empty((M, N), torch.int16)
+    qg.qgemm_w4a16(dev(q), dev(s), g, dev(x), y, M, N, K)
+    qg.qg_check_device_error()
+    return OF.bf16_decode(host(y))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 128, 128), (17, 128, 256), (300, 264, 512), (512, 384, 1024),
+                                   (1024, 1000, 640), (257, 4096, 4096)])
+def test_prefill_small(qg, M, N, K):
+    w = inputs.weights_f32(N, K, seed=M + N)
+    x = inputs.activations_bf16(M, K, seed=K + 7, outlier_frac=0.01, outlier_scale=50.0)
+    q, s = OQ.quant_int4_rtn(w, 128)
+    y = run(qg, x, q, s, M, N, K)
+    ref = OF.bf16_decode(OG.to_bf16(OG.qgemm_w4a16(x, q, s, 128)))
+    check_gemm(y, ref, "prefill M=%d N=%d K=%d" % (M, N, K))
+
+
+@pytest.mark.parametrize("g", [32, 64, 256])
+def test_prefill_group_sizes(qg, g):
+    M, N, K = 256, 256, 512
+    w = inputs.weights_f32(N, K, seed=g)
+    x = inputs.activations_bf16(M, K, seed=g + 1)
+    q, s = OQ.quant_int4_rtn(w, g)
+    y = run(qg, x, q, s, M, N, K, g)
+    ref = OF.bf16_decode(OG.to_bf16(OG.qgemm_w4a16(x, q, s, g)))
+    check_gemm(y, ref, "prefill g=%d" % g)
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (14336, 4096), (4096, 14336)])
+def test_prefill_config_sampled(qg, N, K):
+    """The prefill workload at full size (M = 8192, 1 % outlier channels x50);
+    parity on a seeded sample of 256 rows, every output finite."""
+    M = 8192
+    w = inputs.weights_f32(N, K, seed=300 + N // 1024 + K // 1024)
+    x = inputs.activations_bf16(M, K, seed=400 + K, outlier_frac=0.01, outlier_scale=50.0)
+    q, s = OQ.quant_int4_rtn(w, 128)
+    y = run(qg, x, q, s, M, N, K)
+    assert np.all(np.isfinite(y))
+    rows = np.sort(np.random.Generator(np.random.PCG64(5)).choice(M, 256, replace=False))
+    ref = OF.bf16_decode(OG.to_bf16(OG.qgemm_w4a16(x[rows], q, s, 128)))
+    check_gemm(y[rows], ref, "prefill config N=%d K=%d" % (N, K))
+
+
+def test_prefill_deterministic(qg):
+    M, N, K = 512, 512, 1024
+    w = inputs.weights_f32(N, K, seed=1)
+    x = inputs.activations_bf16(M, K, seed=2)
+    q, s = OQ.quant_int4_rtn(w, 128)
+    assert np.array_equal(run(qg, x, q, s, M, N, K), run(qg, x, q, s, M, N, K))
