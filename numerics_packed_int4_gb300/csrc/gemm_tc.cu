@@ -34,7 +34,8 @@ constexpr int kBK = 64;                // k per stage (one 128-byte swizzle row 
 constexpr int kStages = 4;
 constexpr int kDeqWarps = 8;
 constexpr int kThreadsTc = (2 + kDeqWarps) * 32;
-constexpr int kXStageBytes = kTileT * kBK * 2;      // 32 KB
+constexpr int kXStageBytes = kTileT * kBK * 2;      // 32 KB activations
+constexpr int kWStageBytes = kTileW * kBK / 2;      // 4 KB packed INT4 weights
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACol0 = 256;                    // A slots follow the accumulator
 constexpr uint32_t kACols = kBK / 2;                // 32 columns (2 bf16 per column)
@@ -44,7 +45,7 @@ struct TcArgs {
   const uint8_t* wq;
   const uint16_t* ws;
   uint16_t* y;
-  int M, N, K, g;
+  int M, N, K, g, lg;
   int tiles_t, tiles_w, group_t;
   unsigned int* err;
   uint32_t cap;
@@ -61,11 +62,13 @@ struct __align__(8) TcSmemTail {
 };
 
 __global__ void __launch_bounds__(kThreadsTc, 1)
-w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs p) {
+w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                const TcArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* xs = smem;                                                     // [kStages][32 KB]
-  TcSmemTail* tl = reinterpret_cast<TcSmemTail*>(smem + kStages * kXStageBytes);
+  uint8_t* wsm = smem + kStages * kXStageBytes;                           // [kStages][4 KB]
+  TcSmemTail* tl = reinterpret_cast<TcSmemTail*>(wsm + kStages * kWStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -91,6 +94,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs p) {
     tl->abort = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tmap_x);
+    tma_prefetch_desc(&tmap_w);
   }
   if (warp == 1) tmem_alloc(&tl->tmem_base, kTmemCols);
   tc_fence_before();
@@ -106,8 +110,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs p) {
       for (int s = 0; s < nslab; ++s) {
         const int st = s % kStages, r = s / kStages;
         if (r > 0 && !mbar_wait(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
-        mbar_arrive_expect_tx(&tl->x_full[st], kXStageBytes);
+        mbar_arrive_expect_tx(&tl->x_full[st], kXStageBytes + kWStageBytes);
         tma_load_2d(xs + st * kXStageBytes, &tmap_x, &tl->x_full[st], s * kBK, m0);
+        tma_load_2d(wsm + st * kWStageBytes, &tmap_w, &tl->x_full[st], s * (kBK / 2), n0);
         issued = s + 1;
       }
       if (*abort) {     // let every copy already issued land before the CTA exits
@@ -141,44 +146,50 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs p) {
     }
   } else {
     // ---------------- dequant producers ----------------
+    // Thread = one weight row (TMEM lane) x one 32-k half of the stage.  The
+    // packed tile arrives by TMA with the activations; decoding stage s+1
+    // overlaps the TMEM store of stage s.
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int row = 32 * q + lane;
     const int n = min(n0 + row, p.N - 1);
-    const uint8_t* wrow = p.wq + (size_t)n * (p.K / 2) + 16 * h;
-    const uint16_t* srow = p.ws + (size_t)n * (p.K / p.g);
+    const uint16_t* srow = p.ws + (size_t)n * (p.K >> p.lg);
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + kACol0 + 16 * h;
-    constexpr int PF = 4;
-    uint4 pw[PF];
+    // decode stage s into 'out' (registers only); false if the wait gave up
+    auto decode = [&](int s, uint32_t (&out)[16]) -> bool {
+      const int st = s % kStages;
+      if (!mbar_wait_warp(&tl->x_full[st], (s / kStages) & 1, p.cap, abort, p.err)) return false;
+      const uint4 w4 = *reinterpret_cast<const uint4*>(wsm + st * kWStageBytes + row * (kBK / 2) + 16 * h);
+      const uint32_t s2 = bf16x2_splat(__ldg(srow + ((s * kBK + 32 * h) >> p.lg)));
+      const uint32_t v[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-    for (int i = 0; i < PF; ++i)
-      if (i < nslab) pw[i] = ldg_stream(wrow + 32 * i);
-    for (int s0 = 0; s0 < nslab; s0 += PF) {
-#pragma unroll
-      for (int u = 0; u < PF; ++u) {
-        const int s = s0 + u;
-        if (s >= nslab || warp_aborted(abort)) break;
-        const uint32_t s2 = bf16x2_splat(__ldg(srow + (s * kBK + 32 * h) / p.g));
-        const uint32_t v[4] = {pw[u].x, pw[u].y, pw[u].z, pw[u].w};
-        if (s + PF < nslab) pw[u] = ldg_stream(wrow + 32 * (s + PF));
-        uint32_t out[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t pq[4], nat[4];
-          int4x8_kperm(v[j], s2, pq);
-          kperm4_to_natural(pq, nat);
-          out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
-          out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
-        }
-        const int st = s % kStages, r = s / kStages;
-        if (r > 0) {
-          if (!mbar_wait_warp(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
-          tc_fence_after();
-        }
-        tmem_st16(lane_base + st * kACols, out);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&tl->a_full[st]);
+      for (int j = 0; j < 4; ++j) {
+        uint32_t pq[4], nat[4];
+        int4x8_kperm(v[j], s2, pq);
+        kperm4_to_natural(pq, nat);
+        out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
+        out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
       }
+      return true;
+    };
+    // store stage s from 'cur' into its TMEM slot while 'nxt' receives stage s+1
+    auto publish = [&](int s, const uint32_t (&cur)[16], uint32_t (&nxt)[16], bool& ok_next) -> bool {
+      const int st = s % kStages, r = s / kStages;
+      if (r > 0) {
+        if (!mbar_wait_warp(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) return false;
+        tc_fence_after();
+      }
+      tmem_st16(lane_base + st * kACols, cur);
+      ok_next = s + 1 < nslab ? decode(s + 1, nxt) : false;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&tl->a_full[st]);
+      return true;
+    };
+    uint32_t bufA[16], bufB[16];
+    bool okA = nslab > 0 && decode(0, bufA), okB = false;
+    for (int s = 0; s < nslab; s += 2) {
+      if (!okA || !publish(s, bufA, bufB, okB)) break;
+      if (s + 1 >= nslab || !okB || !publish(s + 1, bufB, bufA, okA)) break;
     }
 
     // ---------------- epilogue: TMEM -> bf16 -> Y[m][n] ----------------
@@ -228,6 +239,19 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 // bf16 [rows][cols] row-major -> TMA map with a (box_cols x box_rows) box, 128-byte swizzle
+// u8 [rows][cols] row-major -> TMA map with a (box_cols x box_rows) box, no swizzle
+bool make_u8_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_bf16_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -243,24 +267,28 @@ bool make_bf16_tmap(CUtensorMap* m, const void* base, int rows, int cols, int bo
 qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint16_t* x, uint16_t* y,
                         int M, int N, int K, cudaStream_t st, bool* handled) {
   *handled = false;
-  if (M <= 16 || K % kBK != 0 || g % 32 != 0 || K % g != 0) return QG_OK;   // decode path instead
+  if (M <= 16 || K % kBK != 0 || g < 32 || (g & (g - 1)) != 0 || K % g != 0) return QG_OK;   // decode path
   *handled = true;
-  CUtensorMap tmap;
+  CUtensorMap tmap, tmap_w;
   if (!make_bf16_tmap(&tmap, x, M, K, kTileT, kBK))
     return set_error(QG_ERR_CUDA, "qgemm_w4a16: cannot encode the activation tensor map");
+  if (!make_u8_tmap(&tmap_w, w_q, N, K / 2, kTileW, kBK / 2))
+    return set_error(QG_ERR_CUDA, "qgemm_w4a16: cannot encode the weight tensor map");
   unsigned int* err = device_error_word();
   if (!err) return set_error(QG_ERR_CUDA, "qgemm_w4a16: no device error word");
   TcArgs a{};
   a.wq = w_q; a.ws = w_s; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
+  a.lg = 0;
+  while ((1 << a.lg) < g) ++a.lg;
   a.tiles_t = (M + kTileT - 1) / kTileT;
   a.tiles_w = (N + kTileW - 1) / kTileW;
   a.group_t = 8;
   a.err = err;
   a.cap = wait_limit();
-  const int smem = kStages * kXStageBytes + (int)sizeof(TcSmemTail) + 1024;
+  const int smem = kStages * (kXStageBytes + kWStageBytes) + (int)sizeof(TcSmemTail) + 1024;
   if (!ensure_smem(w4a16_tc_kernel, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a16: smem attribute");
   const long long tiles = (long long)a.tiles_t * a.tiles_w;
-  w4a16_tc_kernel<<<(unsigned)tiles, kThreadsTc, smem, st>>>(tmap, a);
+  w4a16_tc_kernel<<<(unsigned)tiles, kThreadsTc, smem, st>>>(tmap, tmap_w, a);
   return check_launch("qgemm_w4a16 (prefill)");
 }
 

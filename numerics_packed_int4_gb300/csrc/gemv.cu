@@ -29,7 +29,6 @@ namespace {
 enum Fmt { F_INT4 = 0, F_FP8 = 1, F_MXFP4 = 2, F_NVFP4 = 3 };
 
 constexpr int kWarps = 8;
-constexpr int kRowsPerCta = 16 * kWarps;
 constexpr int kPF = 4;                 // segments in flight per lane
 
 template <int FMT> struct FmtTraits;
@@ -48,6 +47,7 @@ struct GemvArgs {
   int lg;                  // log2(g) for INT4 (g is a power of two)
   int nseg;                // K / KSEG
   int ncp;                 // X smem row pitch in 16-byte chunks
+  int rg;                  // 16-row groups per CTA (warps split K by kWarps / rg)
 };
 
 QG_DEVICE int swz(int c) { return c ^ ((c >> 3) & 1); }
@@ -145,22 +145,27 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   extern __shared__ __align__(16) uint4 smem[];
   const int M = p.M;
   const int MP = MT * 8;
-  uint4* xs = smem;                                              // [M][ncp]
-  float* red = reinterpret_cast<float*>(smem + (size_t)M * p.ncp); // [128][MP]
+  const int RG = p.rg, KW = kWarps / p.rg;          // row groups x k-split warps
+  const int rows_cta = 16 * RG;
+  uint4* xs = smem;                                                         // [M][ncp]
+  float* red = reinterpret_cast<float*>(smem + (size_t)M * p.ncp);          // [kWarps][16][MP]
+  float* rsum = red + kWarps * 16 * MP;                                     // [rows_cta][MP]
 
+  // k range of this CTA (cluster split) and of this warp (warp split)
   const int ks = gridDim.x, kr = blockIdx.x;
   const int seg_lo = (int)((long long)p.nseg * kr / ks);
   const int seg_hi = (int)((long long)p.nseg * (kr + 1) / ks);
-  const int nseg = seg_hi - seg_lo;
+  const int nseg_cta = seg_hi - seg_lo;
   const int k0 = seg_lo * Tr::KSEG;
-  const int nchunk = nseg * Tr::KSEG / 8;
+  const int nchunk = nseg_cta * Tr::KSEG / 8;
   const size_t row_bytes = (FMT == F_FP8) ? (size_t)p.K : (size_t)p.K / 2;
+  const int row0 = blockIdx.y * rows_cta;
 
   // ---- prologue that touches no input: start the next kernel, warm L2 ------
   pdl_launch_dependents();
-  if (threadIdx.x < kRowsPerCta && nseg > 0) {
-    const int n = min(blockIdx.y * kRowsPerCta + (int)threadIdx.x, p.N - 1);
-    prefetch_l2(p.w + (size_t)n * row_bytes + (size_t)seg_lo * 64, (uint32_t)nseg * 64u);
+  if ((int)threadIdx.x < rows_cta && nseg_cta > 0) {
+    const int n = min(row0 + (int)threadIdx.x, p.N - 1);
+    prefetch_l2(p.w + (size_t)n * row_bytes + (size_t)seg_lo * 64, (uint32_t)nseg_cta * 64u);
   }
   pdl_wait();
 
@@ -174,12 +179,16 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int nb = blockIdx.y * kRowsPerCta + warp * 16;
+  const int rg = warp / KW, kw = warp - rg * KW;
+  const int s_lo = (int)((long long)nseg_cta * kw / KW);
+  const int s_hi = (int)((long long)nseg_cta * (kw + 1) / KW);
+  const int nseg = s_hi - s_lo;                     // this warp's segments (relative to seg_lo)
+  const int nb = row0 + rg * 16;
   const int n0 = min(nb + g, p.N - 1), n1 = min(nb + g + 8, p.N - 1);
   const uint8_t* sr0 = scale_row<FMT>(p, n0);
   const uint8_t* sr1 = scale_row<FMT>(p, n1);
-  const uint8_t* w0 = p.w + (size_t)n0 * row_bytes + (size_t)seg_lo * 64 + 16 * t;
-  const uint8_t* w1 = p.w + (size_t)n1 * row_bytes + (size_t)seg_lo * 64 + 16 * t;
+  const uint8_t* w0 = p.w + (size_t)n0 * row_bytes + (size_t)(seg_lo + s_lo) * 64 + 16 * t;
+  const uint8_t* w1 = p.w + (size_t)n1 * row_bytes + (size_t)(seg_lo + s_lo) * 64 + 16 * t;
 
   const int col0 = min(g, M - 1), col1 = min(8 + g, M - 1);
   const uint4* xr0 = xs + col0 * p.ncp;
@@ -196,8 +205,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
     if (u < nseg) {
       wa[u] = ldg_stream(w0 + 64 * u);
       wb[u] = ldg_stream(w1 + 64 * u);
-      sa[u] = load_scale<FMT>(p, sr0, seg_lo + u, t);
-      sb[u] = load_scale<FMT>(p, sr1, seg_lo + u, t);
+      sa[u] = load_scale<FMT>(p, sr0, seg_lo + s_lo + u, t);
+      sb[u] = load_scale<FMT>(p, sr1, seg_lo + s_lo + u, t);
     }
   }
 
@@ -206,12 +215,13 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
     for (int u = 0; u < kPF; ++u) {
       const int s = s0 + u;
       if (s < nseg) {
+        const int cbase = (s_lo + s) * (Tr::KSEG / 8) + t * Tr::CPL;
 #pragma unroll
         for (int j = 0; j < Tr::CPL; ++j) {
           uint32_t ag[4], ah[4];
           decode_chunk<FMT>(wa[u], sa[u], j, ag);
           decode_chunk<FMT>(wb[u], sb[u], j, ah);
-          const int c = swz(s * (Tr::KSEG / 8) + t * Tr::CPL + j);
+          const int c = swz(cbase + j);
           {
             const uint4 xf = xr0[c];
             mma_bf16(acc[0], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
@@ -227,38 +237,48 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
         if (sn < nseg) {
           wa[u] = ldg_stream(w0 + 64 * sn);
           wb[u] = ldg_stream(w1 + 64 * sn);
-          sa[u] = load_scale<FMT>(p, sr0, seg_lo + sn, t);
-          sb[u] = load_scale<FMT>(p, sr1, seg_lo + sn, t);
+          sa[u] = load_scale<FMT>(p, sr0, seg_lo + s_lo + sn, t);
+          sb[u] = load_scale<FMT>(p, sr1, seg_lo + s_lo + sn, t);
         }
       }
     }
   }
 
-  // ---- partial sums -> shared memory [row][m] ---------------------------------
+  // ---- per-warp partials -> shared memory, reduce the k-split warps ---------
+  {
+    float* rw = red + warp * 16 * MP;
 #pragma unroll
-  for (int i = 0; i < MT; ++i) {
-    const int m = 8 * i + 2 * t;
-    const int r0 = warp * 16 + g, r1 = r0 + 8;
-    red[r0 * MP + m] = acc[i][0];
-    red[r0 * MP + m + 1] = acc[i][1];
-    red[r1 * MP + m] = acc[i][2];
-    red[r1 * MP + m + 1] = acc[i][3];
+    for (int i = 0; i < MT; ++i) {
+      const int m = 8 * i + 2 * t;
+      rw[g * MP + m] = acc[i][0];
+      rw[g * MP + m + 1] = acc[i][1];
+      rw[(g + 8) * MP + m] = acc[i][2];
+      rw[(g + 8) * MP + m + 1] = acc[i][3];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < rows_cta * MP; i += kWarps * 32) {
+    const int r = i / MP, m = i - r * MP;
+    const int rgi = r >> 4, rr = r & 15;
+    float v = 0.f;
+    for (int q = 0; q < KW; ++q) v += red[((rgi * KW + q) * 16 + rr) * MP + m];
+    rsum[i] = v;
   }
   if (ks > 1) cluster_sync(); else __syncthreads();
 
   // ---- cluster reduction of this CTA's share of rows, epilogue, store --------
-  const int rows_per = kRowsPerCta / ks;
+  const int rows_per = rows_cta / ks;
   const int rbeg = kr * rows_per;
   for (int i = threadIdx.x; i < rows_per * M; i += kWarps * 32) {
     const int m = i / rows_per, r = rbeg + (i - m * rows_per);
-    const int n = blockIdx.y * kRowsPerCta + r;
+    const int n = row0 + r;
     float v;
     if (ks > 1) {
-      const uint32_t a = smem_u32(red + r * MP + m);
+      const uint32_t a = smem_u32(rsum + r * MP + m);
       v = 0.f;
       for (int q = 0; q < ks; ++q) v += ld_dsmem_f32(a, q);
     } else {
-      v = red[r * MP + m];
+      v = rsum[r * MP + m];
     }
     if (n < p.N) {
       if constexpr (FMT == F_FP8) v *= __ldg(static_cast<const float*>(p.scales) + n);
@@ -310,27 +330,39 @@ qg_status launch_gemv_t(const GemvArgs& a0, cudaStream_t st, const char* name) {
   using Tr = FmtTraits<FMT>;
   GemvArgs a = a0;
   a.nseg = a.K / Tr::KSEG;
-  const int rb = (a.N + kRowsPerCta - 1) / kRowsPerCta;
-  const int target = 2 * sm_count();
-  int ks = 1;
-  while (ks < 8 && rb * ks < target && a.nseg >= 2 * ks) ks *= 2;
-  // activation slice must fit in shared memory
-  auto smem_bytes = [&](int kk) {
-    const int nseg_max = (a.nseg + kk - 1) / kk;
+  const int row_groups = (a.N + 15) / 16;
+  auto kern = gemv_kernel<FMT, MT>;
+  auto smem_for = [&](int ks, int rg) {
+    const int nseg_max = (a.nseg + ks - 1) / ks;
     int ncp = nseg_max * Tr::KSEG / 8;
-    const int want = (FMT == F_FP8) ? 1 : 2;
+    const int want = (FMT == F_FP8) ? 1 : 2;          // bank-conflict-free pitch (mod 8)
     while ((ncp & 7) != want) ++ncp;
     a.ncp = ncp;
-    return (size_t)a.M * ncp * 16 + (size_t)kRowsPerCta * MT * 8 * 4;
+    return (size_t)a.M * ncp * 16 + (size_t)(kWarps * 16 + 16 * rg) * MT * 8 * 4;
   };
-  size_t smem = smem_bytes(ks);
-  while (smem > 200 * 1024 && ks < 8) { ks *= 2; smem = smem_bytes(ks); }
-  if (smem > 200 * 1024)
+  // K split over a cluster only when the activation slice does not fit
+  int ks = 1;
+  while (smem_for(ks, 8) > 160 * 1024 && ks < 8) ks *= 2;
+  if (smem_for(ks, 8) > 200 * 1024)
     return set_error(QG_ERR_UNSUPPORTED_SHAPE, "%s: activation slice too large for one CTA", name);
+  // rows per CTA: the fewest that keep every CTA resident in one wave
+  const int cap_sm = sm_count();
+  int rg = 1;
+  for (;;) {
+    const size_t smem = smem_for(ks, rg);
+    if (!ensure_smem(kern, (int)smem)) return set_error(QG_ERR_CUDA, "%s: cannot set shared memory size", name);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem) != cudaSuccess)
+      per_sm = 1;
+    const long long ctas = (long long)((row_groups + rg - 1) / rg) * ks;
+    const bool kw_ok = (kWarps / rg) <= (a.nseg + ks - 1) / ks;
+    if ((ctas <= (long long)per_sm * cap_sm / ks * ks && kw_ok) || rg == kWarps) break;
+    rg *= 2;
+  }
+  a.rg = rg;
+  const size_t smem = smem_for(ks, rg);
+  const int rb = (row_groups + rg - 1) / rg;
 
-  auto kern = gemv_kernel<FMT, MT>;
-  if (!ensure_smem(kern, (int)smem))
-    return set_error(QG_ERR_CUDA, "%s: cannot set shared memory size", name);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ks, rb, 1);
   cfg.blockDim = dim3(kWarps * 32, 1, 1);

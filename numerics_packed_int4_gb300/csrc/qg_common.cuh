@@ -12,7 +12,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/qgemm.h"
+#include "qgemm.h"
 
 #define QG_HOST_DEVICE __host__ __device__ __forceinline__
 #define QG_DEVICE __device__ __forceinline__
