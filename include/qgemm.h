@@ -63,6 +63,13 @@ enum { QG_FMT_INT4 = 0, QG_FMT_FP8 = 1, QG_FMT_MXFP4 = 2, QG_FMT_NVFP4 = 3 };
  * Weight-only GEMM/GEMV (W x A16): Y = X . dequant(W)^T, fp32 accumulate.
  * M <= 16 runs the HBM-streaming decode kernel; larger M the prefill kernel.
  * Shape rules: M >= 1, N >= 1, N % 8 == 0, K % 128 == 0.
+ * Stream overlap: the decode kernel is launched with programmatic dependent
+ * launch.  It starts streaming its weights and scales while the previous
+ * kernel in the stream may still be running, and waits for that kernel before
+ * it reads X or writes Y.  Only the decode kernels allow this early start,
+ * and they write nothing but Y, so the one rule for callers is: the weights
+ * or scales of a decode call must not be the Y of the decode call enqueued
+ * just before it.
  * ------------------------------------------------------------------------ */
 
 /* INT4 weights with one bf16 scale per group of g along K.

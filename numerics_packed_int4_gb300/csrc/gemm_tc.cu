@@ -31,7 +31,7 @@ namespace {
 constexpr int kTileW = 128;            // weight rows (MMA M)
 constexpr int kTileT = 256;            // tokens (MMA N)
 constexpr int kBK = 64;                // k per stage (one 128-byte swizzle row of bf16)
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kDeqWarps = 8;
 constexpr int kThreadsTc = (2 + kDeqWarps) * 32;
 constexpr int kXStageBytes = kTileT * kBK * 2;      // 32 KB activations

@@ -101,3 +101,25 @@ def test_zero_rows_and_zero_m(qg):
     assert np.all(y == 0)
     y0 = empty((1, N), torch.int16)
     qg.qgemm_w4a16(dev(Wd["q"]), dev(Wd["s"]), 128, dev(x), y0, 0, N, K)   # M = 0 is a no-op
+
+
+def test_chained_gemvs_wait_for_the_previous_output(qg):
+    """Layer chain on one stream, no host sync: y1 = W1.x, y2 = W2.y1, y3 = W3.y2
+    (the decode kernels overlap their weight streaming with the previous
+    kernel, so each must still read the previous kernel's finished output)."""
+    N = K = 4096
+    Ws = [quantized(f, N, K, seed=40 + i) for i, f in enumerate(["int4", "fp8", "nvfp4"])]
+    x = inputs.activations_bf16(1, K, seed=41)
+    d = [dev(x)] + [empty((1, N), torch.int16) for _ in range(3)]
+    dq = [(dev(W["q"]), dev(W["s"])) for W in Ws]
+    gs = dev(np.array([Ws[2]["gs"]], np.float32))
+    for rep in range(3):
+        qg.qgemm_w4a16(dq[0][0], dq[0][1], 128, d[0], d[1], 1, N, K)
+        qg.qgemm_w8a16(dq[1][0], dq[1][1], d[1], d[2], 1, N, K)
+        qg.qgemm_fp4a16(dq[2][0], dq[2][1], Q.QG_SCALE_E4M3, 16, gs, d[2], d[3], 1, N, K)
+    qg.qg_check_device_error()
+    ref = x
+    for W, fmt in zip(Ws, ["int4", "fp8", "nvfp4"]):
+        ref = OG.to_bf16(OG.gemm_bf16_f64(ref, W["deq"], W["epi"]))
+    y = OF.bf16_decode(host(d[3]))
+    check_gemm(y, OF.bf16_decode(ref), "chained")
