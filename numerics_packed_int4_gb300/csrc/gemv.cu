@@ -29,7 +29,9 @@ namespace {
 enum Fmt { F_INT4 = 0, F_FP8 = 1, F_MXFP4 = 2, F_NVFP4 = 3 };
 
 constexpr int kWarps = 8;
-constexpr int kPF = 4;                 // segments in flight per lane
+constexpr int kRing = 6;               // weight segments in flight per warp (cp.async ring)
+constexpr int kPFS = 3;                // scale prefetch distance (segments); divides kRing
+static_assert(kRing % kPFS == 0, "the scale ring index u % kPFS must equal s % kPFS");
 
 template <int FMT> struct FmtTraits;
 template <> struct FmtTraits<F_INT4>  { static constexpr int KSEG = 128, CPL = 4; };
@@ -93,9 +95,7 @@ QG_DEVICE Scale load_scale(const GemvArgs& p, const uint8_t* srow, int seg, int 
 // any input.
 QG_DEVICE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 QG_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-QG_DEVICE void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
-}
+
 
 // Decode chunk j (8 k-values) of the lane's 16-byte word into A pairs:
 // a[0], a[1] for the first mma (lo / hi k-slots), a[2], a[3] for the second.
@@ -127,6 +127,14 @@ QG_DEVICE uint4 perm_x(const uint4& u) {
 
 QG_DEVICE uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
+// 16-byte asynchronous global -> shared copy that bypasses L1 (cp.async.cg)
+QG_DEVICE void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+QG_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+QG_DEVICE void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
 QG_DEVICE void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -147,8 +155,9 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   const int MP = MT * 8;
   const int RG = p.rg, KW = kWarps / p.rg;          // row groups x k-split warps
   const int rows_cta = 16 * RG;
-  uint4* xs = smem;                                                         // [M][ncp]
-  float* red = reinterpret_cast<float*>(smem + (size_t)M * p.ncp);          // [kWarps][16][MP]
+  uint4* wring = smem;                                                      // [kWarps][kRing][2][32]
+  uint4* xs = smem + (size_t)kWarps * kRing * 64;                           // [M][ncp]
+  float* red = reinterpret_cast<float*>(xs + (size_t)M * p.ncp);            // [kWarps][16][MP]
   float* rsum = red + kWarps * 16 * MP;                                     // [rows_cta][MP]
 
   // k range of this CTA (cluster split) and of this warp (warp split)
@@ -160,22 +169,6 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   const int nchunk = nseg_cta * Tr::KSEG / 8;
   const size_t row_bytes = (FMT == F_FP8) ? (size_t)p.K : (size_t)p.K / 2;
   const int row0 = blockIdx.y * rows_cta;
-
-  // ---- prologue that touches no input: start the next kernel, warm L2 ------
-  pdl_launch_dependents();
-  if ((int)threadIdx.x < rows_cta && nseg_cta > 0) {
-    const int n = min(row0 + (int)threadIdx.x, p.N - 1);
-    prefetch_l2(p.w + (size_t)n * row_bytes + (size_t)seg_lo * 64, (uint32_t)nseg_cta * 64u);
-  }
-  pdl_wait();
-
-  // ---- stage the activation slice, permuted and swizzled -------------------
-  for (int i = threadIdx.x; i < M * nchunk; i += kWarps * 32) {
-    const int m = i / nchunk, c = i - m * nchunk;
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * p.K + k0 + 8 * c));
-    xs[m * p.ncp + swz(c)] = perm_x<FMT>(u);
-  }
-  __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -194,33 +187,73 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   const uint4* xr0 = xs + col0 * p.ncp;
   const uint4* xr1 = xs + col1 * p.ncp;
 
-  float acc[MT][4];
+  // Start the next kernel in the stream now.  This grid's weight stream is
+  // issued before waiting for the previous kernel (qgemm.h: weights are never
+  // written by the decode kernels, the only kernels that start early); the
+  // activations are read only after the wait.
+  pdl_launch_dependents();
+  // Each lane streams its own two 16-byte words per segment through a private
+  // ring of kRing segments in shared memory (cp.async; the lane reads back
+  // only what it copied, so no cross-lane synchronization is needed).
+  uint4* ring = wring + (size_t)warp * kRing * 64 + lane;          // [kRing][2][32] uint4 per warp
+  const uint32_t ring_s = smem_u32(ring);
 #pragma unroll
-  for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-
-  uint4 wa[kPF], wb[kPF];
-  Scale sa[kPF], sb[kPF];
-#pragma unroll
-  for (int u = 0; u < kPF; ++u) {
+  for (int u = 0; u < kRing; ++u) {
     if (u < nseg) {
-      wa[u] = ldg_stream(w0 + 64 * u);
-      wb[u] = ldg_stream(w1 + 64 * u);
+      cp_async16(ring_s + (uint32_t)(u * 64) * 16u, w0 + 64 * u);
+      cp_async16(ring_s + (uint32_t)(u * 64 + 32) * 16u, w1 + 64 * u);
+    }
+    cp_async_commit();
+  }
+  Scale sa[kPFS], sb[kPFS];
+#pragma unroll
+  for (int u = 0; u < kPFS; ++u) {
+    if (u < nseg) {
       sa[u] = load_scale<FMT>(p, sr0, seg_lo + s_lo + u, t);
       sb[u] = load_scale<FMT>(p, sr1, seg_lo + s_lo + u, t);
     }
   }
 
-  for (int s0 = 0; s0 < nseg; s0 += kPF) {
+  // ---- previous kernel done: its outputs (our activations) are visible ------
+  pdl_wait();
+  // ---- stage the activation slice, permuted and swizzled -------------------
+  for (int i = threadIdx.x; i < M * nchunk; i += kWarps * 32) {
+    const int m = i / nchunk, c = i - m * nchunk;
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * p.K + k0 + 8 * c));
+    xs[m * p.ncp + swz(c)] = perm_x<FMT>(u);
+  }
+  __syncthreads();
+
+  float acc[MT][4];
 #pragma unroll
-    for (int u = 0; u < kPF; ++u) {
+  for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  for (int s0 = 0; s0 < nseg; s0 += kRing) {
+#pragma unroll
+    for (int u = 0; u < kRing; ++u) {
       const int s = s0 + u;
       if (s < nseg) {
+        cp_async_wait<kRing - 1>();
+        const uint4 wa = ring[u * 64];
+        const uint4 wb = ring[u * 64 + 32];
+        const int sn = s + kRing;
+        if (sn < nseg) {
+          cp_async16(ring_s + (uint32_t)(u * 64) * 16u, w0 + 64 * sn);
+          cp_async16(ring_s + (uint32_t)(u * 64 + 32) * 16u, w1 + 64 * sn);
+        }
+        cp_async_commit();
+        const int us = u % kPFS;
+        const Scale s_a = sa[us], s_b = sb[us];
+        if (s + kPFS < nseg) {
+          sa[us] = load_scale<FMT>(p, sr0, seg_lo + s_lo + s + kPFS, t);
+          sb[us] = load_scale<FMT>(p, sr1, seg_lo + s_lo + s + kPFS, t);
+        }
         const int cbase = (s_lo + s) * (Tr::KSEG / 8) + t * Tr::CPL;
 #pragma unroll
         for (int j = 0; j < Tr::CPL; ++j) {
           uint32_t ag[4], ah[4];
-          decode_chunk<FMT>(wa[u], sa[u], j, ag);
-          decode_chunk<FMT>(wb[u], sb[u], j, ah);
+          decode_chunk<FMT>(wa, s_a, j, ag);
+          decode_chunk<FMT>(wb, s_b, j, ah);
           const int c = swz(cbase + j);
           {
             const uint4 xf = xr0[c];
@@ -233,16 +266,10 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
             mma_bf16(acc[1], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
           }
         }
-        const int sn = s + kPF;
-        if (sn < nseg) {
-          wa[u] = ldg_stream(w0 + 64 * sn);
-          wb[u] = ldg_stream(w1 + 64 * sn);
-          sa[u] = load_scale<FMT>(p, sr0, seg_lo + s_lo + sn, t);
-          sb[u] = load_scale<FMT>(p, sr1, seg_lo + s_lo + sn, t);
-        }
       }
     }
   }
+  cp_async_wait<0>();
 
   // ---- per-warp partials -> shared memory, reduce the k-split warps ---------
   {
@@ -338,12 +365,13 @@ qg_status launch_gemv_t(const GemvArgs& a0, cudaStream_t st, const char* name) {
     const int want = (FMT == F_FP8) ? 1 : 2;          // bank-conflict-free pitch (mod 8)
     while ((ncp & 7) != want) ++ncp;
     a.ncp = ncp;
-    return (size_t)a.M * ncp * 16 + (size_t)(kWarps * 16 + 16 * rg) * MT * 8 * 4;
+    return (size_t)kWarps * kRing * 64 * 16 + (size_t)a.M * ncp * 16 +
+           (size_t)(kWarps * 16 + 16 * rg) * MT * 8 * 4;
   };
   // K split over a cluster only when the activation slice does not fit
   int ks = 1;
-  while (smem_for(ks, 8) > 160 * 1024 && ks < 8) ks *= 2;
-  if (smem_for(ks, 8) > 200 * 1024)
+  while (smem_for(ks, 8) > 200 * 1024 && ks < 8) ks *= 2;
+  if (smem_for(ks, 8) > 220 * 1024)
     return set_error(QG_ERR_UNSUPPORTED_SHAPE, "%s: activation slice too large for one CTA", name);
   // rows per CTA: the fewest that keep every CTA resident in one wave
   const int cap_sm = sm_count();
