@@ -1,0 +1,346 @@
+// W4A8 grouped (MoE) GEMM on the 5th-generation tensor cores.
+//
+// Semantics (Production-Ready W4A8): y[r,n] = a_s[r] * sum_k e4m3(a[r,k]) *
+// q[n,k] * s[n, k/128], every product exact, fp32 accumulation, one bf16
+// rounding at the store.  To keep that exactness on a 16-bit MMA, the
+// weights are formed as fp16(q * s * 2^e_n): q is a 4-bit integer and s a
+// bf16 (8 significant bits), so q * s has at most 11 significant bits and is
+// exact in fp16; the per-row power of two e_n puts the row's largest scale in
+// [2^11, 2^12) so every product stays inside fp16's range, and the epilogue
+// multiplies by 2^-e_n exactly.  E4M3 activations are exact in fp16 too.
+//
+// Orientation and pipeline follow the W4A16 prefill kernel (gemm_tc.cu):
+//   A operand  = weights (128 channels x 16 k), dequantized by 8 warps from a
+//                TMA-staged packed INT4 tile into tensor memory (tcgen05.st);
+//   B operand  = activations (256 rows x 16 k): the E4M3 tile arrives by TMA
+//                and 4 converter warps expand it to fp16 in the 128-byte
+//                swizzled K-major layout (cvt.rn.f16x2.e4m3x2);
+//   D          = fp32 accumulator in TMEM (128 lanes x 256 columns).
+// One CTA computes a 256-row x 128-channel tile of one expert; the tile is
+// located on the device from expert_off, so launching needs no host sync.
+#include <algorithm>
+#include <cmath>
+
+#include "dequant.cuh"
+#include "tc_common.cuh"
+
+namespace qg {
+
+bool make_u8_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols);
+
+namespace {
+
+constexpr int mTW = 128;                 // weight rows per tile (MMA M)
+constexpr int mTT = 256;                 // activation rows per tile (MMA N)
+constexpr int mBK = 64;                  // k per stage
+constexpr int mStages = 4;
+constexpr int mDeqWarps = 8;
+constexpr int mCvtWarps = 4;
+constexpr int mThreads = (2 + mDeqWarps + mCvtWarps) * 32;
+constexpr int mBStage = mTT * mBK * 2;   // 32 KB fp16 activations (swizzled)
+constexpr int mActStage = mTT * mBK;     // 16 KB E4M3 activations (TMA)
+constexpr int mWStage = mTW * mBK / 2;   // 4 KB packed INT4 weights (TMA)
+constexpr uint32_t mTmemCols = 512;
+constexpr uint32_t mACol0 = 256;
+constexpr uint32_t mACols = mBK / 2;
+constexpr uint32_t mDrainCap = 1u << 21;
+
+struct MoeTcArgs {
+  const float* a_s;
+  const int32_t* off;
+  const uint16_t* ws;
+  uint16_t* y;
+  int R, E, N, K;
+  int tiles_w;
+  unsigned int* err;
+  uint32_t cap;
+};
+
+struct __align__(8) MoeTail {
+  uint64_t full[mStages];
+  uint64_t a_full[mStages];
+  uint64_t b_full[mStages];
+  uint64_t empty[mStages];
+  uint64_t acc_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+QG_DEVICE uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+QG_DEVICE uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// two E4M3 codes (low byte first) -> f16x2 (low half first), exact
+QG_DEVICE uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t d;
+  const uint16_t in = (uint16_t)two;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(in));
+  return d;
+}
+QG_DEVICE uint16_t f32_to_f16_bits(float f) {
+  uint16_t r;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+// INT4 nibbles -> fp16 pairs (k_i, k_{i+4}) = q * scale: (1024 + (nib ^ 8)) - 1032
+// is the exact integer q, one fp16 multiply forms the exact product.
+QG_DEVICE void int4x8_kperm_f16(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {
+  p[0] = lop3<kLutAndXor>(v, 0x000F000Fu, 0x64086408u);
+  p[1] = lop3<kLutAndXor>(v >> 4, 0x000F000Fu, 0x64086408u);
+  p[2] = lop3<kLutAndXor>(v >> 8, 0x000F000Fu, 0x64086408u);
+  p[3] = lop3<kLutAndXor>(v >> 12, 0x000F000Fu, 0x64086408u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = f16x2_mul(f16x2_sub(p[i], 0x64086408u), s2);
+}
+
+// Instruction descriptor, kind::f16 with fp16 A and B, fp32 D, both K-major.
+QG_HOST_DEVICE uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__global__ void __launch_bounds__(mThreads, 1)
+moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
+                   const MoeTcArgs p) {
+  // ---- tile of this CTA: expert, weight tile, row tile (before any setup) ----
+  int tile = blockIdx.x, e = -1, r0 = 0, r_end = 0, wt = 0;
+  for (int i = 0; i < p.E; ++i) {
+    const int a = __ldg(p.off + i), b = __ldg(p.off + i + 1);
+    const int nt = b > a ? (b - a + mTT - 1) / mTT : 0;
+    const int cnt = nt * p.tiles_w;
+    if (tile < cnt) {
+      e = i;
+      wt = tile / nt;
+      r0 = a + (tile - wt * nt) * mTT;
+      r_end = b;
+      break;
+    }
+    tile -= cnt;
+  }
+  if (e < 0) return;
+  const int n0 = wt * mTW;
+  const int nslab = p.K / mBK;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* bs = smem;                                    // [mStages][32 KB] fp16, swizzled
+  uint8_t* as8 = bs + mStages * mBStage;                 // [mStages][16 KB] E4M3
+  uint8_t* wsm = as8 + mStages * mActStage;              // [mStages][4 KB] INT4
+  MoeTail* tl = reinterpret_cast<MoeTail*>(wsm + mStages * mWStage);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < mStages; ++s) {
+      mbar_init(&tl->full[s], 1);
+      mbar_init(&tl->a_full[s], mDeqWarps * 32);
+      mbar_init(&tl->b_full[s], mCvtWarps * 32);
+      mbar_init(&tl->empty[s], 1);
+    }
+    mbar_init(&tl->acc_full, 1);
+    mbar_init(&tl->drain, 1);
+    tl->abort = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_w);
+  }
+  if (warp == 1) tmem_alloc(&tl->tmem_base, mTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tl->tmem_base;
+  volatile int* abort = &tl->abort;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int s = 0; s < nslab; ++s) {
+        const int st = s % mStages, r = s / mStages;
+        if (r > 0 && !mbar_wait(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+        mbar_arrive_expect_tx(&tl->full[st], mActStage + mWStage);
+        tma_load_2d(as8 + st * mActStage, &tmap_a, &tl->full[st], s * mBK, r0);
+        tma_load_2d(wsm + st * mWStage, &tmap_w, &tl->full[st], s * (mBK / 2), e * p.N + n0);
+        issued = s + 1;
+      }
+      if (*abort) {
+        for (int s = max(0, issued - mStages); s < issued; ++s)
+          mbar_wait(&tl->full[s % mStages], (s / mStages) & 1, mDrainCap, abort, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(mTW, mTT);
+      bool any = false;
+      for (int s = 0; s < nslab; ++s) {
+        const int st = s % mStages, r = s / mStages;
+        if (!mbar_wait(&tl->a_full[st], r & 1, p.cap, abort, p.err)) break;
+        if (!mbar_wait(&tl->b_full[st], r & 1, p.cap, abort, p.err)) break;
+        tc_fence_after();
+        const uint64_t bdesc = sw128_kmajor_desc(smem_addr(bs + st * mBStage));
+#pragma unroll
+        for (int j = 0; j < mBK / 16; ++j)
+          tc_mma_ts(tmem, tmem + mACol0 + st * mACols + 8 * j, bdesc + 2 * j, idesc, (s | j) != 0);
+        tc_commit(&tl->empty[st]);
+        any = true;
+      }
+      if (!*abort) {
+        tc_commit(&tl->acc_full);
+      } else if (any) {
+        tc_commit(&tl->drain);
+        mbar_wait(&tl->drain, 0, mDrainCap, abort, nullptr);
+      }
+    }
+  } else if (warp >= 2 + mDeqWarps) {
+    // ---------------- converters: E4M3 tile -> fp16 swizzled tile ----------------
+    const int ct = threadIdx.x - (2 + mDeqWarps) * 32;    // 0..127: rows ct and ct + 128
+    for (int s = 0; s < nslab; ++s) {
+      const int st = s % mStages, r = s / mStages;
+      if (!mbar_wait_warp(&tl->full[st], r & 1, p.cap, abort, p.err)) break;
+      if (r > 0 && !mbar_wait_warp(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int row = ct + 128 * hr;
+        const uint8_t* src = as8 + st * mActStage + row * mBK;
+        uint8_t* dst = bs + st * mBStage + row * 128;
+        const int sw = row & 7;
+        // chunk order per row staggered to spread the 64-byte-pitch reads over the banks
+        const int f = (0x22331100 >> (4 * sw)) & 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = (i + f) & 3;
+          const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * c);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t h[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            h[2 * j] = e4m3x2_to_f16x2(w[j] & 0xFFFFu);
+            h[2 * j + 1] = e4m3x2_to_f16x2(w[j] >> 16);
+          }
+          *reinterpret_cast<uint4*>(dst + 16 * ((2 * c) ^ sw)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(dst + 16 * ((2 * c + 1) ^ sw)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
+      mbar_arrive(&tl->b_full[st]);
+    }
+  } else {
+    // ---------------- dequant producers, then the epilogue ----------------
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int row = 32 * q + lane;
+    const int n = min(n0 + row, p.N - 1);
+    const int ng = p.K / 128;
+    const uint16_t* srow = p.ws + ((size_t)e * p.N + n) * ng;
+    // per-row power of two: the row's largest scale lands in [2^11, 2^12)
+    float smax = 0.f;
+    for (int i = 0; i < ng; ++i) smax = fmaxf(smax, fabsf(bf16_bits_to_f32(__ldg(srow + i))));
+    int ex = 0;
+    if (smax > 0.f) {
+      int e2;
+      frexpf(smax, &e2);                       // smax = m * 2^e2, m in [0.5, 1)
+      ex = min(max(12 - e2, -100), 100);
+    }
+    const float up = ldexpf(1.f, ex), down = ldexpf(1.f, -ex);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + mACol0 + 16 * h;
+
+    auto decode = [&](int s, uint32_t (&out)[16]) -> bool {
+      const int st = s % mStages;
+      if (!mbar_wait_warp(&tl->full[st], (s / mStages) & 1, p.cap, abort, p.err)) return false;
+      const uint4 w4 = *reinterpret_cast<const uint4*>(wsm + st * mWStage + row * (mBK / 2) + 16 * h);
+      const float sg = bf16_bits_to_f32(__ldg(srow + (s * mBK) / 128)) * up;
+      const uint32_t s2 = bf16x2_splat(f32_to_f16_bits(sg));
+      const uint32_t v[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t pq[4], nat[4];
+        int4x8_kperm_f16(v[j], s2, pq);
+        kperm4_to_natural(pq, nat);
+        out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
+        out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
+      }
+      return true;
+    };
+    auto publish = [&](int s, const uint32_t (&cur)[16], uint32_t (&nxt)[16], bool& ok_next) -> bool {
+      const int st = s % mStages, r = s / mStages;
+      if (r > 0) {
+        if (!mbar_wait_warp(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) return false;
+        tc_fence_after();
+      }
+      tmem_st16(lane_base + st * mACols, cur);
+      ok_next = s + 1 < nslab ? decode(s + 1, nxt) : false;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&tl->a_full[st]);
+      return true;
+    };
+    uint32_t bufA[16], bufB[16];
+    bool okA = nslab > 0 && decode(0, bufA), okB = false;
+    for (int s = 0; s < nslab; s += 2) {
+      if (!okA || !publish(s, bufA, bufB, okB)) break;
+      if (s + 1 >= nslab || !okB || !publish(s + 1, bufB, bufA, okA)) break;
+    }
+
+    // epilogue: rows of this tile x this thread's channel
+    if (mbar_wait_warp(&tl->acc_full, 0, p.cap, abort, p.err)) {
+      tc_fence_after();
+      const int nn = n0 + row;
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 128 * h + 32 * i, v);
+        tmem_wait_ld();
+        const int mb = r0 + 128 * h + 32 * i;
+        if (nn < p.N) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int m = mb + c;
+            if (m < r_end) {
+              const float val = __uint_as_float(v[c]) * down * __ldg(p.a_s + m);
+              p.y[(size_t)m * p.N + nn] = f32_to_bf16_bits(val);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, mTmemCols);
+  }
+}
+
+}  // namespace
+
+qg_status moe_w4a8_tc(const uint8_t* a_e4m3, const float* a_s, const int32_t* expert_off, const uint8_t* w_q,
+                      const uint16_t* w_s, uint16_t* y, int R, int E, int N, int K, cudaStream_t st) {
+  CUtensorMap tmap_a, tmap_w;
+  if (!make_u8_tmap(&tmap_a, a_e4m3, R, K, mTT, mBK))
+    return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped: cannot encode the activation tensor map");
+  if (!make_u8_tmap(&tmap_w, w_q, E * N, K / 2, mTW, mBK / 2))
+    return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped: cannot encode the weight tensor map");
+  unsigned int* err = device_error_word();
+  if (!err) return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped: no device error word");
+  MoeTcArgs a{};
+  a.a_s = a_s; a.off = expert_off; a.ws = w_s; a.y = y;
+  a.R = R; a.E = E; a.N = N; a.K = K;
+  a.tiles_w = (N + mTW - 1) / mTW;
+  a.err = err;
+  a.cap = wait_limit();
+  const int smem = mStages * (mBStage + mActStage + mWStage) + (int)sizeof(MoeTail) + 1024;
+  if (!ensure_smem(moe_w4a8_tc_kernel, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped: smem attribute");
+  const long long tiles = ((long long)(R + mTT - 1) / mTT + E) * a.tiles_w;
+  moe_w4a8_tc_kernel<<<(unsigned)tiles, mThreads, smem, st>>>(tmap_a, tmap_w, a);
+  return check_launch("qgemm_w4a8_grouped (tcgen05)");
+}
+
+}  // namespace qg

@@ -46,6 +46,22 @@ def test_grouped_small(qg, sizes, N, K):
         check_gemm(y, ref, "grouped %s" % sizes)
 
 
+@pytest.mark.parametrize("sizes,N,K", [([300, 0, 700, 50, 1000], 384, 512), ([512], 272, 1024),
+                                       ([0, 513, 0, 255, 257], 128, 384), ([2048, 2048], 1024, 2048)])
+def test_grouped_tensor_core_path(qg, sizes, N, K):
+    """R >= 512 takes the tcgen05 kernel: uneven experts, empty experts, partial
+    row tiles and a partial channel tile."""
+    E = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R = int(off[-1])
+    x = inputs.activations_bf16(R, K, seed=R + K + 1)
+    a8, a_s = OQ.quant_fp8_block(x, K)
+    wq, ws = expert_weights(E, N, K, seed=90)
+    y = grouped(qg, a8, a_s[:, 0], off, wq, ws, N, K)
+    ref = OF.bf16_decode(OG.to_bf16(OG.w4a8_grouped_f64(a8, a_s[:, 0], off, wq, ws, 128)))
+    check_gemm(y, ref, "grouped tc %s" % sizes)
+
+
 def test_grouped_config_size_sampled(qg):
     """T=4096 top-2 over E=8: R=8192 rows, gate/up N=2*14336, K=4096; parity on
     a seeded sample of 24 rows per expert (full output is checked for
