@@ -10,7 +10,8 @@
 // multiplies by 2^-e_n exactly.  E4M3 activations are exact in fp16 too.
 //
 // Orientation and pipeline follow the W4A16 prefill kernel (gemm_tc.cu):
-//   A operand  = weights (128 channels x 16 k), dequantized by 8 warps from a
+//   A operand  = weights (128 channels x 16 k), dequantized by 16 warps (two
+//                sets taking alternate stages) from a
 //                TMA-staged packed INT4 tile into tensor memory (tcgen05.st);
 //   B operand  = activations (256 rows x 16 k): the E4M3 tile arrives by TMA
 //                and 4 converter warps expand it to fp16 in the 128-byte
@@ -34,7 +35,7 @@ constexpr int mTW = 128;                 // weight rows per tile (MMA M)
 constexpr int mTT = 256;                 // activation rows per tile (MMA N)
 constexpr int mBK = 64;                  // k per stage
 constexpr int mStages = 4;
-constexpr int mDeqWarps = 8;
+constexpr int mDeqWarps = 16;            // two sets of 8: even and odd slabs
 constexpr int mCvtWarps = 4;
 constexpr int mThreads = (2 + mDeqWarps + mCvtWarps) * 32;
 constexpr int mBStage = mTT * mBK * 2;   // 32 KB fp16 activations (swizzled)
@@ -139,7 +140,7 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < mStages; ++s) {
       mbar_init(&tl->full[s], 1);
-      mbar_init(&tl->a_full[s], mDeqWarps * 32);
+      mbar_init(&tl->a_full[s], (mDeqWarps / 2) * 32);   // one parity set per stage
       mbar_init(&tl->b_full[s], mCvtWarps * 32);
       mbar_init(&tl->empty[s], 1);
     }
@@ -233,14 +234,38 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     }
   } else {
     // ---------------- dequant producers, then the epilogue ----------------
-    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int q = warp & 3, h = ((warp - 2) >> 2) & 1, par = (warp - 2) >> 3;
     const int row = 32 * q + lane;
     const int n = min(n0 + row, p.N - 1);
     const int ng = p.K / 128;
     const uint16_t* srow = p.ws + ((size_t)e * p.N + n) * ng;
     // per-row power of two: the row's largest scale lands in [2^11, 2^12)
     float smax = 0.f;
-    for (int i = 0; i < ng; ++i) smax = fmaxf(smax, fabsf(bf16_bits_to_f32(__ldg(srow + i))));
+    {
+      int i = 0;
+      if ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0) {
+        for (; i + 64 <= ng; i += 64) {            // 8 independent 16-byte loads in flight
+          uint4 u[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) u[j] = __ldg(reinterpret_cast<const uint4*>(srow + i) + j);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              smax = fmaxf(smax, fmaxf(fabsf(bf16_lo_to_f32(w[c])), fabsf(bf16_hi_to_f32(w[c]))));
+          }
+        }
+        for (; i + 8 <= ng; i += 8) {
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(srow + i));
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            smax = fmaxf(smax, fmaxf(fabsf(bf16_lo_to_f32(w[c])), fabsf(bf16_hi_to_f32(w[c]))));
+        }
+      }
+      for (; i < ng; ++i) smax = fmaxf(smax, fabsf(bf16_bits_to_f32(__ldg(srow + i))));
+    }
     int ex = 0;
     if (smax > 0.f) {
       int e2;
@@ -250,13 +275,15 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     const float up = ldexpf(1.f, ex), down = ldexpf(1.f, -ex);
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + mACol0 + 16 * h;
 
-    auto decode = [&](int s, uint32_t (&out)[16]) -> bool {
-      const int st = s % mStages;
-      if (!mbar_wait_warp(&tl->full[st], (s / mStages) & 1, p.cap, abort, p.err)) return false;
+    uint16_t sc_next = par < nslab ? __ldg(srow + (par * mBK) / 128) : 0;
+    for (int s = par; s < nslab; s += 2) {
+      const int st = s % mStages, r = s / mStages;
+      const uint32_t s2 = bf16x2_splat(f32_to_f16_bits(bf16_bits_to_f32(sc_next) * up));
+      if (s + 2 < nslab) sc_next = __ldg(srow + ((s + 2) * mBK) / 128);
+      if (!mbar_wait_warp(&tl->full[st], r & 1, p.cap, abort, p.err)) break;
       const uint4 w4 = *reinterpret_cast<const uint4*>(wsm + st * mWStage + row * (mBK / 2) + 16 * h);
-      const float sg = bf16_bits_to_f32(__ldg(srow + (s * mBK) / 128)) * up;
-      const uint32_t s2 = bf16x2_splat(f32_to_f16_bits(sg));
       const uint32_t v[4] = {w4.x, w4.y, w4.z, w4.w};
+      uint32_t out[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         uint32_t pq[4], nat[4];
@@ -265,38 +292,27 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
         out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
         out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
       }
-      return true;
-    };
-    auto publish = [&](int s, const uint32_t (&cur)[16], uint32_t (&nxt)[16], bool& ok_next) -> bool {
-      const int st = s % mStages, r = s / mStages;
       if (r > 0) {
-        if (!mbar_wait_warp(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) return false;
+        if (!mbar_wait_warp(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
         tc_fence_after();
       }
-      tmem_st16(lane_base + st * mACols, cur);
-      ok_next = s + 1 < nslab ? decode(s + 1, nxt) : false;
+      tmem_st16(lane_base + st * mACols, out);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&tl->a_full[st]);
-      return true;
-    };
-    uint32_t bufA[16], bufB[16];
-    bool okA = nslab > 0 && decode(0, bufA), okB = false;
-    for (int s = 0; s < nslab; s += 2) {
-      if (!okA || !publish(s, bufA, bufB, okB)) break;
-      if (s + 1 >= nslab || !okB || !publish(s + 1, bufB, bufA, okA)) break;
     }
 
-    // epilogue: rows of this tile x this thread's channel
+    // epilogue: warp covers lane quarter q and 64 of the 256 row columns
+    const int cq = (warp - 2) >> 2;
     if (mbar_wait_warp(&tl->acc_full, 0, p.cap, abort, p.err)) {
       tc_fence_after();
       const int nn = n0 + row;
 #pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 2; ++i) {
         uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 128 * h + 32 * i, v);
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 64 * cq + 32 * i, v);
         tmem_wait_ld();
-        const int mb = r0 + 128 * h + 32 * i;
+        const int mb = r0 + 64 * cq + 32 * i;
         if (nn < p.N) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
