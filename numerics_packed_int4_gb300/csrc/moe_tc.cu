@@ -37,7 +37,8 @@ constexpr int mBK = 64;                  // k per stage
 constexpr int mStages = 4;
 constexpr int mDeqWarps = 16;            // two sets of 8: even and odd slabs
 constexpr int mCvtWarps = 4;
-constexpr int mThreads = (2 + mDeqWarps + mCvtWarps) * 32;
+constexpr int mSchedWarp = 2 + mDeqWarps + mCvtWarps;   // scheduler warp (see the prefill kernel)
+constexpr int mThreads = (mSchedWarp + 1) * 32;
 constexpr int mBStage = mTT * mBK * 2;   // 32 KB fp16 activations (swizzled)
 constexpr int mActStage = mTT * mBK;     // 16 KB E4M3 activations (TMA)
 constexpr int mWStage = mTW * mBK / 2;   // 4 KB packed INT4 weights (TMA)
@@ -66,6 +67,7 @@ struct __align__(8) MoeTail {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  unsigned int ready;                    // k-slabs whose operands are in place
 };
 
 QG_DEVICE uint32_t f16x2_sub(uint32_t a, uint32_t b) {
@@ -140,13 +142,14 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < mStages; ++s) {
       mbar_init(&tl->full[s], 1);
-      mbar_init(&tl->a_full[s], (mDeqWarps / 2) * 32);   // one parity set per stage
-      mbar_init(&tl->b_full[s], mCvtWarps * 32);
+      mbar_init(&tl->a_full[s], mDeqWarps / 2);    // one parity set per stage, one arrival per warp
+      mbar_init(&tl->b_full[s], mCvtWarps);
       mbar_init(&tl->empty[s], 1);
     }
     mbar_init(&tl->acc_full, 1);
     mbar_init(&tl->drain, 1);
     tl->abort = 0;
+    tl->ready = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_w);
@@ -180,10 +183,10 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     if (lane == 0) {
       const uint32_t idesc = idesc_f16_f32(mTW, mTT);
       bool any = false;
+      unsigned int ready = 0;
       for (int s = 0; s < nslab; ++s) {
-        const int st = s % mStages, r = s / mStages;
-        if (!mbar_wait(&tl->a_full[st], r & 1, p.cap, abort, p.err)) break;
-        if (!mbar_wait(&tl->b_full[st], r & 1, p.cap, abort, p.err)) break;
+        const int st = s % mStages;
+        if (!wait_count(&tl->ready, (unsigned)s, ready, p.cap * 4, abort, p.err)) break;
         tc_fence_after();
         const uint64_t bdesc = sw128_kmajor_desc(smem_addr(bs + st * mBStage));
 #pragma unroll
@@ -197,6 +200,16 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       } else if (any) {
         tc_commit(&tl->drain);
         mbar_wait(&tl->drain, 0, mDrainCap, abort, nullptr);
+      }
+    }
+  } else if (warp == mSchedWarp) {
+    // ---------------- scheduler: publishes how many k-slabs are ready ----------------
+    if (lane == 0) {
+      for (int s = 0; s < nslab; ++s) {
+        const int st = s % mStages, r = s / mStages;
+        if (!mbar_wait(&tl->a_full[st], r & 1, p.cap, abort, p.err)) break;
+        if (!mbar_wait(&tl->b_full[st], r & 1, p.cap, abort, p.err)) break;
+        publish_count(&tl->ready, (unsigned)(s + 1));
       }
     }
   } else if (warp >= 2 + mDeqWarps) {
@@ -230,7 +243,7 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
         }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
-      mbar_arrive(&tl->b_full[st]);
+      mbar_arrive_warp(&tl->b_full[st]);
     }
   } else {
     // ---------------- dequant producers, then the epilogue ----------------
@@ -299,7 +312,7 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       tmem_st16(lane_base + st * mACols, out);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&tl->a_full[st]);
+      mbar_arrive_warp(&tl->a_full[st]);
     }
 
     // epilogue: warp covers lane quarter q and 64 of the 256 row columns

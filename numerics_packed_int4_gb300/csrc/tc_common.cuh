@@ -19,6 +19,12 @@ QG_DEVICE void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.clu
 QG_DEVICE void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
 }
+// One arrival for the whole warp: the warp's lanes synchronise, then lane 0
+// arrives (barriers fed this way are initialised with one count per warp).
+QG_DEVICE void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 QG_DEVICE void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
                :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
@@ -61,6 +67,32 @@ QG_DEVICE bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t cap, vola
     if (err) atomicExch(err, DEV_ERR_TIMEOUT);
   }
   __syncwarp();
+  return false;
+}
+
+// ---- ready counter between a scheduler thread and the MMA issuer ----------
+// The MMA issuer keeps its own memory traffic to a minimum: a scheduler thread
+// does the mbarrier waits for it and publishes how many k-slabs are ready.
+// Every shared-memory operation of the issuing thread stalls behind the MMAs
+// it has queued, so the issuer re-reads the counter only when its cached copy
+// runs out.
+QG_DEVICE void publish_count(unsigned int* ctr, unsigned int v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" :: "r"(smem_addr(ctr)), "r"(v) : "memory");
+}
+// true once *ctr > idx; 'cached' holds the last value read.  Bounded like
+// mbar_wait (the cap counts reads, each at least a shared-memory latency).
+QG_DEVICE bool wait_count(unsigned int* ctr, unsigned int idx, unsigned int& cached, uint32_t cap,
+                          volatile int* abort, unsigned int* err) {
+  if (cached > idx) return true;
+  for (uint32_t i = 0; i < cap; ++i) {
+    unsigned int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(ctr)) : "memory");
+    cached = v;
+    if (v > idx) return true;
+    if ((i & 63u) == 63u && *abort) return false;
+  }
+  *abort = 1;
+  if (err) atomicExch(err, DEV_ERR_TIMEOUT);
   return false;
 }
 
