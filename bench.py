@@ -38,6 +38,20 @@ FORMATS = ["int4", "fp8", "mxfp4", "nvfp4"]
 BYTES_PER_PARAM = {"int4": 0.5 + 2 / 128, "fp8": 1.0, "mxfp4": 0.5 + 1 / 32, "nvfp4": 0.5 + 1 / 16}
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# of each row's main kernel, from one ncu capture, with the launch it was taken
+# on and that launch's algorithmic bytes.  The summaries and the commands are
+# under profiles/.  An entry goes back to None whenever its kernel changes.
+PROFILED_TRAFFIC = {
+    "decode_m1": {"bytes": 30.32e6, "launch": "gemv_kernel INT4 M=1 N=14336 K=4096",
+                  "algorithmic_bytes": 30.30e6, "profile": "profiles/gemv_int4_m1_n14336_k4096.md"},
+    "prefill": {"bytes": 383.8e6, "launch": "w4a16_tc_kernel M=8192 N=14336 K=4096",
+                "algorithmic_bytes": 332.3e6, "profile": "profiles/prefill_w4a16_tc_m8192_n14336_k4096.md"},
+    "moe": {"bytes": 951.3e6, "launch": "moe_w4a8_tc_kernel gate/up R=8192 N=28672 K=4096",
+            "algorithmic_bytes": 987.9e6, "profile": "profiles/moe_w4a8_tc_t4096_e8.md"},
+}
+
+
 def gemv_bytes(fmt, M, N, K):
     """Algorithmic bytes: weights + scales, activations in, outputs out."""
     b = N * K * BYTES_PER_PARAM[fmt] + 2 * M * K + 2 * M * N
@@ -46,6 +60,19 @@ def gemv_bytes(fmt, M, N, K):
     if fmt == "nvfp4":
         b += 4
     return b
+
+
+def traffic_of(row):
+    t = PROFILED_TRAFFIC.get(row)
+    return None if t is None else t["bytes"]
+
+
+def traffic_info(row):
+    t = PROFILED_TRAFFIC.get(row)
+    if t is None:
+        return {}
+    return {"traffic_launch": t["launch"], "traffic_algorithmic_bytes": t["algorithmic_bytes"],
+            "traffic_profile": t["profile"]}
 
 
 def load_peaks():
@@ -499,13 +526,13 @@ def run_ours(args):
             row_out[r] = {"ms": ms, "GB/s": gbs, "launches": wl.launches[r],
                           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                                        "frac": gbs / peaks["hbm"],
-                                       "traffic": None}}
+                                       "traffic": traffic_of(r), **traffic_info(r)}}
         else:
             tf = wl.flops[r] / (ms * 1e-3) / 1e12
             peak = peaks["bf16"]
             row_out[r] = {"ms": ms, "TFLOP/s": tf, "launches": wl.launches[r],
                           "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
-                                       "frac": tf / peak, "traffic": None}}
+                                       "frac": tf / peak, "traffic": traffic_of(r), **traffic_info(r)}}
     dominant = max(rows, key=lambda r: seg_ms_max[r])
     value = aggregate(world * wl.bytes.get("decode_m1", 0.0), seg_ms_max.get("decode_m1", 1.0) * 1e-3) / 1e9
 

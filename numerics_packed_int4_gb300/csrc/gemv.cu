@@ -3,17 +3,24 @@
 //
 // Design ("Your 3090 Isn't Missing Anything...", section 4.3: at M = 1 DRAM
 // bandwidth sets the time; the dequant must stay off the critical path):
-//   * A CTA owns 128 output channels (8 warps x one 16-row mma group) and a
-//     slice of K; the K slices of one row block form a thread-block cluster
-//     (1..8 CTAs) whose partial sums are reduced through distributed shared
-//     memory, so no global scratch and no atomics are needed.
-//   * Each lane streams 16-byte weight words of two rows (g and g+8 of its
-//     mma group) straight from HBM with L1-bypassing loads, keeping a ring of
-//     PF segments in flight, and decodes them in registers into mma.sync
-//     m16n8k16 A fragments (weights are the M=16 side, activations the N=8
-//     side, so one mma covers 256 weights).
+//   * A CTA of 8 warps owns rg 16-row groups (16 * rg output channels); the
+//     kWarps / rg warps of a row group take interleaved K segments and their
+//     partial sums are reduced through shared memory.  The grid is sized to
+//     a single wave.  When the activation slice would not fit in shared
+//     memory, the K range is split over a thread-block cluster (1..8 CTAs)
+//     reduced through distributed shared memory -- no global scratch, no
+//     atomics, deterministic.
+//   * Each warp streams the packed words of its two rows per lane (g and g+8
+//     of the mma group) through a private kRing-deep cp.async.cg ring in
+//     shared memory (16-byte, L1-bypassing), and decodes them in registers
+//     into mma.sync m16n8k16 A fragments (weights are the M = 16 side,
+//     activations the N = 8 side, so one mma covers 256 weights).
 //   * The activation slice is staged once per CTA in shared memory with the k
 //     order permuted to match the decode's pair order and a bank swizzle.
+//   * Programmatic dependent launch: a CTA triggers its dependent at once,
+//     issues its weight prologue, and waits for the previous kernel only
+//     before it reads X (weights and scales must not be the previous decode
+//     kernel's output -- stated in the header).
 //   * fp32 accumulation; the FP8 channel scale / NVFP4 global scale is
 //     applied to the reduced row; one bf16 rounding at the store.
 #include <algorithm>

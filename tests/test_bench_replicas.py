@@ -1,0 +1,61 @@
+"""Host logic of bench.py's N > 1 path on CPU: two gloo ranks (replicas only --
+the path has no data exchange), barrier, max-over-ranks timing and the
+whole-job aggregate."""
+
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    import torch.distributed as dist
+    r, w, lr = bench.dist_env()
+    assert (r, w, lr) == (rank, world, rank)
+    bench.dist_init(w, "gloo")
+    try:
+        bench.dist_barrier(w)
+        # each replica processed the same units; rank 1 was slower
+        elapsed = 2.0 if rank == 1 else 1.0
+        slowest = bench.dist_max(elapsed, w)
+        out[rank] = (slowest, bench.aggregate(w * 100.0, slowest))
+        bench.dist_barrier(w)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_replicas_take_the_slowest_time():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        procs = [ctx.Process(target=_rank, args=(r, world, port, out)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=120)
+        codes = [p.exitcode for p in procs]
+        if any(c is None for c in codes):
+            for p in procs:
+                p.kill()
+            pytest.fail("a gloo rank did not finish")
+        assert codes == [0, 0]
+        res = dict(out)
+    # max over ranks, and units of all ranks over that time
+    assert res[0] == res[1] == (2.0, 100.0)
+
+
+def test_single_process_defaults():
+    import bench
+    assert bench.dist_max(3.5, 1) == 3.5
+    assert bench.aggregate(10.0, 4.0) == 2.5
