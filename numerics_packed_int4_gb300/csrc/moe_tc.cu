@@ -11,12 +11,16 @@
 //
 // Orientation and pipeline follow the W4A16 prefill kernel (gemm_tc.cu):
 //   A operand  = weights (128 channels x 16 k), dequantized by 16 warps (two
-//                sets taking alternate stages) from a
-//                TMA-staged packed INT4 tile into tensor memory (tcgen05.st);
-//   B operand  = activations (256 rows x 16 k): the E4M3 tile arrives by TMA
-//                and 4 converter warps expand it to fp16 in the 128-byte
-//                swizzled K-major layout (cvt.rn.f16x2.e4m3x2);
-//   D          = fp32 accumulator in TMEM (128 lanes x 256 columns).
+//                sets taking alternate k-slabs) from a TMA-staged packed INT4
+//                slab (8-stage ring) into one of 8 tensor-memory slots;
+//   B operand  = activations (256 rows x 16 k): the E4M3 slab arrives by TMA
+//                in its own 4-stage ring; 4 converter warps expand it to fp16
+//                (cvt.rn.f16x2.e4m3x2) into the 128-byte swizzled K-major
+//                layout of a second 4-stage ring, which the MMAs read;
+//   D          = fp32 accumulator in TMEM (128 lanes x 256 columns);
+//   a scheduler warp waits for each slab's operands and publishes a ready
+//   count; the MMA issuer re-reads it only when its cached copy runs out and
+//   commits once per slab (freeing the A slot and the fp16 stage).
 // One CTA computes a 256-row x 128-channel tile of one expert; the tile is
 // located on the device from expert_off, so launching needs no host sync.
 #include <algorithm>
@@ -34,13 +38,17 @@ namespace {
 constexpr int mTW = 128;                 // weight rows per tile (MMA M)
 constexpr int mTT = 256;                 // activation rows per tile (MMA N)
 constexpr int mBK = 64;                  // k per stage
-constexpr int mStages = 4;
+constexpr int mBStages = 4;              // fp16 activation stages (shared memory)
+constexpr int mXStages = 4;              // E4M3 activation stages (TMA)
+constexpr int mASlots = 8;               // TMEM A slots and packed-weight stages
 constexpr int mDeqWarps = 16;            // two sets of 8: even and odd slabs
 constexpr int mCvtWarps = 4;
-constexpr int mSchedWarp = 2 + mDeqWarps + mCvtWarps;   // scheduler warp (see the prefill kernel)
+constexpr int mDeq0 = 3;                 // first dequant warp
+constexpr int mCvt0 = mDeq0 + mDeqWarps; // first converter warp
+constexpr int mSchedWarp = mCvt0 + mCvtWarps;
 constexpr int mThreads = (mSchedWarp + 1) * 32;
 constexpr int mBStage = mTT * mBK * 2;   // 32 KB fp16 activations (swizzled)
-constexpr int mActStage = mTT * mBK;     // 16 KB E4M3 activations (TMA)
+constexpr int mXStage = mTT * mBK;       // 16 KB E4M3 activations (TMA)
 constexpr int mWStage = mTW * mBK / 2;   // 4 KB packed INT4 weights (TMA)
 constexpr uint32_t mTmemCols = 512;
 constexpr uint32_t mACol0 = 256;
@@ -59,10 +67,13 @@ struct MoeTcArgs {
 };
 
 struct __align__(8) MoeTail {
-  uint64_t full[mStages];
-  uint64_t a_full[mStages];
-  uint64_t b_full[mStages];
-  uint64_t empty[mStages];
+  uint64_t w_full[mASlots];
+  uint64_t w_empty[mASlots];
+  uint64_t a_full[mASlots];
+  uint64_t a_empty[mASlots];
+  uint64_t b_full[mBStages];
+  uint64_t x_full[mXStages];
+  uint64_t x_empty[mXStages];
   uint64_t acc_full;
   uint64_t drain;
   uint32_t tmem_base;
@@ -133,18 +144,23 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* bs = smem;                                    // [mStages][32 KB] fp16, swizzled
-  uint8_t* as8 = bs + mStages * mBStage;                 // [mStages][16 KB] E4M3
-  uint8_t* wsm = as8 + mStages * mActStage;              // [mStages][4 KB] INT4
-  MoeTail* tl = reinterpret_cast<MoeTail*>(wsm + mStages * mWStage);
+  uint8_t* bs = smem;                                    // [mBStages][32 KB] fp16, swizzled
+  uint8_t* as8 = bs + mBStages * mBStage;                // [mXStages][16 KB] E4M3
+  uint8_t* wsm = as8 + mXStages * mXStage;               // [mASlots][4 KB] INT4
+  MoeTail* tl = reinterpret_cast<MoeTail*>(wsm + mASlots * mWStage);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < mStages; ++s) {
-      mbar_init(&tl->full[s], 1);
-      mbar_init(&tl->a_full[s], mDeqWarps / 2);    // one parity set per stage, one arrival per warp
-      mbar_init(&tl->b_full[s], mCvtWarps);
-      mbar_init(&tl->empty[s], 1);
+    for (int s = 0; s < mASlots; ++s) {
+      mbar_init(&tl->w_full[s], 1);
+      mbar_init(&tl->w_empty[s], mDeqWarps / 2);   // the parity set that decoded it
+      mbar_init(&tl->a_full[s], mDeqWarps / 2);    // one arrival per warp of that set
+      mbar_init(&tl->a_empty[s], 1);               // tcgen05.commit of the slab's MMAs
+    }
+    for (int s = 0; s < mBStages; ++s) mbar_init(&tl->b_full[s], mCvtWarps);
+    for (int s = 0; s < mXStages; ++s) {
+      mbar_init(&tl->x_full[s], 1);
+      mbar_init(&tl->x_empty[s], mCvtWarps);
     }
     mbar_init(&tl->acc_full, 1);
     mbar_init(&tl->drain, 1);
@@ -162,20 +178,35 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
   volatile int* abort = &tl->abort;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: packed weights (runs ahead) ----------------
     if (lane == 0) {
       int issued = 0;
       for (int s = 0; s < nslab; ++s) {
-        const int st = s % mStages, r = s / mStages;
-        if (r > 0 && !mbar_wait(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
-        mbar_arrive_expect_tx(&tl->full[st], mActStage + mWStage);
-        tma_load_2d(as8 + st * mActStage, &tmap_a, &tl->full[st], s * mBK, r0);
-        tma_load_2d(wsm + st * mWStage, &tmap_w, &tl->full[st], s * (mBK / 2), e * p.N + n0);
+        const int st = s % mASlots, r = s / mASlots;
+        if (r > 0 && !mbar_wait(&tl->w_empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+        mbar_arrive_expect_tx(&tl->w_full[st], mWStage);
+        tma_load_2d(wsm + st * mWStage, &tmap_w, &tl->w_full[st], s * (mBK / 2), e * p.N + n0);
+        issued = s + 1;
+      }
+      if (*abort) {     // let every copy already issued land before the CTA exits
+        for (int s = max(0, issued - mASlots); s < issued; ++s)
+          mbar_wait(&tl->w_full[s % mASlots], (s / mASlots) & 1, mDrainCap, abort, nullptr);
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- TMA producer: E4M3 activations ----------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int s = 0; s < nslab; ++s) {
+        const int st = s % mXStages, r = s / mXStages;
+        if (r > 0 && !mbar_wait(&tl->x_empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+        mbar_arrive_expect_tx(&tl->x_full[st], mXStage);
+        tma_load_2d(as8 + st * mXStage, &tmap_a, &tl->x_full[st], s * mBK, r0);
         issued = s + 1;
       }
       if (*abort) {
-        for (int s = max(0, issued - mStages); s < issued; ++s)
-          mbar_wait(&tl->full[s % mStages], (s / mStages) & 1, mDrainCap, abort, nullptr);
+        for (int s = max(0, issued - mXStages); s < issued; ++s)
+          mbar_wait(&tl->x_full[s % mXStages], (s / mXStages) & 1, mDrainCap, abort, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -185,14 +216,14 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       bool any = false;
       unsigned int ready = 0;
       for (int s = 0; s < nslab; ++s) {
-        const int st = s % mStages;
+        const int sb = s % mBStages, sa = s % mASlots;
         if (!wait_count(&tl->ready, (unsigned)s, ready, p.cap * 4, abort, p.err)) break;
         tc_fence_after();
-        const uint64_t bdesc = sw128_kmajor_desc(smem_addr(bs + st * mBStage));
+        const uint64_t bdesc = sw128_kmajor_desc(smem_addr(bs + sb * mBStage));
 #pragma unroll
         for (int j = 0; j < mBK / 16; ++j)
-          tc_mma_ts(tmem, tmem + mACol0 + st * mACols + 8 * j, bdesc + 2 * j, idesc, (s | j) != 0);
-        tc_commit(&tl->empty[st]);
+          tc_mma_ts(tmem, tmem + mACol0 + sa * mACols + 8 * j, bdesc + 2 * j, idesc, (s | j) != 0);
+        tc_commit(&tl->a_empty[sa]);                   // frees the A slot and the fp16 stage
         any = true;
       }
       if (!*abort) {
@@ -206,48 +237,51 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
     // ---------------- scheduler: publishes how many k-slabs are ready ----------------
     if (lane == 0) {
       for (int s = 0; s < nslab; ++s) {
-        const int st = s % mStages, r = s / mStages;
-        if (!mbar_wait(&tl->a_full[st], r & 1, p.cap, abort, p.err)) break;
-        if (!mbar_wait(&tl->b_full[st], r & 1, p.cap, abort, p.err)) break;
+        if (!mbar_wait(&tl->a_full[s % mASlots], (s / mASlots) & 1, p.cap, abort, p.err)) break;
+        if (!mbar_wait(&tl->b_full[s % mBStages], (s / mBStages) & 1, p.cap, abort, p.err)) break;
         publish_count(&tl->ready, (unsigned)(s + 1));
       }
     }
-  } else if (warp >= 2 + mDeqWarps) {
-    // ---------------- converters: E4M3 tile -> fp16 swizzled tile ----------------
-    const int ct = threadIdx.x - (2 + mDeqWarps) * 32;    // 0..127: rows ct and ct + 128
+  } else if (warp >= mCvt0) {
+    // ---------------- converters: E4M3 stage -> fp16 swizzled stage ----------------
+    // Warp cw converts rows 64cw..64cw+63; per i < 8 a lane takes 16 bytes
+    // (chunk lane % 4) of row 64cw + 8i + lane / 4, so each shared-memory
+    // access covers 8 whole rows (conflict-free on both sides).
+    const int cw = warp - mCvt0, ch = lane & 3;
     for (int s = 0; s < nslab; ++s) {
-      const int st = s % mStages, r = s / mStages;
-      if (!mbar_wait_warp(&tl->full[st], r & 1, p.cap, abort, p.err)) break;
-      if (r > 0 && !mbar_wait_warp(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+      const int sx = s % mXStages, sb = s % mBStages, sp = s - mBStages;
+      if (!mbar_wait_warp(&tl->x_full[sx], (s / mXStages) & 1, p.cap, abort, p.err)) break;
+      uint4 cur[8];
+      const uint8_t* xsrc = as8 + sx * mXStage + (64 * cw + (lane >> 2)) * mBK + 16 * ch;
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int row = ct + 128 * hr;
-        const uint8_t* src = as8 + st * mActStage + row * mBK;
-        uint8_t* dst = bs + st * mBStage + row * 128;
-        const int sw = row & 7;
-        // chunk order per row staggered to spread the 64-byte-pitch reads over the banks
-        const int f = (0x22331100 >> (4 * sw)) & 3;
+      for (int i = 0; i < 8; ++i) cur[i] = *reinterpret_cast<const uint4*>(xsrc + 8 * i * mBK);
+      mbar_arrive_warp(&tl->x_empty[sx]);           // E4M3 stage read: the copy may refill it
+      // the fp16 stage last held slab sp: wait until that slab's MMAs completed
+      if (sp >= 0 && !mbar_wait_warp(&tl->a_empty[sp % mASlots], (sp / mASlots) & 1, p.cap, abort, p.err))
+        break;
+      uint8_t* stage = bs + sb * mBStage;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = (i + f) & 3;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * c);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          uint32_t h[8];
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t w[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
+        uint32_t h[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            h[2 * j] = e4m3x2_to_f16x2(w[j] & 0xFFFFu);
-            h[2 * j + 1] = e4m3x2_to_f16x2(w[j] >> 16);
-          }
-          *reinterpret_cast<uint4*>(dst + 16 * ((2 * c) ^ sw)) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(dst + 16 * ((2 * c + 1) ^ sw)) = make_uint4(h[4], h[5], h[6], h[7]);
+        for (int j = 0; j < 4; ++j) {
+          h[2 * j] = e4m3x2_to_f16x2(w[j] & 0xFFFFu);
+          h[2 * j + 1] = e4m3x2_to_f16x2(w[j] >> 16);
         }
+        const int rr = 64 * cw + 8 * i + (lane >> 2);
+        uint8_t* dst = stage + rr * 128;
+        const int sw = rr & 7;
+        *reinterpret_cast<uint4*>(dst + 16 * ((2 * ch) ^ sw)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(dst + 16 * ((2 * ch + 1) ^ sw)) = make_uint4(h[4], h[5], h[6], h[7]);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
-      mbar_arrive_warp(&tl->b_full[st]);
+      mbar_arrive_warp(&tl->b_full[sb]);
     }
   } else {
     // ---------------- dequant producers, then the epilogue ----------------
-    const int q = warp & 3, h = ((warp - 2) >> 2) & 1, par = (warp - 2) >> 3;
+    const int dw = warp - mDeq0;
+    const int q = warp & 3, h = (dw >> 2) & 1, par = dw >> 3;
     const int row = 32 * q + lane;
     const int n = min(n0 + row, p.N - 1);
     const int ng = p.K / 128;
@@ -290,11 +324,11 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
 
     uint16_t sc_next = par < nslab ? __ldg(srow + (par * mBK) / 128) : 0;
     for (int s = par; s < nslab; s += 2) {
-      const int st = s % mStages, r = s / mStages;
+      const int sa = s % mASlots, ra = s / mASlots;
       const uint32_t s2 = bf16x2_splat(f32_to_f16_bits(bf16_bits_to_f32(sc_next) * up));
       if (s + 2 < nslab) sc_next = __ldg(srow + ((s + 2) * mBK) / 128);
-      if (!mbar_wait_warp(&tl->full[st], r & 1, p.cap, abort, p.err)) break;
-      const uint4 w4 = *reinterpret_cast<const uint4*>(wsm + st * mWStage + row * (mBK / 2) + 16 * h);
+      if (!mbar_wait_warp(&tl->w_full[sa], ra & 1, p.cap, abort, p.err)) break;
+      const uint4 w4 = *reinterpret_cast<const uint4*>(wsm + sa * mWStage + row * (mBK / 2) + 16 * h);
       const uint32_t v[4] = {w4.x, w4.y, w4.z, w4.w};
       uint32_t out[16];
 #pragma unroll
@@ -305,18 +339,19 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
         out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
         out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
       }
-      if (r > 0) {
-        if (!mbar_wait_warp(&tl->empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+      mbar_arrive_warp(&tl->w_empty[sa]);           // packed slab decoded: its stage may be refilled
+      if (ra > 0) {
+        if (!mbar_wait_warp(&tl->a_empty[sa], (ra - 1) & 1, p.cap, abort, p.err)) break;
         tc_fence_after();
       }
-      tmem_st16(lane_base + st * mACols, out);
+      tmem_st16(lane_base + sa * mACols, out);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(&tl->a_full[st]);
+      mbar_arrive_warp(&tl->a_full[sa]);
     }
 
     // epilogue: warp covers lane quarter q and 64 of the 256 row columns
-    const int cq = (warp - 2) >> 2;
+    const int cq = dw >> 2;
     if (mbar_wait_warp(&tl->acc_full, 0, p.cap, abort, p.err)) {
       tc_fence_after();
       const int nn = n0 + row;
@@ -365,7 +400,7 @@ qg_status moe_w4a8_tc(const uint8_t* a_e4m3, const float* a_s, const int32_t* ex
   a.tiles_w = (N + mTW - 1) / mTW;
   a.err = err;
   a.cap = wait_limit();
-  const int smem = mStages * (mBStage + mActStage + mWStage) + (int)sizeof(MoeTail) + 1024;
+  const int smem = mBStages * mBStage + mXStages * mXStage + mASlots * mWStage + (int)sizeof(MoeTail) + 1024;
   if (!ensure_smem(moe_w4a8_tc_kernel, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped: smem attribute");
   const long long tiles = ((long long)(R + mTT - 1) / mTT + E) * a.tiles_w;
   moe_w4a8_tc_kernel<<<(unsigned)tiles, mThreads, smem, st>>>(tmap_a, tmap_w, a);
