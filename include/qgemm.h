@@ -215,6 +215,14 @@ QG_API const char* qg_last_error_string(void);
  * Intended for tests that exercise the timeout path.                        */
 QG_API void qg_set_wait_limit(uint32_t iterations);
 
+/* Failure-path self-test; the method has no counterpart.  Launches one CTA
+ * whose thread waits on an mbarrier that nothing arrives at, giving up after
+ * `polls` bounded polls (each suspends for at most about 1 us).  The kernel
+ * records a timeout in the device error word and returns -- it never traps --
+ * so the next qg_check_device_error reports QG_ERR_TIMEOUT and the context
+ * stays usable.  polls must be in 1 .. 1<<20 (else QG_ERR_INVALID_ARG).      */
+QG_API qg_status qg_selftest_wait_timeout(uint32_t polls, qg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -6,6 +6,7 @@
 #include <unordered_map>
 
 #include "qg_common.cuh"
+#include "tc_common.cuh"
 
 namespace {
 
@@ -90,12 +91,36 @@ bool ensure_smem_attr(const void* kernel, int bytes) {
 
 }  // namespace qg
 
+// A wait that nothing satisfies: the mbarrier expects one arrival that never
+// comes, so the bounded wait gives up, records the timeout and returns.
+__global__ void selftest_wait_kernel(uint32_t polls, unsigned int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    qg::mbar_init(&bar, 1);
+    abort = 0;
+    qg::mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) qg::mbar_wait(&bar, 0, polls, &abort, err);
+  __syncthreads();
+}
+
 extern "C" {
 
 const char* qg_last_error_string(void) { return g_msg; }
 
 void qg_set_wait_limit(uint32_t iterations) {
   g_wait_limit = iterations ? iterations : kDefaultWaitLimit;
+}
+
+qg_status qg_selftest_wait_timeout(uint32_t polls, qg_stream_t stream) {
+  if (polls < 1 || polls > (1u << 20))
+    return qg::set_error(QG_ERR_INVALID_ARG, "qg_selftest_wait_timeout: polls must be in 1 .. 1<<20");
+  unsigned int* err = qg::device_error_word();
+  if (!err) return qg::set_error(QG_ERR_CUDA, "qg_selftest_wait_timeout: no error word");
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(polls, err);
+  return qg::check_launch("qg_selftest_wait_timeout");
 }
 
 qg_status qg_check_device_error(qg_stream_t stream) {

@@ -231,12 +231,43 @@ __global__ void __launch_bounds__(kThreads) gather_fp8_kernel(
   if (threadIdx.x == 0) dst_s[r] = src_s[t];
 }
 
+// SiLU(g) * u in fp32 with the fast exponential and division intrinsics: the
+// value is quantized to E4M3 (3 mantissa bits) right after, so their few-ulp
+// error is far below the code spacing.  g -> -inf gives 1 + e^-g = inf and
+// g / inf = 0; g -> +inf gives g / 1.
 QG_DEVICE void swiglu8(const uint16_t* gu, int I, int c, float (&h)[8]) {
   float gv[8], uv[8];
   Load8<uint16_t>::run(gu + c * 8, gv);
   Load8<uint16_t>::run(gu + I + c * 8, uv);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) h[i] = __fmul_rn(__fdiv_rn(gv[i], 1.f + expf(-gv[i])), uv[i]);
+  for (int i = 0; i < 8; ++i) h[i] = __fdividef(gv[i], 1.f + __expf(-gv[i])) * uv[i];
+}
+
+// One row per CTA with the row's SwiGLU values kept in registers: one read of
+// gate/up, the per-row absmax, then the E4M3 codes (CPT chunks of 8 per thread).
+template <int CPT>
+__global__ void __launch_bounds__(kThreads) swiglu_quant_reg_kernel(
+    const uint16_t* __restrict__ gate_up, uint8_t* __restrict__ q, float* __restrict__ s, int I) {
+  __shared__ float red[kThreads / 32];
+  const uint16_t* gu = gate_up + (long long)blockIdx.x * 2 * I;
+  const int nc = I / 8;
+  float h[CPT][8];
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c = threadIdx.x + j * kThreads;
+    if (c < nc) {
+      swiglu8(gu, I, c, h[j]);
+      m = fmaxf(m, absmax8(h[j]));
+    }
+  }
+  const float sc = fp8_scale(cta_max(m, red));
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c = threadIdx.x + j * kThreads;
+    if (c < nc) *reinterpret_cast<uint2*>(q + (long long)blockIdx.x * I + c * 8) = fp8_codes8(h[j], sc);
+  }
+  if (threadIdx.x == 0) s[blockIdx.x] = sc;
 }
 
 __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(
@@ -435,7 +466,13 @@ qg_status qg_swiglu_quant_fp8(const uint16_t* gate_up, uint8_t* q, float* s, int
   QG_REQUIRE(I % 8 == 0, QG_ERR_UNSUPPORTED_SHAPE, "qg_swiglu_quant_fp8: I %% 8 != 0");
   QG_REQUIRE(aligned16(gate_up) && aligned16(q), QG_ERR_MISALIGNED, "qg_swiglu_quant_fp8: misaligned");
   if (R == 0) return QG_OK;
-  qg::swiglu_quant_kernel<<<R, qg::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(gate_up, q, s, I);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int cpt = (I / 8 + qg::kThreads - 1) / qg::kThreads;    // chunks per thread
+  if (cpt <= 1)      qg::swiglu_quant_reg_kernel<1><<<R, qg::kThreads, 0, st>>>(gate_up, q, s, I);
+  else if (cpt <= 2) qg::swiglu_quant_reg_kernel<2><<<R, qg::kThreads, 0, st>>>(gate_up, q, s, I);
+  else if (cpt <= 4) qg::swiglu_quant_reg_kernel<4><<<R, qg::kThreads, 0, st>>>(gate_up, q, s, I);
+  else if (cpt <= 8) qg::swiglu_quant_reg_kernel<8><<<R, qg::kThreads, 0, st>>>(gate_up, q, s, I);
+  else               qg::swiglu_quant_kernel<<<R, qg::kThreads, 0, st>>>(gate_up, q, s, I);
   return qg::check_launch("qg_swiglu_quant_fp8");
 }
 

@@ -38,6 +38,7 @@ SIGNATURES = {
     "qg_moe_combine": [P, P, P, P, I, I, I, I, P],
     "qg_dequant_weights": [I, P, P, I, P, I, I, P],
     "qg_check_device_error": [P],
+    "qg_selftest_wait_timeout": [U32, P],
 }
 
 _lib = None
@@ -164,6 +165,10 @@ def qg_dequant_weights(fmt, w, scales, g, w_out, N, K, stream=None):
 
 def qg_check_device_error(stream=None):
     return _call("qg_check_device_error", stream=stream)
+
+
+def qg_selftest_wait_timeout(polls, stream=None):
+    return _call("qg_selftest_wait_timeout", int(polls), stream=stream)
 
 
 def qg_set_wait_limit(iterations):
