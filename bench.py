@@ -47,7 +47,7 @@ PROFILED_TRAFFIC = {
                   "algorithmic_bytes": 30.30e6, "profile": "profiles/gemv_int4_m1_n14336_k4096.md"},
     "prefill": {"bytes": 383.8e6, "launch": "w4a16_tc_kernel M=8192 N=14336 K=4096",
                 "algorithmic_bytes": 332.3e6, "profile": "profiles/prefill_w4a16_tc_m8192_n14336_k4096.md"},
-    "moe": {"bytes": 951.3e6, "launch": "moe_w4a8_tc_kernel gate/up R=8192 N=28672 K=4096",
+    "moe": {"bytes": 953.4e6, "launch": "moe_w4a8_tc_kernel gate/up R=8192 N=28672 K=4096",
             "algorithmic_bytes": 987.9e6, "profile": "profiles/moe_w4a8_tc_t4096_e8.md"},
 }
 
@@ -140,7 +140,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except Exception:
@@ -149,7 +149,14 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def wait_ready(self, timeout=3.0):
+        """Block until the sampler has produced its first line (it takes a
+        moment to start), so that samples cover the timed region."""
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < timeout:
+            time.sleep(0.01)
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -159,10 +166,13 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen between t0 and t1
+        (perf_counter seconds; the timed region), all samples if not given."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = [ln for t, ln in self.lines if t0 is None or (t0 <= t <= t1 + 0.025)]
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 8:
                 continue
@@ -496,9 +506,11 @@ def run_ours(args):
     dist_barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.wait_ready()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         t_wall = time.perf_counter()
+        t_region0 = t_wall
         start.record(stream)
         for _ in range(args.steps):
             for r in rows:
@@ -510,7 +522,9 @@ def run_ours(args):
                 ev[r].append((a, b))
         end.record(stream)
         torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
+        t_region1 = time.perf_counter()
+        t_wall = t_region1 - t_wall
+        time.sleep(0.03)                       # let the sampler deliver the region's last line
     dist_barrier(world)
     qg.qg_check_device_error()
     total_ms = dist_max(start.elapsed_time(end), world, dev)
@@ -537,7 +551,7 @@ def run_ours(args):
     value = aggregate(world * wl.bytes.get("decode_m1", 0.0), seg_ms_max.get("decode_m1", 1.0) * 1e-3) / 1e9
 
     e2e = e2e_decode_m1(torch, qg, wl, dev, steps=max(2, min(args.steps, 5))) if "decode_m1" in rows else None
-    clocks = clk.summary()
+    clocks = clk.summary(t_region0, t_region1)
     launches_per_step = sum((wl.launches[r] or 0) for r in rows)
 
     if rank != 0:
