@@ -36,6 +36,8 @@
 // Every wait is bounded; on expiry the CTA records a timeout in the device
 // error word, drains its in-flight copies and MMAs, frees its tensor memory
 // and returns.
+#include <algorithm>
+
 #include "dequant.cuh"
 #include "tc_common.cuh"
 
@@ -74,12 +76,24 @@ struct __align__(8) TcSmemTail {
   uint64_t w_empty[kASlots];
   uint64_t a_full[kASlots];
   uint64_t a_empty[kASlots];
-  uint64_t acc_full;
+  uint64_t acc_full;                   // all MMAs of the current tile done (one phase per tile)
+  uint64_t acc_empty;                  // the epilogue has read the accumulator (one phase per tile)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  unsigned int ready;                  // k-slabs whose operands are in place
+  unsigned int ready;                  // k-slabs (counted over all tiles of the CTA) whose operands are in place
 };
+
+// Grouped raster: group_t token tiles share a wave.  Tile index -> first token and channel.
+QG_DEVICE void tile_origin(const TcArgs& p, int tile, int& m0, int& n0) {
+  const int per_group = p.group_t * p.tiles_w;
+  const int grp = tile / per_group;
+  const int first_t = grp * p.group_t;
+  const int gsize = min(p.group_t, p.tiles_t - first_t);
+  const int within = tile - grp * per_group;
+  m0 = (first_t + within % gsize) * kTileT;
+  n0 = (within / gsize) * kTileW;
+}
 
 __global__ void __launch_bounds__(kThreadsTc, 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
@@ -92,16 +106,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- tile of this CTA (grouped raster: group_t token tiles share a wave) --
-  const int per_group = p.group_t * p.tiles_w;
-  const int grp = blockIdx.x / per_group;
-  const int first_t = grp * p.group_t;
-  const int gsize = min(p.group_t, p.tiles_t - first_t);
-  const int within = blockIdx.x - grp * per_group;
-  const int tt = first_t + within % gsize;
-  const int wt = within / gsize;
-  const int m0 = tt * kTileT, n0 = wt * kTileW;
+  // ---- persistent: this CTA computes tiles blockIdx.x, + gridDim.x, ... ----
+  // Every role walks the same sequence of k-slabs over all of the CTA's tiles;
+  // g counts them, and every ring index and barrier phase derives from g.
   const int nslab = p.K / kBK;
+  const int ntiles_total = p.tiles_t * p.tiles_w;
+  const int ntiles = (ntiles_total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int total = ntiles * nslab;
+  auto tile_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -114,6 +126,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       mbar_init(&tl->a_empty[s], 1);
     }
     mbar_init(&tl->acc_full, 1);
+    mbar_init(&tl->acc_empty, kDeqWarps);          // every epilogue warp, once per tile
     mbar_init(&tl->drain, 1);
     tl->abort = 0;
     tl->ready = 0;
@@ -131,33 +144,37 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   if (warp == 0) {
     // ---------------- TMA producer: activations ----------------
     if (lane == 0) {
-      int issued = 0;
-      for (int s = 0; s < nslab; ++s) {
-        const int st = s % kStages, sp = s - kStages;   // stage last held slab sp
-        if (sp >= 0 && !mbar_wait(&tl->a_empty[sp % kASlots], (sp / kASlots) & 1, p.cap, abort, p.err)) break;
+      int issued = 0, s = 0, i = 0, m0 = 0, n0 = 0;
+      if (total > 0) tile_origin(p, tile_of(0), m0, n0);
+      for (int g = 0; g < total; ++g, ++s) {
+        if (s == nslab) { s = 0; tile_origin(p, tile_of(++i), m0, n0); }
+        const int st = g % kStages, gp = g - kStages;   // stage last held slab gp
+        if (gp >= 0 && !mbar_wait(&tl->a_empty[gp % kASlots], (gp / kASlots) & 1, p.cap, abort, p.err)) break;
         mbar_arrive_expect_tx(&tl->x_full[st], kXStageBytes);
         tma_load_2d(xs + st * kXStageBytes, &tmap_x, &tl->x_full[st], s * kBK, m0);
-        issued = s + 1;
+        issued = g + 1;
       }
       if (*abort) {     // let every copy already issued land before the CTA exits
-        for (int s = max(0, issued - kStages); s < issued; ++s)
-          mbar_wait(&tl->x_full[s % kStages], (s / kStages) & 1, kDrainCap, abort, nullptr);
+        for (int g = max(0, issued - kStages); g < issued; ++g)
+          mbar_wait(&tl->x_full[g % kStages], (g / kStages) & 1, kDrainCap, abort, nullptr);
       }
     }
   } else if (warp == 2) {
     // ---------------- TMA producer: packed weights (runs ahead) ----------------
     if (lane == 0) {
-      int issued = 0;
-      for (int s = 0; s < nslab; ++s) {
-        const int st = s % kASlots, r = s / kASlots;
+      int issued = 0, s = 0, i = 0, m0 = 0, n0 = 0;
+      if (total > 0) tile_origin(p, tile_of(0), m0, n0);
+      for (int g = 0; g < total; ++g, ++s) {
+        if (s == nslab) { s = 0; tile_origin(p, tile_of(++i), m0, n0); }
+        const int st = g % kASlots, r = g / kASlots;
         if (r > 0 && !mbar_wait(&tl->w_empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
         mbar_arrive_expect_tx(&tl->w_full[st], kWStageBytes);
         tma_load_2d(wsm + st * kWStageBytes, &tmap_w, &tl->w_full[st], s * (kBK / 2), n0);
-        issued = s + 1;
+        issued = g + 1;
       }
       if (*abort) {
-        for (int s = max(0, issued - kASlots); s < issued; ++s)
-          mbar_wait(&tl->w_full[s % kASlots], (s / kASlots) & 1, kDrainCap, abort, nullptr);
+        for (int g = max(0, issued - kASlots); g < issued; ++g)
+          mbar_wait(&tl->w_full[g % kASlots], (g / kASlots) & 1, kDrainCap, abort, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -166,20 +183,29 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       const uint32_t idesc = idesc_bf16_f32(kTileW, kTileT);
       bool any = false;
       unsigned int ready = 0;
-      for (int s = 0; s < nslab; ++s) {
-        const int st = s % kStages, sa = s % kASlots;
-        if (!wait_count(&tl->ready, (unsigned)s, ready, p.cap * 4, abort, p.err)) break;
-        tc_fence_after();
-        const uint64_t bdesc = sw128_kmajor_desc(smem_addr(xs + st * kXStageBytes));
+      int g = 0;
+      for (int i = 0; i < ntiles && !*abort; ++i) {
+        // the accumulator is free once the epilogue has read the previous tile
+        if (i > 0) {
+          if (!mbar_wait(&tl->acc_empty, (i - 1) & 1, p.cap, abort, p.err)) break;
+          tc_fence_after();
+        }
+        bool ok = true;
+        for (int s = 0; s < nslab; ++s, ++g) {
+          const int st = g % kStages, sa = g % kASlots;
+          if (!wait_count(&tl->ready, (unsigned)g, ready, p.cap * 4, abort, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t bdesc = sw128_kmajor_desc(smem_addr(xs + st * kXStageBytes));
 #pragma unroll
-        for (int j = 0; j < kBK / 16; ++j)
-          tc_mma_ts(tmem, tmem + kACol0 + sa * kACols + 8 * j, bdesc + 2 * j, idesc, (s | j) != 0);
-        tc_commit(&tl->a_empty[sa]);                   // frees the A slot and the activation stage
-        any = true;
-      }
-      if (!*abort) {
+          for (int j = 0; j < kBK / 16; ++j)
+            tc_mma_ts(tmem, tmem + kACol0 + sa * kACols + 8 * j, bdesc + 2 * j, idesc, (s | j) != 0);
+          tc_commit(&tl->a_empty[sa]);                 // frees the A slot and the activation stage
+          any = true;
+        }
+        if (!ok) break;
         tc_commit(&tl->acc_full);
-      } else if (any) {
+      }
+      if (*abort && any) {
         tc_commit(&tl->drain);                         // every MMA issued so far completes
         mbar_wait(&tl->drain, 0, kDrainCap, abort, nullptr);
       }
@@ -187,30 +213,88 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   } else if (warp == kSchedWarp) {
     // ---------------- scheduler ----------------
     if (lane == 0) {
-      for (int s = 0; s < nslab; ++s) {
-        if (!mbar_wait(&tl->a_full[s % kASlots], (s / kASlots) & 1, p.cap, abort, p.err)) break;
-        if (!mbar_wait(&tl->x_full[s % kStages], (s / kStages) & 1, p.cap, abort, p.err)) break;
-        publish_count(&tl->ready, (unsigned)(s + 1));
+      for (int g = 0; g < total; ++g) {
+        if (!mbar_wait(&tl->a_full[g % kASlots], (g / kASlots) & 1, p.cap, abort, p.err)) break;
+        if (!mbar_wait(&tl->x_full[g % kStages], (g / kStages) & 1, p.cap, abort, p.err)) break;
+        publish_count(&tl->ready, (unsigned)(g + 1));
       }
     }
   } else {
-    // ---------------- dequant producers ----------------
-    // Thread = one weight row (TMEM lane) x one 32-k half of a stage; the two
-    // sets of 8 warps take alternate stages, so each warp has two stage
-    // periods for its load-decode-store chain.  The packed tile arrives by
-    // TMA with the activations; the group scale is fetched one stage ahead.
+    // ---------------- dequant producers and the epilogue ----------------
+    // Thread = one weight row (TMEM lane) x one 32-k half of a slab; the two
+    // sets of 8 warps take alternate slabs (g even / odd), so each warp has
+    // two slab periods for its load-decode-store chain.  The group scale is
+    // fetched two slabs ahead.  The epilogue of tile e runs once this warp is
+    // about to produce the slab kASlots past the start of tile e+1: by then
+    // the MMAs already have kASlots slabs of tile e+1 to work on while the
+    // epilogue stores, and no slot this warp needs is held by a tile-(e+1) MMA
+    // (which waits for the epilogue).
     const int dw = warp - kDeq0;
     const int q = warp & 3, h = (dw >> 2) & 1, par = dw >> 3;
     const int row = 32 * q + lane;
-    const int n = min(n0 + row, p.N - 1);
-    const uint16_t* srow = p.ws + (size_t)n * (p.K >> p.lg);
+    const int cq = dw >> 2;                         // epilogue: 64 of the 256 token columns
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + kACol0 + 16 * h;
-    uint16_t sc_next = par < nslab ? __ldg(srow + ((par * kBK + 32 * h) >> p.lg)) : 0;
-    for (int s = par; s < nslab; s += 2) {
-      const int sa = s % kASlots, ra = s / kASlots;
-      const uint32_t s2 = bf16x2_splat(sc_next);
-      if (s + 2 < nslab) sc_next = __ldg(srow + (((s + 2) * kBK + 32 * h) >> p.lg));
-      if (!mbar_wait_warp(&tl->w_full[sa], ra & 1, p.cap, abort, p.err)) break;
+    // scale cursor: tile index, slab in the tile, this thread's scale row
+    struct Cur { int i, s; const uint16_t* srow; };
+    auto set_row = [&](Cur& c) {
+      if (c.i < ntiles) {
+        int m0, n0;
+        tile_origin(p, tile_of(c.i), m0, n0);
+        c.srow = p.ws + (size_t)min(n0 + row, p.N - 1) * (p.K >> p.lg);
+      }
+    };
+    auto advance = [&](Cur& c, int by) {
+      c.s += by;
+      while (c.s >= nslab) { c.s -= nslab; ++c.i; set_row(c); }
+    };
+    auto scale_of = [&](const Cur& c) -> uint16_t {
+      return c.i < ntiles ? __ldg(c.srow + ((c.s * kBK + 32 * h) >> p.lg)) : (uint16_t)0;
+    };
+    // epilogue of tile e: TMEM -> registers -> (accumulator free) -> bf16 -> Y
+    auto epilogue = [&](int e) -> bool {
+      if (!mbar_wait_warp(&tl->acc_full, e & 1, p.cap, abort, p.err)) return false;
+      tc_fence_after();
+      uint32_t v[64];
+      {
+        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 64 * cq, v0);
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 64 * cq + 32, v1);
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive_warp(&tl->acc_empty);             // the MMAs of the next tile may overwrite it
+      int m0, n0;
+      tile_origin(p, tile_of(e), m0, n0);
+      const int nn = n0 + row;
+      const int mb = m0 + 64 * cq;
+      if (nn < p.N) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (mb + c < p.M) p.y[(size_t)(mb + c) * p.N + nn] = f32_to_bf16_bits(__uint_as_float(v[c]));
+      }
+      return true;
+    };
+    int e_next = 0;                                 // next tile whose epilogue this warp owes
+    bool ok = true;
+    Cur pf{0, 0, nullptr};
+    set_row(pf);
+    advance(pf, par);
+    uint16_t sc_cur = scale_of(pf);
+    advance(pf, 2);
+    uint16_t sc_nxt = scale_of(pf);
+    for (int g = par; g < total; g += 2) {
+      while (e_next < ntiles - 1 && g >= (e_next + 1) * nslab + kASlots) {
+        if (!(ok = epilogue(e_next))) break;
+        ++e_next;
+      }
+      if (!ok) break;
+      const int sa = g % kASlots, ra = g / kASlots;
+      const uint32_t s2 = bf16x2_splat(sc_cur);
+      sc_cur = sc_nxt;
+      advance(pf, 2);                               // pf now at slab g + 4
+      sc_nxt = scale_of(pf);
+      if (!mbar_wait_warp(&tl->w_full[sa], ra & 1, p.cap, abort, p.err)) { ok = false; break; }
       const uint4 w4 = *reinterpret_cast<const uint4*>(wsm + sa * kWStageBytes + row * (kBK / 2) + 16 * h);
       const uint32_t v[4] = {w4.x, w4.y, w4.z, w4.w};
       uint32_t out[16];
@@ -224,7 +308,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       }
       mbar_arrive_warp(&tl->w_empty[sa]);           // packed slab decoded: its stage may be refilled
       if (ra > 0) {
-        if (!mbar_wait_warp(&tl->a_empty[sa], (ra - 1) & 1, p.cap, abort, p.err)) break;
+        if (!mbar_wait_warp(&tl->a_empty[sa], (ra - 1) & 1, p.cap, abort, p.err)) { ok = false; break; }
         tc_fence_after();
       }
       tmem_st16(lane_base + sa * kACols, out);
@@ -232,25 +316,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       tc_fence_before();
       mbar_arrive_warp(&tl->a_full[sa]);
     }
-
-    // ---------------- epilogue: TMEM -> bf16 -> Y[m][n] ----------------
-    // warp covers lane quarter q and 64 of the 256 token columns
-    const int cq = dw >> 2;
-    if (mbar_wait_warp(&tl->acc_full, 0, p.cap, abort, p.err)) {
-      tc_fence_after();
-      const int nn = n0 + row;
-#pragma unroll 1
-      for (int i = 0; i < 2; ++i) {
-        uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 64 * cq + 32 * i, v);
-        tmem_wait_ld();
-        const int mb = m0 + 64 * cq + 32 * i;
-        if (nn < p.N) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (mb + c < p.M) p.y[(size_t)(mb + c) * p.N + nn] = f32_to_bf16_bits(__uint_as_float(v[c]));
-        }
-      }
+    while (ok && e_next < ntiles) {
+      if (!(ok = epilogue(e_next))) break;
+      ++e_next;
     }
   }
 
@@ -331,7 +399,8 @@ qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const ui
   const int smem = kStages * kXStageBytes + kASlots * kWStageBytes + (int)sizeof(TcSmemTail) + 1024;
   if (!ensure_smem(w4a16_tc_kernel, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a16: smem attribute");
   const long long tiles = (long long)a.tiles_t * a.tiles_w;
-  w4a16_tc_kernel<<<(unsigned)tiles, kThreadsTc, smem, st>>>(tmap, tmap_w, a);
+  const int grid = (int)std::min<long long>(tiles, (long long)sm_count());   // persistent: one CTA per SM
+  w4a16_tc_kernel<<<grid, kThreadsTc, smem, st>>>(tmap, tmap_w, a);
   return check_launch("qgemm_w4a16 (prefill)");
 }
 
