@@ -12,14 +12,22 @@
 //   * B operand = activations, 256 tokens x 64 k per stage, TMA-loaded into
 //     shared memory in the 128-byte swizzled K-major layout.
 //   * D = fp32 accumulator in tensor memory, 128 lanes x 256 columns.
-// One CTA computes a 256-token x 128-channel output tile:
+// Persistent: one CTA per SM walks the tiles blockIdx.x, + gridDim.x, ... of
+// 256 tokens x 128 channels (grouped raster: 8 token tiles share a wave), and
+// every role counts the k-slabs of all its tiles in one sequence, so the
+// rings simply continue from one tile into the next.
 //   warp 0      TMA producer for the activations (one elected lane)
 //   warp 1      TMEM allocator + MMA issuer (one elected lane)
 //   warp 2      TMA producer for the packed weights, which runs ahead
-//   warps 3..18 dequant producers during the K loop (lane quarter = warp % 4,
-//               k half and stage parity from (warp - 3) / 4), then the epilogue
+//   warps 3..18 dequant producers (lane quarter = warp % 4, k half and slab
+//               parity from (warp - 3) / 4), and the epilogue
 //   warp 19     scheduler: waits for each k-slab's operands and publishes a
 //               ready count that the MMA issuer polls
+// The epilogue of a tile is done by the dequant warps once they have
+// produced the first 8 slabs of the next tile: they read the accumulator
+// into registers, release it (acc_empty, which the issuer waits for before
+// the next tile's first MMA) and store while the MMAs of the next tile run
+// (measured on GB300: 1.50 -> 1.61 PFLOP/s at M=8192, N=14336, K=4096).
 // Three rings decouple them so that only the activation copy latency sits in
 // front of the MMAs: 6 activation stages in shared memory (x_full: TMA bytes
 // landed), 8 packed-weight stages (w_full / w_empty: the dequant warps holding
