@@ -31,6 +31,19 @@ def test_prefill_small(qg, M, N, K):
     check_gemm(y, ref, "prefill M=%d N=%d K=%d" % (M, N, K))
 
 
+@pytest.mark.parametrize("M,N,K", [(2000, 2600, 128), (1800, 3000, 384), (4100, 1200, 512)])
+def test_prefill_multi_tile_per_cta(qg, M, N, K):
+    """More tiles than SMs, so each persistent CTA computes several tiles and
+    overlaps one tile's epilogue with the next; K = 128 and 384 give 2 and 6
+    k-slabs per tile (fewer than the 8 dequant slots); ragged M and N."""
+    w = inputs.weights_f32(N, K, seed=M + 3 * N)
+    x = inputs.activations_bf16(M, K, seed=K + 11, outlier_frac=0.01, outlier_scale=50.0)
+    q, s = OQ.quant_int4_rtn(w, 128)
+    y = run(qg, x, q, s, M, N, K)
+    ref = OF.bf16_decode(OG.to_bf16(OG.qgemm_w4a16(x, q, s, 128)))
+    check_gemm(y, ref, "prefill M=%d N=%d K=%d" % (M, N, K))
+
+
 @pytest.mark.parametrize("g", [32, 64, 256])
 def test_prefill_group_sizes(qg, g):
     M, N, K = 256, 256, 512
