@@ -431,6 +431,16 @@ def cpu_cores():
 # arms
 # ----------------------------------------------------------------------------
 
+def bench_config(rows, world):
+    """The workload of the bench line (shared by both arms)."""
+    return {"workload": "decode sweep M in {1,4,16} x {4096^2, 14336x4096, 4096x14336} x "
+                        "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill W4A16 M=8192 + "
+                        "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2",
+            "rows": rows, "l2": "inputs larger than L2: every weight matrix read once per step; "
+                                "step working set > 1 GB vs 129 MB L2",
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if world > 1:
@@ -453,9 +463,10 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": 1e3 * el / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": "decode sweep M=1 (oracle sample: %s)" % desc},
+        "config": bench_config(args.rows.split(","), world),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": "one M=1 GEMV per step: %s" % desc},
+                         "sample": "each step one M=1 GEMV of the decode sweep through the oracle "
+                                   "(dequantization + fp64 product): %s; value = its effective GB/s" % desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -561,12 +572,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded: weights N(0,0.02), activations N(0,1))",
-        "config": {"workload": "decode sweep M in {1,4,16} x {4096^2, 14336x4096, 4096x14336} x "
-                               "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill W4A16 M=8192 + "
-                               "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2",
-                   "rows": rows, "l2": "inputs larger than L2: every weight matrix read once per step; "
-                                       "step working set > 1 GB vs 129 MB L2",
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": bench_config(rows, world),
         "secondary": None,
         "roofline": dict(row_out[dominant]["roofline"], kernel=dominant),
         "roofline_value": dict(row_out["decode_m1"]["roofline"], kernel="decode_m1") if "decode_m1" in row_out else None,
