@@ -128,6 +128,27 @@ def w4a8_grouped_f64(a_codes, a_s, expert_off, packed, s_bits, g):
     return y
 
 
+def w4a8_fp8s_grouped_f64(a_codes, a_s, expert_off, w8_codes, cs8):
+    """W4A8 with FP8 group scales ("Production-Ready W4A8", "Accurate W4A8
+    Kernel"): rows sorted by expert, expert e's weights are the E4M3 codes
+    w8 = E4M3(q * s8) and its fp32 channel scales cs8;
+    y64[r, n] = a_s[r] * cs8_e[n] * sum_k e4m3(a[r,k]) * e4m3(w8_e[n,k])
+    (the per-token and per-channel scales applied in the epilogue, "outer
+    vector scaling")."""
+    a = F.e4m3_decode(a_codes)
+    R = a.shape[0]
+    E, N = np.asarray(w8_codes).shape[:2]
+    y = np.zeros((R, N))
+    for e in range(E):
+        r0, r1 = int(expert_off[e]), int(expert_off[e + 1])
+        if r1 <= r0:
+            continue
+        w = F.e4m3_decode(w8_codes[e])
+        y[r0:r1] = (a[r0:r1] @ w.T) * np.asarray(a_s[r0:r1], np.float64)[:, None] \
+            * np.asarray(cs8[e], np.float64)[None, :]
+    return y
+
+
 def swiglu_f32(gate_up_bits, inter):
     """h = SiLU(gate) * up from the bf16 projection output, in fp32.
 

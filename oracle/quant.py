@@ -161,6 +161,42 @@ def quant_fp8_block(x, g):
 
 
 # ----------------------------------------------------------------------------
+# FP8 group scales for W4A8 with an FP8 x FP8 matmul ("Production-Ready W4A8",
+# "Accurate W4A8 Kernel")
+# ----------------------------------------------------------------------------
+
+def fp8_group_scales(s_bits):
+    """The page's W4A8 recipe for the bf16 group scales of an INT4 checkpoint.
+
+    1. Quantize each output channel's row of bf16 group scales to FP8 with the
+       same per-token quantizer the activations use: cs[n] = max_g |s[n,g]| /
+       448 (fp32), code = E4M3(s[n,g] / cs[n]) (quant_fp8_block with the block
+       = the whole row).
+    2. Scale the FP8 scales by 1/8 so that every INT4 value times a scale
+       stays inside the E4M3 range, and compensate by multiplying the channel
+       scales by 8: s8 = E4M3(decode(code) / 8) (exact for codes >= 2^-3,
+       otherwise one more E4M3 rounding), cs8 = cs * 8 (exact).
+    Returns (s8 E4M3 codes [N, G] uint8, cs8 float32 [N]).
+    """
+    s = F.bf16_decode(s_bits).astype(F32)
+    codes, cs = quant_fp8_block(s, s.shape[-1])
+    s8 = F.e4m3_encode((F.e4m3_decode(codes).astype(F32) * F32(0.125)).astype(F32))
+    return s8, (cs[..., 0] * F32(8.0)).astype(F32)
+
+
+def fp8_lut_weights(packed, s8_codes, g=128):
+    """Weights of the W4A8 FP8 matmul: E4M3(q * s8) for every INT4 value q
+    and its group's FP8 scale -- the contents of the page's per-scale lookup
+    table ("there are only 16 possible values of s * w"), one E4M3
+    round-to-nearest-even of the exact product.  Returns E4M3 codes [N, K]."""
+    q = F.int4_decode(unpack_nibbles(packed)).astype(np.float64)
+    s8 = F.e4m3_decode(s8_codes).astype(np.float64)
+    N, K = q.shape
+    prod = (q.reshape(N, K // g, g) * s8[..., None]).reshape(N, K)     # exact (<= 8 significant bits)
+    return F.e4m3_encode(prod.astype(F32))
+
+
+# ----------------------------------------------------------------------------
 # weight quantizers (load-time; the GPU kernels consume their output)
 # ----------------------------------------------------------------------------
 

@@ -440,3 +440,105 @@ def test_output_narrowing_is_a_single_rounding():
     assert F.bf16_decode(G.to_bf16(np.float64(y))) == 1.0 + 2.0 ** -7
     y32 = np.float32(y)            # 1 + 2**-8 exactly (the 2**-30 is lost)
     assert F.bf16_decode(G.to_bf16(np.float64(y32))) == 1.0
+
+
+# ----------------------------------------------------------------------------
+# W4A8 with FP8 group scales ("Production-Ready W4A8", "Accurate W4A8 Kernel")
+# ----------------------------------------------------------------------------
+
+def _e4m3_values():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = F.e4m3_decode(codes)
+    fin = np.isfinite(vals)
+    return codes[fin], vals[fin]
+
+
+def test_fp8_group_scales_never_clip_int4_products():
+    """The page scales the FP8 scales by 1/8 so that 'weights are guaranteed
+    to be in FP8 range after multiplication by INT4 values': every finite E4M3
+    scale divided by 8 times every INT4 value is within +-448."""
+    codes, vals = _e4m3_values()
+    s8 = F.e4m3_decode(F.e4m3_encode((vals.astype(np.float32) * np.float32(0.125)).astype(np.float32)))
+    prod = np.abs(np.arange(-8, 8, dtype=np.float64)[:, None] * s8[None, :])
+    assert prod.max() == 448.0                      # reached by q = -8 and the largest scale 448 / 8
+    # without the 1/8 the same products overflow E4M3 (the clipping the page shows)
+    assert (np.abs(np.arange(-8, 8)[:, None] * vals[None, :]) > 448).any()
+
+
+def test_fp8_group_scales_worked_example():
+    """One channel with bf16 group scales s, s/2, s/4, 0 (exact ratios):
+    cs = s/448, the codes of 448, 224, 112, 0; after the 1/8: 56, 28, 14, 0;
+    channel scale times 8 (reading of 'quantize each column of BF16 group-wise
+    scales to FP8' with the activation quantizer, then 'scale the FP8 scales
+    by 1/8 ... multiplying per-channel scales by eight')."""
+    s = np.float32(0.02)
+    row = np.array([[s, s / 2, s / 4, 0.0]], np.float32)
+    bits = F.bf16_encode(row)
+    s8, cs8 = Q.fp8_group_scales(bits)
+    sb = F.bf16_decode(bits)[0, 0]
+    assert list(F.e4m3_decode(s8)[0]) == [56.0, 28.0, 14.0, 0.0]
+    assert float(cs8[0]) == float(np.float32(np.float32(sb) / np.float32(448.0)) * np.float32(8.0))
+    # the E4M3 codes themselves, from the format definition: 56 = 1.75 * 2^5 -> e = 12, m = 6
+    assert list(s8[0]) == [(12 << 3) | 6, (11 << 3) | 6, (10 << 3) | 6, 0]
+
+
+def test_fp8_lut_weights_match_brute_force_nearest_code():
+    """E4M3(q * s8) against a brute-force nearest-code search over all 256
+    codes with ties to the even code (an independent formulation)."""
+    codes, vals = _e4m3_values()
+    order = np.argsort(vals, kind="stable")
+    rng = np.random.Generator(np.random.PCG64(17))
+    s8 = rng.choice(codes[(vals > 0) & (vals <= 56)], size=(3, 2)).astype(np.uint8)
+    q = rng.integers(-8, 8, size=(3, 256))
+    packed = Q.pack_nibbles(q.astype(np.int64))
+    got = Q.fp8_lut_weights(packed, s8, g=128)
+    for n in range(3):
+        for k in range(256):
+            x = Fraction(int(q[n, k])) * Fraction(float(F.e4m3_decode(s8[n, k // 128])))
+            best = None
+            for c in codes:
+                v = Fraction(float(F.e4m3_decode(np.uint8(c))))
+                d = abs(v - x)
+                key = (d, int(c) & 1)                 # nearest, then the even code
+                if best is None or key < best[0]:
+                    best = (key, c)
+            want = F.e4m3_decode(np.uint8(best[1]))
+            assert F.e4m3_decode(got[n, k]) == want, (n, k, q[n, k])
+
+
+def test_w4a8_fp8s_grouped_matches_exact_brute_force():
+    """The grouped product with the outer per-token x per-channel scaling,
+    against exact rational arithmetic."""
+    rng = np.random.Generator(np.random.PCG64(23))
+    E, N, K, off = 2, 3, 64, np.array([0, 2, 5], np.int32)
+    a = rng.integers(0, 256, size=(5, K)).astype(np.uint8)
+    a[(a & 0x7F) == 0x7F] = 0                         # no NaN codes
+    a_s = rng.random(5).astype(np.float32)
+    w8 = rng.integers(0, 256, size=(E, N, K)).astype(np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0
+    cs8 = rng.random((E, N)).astype(np.float32)
+    y = G.w4a8_fp8s_grouped_f64(a, a_s, off, w8, cs8)
+    for e in range(E):
+        for r in range(off[e], off[e + 1]):
+            for n in range(N):
+                acc = sum(Fraction(float(F.e4m3_decode(a[r, k]))) * Fraction(float(F.e4m3_decode(w8[e, n, k])))
+                          for k in range(K))
+                want = acc * Fraction(float(a_s[r])) * Fraction(float(cs8[e, n]))
+                assert abs(Fraction(y[r, n]) - want) <= abs(want) * Fraction(1, 2 ** 50)
+
+
+def test_fp8_group_scale_recipe_stays_close_to_exact_w4a8():
+    """Invariant: the recipe adds one E4M3 rounding per weight (3 mantissa
+    bits), so on RTN-quantized N(0, 0.02) weights its output stays within a
+    few percent of the exact W4A8 product."""
+    from numerics_packed_int4_gb300 import inputs
+    N, K, R = 64, 512, 32
+    q, s = Q.quant_int4_rtn(inputs.weights_f32(N, K, seed=5), 128)
+    s8, cs8 = Q.fp8_group_scales(s)
+    w8 = Q.fp8_lut_weights(q, s8)
+    a, a_s = Q.quant_fp8_block(F.bf16_decode(inputs.activations_bf16(R, K, seed=6)), K)
+    off = np.array([0, R], np.int32)
+    exact = G.w4a8_grouped_f64(a, a_s[:, 0], off, q[None], s[None], 128)
+    recipe = G.w4a8_fp8s_grouped_f64(a, a_s[:, 0], off, w8[None], cs8[None])
+    rel = np.linalg.norm(recipe - exact) / np.linalg.norm(exact)
+    assert 1e-3 < rel < 5e-2
