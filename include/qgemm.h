@@ -145,6 +145,31 @@ QG_API qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,
                              const uint16_t* w_s, int g, uint16_t* y, int R,
                              int E, int N, int K, qg_stream_t stream);
 
+/* W4A8 grouped GEMM with FP8 group scales and an FP8 x FP8 matmul
+ * (Production-Ready W4A8, "Accurate W4A8 Kernel": the group scales are
+ * quantized to FP8 per output channel, pre-scaled by 1/8 with the channel
+ * scale times 8, and each weight becomes E4M3(q * s8) -- the page's per-scale
+ * lookup table -- so the tensor cores run E4M3 x E4M3 with fp32 accumulation
+ * and the per-token and per-channel scales are applied in the epilogue):
+ *   y[r,n] = bf16( a_s[r] * cs8_e[n] * sum_k e4m3(a[r,k]) * E4M3(q_e[n,k] * s8_e[n,k/128]) )
+ * One extra E4M3 rounding per weight against qgemm_w4a8_grouped.
+ *   a_e4m3, a_s, expert_off, w_q, y as qgemm_w4a8_grouped;
+ *   w_s8 [E][N][K/128] E4M3 codes, w_cs8 [E][N] fp32 (qg_w4a8_fp8_scales).
+ * Rules: K % 128 == 0, N % 16 == 0, R >= 0, E >= 1.                          */
+QG_API qg_status qgemm_w4a8_grouped_fp8s(const uint8_t* a_e4m3, const float* a_s,
+                                  const int32_t* expert_off, const uint8_t* w_q,
+                                  const uint8_t* w_s8, const float* w_cs8, uint16_t* y,
+                                  int R, int E, int N, int K, qg_stream_t stream);
+
+/* The group scales of qgemm_w4a8_grouped_fp8s from an INT4 checkpoint's bf16
+ * group scales (same page): per row, cs = max|s| / 448 in fp32 (zero row: 1),
+ * code = E4M3_RNE_satfinite(s / cs) (IEEE division) -- the activation
+ * quantizer applied to the row of scales -- then s8 = E4M3(decode(code) / 8)
+ * and cs8 = 8 * cs.
+ *   w_s [rows][G] bf16 -> w_s8 [rows][G] E4M3 codes, w_cs8 [rows] fp32.      */
+QG_API qg_status qg_w4a8_fp8_scales(const uint16_t* w_s, uint8_t* w_s8, float* w_cs8,
+                             int rows, int G, qg_stream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * Load-time weight quantizers (fp32 weights -> the formats above).
  * ------------------------------------------------------------------------ */

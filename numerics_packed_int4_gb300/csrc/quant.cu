@@ -312,6 +312,29 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
   *reinterpret_cast<uint4*>(out + (long long)t * H + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// ---- FP8 group scales of the W4A8 FP8 x FP8 path (one warp per row) --------
+// Production-Ready W4A8, "Accurate W4A8 Kernel": the per-token FP8 quantizer
+// applied to each output channel's row of bf16 group scales, then the FP8
+// scales times 1/8 and the channel scale times 8.
+__global__ void __launch_bounds__(kThreads) w4a8_fp8_scales_kernel(
+    const uint16_t* __restrict__ w_s, uint8_t* __restrict__ s8, float* __restrict__ cs8, int rows, int G) {
+  const long long row = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint16_t* src = w_s + row * G;
+  float m = 0.f;
+  for (int g = lane; g < G; g += 32) m = fmaxf(m, fabsf(bf16_bits_to_f32(src[g])));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float cs = fp8_scale(m);
+  for (int g = lane; g < G; g += 32) {
+    const uint32_t code = f32x2_to_e4m3x2(0.f, __fdiv_rn(bf16_bits_to_f32(src[g]), cs)) & 0xFFu;
+    const float eighth = e4m3_to_f32(code) * 0.125f;                 // exact in fp32
+    s8[row * G + g] = uint8_t(f32x2_to_e4m3x2(0.f, eighth) & 0xFFu);
+  }
+  if (lane == 0) cs8[row] = cs * 8.f;
+}
+
 // ---- launch helpers ----------------------------------------------------------
 inline unsigned grid_for(long long nchunks) { return unsigned((nchunks + kThreads - 1) / kThreads); }
 
@@ -487,6 +510,17 @@ qg_status qg_moe_combine(const uint16_t* down, const int32_t* row_of, const floa
   qg::combine_kernel<<<grid, qg::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       down, row_of, weight, out, topk, R, H);
   return qg::check_launch("qg_moe_combine");
+}
+
+qg_status qg_w4a8_fp8_scales(const uint16_t* w_s, uint8_t* w_s8, float* w_cs8, int rows, int G,
+                             qg_stream_t stream) {
+  QG_REQUIRE(w_s && w_s8 && w_cs8, QG_ERR_INVALID_ARG, "qg_w4a8_fp8_scales: NULL pointer");
+  QG_REQUIRE(rows >= 0 && G > 0, QG_ERR_INVALID_ARG, "qg_w4a8_fp8_scales: bad sizes");
+  if (rows == 0) return QG_OK;
+  const long long threads = (long long)rows * 32;
+  qg::w4a8_fp8_scales_kernel<<<unsigned((threads + qg::kThreads - 1) / qg::kThreads), qg::kThreads, 0,
+                              reinterpret_cast<cudaStream_t>(stream)>>>(w_s, w_s8, w_cs8, rows, G);
+  return qg::check_launch("qg_w4a8_fp8_scales");
 }
 
 }  // extern "C"

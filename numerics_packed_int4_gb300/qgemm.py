@@ -29,6 +29,8 @@ SIGNATURES = {
     "quant_act_mxfp4": [P, P, P, I, I, I, P],
     "quant_act_fp8_block": [P, P, P, I, I, I, P],
     "qgemm_w4a8_grouped": [P, P, P, P, P, I, P, I, I, I, I, P],
+    "qgemm_w4a8_grouped_fp8s": [P, P, P, P, P, P, P, I, I, I, I, P],
+    "qg_w4a8_fp8_scales": [P, P, P, I, I, P],
     "qg_quantize_weights_int4": [P, P, P, I, I, I, P],
     "qg_quantize_weights_fp8": [P, P, P, I, I, P],
     "qg_quantize_weights_mxfp4": [P, P, P, I, I, I, P],
@@ -126,6 +128,15 @@ def quant_act_fp8_block(x, q, s, g, M, K, stream=None):
 def qgemm_w4a8_grouped(a_e4m3, a_s, expert_off, w_q, w_s, g, y, R, E, N, K, stream=None):
     return _call("qgemm_w4a8_grouped", _ptr(a_e4m3), _ptr(a_s), _ptr(expert_off), _ptr(w_q),
                  _ptr(w_s), g, _ptr(y), R, E, N, K, stream=stream)
+
+
+def qgemm_w4a8_grouped_fp8s(a_e4m3, a_s, expert_off, w_q, w_s8, w_cs8, y, R, E, N, K, stream=None):
+    return _call("qgemm_w4a8_grouped_fp8s", _ptr(a_e4m3), _ptr(a_s), _ptr(expert_off), _ptr(w_q),
+                 _ptr(w_s8), _ptr(w_cs8), _ptr(y), R, E, N, K, stream=stream)
+
+
+def qg_w4a8_fp8_scales(w_s, w_s8, w_cs8, rows, G, stream=None):
+    return _call("qg_w4a8_fp8_scales", _ptr(w_s), _ptr(w_s8), _ptr(w_cs8), rows, G, stream=stream)
 
 
 def qg_quantize_weights_int4(w, w_q, w_s, g, N, K, stream=None):
