@@ -6,6 +6,8 @@ One step = one pass over every row of the hot path at its workload size:
   prefill        W4A16 GEMM, M = 8192, same three (N, K), INT4 g128
   quantizers     4096 x 7168 bf16 -> FP8 E4M3 per 1x128, MXFP4 (E8M0 per 16)
   MoE            W4A8 layer, T = 4096, hidden 4096, inter 14336, E = 8, top-2
+  MoE, FP8 scales  the same layer on the FP8-group-scale recipe (E4M3 x E4M3
+                 tensor-core GEMMs; roofline against the FP8 dense peak)
 Each row is one CUDA graph; CUDA events between the graphs time every row
 inside the timed region.  The headline value is the metric's first quantity:
 effective HBM GB/s of the M = 1 GEMVs (algorithmic bytes / time); the
@@ -79,10 +81,13 @@ def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
-                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
+        pk = dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                  bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
     except Exception:
-        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+        pk = dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+    # dense FP8: the measured bf16 peak x the nominal fp8/bf16 ratio (4.5 / 2.25)
+    pk["fp8"] = 2.0 * pk["bf16"]
+    return pk
 
 
 # ----------------------------------------------------------------------------
@@ -281,7 +286,7 @@ class Workload:
             self.QFs = t.empty((4096, 56), dtype=t.float32, device=self.dev)
             self.QM = t.empty((4096, 3584), dtype=t.uint8, device=self.dev)
             self.QMs = t.empty((4096, 448), dtype=t.uint8, device=self.dev)
-        if "moe" in self.rows:
+        if "moe" in self.rows or "moe_fp8s" in self.rows:
             self._build_moe(inputs)
 
     def _build_moe(self, inputs):
@@ -314,6 +319,13 @@ class Workload:
             self.qg.qg_quantize_weights_int4(w, w2q[e], w2s[e], 128, H, I)
             del w
         m.update(w1q=w1q, w1s=w1s, w2q=w2q, w2s=w2s)
+        if "moe_fp8s" in self.rows:                       # load-time scale preparation
+            m["w1s8"] = t.empty((H // 128, E * 2 * I), dtype=t.uint8, device=dev)      # group-major
+            m["w1cs8"] = t.empty((E, 2 * I), dtype=t.float32, device=dev)
+            m["w2s8"] = t.empty((I // 128, E * H), dtype=t.uint8, device=dev)
+            m["w2cs8"] = t.empty((E, H), dtype=t.float32, device=dev)
+            self.qg.qg_w4a8_fp8_scales(w1s, m["w1s8"], m["w1cs8"], E * 2 * I, H // 128)
+            self.qg.qg_w4a8_fp8_scales(w2s, m["w2s8"], m["w2cs8"], E * H, I // 128)
         m["xq"] = t.empty((T, H), dtype=t.uint8, device=dev)
         m["xs"] = t.empty((T,), dtype=t.float32, device=dev)
         m["aq"] = t.empty((R, H), dtype=t.uint8, device=dev)
@@ -348,6 +360,17 @@ class Workload:
             qg.qg_swiglu_quant_fp8(m["gu"], m["hq"], m["hs"], R, I)
             qg.qgemm_w4a8_grouped(m["hq"], m["hs"], m["off"], m["w2q"], m["w2s"], 128, m["down"], R, E, H, I)
             qg.qg_moe_combine(m["down"], m["row_of"], m["wt"], m["out"], T, topk, R, H)
+        elif name == "moe_fp8s":
+            m = self.moe
+            T, E, H, I, R, topk = m["T"], m["E"], m["H"], m["I"], m["R"], m["topk"]
+            qg.quant_act_fp8_block(m["x"], m["xq"], m["xs"], H, T, H)
+            qg.qg_moe_gather_fp8(m["xq"], m["xs"], m["rows"], m["aq"], m["as"], R, T, H)
+            qg.qgemm_w4a8_grouped_fp8s(m["aq"], m["as"], m["off"], m["w1q"], m["w1s8"], m["w1cs8"], m["gu"],
+                                       R, E, 2 * I, H)
+            qg.qg_swiglu_quant_fp8(m["gu"], m["hq"], m["hs"], R, I)
+            qg.qgemm_w4a8_grouped_fp8s(m["hq"], m["hs"], m["off"], m["w2q"], m["w2s8"], m["w2cs8"], m["down"],
+                                       R, E, H, I)
+            qg.qg_moe_combine(m["down"], m["row_of"], m["wt"], m["out"], T, topk, R, H)
 
     def accounting(self):
         for M in (1, 4, 16):
@@ -360,9 +383,10 @@ class Workload:
         if "quant" in self.rows:
             M, K = 4096, 7168
             self.bytes["quant"] = M * K * (2 + 1) + M * K // 128 * 4 + M * K * 2 + M * K // 2 + M * K // 16
-        if "moe" in self.rows:
-            m = self.moe
-            self.flops["moe"] = 2.0 * m["R"] * (2 * m["I"] * m["H"] + m["H"] * m["I"])
+        for r in ("moe", "moe_fp8s"):
+            if r in self.rows:
+                m = self.moe
+                self.flops[r] = 2.0 * m["R"] * (2 * m["I"] * m["H"] + m["H"] * m["I"])
 
 
 def count_launches(torch, fn):
@@ -435,7 +459,8 @@ def bench_config(rows, world):
     """The workload of the bench line (shared by both arms)."""
     return {"workload": "decode sweep M in {1,4,16} x {4096^2, 14336x4096, 4096x14336} x "
                         "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill W4A16 M=8192 + "
-                        "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2",
+                        "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2 (bf16 group scales; "
+                        "FP8 group scales)",
             "rows": rows, "l2": "inputs larger than L2: every weight matrix read once per step; "
                                 "step working set > 1 GB vs 129 MB L2",
             "parallelism": "replicas" if world > 1 else "single"}
@@ -554,10 +579,13 @@ def run_ours(args):
                                        "traffic": traffic_of(r), **traffic_info(r)}}
         else:
             tf = wl.flops[r] / (ms * 1e-3) / 1e12
-            peak = peaks["bf16"]
+            fp8 = r == "moe_fp8s"
+            peak = peaks["fp8"] if fp8 else peaks["bf16"]
             row_out[r] = {"ms": ms, "TFLOP/s": tf, "launches": wl.launches[r],
                           "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                                        "frac": tf / peak, "traffic": traffic_of(r), **traffic_info(r)}}
+            if fp8:
+                row_out[r]["roofline"]["peak_kind"] = "fp8 dense = measured bf16 x 2 (nominal ratio)"
     dominant = max(rows, key=lambda r: seg_ms_max[r])
     value = aggregate(world * wl.bytes.get("decode_m1", 0.0), seg_ms_max.get("decode_m1", 1.0) * 1e-3) / 1e9
 
@@ -662,7 +690,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe")
+    ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe,moe_fp8s")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)

@@ -154,7 +154,8 @@ QG_API qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,
  *   y[r,n] = bf16( a_s[r] * cs8_e[n] * sum_k e4m3(a[r,k]) * E4M3(q_e[n,k] * s8_e[n,k/128]) )
  * One extra E4M3 rounding per weight against qgemm_w4a8_grouped.
  *   a_e4m3, a_s, expert_off, w_q, y as qgemm_w4a8_grouped;
- *   w_s8 [E][N][K/128] E4M3 codes, w_cs8 [E][N] fp32 (qg_w4a8_fp8_scales).
+ *   w_s8 [K/128][E*N] E4M3 codes, group-major (qg_w4a8_fp8_scales with
+ *   rows = E*N), w_cs8 [E][N] fp32.
  * Rules: K % 128 == 0, N % 16 == 0, R >= 0, E >= 1.                          */
 QG_API qg_status qgemm_w4a8_grouped_fp8s(const uint8_t* a_e4m3, const float* a_s,
                                   const int32_t* expert_off, const uint8_t* w_q,
@@ -166,7 +167,9 @@ QG_API qg_status qgemm_w4a8_grouped_fp8s(const uint8_t* a_e4m3, const float* a_s
  * code = E4M3_RNE_satfinite(s / cs) (IEEE division) -- the activation
  * quantizer applied to the row of scales -- then s8 = E4M3(decode(code) / 8)
  * and cs8 = 8 * cs.
- *   w_s [rows][G] bf16 -> w_s8 [rows][G] E4M3 codes, w_cs8 [rows] fp32.      */
+ *   w_s [rows][G] bf16 -> w_s8 [G][rows] E4M3 codes (group-major: the
+ *   GEMM's warps then read 32 consecutive channels' scales at once),
+ *   w_cs8 [rows] fp32.                                                      */
 QG_API qg_status qg_w4a8_fp8_scales(const uint16_t* w_s, uint8_t* w_s8, float* w_cs8,
                              int rows, int G, qg_stream_t stream);
 

@@ -371,18 +371,21 @@ bool make_u8_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Byte matrix staged in the 128-byte swizzled layout a K-major MMA operand
-// descriptor reads (box_cols must be 128).
-bool make_u8_tmap_sw128(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols) {
+// Byte matrix staged in a swizzled shared-memory layout: 128-byte swizzle (the
+// layout a K-major MMA operand descriptor reads; box_cols == 128) or 64-byte
+// swizzle (box_cols == 64: 16-byte chunk c of row r lands at chunk
+// c ^ ((r >> 1) & 3), so 8 consecutive rows read at one chunk offset hit 8
+// different bank groups).
+bool make_u8_tmap_swizzled(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn || box_cols != 128) return false;
+  if (!fn || (box_cols != 128 && box_cols != 64)) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols};
   const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, box_cols == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_bf16_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols) {

@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kThreads) w4a8_fp8_scales_kernel(
   for (int g = lane; g < G; g += 32) {
     const uint32_t code = f32x2_to_e4m3x2(0.f, __fdiv_rn(bf16_bits_to_f32(src[g]), cs)) & 0xFFu;
     const float eighth = e4m3_to_f32(code) * 0.125f;                 // exact in fp32
-    s8[row * G + g] = uint8_t(f32x2_to_e4m3x2(0.f, eighth) & 0xFFu);
+    s8[(long long)g * rows + row] = uint8_t(f32x2_to_e4m3x2(0.f, eighth) & 0xFFu);   // group-major
   }
   if (lane == 0) cs8[row] = cs * 8.f;
 }

@@ -17,12 +17,14 @@ pytestmark = pytest.mark.gpu
 
 
 def gpu_scales(qg, s_bits):
+    """The GPU scale preparation; its group-major [G][rows] codes come back
+    transposed to the oracle's [rows][G]."""
     rows, G = s_bits.shape
-    s8 = empty((max(rows, 1), G), torch.uint8)
+    s8 = empty((G, max(rows, 1)), torch.uint8)
     cs8 = empty((max(rows, 1),), torch.float32)
     qg.qg_w4a8_fp8_scales(dev(s_bits), s8, cs8, rows, G)
     qg.qg_check_device_error()
-    return host(s8)[:rows], host(cs8)[:rows]
+    return np.ascontiguousarray(host(s8)[:, :rows].T), host(cs8)[:rows]
 
 
 @pytest.mark.parametrize("rows,G", [(1, 1), (7, 32), (300, 32), (129, 5), (64, 112), (33, 257)])
@@ -73,7 +75,7 @@ def grouped_fp8s(qg, a8, a_s, off, wq, ws, N, K):
     """The GPU path end to end: scale preparation, then the grouped GEMM."""
     R, E = a8.shape[0], wq.shape[0]
     G = K // 128
-    s8 = empty((E * N, G), torch.uint8)
+    s8 = empty((G, E * N), torch.uint8)
     cs8 = empty((E * N,), torch.float32)
     qg.qg_w4a8_fp8_scales(dev(ws.reshape(E * N, G)), s8, cs8, E * N, G)
     y = empty((max(R, 1), N), torch.int16)
@@ -104,6 +106,21 @@ def test_grouped_fp8s(qg, sizes, N, K):
     y = grouped_fp8s(qg, a8, a_s[:, 0], off, wq, ws, N, K)
     if R:
         check_gemm(y, reference(a8, a_s[:, 0], off, wq, ws), "fp8s %s" % sizes)
+
+
+@pytest.mark.parametrize("sizes,N,K", [([700, 900, 1000], 2048, 384), ([2000, 0, 600], 2560, 1024),
+                                       ([4100], 1200, 512), ([33, 1500, 7, 1100], 1664, 128)])
+def test_grouped_fp8s_several_tiles_per_cta(qg, sizes, N, K):
+    """More tiles than SMs, so the persistent CTAs walk several tiles across
+    expert boundaries; K from one slab to more than the 8 weight slots."""
+    E = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R = int(off[-1])
+    x = inputs.activations_bf16(R, K, seed=R + K + 11)
+    a8, a_s = OQ.quant_fp8_block(x, K)
+    wq, ws = expert_weights(E, N, K, seed=140)
+    y = grouped_fp8s(qg, a8, a_s[:, 0], off, wq, ws, N, K)
+    check_gemm(y, reference(a8, a_s[:, 0], off, wq, ws), "fp8s multi-tile %s" % sizes)
 
 
 def test_grouped_fp8s_all_empty(qg):
