@@ -57,7 +57,9 @@ constexpr int kTileT = 256;            // tokens (MMA N)
 constexpr int kBK = 64;                // k per stage (one 128-byte swizzle row of bf16)
 constexpr int kStages = 6;             // activation stages (shared memory)
 constexpr int kASlots = 8;             // dequantized-weight slots (tensor memory) and packed-weight stages
-constexpr int kDeqWarps = 16;             // two sets of 8: even and odd slabs
+constexpr int kDeqWarps = 16;             // four sets of 4 (one per TMEM lane quarter)
+constexpr int kDeqSet = 4;
+constexpr int kDeqSets = kDeqWarps / kDeqSet;
 constexpr int kDeq0 = 3;                            // first dequant warp
 constexpr int kSchedWarp = kDeq0 + kDeqWarps;       // scheduler warp
 constexpr int kThreadsTc = (kSchedWarp + 1) * 32;
@@ -129,8 +131,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     }
     for (int s = 0; s < kASlots; ++s) {
       mbar_init(&tl->w_full[s], 1);
-      mbar_init(&tl->w_empty[s], kDeqWarps / 2);   // the warps of the parity set that read it
-      mbar_init(&tl->a_full[s], kDeqWarps / 2);    // one parity set per slot, one arrival per warp
+      mbar_init(&tl->w_empty[s], kDeqSet);         // the set of 4 warps that read it
+      mbar_init(&tl->a_full[s], kDeqSet);          // one arrival per warp of that set
       mbar_init(&tl->a_empty[s], 1);
     }
     mbar_init(&tl->acc_full, 1);
@@ -229,19 +231,20 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     }
   } else {
     // ---------------- dequant producers and the epilogue ----------------
-    // Thread = one weight row (TMEM lane) x one 32-k half of a slab; the two
-    // sets of 8 warps take alternate slabs (g even / odd), so each warp has
-    // two slab periods for its load-decode-store chain.  The group scale is
-    // fetched two slabs ahead.  The epilogue of tile e runs once this warp is
+    // Thread = one weight row (TMEM lane) of a 64-k slab; the four sets of 4
+    // warps (one per TMEM lane quarter) take every fourth slab (g mod 4), so
+    // each warp has four slab periods for its load-decode-store chain.  The
+    // group scales (one per 32-k half: g may be 32) are fetched one own slab
+    // ahead.  The epilogue of tile e runs once this warp is
     // about to produce the slab kASlots past the start of tile e+1: by then
     // the MMAs already have kASlots slabs of tile e+1 to work on while the
     // epilogue stores, and no slot this warp needs is held by a tile-(e+1) MMA
     // (which waits for the epilogue).
     const int dw = warp - kDeq0;
-    const int q = warp & 3, h = (dw >> 2) & 1, par = dw >> 3;
+    const int q = warp & 3, set = dw >> 2;
     const int row = 32 * q + lane;
-    const int cq = dw >> 2;                         // epilogue: 64 of the 256 token columns
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + kACol0 + 16 * h;
+    const int cq = set;                             // epilogue: 64 of the 256 token columns
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + kACol0;
     // scale cursor: tile index, slab in the tile, this thread's scale row
     struct Cur { int i, s; const uint16_t* srow; };
     auto set_row = [&](Cur& c) {
@@ -255,7 +258,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       c.s += by;
       while (c.s >= nslab) { c.s -= nslab; ++c.i; set_row(c); }
     };
-    auto scale_of = [&](const Cur& c) -> uint16_t {
+    auto scale_of = [&](const Cur& c, int h) -> uint16_t {
       return c.i < ntiles ? __ldg(c.srow + ((c.s * kBK + 32 * h) >> p.lg)) : (uint16_t)0;
     };
     // epilogue of tile e: TMEM -> registers -> (accumulator free) -> bf16 -> Y
@@ -287,29 +290,32 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     bool ok = true;
     Cur pf{0, 0, nullptr};
     set_row(pf);
-    advance(pf, par);
-    uint16_t sc_cur = scale_of(pf);
-    advance(pf, 2);
-    uint16_t sc_nxt = scale_of(pf);
-    for (int g = par; g < total; g += 2) {
+    advance(pf, set);
+    uint16_t sc_cur0 = scale_of(pf, 0), sc_cur1 = scale_of(pf, 1);
+    advance(pf, kDeqSets);
+    uint16_t sc_nxt0 = scale_of(pf, 0), sc_nxt1 = scale_of(pf, 1);
+    for (int g = set; g < total; g += kDeqSets) {
       while (e_next < ntiles - 1 && g >= (e_next + 1) * nslab + kASlots) {
         if (!(ok = epilogue(e_next))) break;
         ++e_next;
       }
       if (!ok) break;
       const int sa = g % kASlots, ra = g / kASlots;
-      const uint32_t s2 = bf16x2_splat(sc_cur);
-      sc_cur = sc_nxt;
-      advance(pf, 2);                               // pf now at slab g + 4
-      sc_nxt = scale_of(pf);
+      const uint32_t s2a = bf16x2_splat(sc_cur0), s2b = bf16x2_splat(sc_cur1);
+      sc_cur0 = sc_nxt0;
+      sc_cur1 = sc_nxt1;
+      advance(pf, kDeqSets);                        // pf now at this set's slab after the next
+      sc_nxt0 = scale_of(pf, 0);
+      sc_nxt1 = scale_of(pf, 1);
       if (!mbar_wait_warp(&tl->w_full[sa], ra & 1, p.cap, abort, p.err)) { ok = false; break; }
-      const uint4 w4 = *reinterpret_cast<const uint4*>(wsm + sa * kWStageBytes + row * (kBK / 2) + 16 * h);
-      const uint32_t v[4] = {w4.x, w4.y, w4.z, w4.w};
-      uint32_t out[16];
+      const uint4 wa = *reinterpret_cast<const uint4*>(wsm + sa * kWStageBytes + row * (kBK / 2));
+      const uint4 wb = *reinterpret_cast<const uint4*>(wsm + sa * kWStageBytes + row * (kBK / 2) + 16);
+      const uint32_t v[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      uint32_t out[32];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         uint32_t pq[4], nat[4];
-        int4x8_kperm(v[j], s2, pq);
+        int4x8_kperm(v[j], j < 4 ? s2a : s2b, pq);
         kperm4_to_natural(pq, nat);
         out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
         out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
@@ -319,7 +325,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         if (!mbar_wait_warp(&tl->a_empty[sa], (ra - 1) & 1, p.cap, abort, p.err)) { ok = false; break; }
         tc_fence_after();
       }
-      tmem_st16(lane_base + sa * kACols, out);
+      {
+        const uint32_t (&o0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&out[0]);
+        const uint32_t (&o1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&out[16]);
+        tmem_st16(lane_base + sa * kACols, o0);
+        tmem_st16(lane_base + sa * kACols + 16, o1);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&tl->a_full[sa]);
