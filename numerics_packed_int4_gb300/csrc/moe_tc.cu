@@ -22,16 +22,18 @@
 //   warp 1       TMEM allocation for the pair; in the even CTA one lane issues
 //                the MMAs, one multicast tcgen05.commit per slab
 //   warp 2       TMA producer for the CTA's 128 E4M3 activation rows (8 stages)
-//   warps 3-18   dequant producers (two sets of 8 taking alternate slabs) into
-//                8 tensor-memory slots, then the epilogue
+//   warps 3-18   dequant producers (four sets of 4, one warp per TMEM lane
+//                quarter, each set taking every fourth slab; a thread decodes
+//                its row's whole 64-k slab) into 8 tensor-memory slots, then
+//                the epilogue
 //   warps 19-22  converters: E4M3 stage -> fp16 stage in the 128-byte swizzled
 //                K-major layout (cvt.rn.f16x2.e4m3x2), 8 stages
 //   warp 23      scheduler (even CTA): waits for slab_full and publishes the
 //                ready count that the MMA issuer polls
 //   warps 24-27  relays (odd CTA): each takes every fourth slab, waits for the
 //                CTA's local half_full and arrives on the even CTA's slab_full
-// Barriers: slab_full (even CTA: its 8 dequant + 4 converter warps of the slab
-// and one relay arrival), half_full (odd CTA: the same 12 local arrivals),
+// Barriers: slab_full (even CTA: its 4 dequant + 4 converter warps of the slab
+// and one relay arrival), half_full (odd CTA: the same 8 local arrivals),
 // a_empty (the pair's MMAs of the slab completed; frees the A slot and the
 // fp16 stage in both CTAs), x_full / x_empty (E4M3 stage), w_full / w_empty
 // (packed weights), acc_full.  The relays exist because the cross-CTA arrive
@@ -60,7 +62,9 @@ constexpr int mHT = mTT / 2;             // activation rows held by each CTA
 constexpr int mBK = 64;                  // k per slab
 constexpr int mSlots = 8;                // fp16 stages = TMEM A slots = packed-weight stages
 constexpr int mXStages = 8;              // E4M3 stages
-constexpr int mDeqWarps = 16;            // two sets of 8: even and odd slabs
+constexpr int mDeqWarps = 16;            // four sets of 4 (one per TMEM lane quarter)
+constexpr int mDeqSet = 4;
+constexpr int mDeqSets = mDeqWarps / mDeqSet;
 constexpr int mCvtWarps = 4;
 constexpr int mRelays = 4;
 constexpr int mDeq0 = 3;
@@ -71,7 +75,7 @@ constexpr int mThreads = (mRelay0 + mRelays) * 32;
 constexpr int mBStage = mHT * mBK * 2;   // 16 KB fp16 activations (swizzled)
 constexpr int mXStage = mHT * mBK;       // 8 KB E4M3 activations (TMA)
 constexpr int mWStage = mTW * mBK / 2;   // 4 KB packed INT4 weights (TMA)
-constexpr int mLocalArrivals = mDeqWarps / 2 + mCvtWarps;   // per CTA per slab
+constexpr int mLocalArrivals = mDeqSet + mCvtWarps;   // per CTA per slab
 constexpr uint32_t mTmemCols = 512;
 constexpr uint32_t mACol0 = 256;
 constexpr uint32_t mACols = mBK / 2;
@@ -179,7 +183,7 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       mbar_init(&tl->half_full[s], mLocalArrivals);
       mbar_init(&tl->a_empty[s], 1);                      // the pair's multicast commit
       mbar_init(&tl->w_full[s], 1);
-      mbar_init(&tl->w_empty[s], mDeqWarps / 2);
+      mbar_init(&tl->w_empty[s], mDeqSet);
     }
     for (int s = 0; s < mXStages; ++s) {
       mbar_init(&tl->x_full[s], 1);
@@ -313,7 +317,7 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
   } else {
     // ---------------- dequant producers, then the epilogue ----------------
     const int dw = warp - mDeq0;
-    const int q = warp & 3, h = (dw >> 2) & 1, par = dw >> 3;
+    const int q = warp & 3, set = dw >> 2;
     const int row = 32 * q + lane;
     const int n = min(n0 + row, p.N - 1);
     const int ng = p.K / 128;
@@ -352,19 +356,20 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       ex = min(max(12 - e2, -100), 100);
     }
     const float up = ldexpf(1.f, ex), down = ldexpf(1.f, -ex);
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + mACol0 + 16 * h;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + mACol0;
 
-    uint16_t sc_next = par < nslab ? __ldg(srow + (par * mBK) / 128) : 0;
-    for (int s = par; s < nslab; s += 2) {
+    uint16_t sc_next = set < nslab ? __ldg(srow + (set * mBK) / 128) : 0;
+    for (int s = set; s < nslab; s += mDeqSets) {
       const int sa = s % mSlots, ra = s / mSlots;
       const uint32_t s2 = bf16x2_splat(f32_to_f16_bits(bf16_bits_to_f32(sc_next) * up));
-      if (s + 2 < nslab) sc_next = __ldg(srow + ((s + 2) * mBK) / 128);
+      if (s + mDeqSets < nslab) sc_next = __ldg(srow + ((s + mDeqSets) * mBK) / 128);
       if (!mbar_wait_warp(&tl->w_full[sa], ra & 1, p.cap, abort, p.err)) break;
-      const uint4 w4 = *reinterpret_cast<const uint4*>(wsm + sa * mWStage + row * (mBK / 2) + 16 * h);
-      const uint32_t v[4] = {w4.x, w4.y, w4.z, w4.w};
-      uint32_t out[16];
+      const uint4 wa = *reinterpret_cast<const uint4*>(wsm + sa * mWStage + row * (mBK / 2));
+      const uint4 wb = *reinterpret_cast<const uint4*>(wsm + sa * mWStage + row * (mBK / 2) + 16);
+      const uint32_t v[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      uint32_t out[32];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         uint32_t pq[4], nat[4];
         int4x8_kperm_f16(v[j], s2, pq);
         kperm4_to_natural(pq, nat);
@@ -376,7 +381,12 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
         if (!mbar_wait_warp(&tl->a_empty[sa], (ra - 1) & 1, p.cap, abort, p.err)) break;
         tc_fence_after();
       }
-      tmem_st16(lane_base + sa * mACols, out);
+      {
+        const uint32_t (&o0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&out[0]);
+        const uint32_t (&o1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&out[16]);
+        tmem_st16(lane_base + sa * mACols, o0);
+        tmem_st16(lane_base + sa * mACols + 16, o1);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&local_full[sa]);
