@@ -49,6 +49,19 @@ def dequant_int4(packed, s_bits, g):
     return F.bf16_encode(prod.reshape(q.shape))
 
 
+def dequant_int4_zp(packed, s_bits, z, g):
+    """Canonical asymmetric INT4 dequant ("Numerics": x = s (q - z); vLLM's
+    ``(iweights - zeros) * scales``): bf16_RNE((q - z) * s) with q, z unsigned
+    nibbles.  q - z is an integer in [-15, 15] and s a bf16, so the fp32
+    product is exact and there is one rounding."""
+    q = Q.unpack_nibbles(packed).astype(np.int64)
+    zz = np.asarray(z).astype(np.int64)
+    d = (q.reshape(q.shape[:-1] + (-1, g)) - zz[..., None]).astype(F32)
+    s = F.bf16_decode(s_bits).astype(F32)
+    prod = (d * s[..., None]).astype(F32)                                     # exact
+    return F.bf16_encode(prod.reshape(q.shape))
+
+
 def dequant_fp8(codes):
     return F.bf16_encode(F.e4m3_decode(codes))
 

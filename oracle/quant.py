@@ -224,6 +224,34 @@ def quant_int4_rtn(w, g):
     return pack_nibbles((q & 0xF).reshape(np.asarray(w).shape)), s_bits
 
 
+def quant_int4_zp(w, g):
+    """Asymmetric INT4 with a zero point per group of g.
+
+    "Numerics" gives the affine map x = s * (q - z) with an integer zero point
+    z (z != 0: asymmetric) and vLLM's dequant line ``(iweights - zeros) *
+    scales``, but prints no quantizer.  Reading (min-max, the plainest one):
+    per group lo = min(w), hi = max(w); s = bf16_RNE((hi - lo) / 15) with the
+    subtraction and division in fp32; a group with hi == lo, or whose bf16
+    scale underflows to zero, gets s = 1 (the page's all-zero-group policy);
+    z = clamp(round_half_even(-lo / s), 0, 15); q = clamp(round_half_even(w / s)
+    + z, 0, 15), every division in fp32.  q and z are unsigned nibbles.
+    Returns (packed [N, K/2] uint8 unsigned nibbles, scales [N, K/g] bf16 bits,
+    zero points [N, K/g] uint8).  parity unpinned beyond its invariants.
+    """
+    wb = _blocks(np.asarray(w, dtype=F32), g)
+    lo = np.min(wb, axis=-1)
+    hi = np.max(wb, axis=-1)
+    s_bits = F.bf16_encode(((hi - lo).astype(F32) / F32(15.0)).astype(F32))
+    s_val = F.bf16_decode(s_bits).astype(F32)
+    flat = s_val == 0
+    s_bits = np.where(flat, np.uint16(0x3F80), s_bits).astype(np.uint16)
+    s_val = np.where(flat, F32(1.0), s_val).astype(F32)
+    z = np.clip(np.rint((-lo / s_val).astype(F32)), 0, 15).astype(np.int64)
+    t = (wb / s_val[..., None]).astype(F32)
+    q = np.clip(np.rint(t) + z[..., None], 0, 15).astype(np.int64)
+    return pack_nibbles(q.reshape(np.asarray(w).shape)), s_bits, z.astype(np.uint8)
+
+
 def quant_fp8_channel(w):
     """FP8 E4M3 with one fp32 scale per output channel (row of W [N, K]).
 

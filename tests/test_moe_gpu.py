@@ -127,3 +127,26 @@ def test_moe_layer_small(qg):
     out_ref = OG.moe_combine(down_ref, rows, wts, T)
     check_gemm(OF.bf16_decode(host(gu)), OF.bf16_decode(gu_ref), "gate/up")
     check_gemm(OF.bf16_decode(host(out)), OF.bf16_decode(out_ref), "moe out")
+
+
+@pytest.mark.parametrize("R,I", [(1, 8), (37, 384), (300, 1408), (64, 14336)])
+def test_swiglu_quant_vs_oracle(qg, R, I):
+    """SwiGLU + per-row FP8 requantization against the oracle's fp64 SwiGLU
+    (rounded once to fp32) and FP8 quantizer.  The kernel evaluates SiLU with
+    the fast exponential and division, so h carries a few fp32 ulps of error:
+    a code may differ by one E4M3 step where h / s lies within those ulps of a
+    rounding midpoint, the row scale by a few ulps, and nothing more."""
+    gu = OF.bf16_encode((inputs.activations_bf16(R, 2 * I, seed=R + I).astype(np.uint32) << 16)
+                        .view(np.float32) * np.float32(3.0))
+    hq, hs = empty((R, I), torch.uint8), empty((R,), torch.float32)
+    qg.qg_swiglu_quant_fp8(dev(gu), hq, hs, R, I)
+    qg.qg_check_device_error()
+    ref_q, ref_s = OQ.quant_fp8_block(OG.swiglu_f32(gu, I), I)
+    q, s = host(hq), host(hs)
+    assert np.allclose(s, ref_s[:, 0], rtol=4 * 2.0 ** -23, atol=0)
+    # compare by E4M3 grid position: sign-magnitude code -> ordinal
+    ordv = lambda c: np.where(c & 0x80, -(c.astype(np.int32) & 0x7F), c.astype(np.int32) & 0x7F)
+    d = np.abs(ordv(q) - ordv(ref_q))
+    assert d.max() <= 1, d.max()
+    assert np.mean(d != 0) < 1e-3, np.mean(d != 0)
+

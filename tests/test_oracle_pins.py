@@ -346,6 +346,69 @@ def test_int4_rtn_invariants():
             assert np.all(np.abs(q[i, g] * s[i, g] - wb[i, g]) <= s[i, g] / 2 * (1 + 2.0 ** -7))
 
 
+def test_int4_zp_worked_example():
+    """A hand-derived group of 4 (g = 4) under the asymmetric reading of
+    "Numerics" (x = s (q - z)): lo = -0.3, hi = 1.2, (hi - lo) / 15 = 0.1 in
+    fp32, whose bf16 rounding is 0x3DCD = 0.10009765625; z = rint(0.3 / s) =
+    rint(2.997..) = 3; q = rint(w / s) + z = (-3, 0, 4, 12) + 3 = (0, 3, 7, 15).
+    Dequant (q - z) s = (-3, 0, 4, 12) * s = (-0.30029296875, 0, 0.400390625,
+    1.201171875), whose bf16 roundings are (-0.30078125, 0, 0.400390625,
+    1.203125) (0.201171875 * 128 = 25.75 rounds up to 26)."""
+    w = np.array([[-0.3, 0.0, 0.45, 1.2]], np.float32)
+    packed, sb, z = Q.quant_int4_zp(w, 4)
+    assert int(sb[0, 0]) == 0x3DCD and int(z[0, 0]) == 3
+    assert list(Q.unpack_nibbles(packed)[0]) == [0, 3, 7, 15]
+    deq = F.bf16_decode(G.dequant_int4_zp(packed, sb, z, 4))[0]
+    assert list(deq) == [-0.30078125, 0.0, 0.400390625, 1.203125]
+
+
+def test_int4_zp_invariants():
+    r = np.random.Generator(np.random.PCG64(17))
+    w = (r.standard_normal((8, 512)) * 0.02 + 0.01).astype(np.float32)
+    w[3, 64:128] = 0
+    w[5, 0:64] = 0.25                                # constant nonzero group
+    packed, sb, z = Q.quant_int4_zp(w, 64)
+    q = Q.unpack_nibbles(packed).reshape(8, 8, 64).astype(np.int64)
+    s = F.bf16_decode(sb)
+    assert sb[3, 1] == 0x3F80 and z[3, 1] == 0 and np.all(q[3, 1] == 0)   # all-zero policy
+    assert sb[5, 0] == 0x3F80                        # flat group: s = 1 as well
+    assert np.all(z <= 15) and np.all(q <= 15)
+    wb = w.reshape(8, 8, 64).astype(np.float64)
+    for i in range(8):
+        for g in range(8):
+            if (i, g) in ((3, 1), (5, 0)):
+                continue
+            lo_i, hi_i = np.argmin(wb[i, g]), np.argmax(wb[i, g])
+            assert q[i, g, lo_i] == 0 or z[i, g] == 0    # the minimum maps to code 0 (unless z clamps)
+            err = np.abs((q[i, g] - int(z[i, g])) * s[i, g] - wb[i, g])
+            assert np.all(err <= s[i, g] * (0.5 + 2.0 ** -6)), (i, g, err.max() / s[i, g])
+
+
+def test_int4_zp_at_z8_is_the_symmetric_dequant():
+    """With z = 8 and the unsigned nibble u = q + 8, s (u - z) is s q: the
+    asymmetric dequant must reproduce the (separately pinned) symmetric one bit
+    for bit, for every q in [-8, 7] and a spread of bf16 scales."""
+    r = np.random.Generator(np.random.PCG64(18))
+    s_bits = r.integers(0x2000, 0x5000, (32, 2)).astype(np.uint16)
+    q = np.tile(np.arange(-8, 8), 16).reshape(1, 256).repeat(32, 0)
+    sym = G.dequant_int4(Q.pack_nibbles(q & 0xF), s_bits, 128)
+    asym = G.dequant_int4_zp(Q.pack_nibbles(q + 8), s_bits, np.full((32, 2), 8, np.uint8), 128)
+    assert np.array_equal(sym, asym)
+
+
+def test_dequant_int4_zp_is_one_rounding_of_the_exact_product():
+    r = np.random.Generator(np.random.PCG64(19))
+    s_bits = r.integers(0x3000, 0x4400, 16).astype(np.uint16)
+    u = np.arange(16)
+    for zv in range(16):
+        packed = Q.pack_nibbles(np.tile(u, 4).reshape(1, 64).repeat(16, 0))
+        deq = F.bf16_decode(G.dequant_int4_zp(packed, s_bits.reshape(16, 1), np.full((16, 1), zv, np.uint8), 64))
+        for n in range(16):
+            sv = Fraction(float(F.bf16_decode(s_bits[n])))
+            for k in range(16):
+                assert Fraction(float(deq[n, k])) == _nearest_bf16_fraction((int(u[k]) - zv) * sv)
+
+
 def test_nvfp4_invariants():
     r = np.random.Generator(np.random.PCG64(15))
     w = (r.standard_normal((8, 256)) * 0.02).astype(np.float32)
