@@ -85,6 +85,19 @@ QG_API qg_status qgemm_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g,
                       const uint16_t* x, uint16_t* y, int M, int N, int K,
                       qg_stream_t stream);
 
+/* W4A16 with asymmetric INT4: unsigned 4-bit codes and one zero point per
+ * group ("Numerics": x = s (q - z), z an integer, z != 0 asymmetric; the
+ * dequant line (iweights - zeros) * scales).  y[m,n] = sum_k x[m,k] *
+ * bf16_RNE((q[n,k] - z[n,k/g]) * s[n,k/g]), fp32 accumulation, one bf16
+ * rounding.  Same kernels as qgemm_w4a16 (GEMV for M <= 16, tcgen05 above).
+ *   w_q [N][K/2] unsigned nibbles (even k low)   w_s [N][K/g] bf16
+ *   w_z [N][K/g] uint8 zero points in [0, 15]    x [M][K] bf16  y [M][N] bf16
+ * Rules as qgemm_w4a16 (g a power of two >= 32 dividing K, K % 128 == 0,
+ * N % 8 == 0); w_z needs no alignment.                                      */
+QG_API qg_status qgemm_w4a16_zp(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g,
+                         const uint16_t* x, uint16_t* y, int M, int N, int K,
+                         qg_stream_t stream);
+
 /* FP8 E4M3 weights with one fp32 scale per output channel.
  * y[m,n] = w_cs[n] * sum_k x[m,k] * e4m3(w[n,k]); the E4M3 -> bf16 decode is
  * exact ("Every E4M3 and E2M1 value is exactly representable in FP16/BF16",
@@ -183,6 +196,14 @@ QG_API qg_status qg_w4a8_fp8_scales(const uint16_t* w_s, uint8_t* w_s8, float* w
  * "Define an all-zero-group policy such as s=1").  K % g == 0, g % 8 == 0. */
 QG_API qg_status qg_quantize_weights_int4(const float* w, uint8_t* w_q, uint16_t* w_s, int g,
                                    int N, int K, qg_stream_t stream);
+/* Asymmetric INT4 with zero points, one per group of g (the reading of
+ * "Numerics" for a quantizer the pages do not print): lo/hi = group min/max,
+ * s = bf16_RNE((hi - lo) / 15) in fp32 (flat group or s rounding to 0: s = 1),
+ * z = clamp(rint(-lo / s), 0, 15), q = clamp(rint(w / s) + z, 0, 15) with IEEE
+ * fp32 divisions.  w [N][K] fp32 -> w_q [N][K/2] unsigned nibbles, w_s [N][K/g]
+ * bf16, w_z [N][K/g] uint8.  g a power of two in [8, 256] dividing K.       */
+QG_API qg_status qg_quantize_weights_int4_zp(const float* w, uint8_t* w_q, uint16_t* w_s,
+                                      uint8_t* w_z, int g, int N, int K, qg_stream_t stream);
 /* FP8 E4M3 per output channel: cs = absmax/448 (zero row: 1), code =
  * E4M3_RNE_satfinite(w / cs).  K % 8 == 0.                                  */
 QG_API qg_status qg_quantize_weights_fp8(const float* w, uint8_t* w_e4m3, float* w_cs,
@@ -230,6 +251,12 @@ QG_API qg_status qg_moe_combine(const uint16_t* down, const int32_t* row_of,
  * NULL); MXFP4 -> E8M0 [N][K/32]; NVFP4 -> E4M3 [N][K/16].  K % 128 == 0.    */
 QG_API qg_status qg_dequant_weights(int fmt, const uint8_t* w, const void* scales, int g,
                              uint16_t* w_out, int N, int K, qg_stream_t stream);
+/* Test-only: the canonical asymmetric INT4 dequant bf16_RNE((q - z) * s) of a
+ * whole matrix, with the decode routine of qgemm_w4a16_zp.  Arguments as
+ * qgemm_w4a16_zp; w_out [N][K] bf16.  K % 128 == 0.                         */
+QG_API qg_status qg_dequant_weights_int4_zp(const uint8_t* w_q, const uint16_t* w_s,
+                                     const uint8_t* w_z, int g, uint16_t* w_out, int N, int K,
+                                     qg_stream_t stream);
 
 /* Synchronizes the stream, then reads and clears this device's error word.
  * Returns QG_ERR_TIMEOUT if a kernel gave up on a wait, QG_ERR_CUDA on an

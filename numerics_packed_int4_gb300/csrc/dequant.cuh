@@ -3,7 +3,9 @@
 // Every routine produces the canonical dequantized weight bit for bit:
 //   INT4   bf16_RNE(q * s): the nibble becomes the exact bf16 integer q with
 //          the magic-number trick ((u | 0x4300) - 136 with u = q + 8), then one
-//          bf16 multiply by the group scale rounds the exact product once;
+//          bf16 multiply by the group scale rounds the exact product once; with
+//          a zero point, bf16_RNE((u - z) * s) the same way ((u | 0x4300) -
+//          (128 + z));
 //   E4M3   exact: sign and the 7 exponent/mantissa bits move into bf16
 //          position with shift/and/or (the FP8 -> FP16 bit trick described in
 //          "Your 3090 Isn't Missing Anything...", section 4.1, with the bf16
@@ -41,6 +43,22 @@ QG_DEVICE void int4x8_kperm(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {
   p[3] = lop3<kLutAndXor>(v >> 12, 0x000F000Fu, 0x43084308u);
 #pragma unroll
   for (int i = 0; i < 4; ++i) p[i] = bf16x2_mul(bf16x2_sub(p[i], kBf16x2_136), s2);
+}
+
+// ---- INT4 with a zero point -----------------------------------------------------
+// Unsigned nibble u, group zero point z and scale s: (u | 0x4300) is the exact
+// bf16 128 + u; subtracting zb2 = bf16x2(128 + z) leaves the exact integer
+// u - z in [-15, 15], and one bf16 multiply by s rounds (u - z) * s once --
+// the canonical bf16_RNE((q - z) * s), at the cost of the symmetric decode.
+QG_DEVICE uint32_t bf16x2_zero128(uint32_t z) { return (0x4300u | (z & 0xFu)) * 0x00010001u; }
+// p[i] = (k_i, k_{i+4}) for i = 0..3
+QG_DEVICE void int4zp_x8_kperm(uint32_t v, uint32_t s2, uint32_t zb2, uint32_t (&p)[4]) {
+  p[0] = lop3<kLutAndOr>(v, 0x000F000Fu, 0x43004300u);      // 0x4300 | nibble = 128 + u
+  p[1] = lop3<kLutAndOr>(v >> 4, 0x000F000Fu, 0x43004300u);
+  p[2] = lop3<kLutAndOr>(v >> 8, 0x000F000Fu, 0x43004300u);
+  p[3] = lop3<kLutAndOr>(v >> 12, 0x000F000Fu, 0x43004300u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = bf16x2_mul(bf16x2_sub(p[i], zb2), s2);
 }
 
 // ---- E2M1 -------------------------------------------------------------------

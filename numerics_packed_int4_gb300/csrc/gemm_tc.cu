@@ -73,6 +73,7 @@ constexpr uint32_t kDrainCap = 1u << 21;            // waits on work already iss
 struct TcArgs {
   const uint8_t* wq;
   const uint16_t* ws;
+  const uint8_t* wz;                   // zero points [N][K/g] (asymmetric INT4) or nullptr
   uint16_t* y;
   int M, N, K, g, lg;
   int tiles_t, tiles_w, group_t;
@@ -105,6 +106,7 @@ QG_DEVICE void tile_origin(const TcArgs& p, int tile, int& m0, int& n0) {
   n0 = (within / gsize) * kTileW;
 }
 
+template <bool ZP>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                 const TcArgs p) {
@@ -246,20 +248,29 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     const int cq = set;                             // epilogue: 64 of the 256 token columns
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + kACol0;
     // scale cursor: tile index, slab in the tile, this thread's scale row
-    struct Cur { int i, s; const uint16_t* srow; };
+    // (and, with zero points, its zero-point row)
+    struct Cur { int i, s; const uint16_t* srow; const uint8_t* zrow; };
     auto set_row = [&](Cur& c) {
       if (c.i < ntiles) {
         int m0, n0;
         tile_origin(p, tile_of(c.i), m0, n0);
-        c.srow = p.ws + (size_t)min(n0 + row, p.N - 1) * (p.K >> p.lg);
+        const size_t r = (size_t)min(n0 + row, p.N - 1) * (p.K >> p.lg);
+        c.srow = p.ws + r;
+        if constexpr (ZP) c.zrow = p.wz + r;
       }
     };
     auto advance = [&](Cur& c, int by) {
       c.s += by;
       while (c.s >= nslab) { c.s -= nslab; ++c.i; set_row(c); }
     };
-    auto scale_of = [&](const Cur& c, int h) -> uint16_t {
-      return c.i < ntiles ? __ldg(c.srow + ((c.s * kBK + 32 * h) >> p.lg)) : (uint16_t)0;
+    // group scale of the 32-k half h (bits 0-15) and, with zero points, its
+    // zero point (bits 16-19)
+    auto scale_of = [&](const Cur& c, int h) -> uint32_t {
+      if (c.i >= ntiles) return 0u;
+      const int grp = (c.s * kBK + 32 * h) >> p.lg;
+      uint32_t v = __ldg(c.srow + grp);
+      if constexpr (ZP) v |= (uint32_t)__ldg(c.zrow + grp) << 16;
+      return v;
     };
     // epilogue of tile e: TMEM -> registers -> (accumulator free) -> bf16 -> Y
     auto epilogue = [&](int e) -> bool {
@@ -288,12 +299,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     };
     int e_next = 0;                                 // next tile whose epilogue this warp owes
     bool ok = true;
-    Cur pf{0, 0, nullptr};
+    Cur pf{0, 0, nullptr, nullptr};
     set_row(pf);
     advance(pf, set);
-    uint16_t sc_cur0 = scale_of(pf, 0), sc_cur1 = scale_of(pf, 1);
+    uint32_t sc_cur0 = scale_of(pf, 0), sc_cur1 = scale_of(pf, 1);
     advance(pf, kDeqSets);
-    uint16_t sc_nxt0 = scale_of(pf, 0), sc_nxt1 = scale_of(pf, 1);
+    uint32_t sc_nxt0 = scale_of(pf, 0), sc_nxt1 = scale_of(pf, 1);
     for (int g = set; g < total; g += kDeqSets) {
       while (e_next < ntiles - 1 && g >= (e_next + 1) * nslab + kASlots) {
         if (!(ok = epilogue(e_next))) break;
@@ -302,6 +313,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       if (!ok) break;
       const int sa = g % kASlots, ra = g / kASlots;
       const uint32_t s2a = bf16x2_splat(sc_cur0), s2b = bf16x2_splat(sc_cur1);
+      const uint32_t z2a = bf16x2_zero128(sc_cur0 >> 16), z2b = bf16x2_zero128(sc_cur1 >> 16);
       sc_cur0 = sc_nxt0;
       sc_cur1 = sc_nxt1;
       advance(pf, kDeqSets);                        // pf now at this set's slab after the next
@@ -315,7 +327,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         uint32_t pq[4], nat[4];
-        int4x8_kperm(v[j], j < 4 ? s2a : s2b, pq);
+        if constexpr (ZP)
+          int4zp_x8_kperm(v[j], j < 4 ? s2a : s2b, j < 4 ? z2a : z2b, pq);
+        else
+          int4x8_kperm(v[j], j < 4 ? s2a : s2b, pq);
         kperm4_to_natural(pq, nat);
         out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
         out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
@@ -411,20 +426,20 @@ bool make_bf16_tmap(CUtensorMap* m, const void* base, int rows, int cols, int bo
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint16_t* x, uint16_t* y,
-                        int M, int N, int K, cudaStream_t st, bool* handled) {
+qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g, const uint16_t* x,
+                        uint16_t* y, int M, int N, int K, cudaStream_t st, bool* handled, const char* name) {
   *handled = false;
   if (M <= 16 || K % kBK != 0 || g < 32 || (g & (g - 1)) != 0 || K % g != 0) return QG_OK;   // decode path
   *handled = true;
   CUtensorMap tmap, tmap_w;
   if (!make_bf16_tmap(&tmap, x, M, K, kTileT, kBK))
-    return set_error(QG_ERR_CUDA, "qgemm_w4a16: cannot encode the activation tensor map");
+    return set_error(QG_ERR_CUDA, "%s: cannot encode the activation tensor map", name);
   if (!make_u8_tmap(&tmap_w, w_q, N, K / 2, kTileW, kBK / 2))
-    return set_error(QG_ERR_CUDA, "qgemm_w4a16: cannot encode the weight tensor map");
+    return set_error(QG_ERR_CUDA, "%s: cannot encode the weight tensor map", name);
   unsigned int* err = device_error_word();
-  if (!err) return set_error(QG_ERR_CUDA, "qgemm_w4a16: no device error word");
+  if (!err) return set_error(QG_ERR_CUDA, "%s: no device error word", name);
   TcArgs a{};
-  a.wq = w_q; a.ws = w_s; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
+  a.wq = w_q; a.ws = w_s; a.wz = w_z; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
   a.lg = 0;
   while ((1 << a.lg) < g) ++a.lg;
   a.tiles_t = (M + kTileT - 1) / kTileT;
@@ -433,11 +448,12 @@ qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const ui
   a.err = err;
   a.cap = wait_limit();
   const int smem = kStages * kXStageBytes + kASlots * kWStageBytes + (int)sizeof(TcSmemTail) + 1024;
-  if (!ensure_smem(w4a16_tc_kernel, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a16: smem attribute");
+  auto kern = w_z ? w4a16_tc_kernel<true> : w4a16_tc_kernel<false>;
+  if (!ensure_smem(kern, smem)) return set_error(QG_ERR_CUDA, "%s: smem attribute", name);
   const long long tiles = (long long)a.tiles_t * a.tiles_w;
   const int grid = (int)std::min<long long>(tiles, (long long)sm_count());   // persistent: one CTA per SM
-  w4a16_tc_kernel<<<grid, kThreadsTc, smem, st>>>(tmap, tmap_w, a);
-  return check_launch("qgemm_w4a16 (prefill)");
+  kern<<<grid, kThreadsTc, smem, st>>>(tmap, tmap_w, a);
+  return check_launch(name);
 }
 
 }  // namespace qg

@@ -33,7 +33,7 @@
 namespace qg {
 namespace {
 
-enum Fmt { F_INT4 = 0, F_FP8 = 1, F_MXFP4 = 2, F_NVFP4 = 3 };
+enum Fmt { F_INT4 = 0, F_FP8 = 1, F_MXFP4 = 2, F_NVFP4 = 3, F_INT4Z = 4 };
 
 constexpr int kWarps = 8;
 constexpr int kRing = 6;               // weight segments in flight per warp (cp.async ring)
@@ -42,6 +42,7 @@ static_assert(kRing % kPFS == 0, "the scale ring index u % kPFS must equal s % k
 
 template <int FMT> struct FmtTraits;
 template <> struct FmtTraits<F_INT4>  { static constexpr int KSEG = 128, CPL = 4; };
+template <> struct FmtTraits<F_INT4Z> { static constexpr int KSEG = 128, CPL = 4; };
 template <> struct FmtTraits<F_MXFP4> { static constexpr int KSEG = 128, CPL = 4; };
 template <> struct FmtTraits<F_NVFP4> { static constexpr int KSEG = 128, CPL = 4; };
 template <> struct FmtTraits<F_FP8>   { static constexpr int KSEG = 64,  CPL = 2; };
@@ -49,6 +50,7 @@ template <> struct FmtTraits<F_FP8>   { static constexpr int KSEG = 64,  CPL = 2
 struct GemvArgs {
   const uint8_t* w;        // packed weights [N][row_bytes]
   const void* scales;      // per-format scale array (or channel scales for FP8)
+  const uint8_t* zeros;    // INT4 zero points [N][K/g] (F_INT4Z) or nullptr
   const float* gscale;     // NVFP4 global scale (device scalar) or nullptr
   const uint16_t* x;       // [M][K] bf16
   uint16_t* y;             // [M][N] bf16
@@ -77,18 +79,29 @@ struct Scale { uint32_t a, b; };
 template <int FMT>
 QG_DEVICE const uint8_t* scale_row(const GemvArgs& p, int n) {
   const uint8_t* base = static_cast<const uint8_t*>(p.scales);
-  if constexpr (FMT == F_INT4) return base + (size_t)n * (size_t)(p.K >> p.lg) * 2;
+  if constexpr (FMT == F_INT4 || FMT == F_INT4Z) return base + (size_t)n * (size_t)(p.K >> p.lg) * 2;
   if constexpr (FMT == F_MXFP4) return base + (size_t)n * (size_t)(p.K / 32);
   if constexpr (FMT == F_NVFP4) return base + (size_t)n * (size_t)(p.K / 16);
   return base;
 }
 
+// Zero-point row of output channel n (F_INT4Z only).
 template <int FMT>
-QG_DEVICE Scale load_scale(const GemvArgs& p, const uint8_t* srow, int seg, int t) {
+QG_DEVICE const uint8_t* zero_row(const GemvArgs& p, int n) {
+  if constexpr (FMT == F_INT4Z) return p.zeros + (size_t)n * (size_t)(p.K >> p.lg);
+  return nullptr;
+}
+
+template <int FMT>
+QG_DEVICE Scale load_scale(const GemvArgs& p, const uint8_t* srow, const uint8_t* zrow, int seg, int t) {
   Scale s{0u, 0u};
   if constexpr (FMT == F_INT4) {
     const int grp = (seg * 128 + 32 * t) >> p.lg;
     s.a = bf16x2_splat(__ldg(reinterpret_cast<const uint16_t*>(srow) + grp));
+  } else if constexpr (FMT == F_INT4Z) {
+    const int grp = (seg * 128 + 32 * t) >> p.lg;
+    s.a = bf16x2_splat(__ldg(reinterpret_cast<const uint16_t*>(srow) + grp));
+    s.b = bf16x2_zero128(__ldg(zrow + grp));
   } else if constexpr (FMT == F_MXFP4) {
     s.a = __ldg(srow + seg * 4 + t);
   } else if constexpr (FMT == F_NVFP4) {
@@ -111,6 +124,8 @@ QG_DEVICE void decode_chunk(const uint4& w, const Scale& s, int j, uint32_t (&a)
   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
   if constexpr (FMT == F_INT4) {
     int4x8_kperm(ww[j], s.a, a);
+  } else if constexpr (FMT == F_INT4Z) {
+    int4zp_x8_kperm(ww[j], s.a, s.b, a);
   } else if constexpr (FMT == F_MXFP4) {
     e2m1x8_kperm(ww[j], e8m0_to_bf16x2(s.a), a);
   } else if constexpr (FMT == F_NVFP4) {
@@ -187,6 +202,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   const int n0 = min(nb + g, p.N - 1), n1 = min(nb + g + 8, p.N - 1);
   const uint8_t* sr0 = scale_row<FMT>(p, n0);
   const uint8_t* sr1 = scale_row<FMT>(p, n1);
+  const uint8_t* zr0 = zero_row<FMT>(p, n0);
+  const uint8_t* zr1 = zero_row<FMT>(p, n1);
   const uint8_t* w0 = p.w + (size_t)n0 * row_bytes + (size_t)(seg_lo + s_lo) * 64 + 16 * t;
   const uint8_t* w1 = p.w + (size_t)n1 * row_bytes + (size_t)(seg_lo + s_lo) * 64 + 16 * t;
 
@@ -216,8 +233,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
 #pragma unroll
   for (int u = 0; u < kPFS; ++u) {
     if (u < nseg) {
-      sa[u] = load_scale<FMT>(p, sr0, seg_lo + s_lo + u, t);
-      sb[u] = load_scale<FMT>(p, sr1, seg_lo + s_lo + u, t);
+      sa[u] = load_scale<FMT>(p, sr0, zr0, seg_lo + s_lo + u, t);
+      sb[u] = load_scale<FMT>(p, sr1, zr1, seg_lo + s_lo + u, t);
     }
   }
 
@@ -252,8 +269,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
         const int us = u % kPFS;
         const Scale s_a = sa[us], s_b = sb[us];
         if (s + kPFS < nseg) {
-          sa[us] = load_scale<FMT>(p, sr0, seg_lo + s_lo + s + kPFS, t);
-          sb[us] = load_scale<FMT>(p, sr1, seg_lo + s_lo + s + kPFS, t);
+          sa[us] = load_scale<FMT>(p, sr0, zr0, seg_lo + s_lo + s + kPFS, t);
+          sb[us] = load_scale<FMT>(p, sr1, zr1, seg_lo + s_lo + s + kPFS, t);
         }
         const int cbase = (s_lo + s) * (Tr::KSEG / 8) + t * Tr::CPL;
 #pragma unroll
@@ -327,8 +344,9 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
 // test-only canonical dequantization (same decode routines, natural order)
 // ---------------------------------------------------------------------------
 template <int FMT>
-__global__ void dequant_kernel(const uint8_t* __restrict__ w, const void* __restrict__ scales, int g,
-                               uint16_t* __restrict__ out, int N, int K) {
+__global__ void dequant_kernel(const uint8_t* __restrict__ w, const void* __restrict__ scales,
+                               const uint8_t* __restrict__ zeros, int g, uint16_t* __restrict__ out, int N,
+                               int K) {
   using Tr = FmtTraits<FMT>;
   const int t = threadIdx.x & 3;              // position inside a 64-byte segment
   const long long lane_id = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 2;
@@ -339,8 +357,8 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ w, const void* __rest
   const size_t row_bytes = (FMT == F_FP8) ? (size_t)K : (size_t)K / 2;
   const uint4 wv = *reinterpret_cast<const uint4*>(w + (size_t)n * row_bytes + seg * 64 + 16 * t);
   GemvArgs p{};
-  p.scales = scales; p.K = K; p.g = g; p.lg = 31 - __clz(g);
-  const Scale s = load_scale<FMT>(p, scale_row<FMT>(p, n), seg, t);
+  p.scales = scales; p.zeros = zeros; p.K = K; p.g = g; p.lg = 31 - __clz(g);
+  const Scale s = load_scale<FMT>(p, scale_row<FMT>(p, n), zero_row<FMT>(p, n), seg, t);
   uint16_t* o = out + (size_t)n * K + (size_t)seg * Tr::KSEG + t * Tr::CPL * 8;
 #pragma unroll
   for (int j = 0; j < Tr::CPL; ++j) {
@@ -450,14 +468,16 @@ qg_status check_common(const void* w, const void* x, const void* y, int M, int N
 
 }  // namespace
 
-// entry for the prefill path (gemm_tc.cu) when it declines a shape
-qg_status gemv_w4a16_any_m(const uint8_t* w_q, const uint16_t* w_s, int g, const uint16_t* x,
-                           uint16_t* y, int M, int N, int K, cudaStream_t st) {
+// entry for the prefill path (gemm_tc.cu) when it declines a shape; w_z
+// (zero points) selects the asymmetric format
+qg_status gemv_w4a16_any_m(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g,
+                           const uint16_t* x, uint16_t* y, int M, int N, int K, cudaStream_t st,
+                           const char* name) {
   GemvArgs a{};
-  a.w = w_q; a.scales = w_s; a.x = x; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
+  a.w = w_q; a.scales = w_s; a.zeros = w_z; a.x = x; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
   a.lg = 0;
   while ((1 << a.lg) < g) ++a.lg;
-  return run_weight_only<F_INT4>(a, st, "qgemm_w4a16");
+  return w_z ? run_weight_only<F_INT4Z>(a, st, name) : run_weight_only<F_INT4>(a, st, name);
 }
 
 }  // namespace qg
@@ -466,8 +486,8 @@ using qg::aligned16;
 
 // prefill dispatcher lives in gemm_tc.cu
 namespace qg {
-qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint16_t* x, uint16_t* y,
-                        int M, int N, int K, cudaStream_t st, bool* handled);
+qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g, const uint16_t* x,
+                        uint16_t* y, int M, int N, int K, cudaStream_t st, bool* handled, const char* name);
 }
 
 extern "C" {
@@ -483,10 +503,27 @@ qg_status qgemm_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (M > 16) {
     bool handled = false;
-    r = qg::prefill_w4a16(w_q, w_s, g, x, y, M, N, K, st, &handled);
+    r = qg::prefill_w4a16(w_q, w_s, nullptr, g, x, y, M, N, K, st, &handled, "qgemm_w4a16");
     if (handled) return r;
   }
-  return qg::gemv_w4a16_any_m(w_q, w_s, g, x, y, M, N, K, st);
+  return qg::gemv_w4a16_any_m(w_q, w_s, nullptr, g, x, y, M, N, K, st, "qgemm_w4a16");
+}
+
+qg_status qgemm_w4a16_zp(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g,
+                         const uint16_t* x, uint16_t* y, int M, int N, int K, qg_stream_t stream) {
+  qg_status r = qg::check_common(w_q, x, y, M, N, K, "qgemm_w4a16_zp");
+  if (r != QG_OK) return r;
+  QG_REQUIRE(w_s && w_z, QG_ERR_INVALID_ARG, "qgemm_w4a16_zp: NULL scales or zero points");
+  QG_REQUIRE(g >= 32 && (g & (g - 1)) == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
+             "qgemm_w4a16_zp: need g a power of two >= 32 dividing K (g=%d)", g);
+  if (M == 0) return QG_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (M > 16) {
+    bool handled = false;
+    r = qg::prefill_w4a16(w_q, w_s, w_z, g, x, y, M, N, K, st, &handled, "qgemm_w4a16_zp");
+    if (handled) return r;
+  }
+  return qg::gemv_w4a16_any_m(w_q, w_s, w_z, g, x, y, M, N, K, st, "qgemm_w4a16_zp");
 }
 
 qg_status qgemm_w8a16(const uint8_t* w_e4m3, const float* w_cs, const uint16_t* x, uint16_t* y,
@@ -544,23 +581,38 @@ qg_status qg_dequant_weights(int fmt, const uint8_t* w, const void* scales, int 
     case QG_FMT_INT4:
       QG_REQUIRE(scales && g >= 32 && (g & (g - 1)) == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
                  "qg_dequant_weights: INT4 needs scales and g a power of two >= 32");
-      qg::dequant_kernel<qg::F_INT4><<<grid(128), threads, 0, st>>>(w, scales, g, w_out, N, K);
+      qg::dequant_kernel<qg::F_INT4><<<grid(128), threads, 0, st>>>(w, scales, nullptr, g, w_out, N, K);
       break;
     case QG_FMT_FP8:
-      qg::dequant_kernel<qg::F_FP8><<<grid(64), threads, 0, st>>>(w, scales, g, w_out, N, K);
+      qg::dequant_kernel<qg::F_FP8><<<grid(64), threads, 0, st>>>(w, scales, nullptr, g, w_out, N, K);
       break;
     case QG_FMT_MXFP4:
       QG_REQUIRE(scales, QG_ERR_INVALID_ARG, "qg_dequant_weights: NULL scales");
-      qg::dequant_kernel<qg::F_MXFP4><<<grid(128), threads, 0, st>>>(w, scales, 32, w_out, N, K);
+      qg::dequant_kernel<qg::F_MXFP4><<<grid(128), threads, 0, st>>>(w, scales, nullptr, 32, w_out, N, K);
       break;
     case QG_FMT_NVFP4:
       QG_REQUIRE(scales, QG_ERR_INVALID_ARG, "qg_dequant_weights: NULL scales");
-      qg::dequant_kernel<qg::F_NVFP4><<<grid(128), threads, 0, st>>>(w, scales, 16, w_out, N, K);
+      qg::dequant_kernel<qg::F_NVFP4><<<grid(128), threads, 0, st>>>(w, scales, nullptr, 16, w_out, N, K);
       break;
     default:
       return qg::set_error(QG_ERR_INVALID_ARG, "qg_dequant_weights: unknown format %d", fmt);
   }
   return qg::check_launch("qg_dequant_weights");
+}
+
+qg_status qg_dequant_weights_int4_zp(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g,
+                                     uint16_t* w_out, int N, int K, qg_stream_t stream) {
+  QG_REQUIRE(w_q && w_s && w_z && w_out, QG_ERR_INVALID_ARG, "qg_dequant_weights_int4_zp: NULL pointer");
+  QG_REQUIRE(N >= 0 && K > 0, QG_ERR_INVALID_ARG, "qg_dequant_weights_int4_zp: bad sizes");
+  QG_REQUIRE(K % 128 == 0 && g >= 32 && (g & (g - 1)) == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
+             "qg_dequant_weights_int4_zp: need K %% 128 == 0 and g a power of two >= 32");
+  QG_REQUIRE(aligned16(w_q) && aligned16(w_out), QG_ERR_MISALIGNED, "qg_dequant_weights_int4_zp: misaligned");
+  if (N == 0) return QG_OK;
+  const int threads = 256;
+  const long long lanes = (long long)N * (K / 128) * 4;
+  qg::dequant_kernel<qg::F_INT4Z><<<unsigned((lanes + threads - 1) / threads), threads, 0,
+                                    reinterpret_cast<cudaStream_t>(stream)>>>(w_q, w_s, w_z, g, w_out, N, K);
+  return qg::check_launch("qg_dequant_weights_int4_zp");
 }
 
 }  // extern "C"

@@ -129,6 +129,42 @@ __global__ void __launch_bounds__(kThreads) int4_rtn_kernel(
   if ((c % GT) == 0) s[c / GT] = sb;
 }
 
+// Asymmetric INT4 with a zero point per group ("Numerics": x = s (q - z)):
+// lo / hi = min / max of the group, s = bf16_RNE((hi - lo) / 15) (fp32
+// subtraction and division; a flat group, or one whose scale rounds to zero,
+// gets s = 1), z = clamp(rint(-lo / s), 0, 15), q = clamp(rint(w / s) + z,
+// 0, 15), unsigned nibbles.
+template <int GT>
+__global__ void __launch_bounds__(kThreads) int4_zp_kernel(
+    const float* __restrict__ w, uint8_t* __restrict__ q, uint16_t* __restrict__ s, uint8_t* __restrict__ z,
+    long long nchunks) {
+  const long long c = blockIdx.x * (long long)kThreads + threadIdx.x;
+  const bool live = c < nchunks;
+  float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (live) Load8<float>::run(w + c * 8, v);
+  float mx = v[0], mn = v[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) { mx = fmaxf(mx, v[i]); mn = fminf(mn, v[i]); }
+  const float hi = group_max<GT>(mx);
+  const float lo = -group_max<GT>(-mn);
+  if (!live) return;
+  uint16_t sb = f32_to_bf16_bits(__fdiv_rn(__fsub_rn(hi, lo), 15.f));
+  float sf = bf16_bits_to_f32(sb);
+  if (sf == 0.f) { sb = 0x3F80; sf = 1.f; }     // flat or all-zero group: s = 1
+  const float zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, sf)), 0.f), 15.f);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float t = fminf(fmaxf(rintf(__fdiv_rn(v[i], sf)) + zf, 0.f), 15.f);
+    packed |= (uint32_t(int(t)) & 0xFu) << (4 * i);
+  }
+  *reinterpret_cast<uint32_t*>(q + c * 4) = packed;
+  if ((c % GT) == 0) {
+    s[c / GT] = sb;
+    z[c / GT] = (uint8_t)int(zf);
+  }
+}
+
 // ===========================================================================
 // large blocks (g > 256, e.g. per-token / per-channel): one CTA per block
 // ===========================================================================
@@ -422,6 +458,29 @@ qg_status qg_quantize_weights_int4(const float* w, uint8_t* w_q, uint16_t* w_s, 
     default: qg::int4_rtn_kernel<32><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, nchunks); break;
   }
   return qg::check_launch("qg_quantize_weights_int4");
+}
+
+qg_status qg_quantize_weights_int4_zp(const float* w, uint8_t* w_q, uint16_t* w_s, uint8_t* w_z, int g, int N,
+                                      int K, qg_stream_t stream) {
+  QG_REQUIRE(w && w_q && w_s && w_z, QG_ERR_INVALID_ARG, "qg_quantize_weights_int4_zp: NULL pointer");
+  QG_REQUIRE(N >= 0 && K > 0, QG_ERR_INVALID_ARG, "qg_quantize_weights_int4_zp: bad sizes");
+  QG_REQUIRE(qg::is_pow2_block(g) && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
+             "qg_quantize_weights_int4_zp: g must be a power of two in [8, 256] dividing K");
+  QG_REQUIRE(aligned16(w) && (reinterpret_cast<uintptr_t>(w_q) & 3) == 0, QG_ERR_MISALIGNED,
+             "qg_quantize_weights_int4_zp: misaligned pointer");
+  const long long nchunks = (long long)N * K / 8;
+  if (nchunks == 0) return QG_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned grid = qg::grid_for(nchunks);
+  switch (g / 8) {
+    case 1:  qg::int4_zp_kernel<1><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, w_z, nchunks); break;
+    case 2:  qg::int4_zp_kernel<2><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, w_z, nchunks); break;
+    case 4:  qg::int4_zp_kernel<4><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, w_z, nchunks); break;
+    case 8:  qg::int4_zp_kernel<8><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, w_z, nchunks); break;
+    case 16: qg::int4_zp_kernel<16><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, w_z, nchunks); break;
+    default: qg::int4_zp_kernel<32><<<grid, qg::kThreads, 0, st>>>(w, w_q, w_s, w_z, nchunks); break;
+  }
+  return qg::check_launch("qg_quantize_weights_int4_zp");
 }
 
 qg_status qg_quantize_weights_fp8(const float* w, uint8_t* w_e4m3, float* w_cs, int N, int K,

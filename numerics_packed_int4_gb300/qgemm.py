@@ -31,6 +31,9 @@ SIGNATURES = {
     "qgemm_w4a8_grouped": [P, P, P, P, P, I, P, I, I, I, I, P],
     "qgemm_w4a8_grouped_fp8s": [P, P, P, P, P, P, P, I, I, I, I, P],
     "qg_w4a8_fp8_scales": [P, P, P, I, I, P],
+    "qgemm_w4a16_zp": [P, P, P, I, P, P, I, I, I, P],
+    "qg_quantize_weights_int4_zp": [P, P, P, P, I, I, I, P],
+    "qg_dequant_weights_int4_zp": [P, P, P, I, P, I, I, P],
     "qg_quantize_weights_int4": [P, P, P, I, I, I, P],
     "qg_quantize_weights_fp8": [P, P, P, I, I, P],
     "qg_quantize_weights_mxfp4": [P, P, P, I, I, I, P],
@@ -137,6 +140,21 @@ def qgemm_w4a8_grouped_fp8s(a_e4m3, a_s, expert_off, w_q, w_s8, w_cs8, y, R, E, 
 
 def qg_w4a8_fp8_scales(w_s, w_s8, w_cs8, rows, G, stream=None):
     return _call("qg_w4a8_fp8_scales", _ptr(w_s), _ptr(w_s8), _ptr(w_cs8), rows, G, stream=stream)
+
+
+def qgemm_w4a16_zp(w_q, w_s, w_z, g, x, y, M, N, K, stream=None):
+    return _call("qgemm_w4a16_zp", _ptr(w_q), _ptr(w_s), _ptr(w_z), g, _ptr(x), _ptr(y), M, N, K,
+                 stream=stream)
+
+
+def qg_quantize_weights_int4_zp(w, w_q, w_s, w_z, g, N, K, stream=None):
+    return _call("qg_quantize_weights_int4_zp", _ptr(w), _ptr(w_q), _ptr(w_s), _ptr(w_z), g, N, K,
+                 stream=stream)
+
+
+def qg_dequant_weights_int4_zp(w_q, w_s, w_z, g, w_out, N, K, stream=None):
+    return _call("qg_dequant_weights_int4_zp", _ptr(w_q), _ptr(w_s), _ptr(w_z), g, _ptr(w_out), N, K,
+                 stream=stream)
 
 
 def qg_quantize_weights_int4(w, w_q, w_s, g, N, K, stream=None):
