@@ -8,6 +8,8 @@ One step = one pass over every row of the hot path at its workload size:
   MoE            W4A8 layer, T = 4096, hidden 4096, inter 14336, E = 8, top-2
   MoE, FP8 scales  the same layer on the FP8-group-scale recipe (E4M3 x E4M3
                  tensor-core GEMMs; roofline against the FP8 dense peak)
+  zero points    asymmetric INT4 (zero point per group of 64): M = 1 GEMVs and
+                 M = 8192 prefill over the same three (N, K)
 Each row is one CUDA graph; CUDA events between the graphs time every row
 inside the timed region.  The headline value is the metric's first quantity:
 effective HBM GB/s of the M = 1 GEMVs (algorithmic bytes / time); the
@@ -37,6 +39,7 @@ if ROOT not in sys.path:
 METRIC = "M=1 effective HBM GB/s (% of peak); M=8192 TFLOP/s (% of bf16 dense peak)"
 SHAPES = [(4096, 4096), (14336, 4096), (4096, 14336)]
 FORMATS = ["int4", "fp8", "mxfp4", "nvfp4"]
+ZP_G = 64                                   # group size of the zero-point rows
 BYTES_PER_PARAM = {"int4": 0.5 + 2 / 128, "fp8": 1.0, "mxfp4": 0.5 + 1 / 32, "nvfp4": 0.5 + 1 / 16}
 
 
@@ -243,6 +246,15 @@ class Workload:
         qg.qg_quantize_weights_nvfp4(w, q, s, gs, N, K)
         return dict(q=q, s=s, gs=gs)
 
+    def _weights_zp(self, w):
+        t = self.t
+        N, K = w.shape
+        d = dict(q=t.empty((N, K // 2), dtype=t.uint8, device=self.dev),
+                 s=t.empty((N, K // ZP_G), dtype=t.int16, device=self.dev),
+                 z=t.empty((N, K // ZP_G), dtype=t.uint8, device=self.dev))
+        self.qg.qg_quantize_weights_int4_zp(w, d["q"], d["s"], d["z"], ZP_G, N, K)
+        return d
+
     def gemv(self, fmt, W, x, y, M, N, K):
         qg = self.qg
         if fmt == "int4":
@@ -258,13 +270,15 @@ class Workload:
         t = self.t
         from numerics_packed_int4_gb300 import inputs
         self.W = {}
-        if any(r.startswith("decode") or r == "prefill" for r in self.rows):
+        if any(r.startswith("decode") or r in ("prefill", "prefill_zp") for r in self.rows):
             for i, (N, K) in enumerate(SHAPES):
                 w = self._randn((N, K), seed=1000 + i, std=0.02)
                 for fmt in FORMATS:
                     if fmt != "int4" and not any(r.startswith("decode") for r in self.rows):
                         continue
                     self.W[(fmt, N, K)] = self._weights(fmt, w)
+                if "decode_zp" in self.rows or "prefill_zp" in self.rows:
+                    self.W[("int4zp", N, K)] = self._weights_zp(w)
                 del w
         self.X, self.Y = {}, {}
         for M in (1, 4, 16):
@@ -272,7 +286,7 @@ class Workload:
                 self.X[(M, K)] = self._bf16(self._randn((M, K), seed=2000 + M * 7 + K))
             for N in sorted({n for n, _ in SHAPES}):
                 self.Y[(M, N)] = t.empty((M, N), dtype=t.int16, device=self.dev)
-        if "prefill" in self.rows:
+        if "prefill" in self.rows or "prefill_zp" in self.rows:
             self.XP = {}
             for K in sorted({k for _, k in SHAPES}):
                 x = self._randn((8192, K), seed=3000 + K)
@@ -350,6 +364,14 @@ class Workload:
             for N, K in SHAPES:
                 W = self.W[("int4", N, K)]
                 qg.qgemm_w4a16(W["q"], W["s"], 128, self.XP[K], self.YP[N], 8192, N, K)
+        elif name == "decode_zp":
+            for N, K in SHAPES:
+                W = self.W[("int4zp", N, K)]
+                qg.qgemm_w4a16_zp(W["q"], W["s"], W["z"], ZP_G, self.X[(1, K)], self.Y[(1, N)], 1, N, K)
+        elif name == "prefill_zp":
+            for N, K in SHAPES:
+                W = self.W[("int4zp", N, K)]
+                qg.qgemm_w4a16_zp(W["q"], W["s"], W["z"], ZP_G, self.XP[K], self.YP[N], 8192, N, K)
         elif name == "quant":
             qg.quant_act_fp8_block(self.XQ, self.QF, self.QFs, 128, 4096, 7168)
             qg.quant_act_mxfp4(self.XQ, self.QM, self.QMs, 16, 4096, 7168)
@@ -382,6 +404,11 @@ class Workload:
                 self.launches[name] = None
         if "prefill" in self.rows:
             self.flops["prefill"] = sum(2.0 * 8192 * N * K for N, K in SHAPES)
+        if "prefill_zp" in self.rows:
+            self.flops["prefill_zp"] = sum(2.0 * 8192 * N * K for N, K in SHAPES)
+        if "decode_zp" in self.rows:
+            self.bytes["decode_zp"] = sum(N * K * (0.5 + 3.0 / ZP_G) + 2 * K + 2 * N for N, K in SHAPES)
+            self.launches["decode_zp"] = None
         if "quant" in self.rows:
             M, K = 4096, 7168
             self.bytes["quant"] = M * K * (2 + 1) + M * K // 128 * 4 + M * K * 2 + M * K // 2 + M * K // 16
@@ -462,7 +489,7 @@ def bench_config(rows, world):
     return {"workload": "decode sweep M in {1,4,16} x {4096^2, 14336x4096, 4096x14336} x "
                         "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill W4A16 M=8192 + "
                         "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2 (bf16 group scales; "
-                        "FP8 group scales)",
+                        "FP8 group scales) + asymmetric INT4 g64 M=1 and M=8192",
             "rows": rows, "l2": "inputs larger than L2: every weight matrix read once per step; "
                                 "step working set > 1 GB vs 129 MB L2",
             "parallelism": "replicas" if world > 1 else "single"}
@@ -692,7 +719,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe,moe_fp8s")
+    ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe,moe_fp8s,"
+                                      "decode_zp,prefill_zp")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
