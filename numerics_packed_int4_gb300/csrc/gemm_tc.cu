@@ -263,14 +263,21 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       c.s += by;
       while (c.s >= nslab) { c.s -= nslab; ++c.i; set_row(c); }
     };
-    // group scale of the 32-k half h (bits 0-15) and, with zero points, its
-    // zero point (bits 16-19)
-    auto scale_of = [&](const Cur& c, int h) -> uint32_t {
-      if (c.i >= ntiles) return 0u;
-      const int grp = (c.s * kBK + 32 * h) >> p.lg;
-      uint32_t v = __ldg(c.srow + grp);
-      if constexpr (ZP) v |= (uint32_t)__ldg(c.zrow + grp) << 16;
-      return v;
+    // group scales of the slab's two 32-k halves (bits 0-15) and, with zero
+    // points, their zero points (bits 16-19); one load when both halves lie
+    // in one group (g >= 64)
+    auto scales_of = [&](const Cur& c, uint32_t& v0, uint32_t& v1) {
+      v0 = v1 = 0u;
+      if (c.i >= ntiles) return;
+      const int g0 = (c.s * kBK) >> p.lg, g1 = (c.s * kBK + 32) >> p.lg;
+      v0 = __ldg(c.srow + g0);
+      if constexpr (ZP) v0 |= (uint32_t)__ldg(c.zrow + g0) << 16;
+      if (g1 == g0) {
+        v1 = v0;
+      } else {
+        v1 = __ldg(c.srow + g1);
+        if constexpr (ZP) v1 |= (uint32_t)__ldg(c.zrow + g1) << 16;
+      }
     };
     // epilogue of tile e: TMEM -> registers -> (accumulator free) -> bf16 -> Y
     auto epilogue = [&](int e) -> bool {
@@ -302,9 +309,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     Cur pf{0, 0, nullptr, nullptr};
     set_row(pf);
     advance(pf, set);
-    uint32_t sc_cur0 = scale_of(pf, 0), sc_cur1 = scale_of(pf, 1);
+    uint32_t sc_cur0, sc_cur1, sc_nxt0, sc_nxt1;
+    scales_of(pf, sc_cur0, sc_cur1);
     advance(pf, kDeqSets);
-    uint32_t sc_nxt0 = scale_of(pf, 0), sc_nxt1 = scale_of(pf, 1);
+    scales_of(pf, sc_nxt0, sc_nxt1);
     for (int g = set; g < total; g += kDeqSets) {
       while (e_next < ntiles - 1 && g >= (e_next + 1) * nslab + kASlots) {
         if (!(ok = epilogue(e_next))) break;
@@ -317,8 +325,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       sc_cur0 = sc_nxt0;
       sc_cur1 = sc_nxt1;
       advance(pf, kDeqSets);                        // pf now at this set's slab after the next
-      sc_nxt0 = scale_of(pf, 0);
-      sc_nxt1 = scale_of(pf, 1);
+      scales_of(pf, sc_nxt0, sc_nxt1);
       if (!mbar_wait_warp(&tl->w_full[sa], ra & 1, p.cap, abort, p.err)) { ok = false; break; }
       const uint4 wa = *reinterpret_cast<const uint4*>(wsm + sa * kWStageBytes + row * (kBK / 2));
       const uint4 wb = *reinterpret_cast<const uint4*>(wsm + sa * kWStageBytes + row * (kBK / 2) + 16);
