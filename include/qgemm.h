@@ -158,6 +158,24 @@ QG_API qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,
                              const uint16_t* w_s, int g, uint16_t* y, int R,
                              int E, int N, int K, qg_stream_t stream);
 
+/* The same W4A8 grouped GEMM (exact bf16 group scales, identical result) for
+ * activations handed over as fp16: a_f16[r,k] = the value of the E4M3 code
+ * a_e4m3[r,k], exactly (every E4M3 value is an fp16; qg_e4m3_to_f16 makes the
+ * copy, or a producer writes it directly).  With the activations in HBM as
+ * fp16 they reach the tensor cores by TMA with no restaging in the kernel
+ * (one CTA per SM, tcgen05 kind::f16), for one more read of R*K*2 bytes.
+ *   a_f16 [R][K] fp16; the other arguments as qgemm_w4a8_grouped.
+ * Rules: g == 128, K % 128 == 0, N % 16 == 0, R >= 0, E >= 1.               */
+QG_API qg_status qgemm_w4a8_grouped_f16act(const uint16_t* a_f16, const float* a_s,
+                                    const int32_t* expert_off, const uint8_t* w_q,
+                                    const uint16_t* w_s, int g, uint16_t* y, int R, int E,
+                                    int N, int K, qg_stream_t stream);
+
+/* E4M3 codes -> their values as fp16 (exact; NaN codes give fp16 NaN).
+ *   q [n] u8 (8-byte aligned) -> out [n] fp16 (16-byte aligned).  n % 8 == 0. */
+QG_API qg_status qg_e4m3_to_f16(const uint8_t* q, uint16_t* out, long long n,
+                         qg_stream_t stream);
+
 /* W4A8 grouped GEMM with FP8 group scales and an FP8 x FP8 matmul
  * (Production-Ready W4A8, "Accurate W4A8 Kernel": the group scales are
  * quantized to FP8 per output channel, pre-scaled by 1/8 with the channel

@@ -61,6 +61,41 @@ QG_DEVICE void int4zp_x8_kperm(uint32_t v, uint32_t s2, uint32_t zb2, uint32_t (
   for (int i = 0; i < 4; ++i) p[i] = bf16x2_mul(bf16x2_sub(p[i], zb2), s2);
 }
 
+// ---- fp16 forms (W4A8: exact products on a 16-bit MMA) ------------------------
+QG_DEVICE uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+QG_DEVICE uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// two E4M3 codes (low byte first) -> f16x2 (low half first), exact
+QG_DEVICE uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t d;
+  const uint16_t in = (uint16_t)two;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(in));
+  return d;
+}
+QG_DEVICE uint16_t f32_to_f16_bits(float f) {
+  uint16_t r;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+// INT4 nibbles -> fp16 pairs (k_i, k_{i+4}) = q * scale: (1024 + (nib ^ 8)) - 1032
+// is the exact integer q, one fp16 multiply forms the exact product.
+QG_DEVICE void int4x8_kperm_f16(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {
+  p[0] = lop3<kLutAndXor>(v, 0x000F000Fu, 0x64086408u);
+  p[1] = lop3<kLutAndXor>(v >> 4, 0x000F000Fu, 0x64086408u);
+  p[2] = lop3<kLutAndXor>(v >> 8, 0x000F000Fu, 0x64086408u);
+  p[3] = lop3<kLutAndXor>(v >> 12, 0x000F000Fu, 0x64086408u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = f16x2_mul(f16x2_sub(p[i], 0x64086408u), s2);
+}
+
 // ---- E2M1 -------------------------------------------------------------------
 // p[i] = (k_i, k_{i+4}) for i = 0..3, each e2m1 * scale (exact)
 QG_DEVICE void e2m1x8_kperm(uint32_t v, uint32_t scale2, uint32_t (&p)[4]) {

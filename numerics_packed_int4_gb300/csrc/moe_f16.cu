@@ -1,0 +1,448 @@
+// W4A8 grouped (MoE) GEMM with exact bf16 group scales, for activations
+// handed over as fp16 re-encodings of their E4M3 codes.
+//
+// Semantics (Production-Ready W4A8): y[r,n] = a_s[r] * sum_k e4m3(a[r,k]) *
+// q[n,k] * s[n,k/128], every product exact, fp32 accumulation, one bf16
+// rounding at the store -- the same result as qgemm_w4a8_grouped.  Every
+// E4M3 value is exact in fp16, so an fp16 copy of the E4M3 activations is a
+// lossless encoding; with it in HBM the activations go by TMA straight into
+// the MMA's B layout, and the kernel needs none of the shared-memory
+// restaging (E4M3 -> fp16 converter warps) that bounds the E4M3-input kernel,
+// nor that kernel's CTA pairs.  The weights are formed as fp16(q * s * 2^e_n)
+// -- exact: q * s has at most 11 significant bits, and the per-row power of
+// two e_n puts the row's largest scale in [2^11, 2^12) -- and the epilogue
+// multiplies by 2^-e_n and the token scale.
+//
+// tcgen05.mma.cta_group::1.kind::f16 (fp16 A and B), M = 128 channels,
+// N = 256 activation rows, K = 16:
+//   A operand  = the fp16 weights, written by 16 dequant warps into 8 slots
+//                of tensor memory (64 k = 32 columns per slot);
+//   B operand  = the fp16 activations, TMA-loaded in the 128-byte swizzled
+//                K-major layout (64 k per 128-byte row, 32 KB per stage);
+//   D          = fp32 accumulator in TMEM columns 0-255.
+// Persistent, one CTA per SM over the (expert, 128-channel block, 256-row
+// block) tile list with row blocks inner, the rings running on across tiles
+// and the epilogue of a tile overlapping the next tile's MMAs.  Roles: warp 0
+// TMA for the packed weights (8 stages), warp 1 TMEM + MMA issuer, warp 2 TMA
+// for the activations (6 stages), warps 3-18 dequant (four sets of four, one
+// warp per TMEM lane quarter, a thread decoding its row's 64-k slab, each set
+// taking every fourth slab) and the epilogue, warp 19 scheduler (waits for
+// each slab's operands and publishes the ready count the issuer polls).
+// Every wait is bounded.
+#include <algorithm>
+
+#include "dequant.cuh"
+#include "tc_common.cuh"
+
+namespace qg {
+
+bool make_u8_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols);
+bool make_bf16_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols);
+
+namespace {
+
+constexpr int hTW = 128;                 // weight rows per tile (MMA M)
+constexpr int hTT = 256;                 // activation rows per tile (MMA N)
+constexpr int hBK = 64;                  // k per slab: one 128-byte row of fp16
+constexpr int hXStages = 6;              // activation stages (<= hSlots: released through a_empty)
+constexpr int hSlots = 8;                // TMEM A slots and packed-weight stages
+constexpr int hDeqWarps = 16;            // four sets of 4 (one per TMEM lane quarter)
+constexpr int hDeqSet = 4;
+constexpr int hDeqSets = hDeqWarps / hDeqSet;
+constexpr int hDeq0 = 3;
+constexpr int hSchedWarp = hDeq0 + hDeqWarps;
+constexpr int hThreads = (hSchedWarp + 1) * 32;
+constexpr int hXStage = hTT * hBK * 2;   // 32 KB fp16 activations
+constexpr int hWStage = hTW * hBK / 2;   // 4 KB packed INT4
+constexpr uint32_t hTmemCols = 512;
+constexpr uint32_t hACol0 = 256;
+constexpr uint32_t hACols = hBK / 2;     // 32 columns: 64 fp16 per lane
+constexpr uint32_t hDrainCap = 1u << 21;
+static_assert(hXStages <= hSlots, "activation stages are released through the A-slot barriers");
+
+struct F16Args {
+  const float* a_s;
+  const int32_t* off;
+  const uint16_t* ws;                    // [E*N][K/128] bf16
+  uint16_t* y;
+  int R, E, N, K;
+  int tiles_w;
+  unsigned int* err;
+  uint32_t cap;
+};
+
+struct __align__(8) F16Tail {
+  uint64_t x_full[hXStages];
+  uint64_t w_full[hSlots];
+  uint64_t w_empty[hSlots];
+  uint64_t a_full[hSlots];
+  uint64_t a_empty[hSlots];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  unsigned int ready;
+};
+
+struct HTile {
+  int e, r0, r_end, n0;
+};
+QG_DEVICE void expert_rows(const F16Args& p, int i, int& a, int& b) {
+  a = min(max(__ldg(p.off + i), 0), p.R);
+  b = min(max(__ldg(p.off + i + 1), a), p.R);
+}
+QG_DEVICE int tile_count(const F16Args& p) {
+  int n = 0;
+  for (int i = 0; i < p.E; ++i) {
+    int a, b;
+    expert_rows(p, i, a, b);
+    n += (b - a + hTT - 1) / hTT * p.tiles_w;
+  }
+  return n;
+}
+QG_DEVICE HTile tile_at(const F16Args& p, int t) {
+  for (int i = 0; i < p.E; ++i) {
+    int a, b;
+    expert_rows(p, i, a, b);
+    const int nt = (b - a + hTT - 1) / hTT;
+    const int cnt = nt * p.tiles_w;
+    if (t < cnt) {
+      const int wt = t / nt;
+      return HTile{i, a + (t - wt * nt) * hTT, b, wt * hTW};
+    }
+    t -= cnt;
+  }
+  return HTile{0, 0, 0, 0};
+}
+
+// Per-row power of two: the row's largest |scale| lands in [2^11, 2^12), so
+// every fp16 product q * s * 2^ex is exact and in range.  A group scale more
+// than 2^24 below its row's largest would turn subnormal in fp16; RTN scales
+// of one weight row never spread that far.
+QG_DEVICE int row_exponent(const uint16_t* srow, int ng) {
+  float smax = 0.f;
+  int i = 0;
+  if ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0) {
+    for (; i + 8 <= ng; i += 8) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(srow + i));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        smax = fmaxf(smax, fmaxf(fabsf(bf16_lo_to_f32(w[c])), fabsf(bf16_hi_to_f32(w[c]))));
+    }
+  }
+  for (; i < ng; ++i) smax = fmaxf(smax, fabsf(bf16_bits_to_f32(__ldg(srow + i))));
+  if (!(smax > 0.f)) return 0;
+  int e2;
+  frexpf(smax, &e2);                       // smax = m * 2^e2, m in [0.5, 1)
+  return min(max(12 - e2, -100), 100);
+}
+
+__global__ void __launch_bounds__(hThreads, 1)
+moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
+               const F16Args p) {
+  const int ntiles_total = tile_count(p);
+  const int ntiles = ((int)blockIdx.x < ntiles_total)
+                         ? (ntiles_total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  if (ntiles == 0) return;
+  const int nslab = p.K / hBK;
+  const int total = ntiles * nslab;
+  auto tile_of = [&](int i) { return tile_at(p, (int)blockIdx.x + i * (int)gridDim.x); };
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* xs = smem;                                    // [hXStages][32 KB] fp16, swizzled
+  uint8_t* wsm = xs + hXStages * hXStage;                // [hSlots][4 KB] INT4
+  F16Tail* tl = reinterpret_cast<F16Tail*>(wsm + hSlots * hWStage);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < hXStages; ++s) mbar_init(&tl->x_full[s], 1);
+    for (int s = 0; s < hSlots; ++s) {
+      mbar_init(&tl->w_full[s], 1);
+      mbar_init(&tl->w_empty[s], hDeqSet);
+      mbar_init(&tl->a_full[s], hDeqSet);
+      mbar_init(&tl->a_empty[s], 1);
+    }
+    mbar_init(&tl->acc_full, 1);
+    mbar_init(&tl->acc_empty, hDeqWarps);
+    mbar_init(&tl->drain, 1);
+    tl->abort = 0;
+    tl->ready = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_w);
+  }
+  if (warp == 1) tmem_alloc(&tl->tmem_base, hTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tl->tmem_base;
+  volatile int* abort = &tl->abort;
+
+  if (warp == 0) {
+    // ---------------- TMA producer: packed weights ----------------
+    if (lane == 0) {
+      int issued = 0, s = 0, i = 0;
+      HTile t = tile_of(0);
+      for (int g = 0; g < total; ++g, ++s) {
+        if (s == nslab) { s = 0; t = tile_of(++i); }
+        const int st = g % hSlots, r = g / hSlots;
+        if (r > 0 && !mbar_wait(&tl->w_empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+        mbar_arrive_expect_tx(&tl->w_full[st], hWStage);
+        tma_load_2d(wsm + st * hWStage, &tmap_w, &tl->w_full[st], s * (hBK / 2), t.e * p.N + t.n0);
+        issued = g + 1;
+      }
+      if (*abort) {
+        for (int g = max(0, issued - hSlots); g < issued; ++g)
+          mbar_wait(&tl->w_full[g % hSlots], (g / hSlots) & 1, hDrainCap, abort, nullptr);
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- TMA producer: fp16 activations ----------------
+    if (lane == 0) {
+      int issued = 0, s = 0, i = 0;
+      HTile t = tile_of(0);
+      for (int g = 0; g < total; ++g, ++s) {
+        if (s == nslab) { s = 0; t = tile_of(++i); }
+        const int st = g % hXStages, gp = g - hXStages;   // stage last held slab gp
+        if (gp >= 0 && !mbar_wait(&tl->a_empty[gp % hSlots], (gp / hSlots) & 1, p.cap, abort, p.err)) break;
+        mbar_arrive_expect_tx(&tl->x_full[st], hXStage);
+        tma_load_2d(xs + st * hXStage, &tmap_a, &tl->x_full[st], s * hBK, t.r0);
+        issued = g + 1;
+      }
+      if (*abort) {
+        for (int g = max(0, issued - hXStages); g < issued; ++g)
+          mbar_wait(&tl->x_full[g % hXStages], (g / hXStages) & 1, hDrainCap, abort, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(hTW, hTT);
+      bool any = false;
+      unsigned int ready = 0;
+      int g = 0;
+      for (int i = 0; i < ntiles && !*abort; ++i) {
+        if (i > 0) {              // the accumulator is free once the epilogue has read the previous tile
+          if (!mbar_wait(&tl->acc_empty, (i - 1) & 1, p.cap, abort, p.err)) break;
+          tc_fence_after();
+        }
+        bool ok = true;
+        for (int s = 0; s < nslab; ++s, ++g) {
+          const int st = g % hXStages, sa = g % hSlots;
+          if (!wait_count(&tl->ready, (unsigned)g, ready, p.cap * 4, abort, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t bdesc = sw128_kmajor_desc(smem_addr(xs + st * hXStage));
+#pragma unroll
+          for (int j = 0; j < hBK / 16; ++j)
+            tc_mma_ts(tmem, tmem + hACol0 + sa * hACols + 8 * j, bdesc + 2 * j, idesc, (s | j) != 0);
+          tc_commit(&tl->a_empty[sa]);                   // frees the A slot and the activation stage
+          any = true;
+        }
+        if (!ok) break;
+        tc_commit(&tl->acc_full);
+      }
+      if (*abort && any) {
+        tc_commit(&tl->drain);
+        mbar_wait(&tl->drain, 0, hDrainCap, abort, nullptr);
+      }
+    }
+  } else if (warp == hSchedWarp) {
+    // ---------------- scheduler ----------------
+    if (lane == 0) {
+      for (int g = 0; g < total; ++g) {
+        if (!mbar_wait(&tl->a_full[g % hSlots], (g / hSlots) & 1, p.cap, abort, p.err)) break;
+        if (!mbar_wait(&tl->x_full[g % hXStages], (g / hXStages) & 1, p.cap, abort, p.err)) break;
+        publish_count(&tl->ready, (unsigned)(g + 1));
+      }
+    }
+  } else {
+    // ---------------- dequant producers, then the epilogues ----------------
+    // The epilogue of tile e runs once this warp is about to produce the slab
+    // hSlots past the start of tile e+1 (no slot it needs is then held by a
+    // tile-(e+1) MMA, which waits for the epilogue).
+    const int dw = warp - hDeq0;
+    const int q = warp & 3, set = dw >> 2;
+    const int row = 32 * q + lane;
+    const int cq = set;                              // epilogue: 64 of the 256 activation rows
+    const int ng = p.K / 128;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + hACol0;
+    // scale cursor: tile index, slab in the tile, this thread's scale row and
+    // the row's fp16 exponent shift for that tile
+    struct Cur { int i, s; const uint16_t* srow; float up; };
+    auto set_row = [&](Cur& c) {
+      if (c.i < ntiles) {
+        const HTile t = tile_of(c.i);
+        c.srow = p.ws + ((size_t)t.e * p.N + min(t.n0 + row, p.N - 1)) * ng;
+        c.up = ldexpf(1.f, row_exponent(c.srow, ng));
+      }
+    };
+    auto advance = [&](Cur& c, int by) {
+      c.s += by;
+      while (c.s >= nslab) { c.s -= nslab; ++c.i; set_row(c); }
+    };
+    // fp16x2 splat of fp16(s * 2^e) for the slab's group (exact)
+    auto scale_of = [&](const Cur& c) -> uint32_t {
+      if (c.i >= ntiles) return 0u;
+      return bf16x2_splat(f32_to_f16_bits(bf16_bits_to_f32(__ldg(c.srow + ((c.s * hBK) >> 7))) * c.up));
+    };
+    auto epilogue = [&](int e) -> bool {
+      if (!mbar_wait_warp(&tl->acc_full, e & 1, p.cap, abort, p.err)) return false;
+      tc_fence_after();
+      const HTile t = tile_of(e);
+      const int nn = t.n0 + row;
+      const int mb = t.r0 + 64 * cq;
+      const float down = ldexpf(1.f, -row_exponent(p.ws + ((size_t)t.e * p.N + min(nn, p.N - 1)) * ng, ng));
+      const float as_lo = mb + lane < t.r_end ? __ldg(p.a_s + mb + lane) : 0.f;
+      const float as_hi = mb + 32 + lane < t.r_end ? __ldg(p.a_s + mb + 32 + lane) : 0.f;
+      uint32_t packed[32];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 64 * cq + 32 * i, v);
+        tmem_wait_ld();
+        const float as = i ? as_hi : as_lo;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float lo = __uint_as_float(v[2 * c]) * down * __shfl_sync(0xffffffffu, as, 2 * c);
+          const float hi = __uint_as_float(v[2 * c + 1]) * down * __shfl_sync(0xffffffffu, as, 2 * c + 1);
+          packed[16 * i + c] = f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_warp(&tl->acc_empty);              // the next tile's MMAs may overwrite it
+      // lanes 2i, 2i+1 (channels n, n+1) swap halves: 4-byte stores
+      const bool odd = lane & 1;
+      const uint32_t sel = odd ? 0x3276u : 0x5410u;
+      const int n2 = nn & ~1;                        // N is even: a pair is in range or out as a whole
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const uint32_t w = prmt(packed[c], __shfl_xor_sync(0xffffffffu, packed[c], 1), sel);
+        const int m = mb + 2 * c + (odd ? 1 : 0);
+        if (n2 < p.N && m < t.r_end) *reinterpret_cast<uint32_t*>(p.y + (size_t)m * p.N + n2) = w;
+      }
+      return true;
+    };
+    int e_next = 0;
+    bool ok = true;
+    Cur pf{0, 0, nullptr, 1.f};
+    set_row(pf);
+    advance(pf, set);
+    uint32_t sc_cur = scale_of(pf);
+    advance(pf, hDeqSets);
+    uint32_t sc_nxt = scale_of(pf);
+    for (int g = set; g < total; g += hDeqSets) {
+      while (e_next < ntiles - 1 && g >= (e_next + 1) * nslab + hSlots) {
+        if (!(ok = epilogue(e_next))) break;
+        ++e_next;
+      }
+      if (!ok) break;
+      const int sa = g % hSlots, ra = g / hSlots;
+      const uint32_t s2 = sc_cur;
+      sc_cur = sc_nxt;
+      advance(pf, hDeqSets);                         // pf now at this set's slab after the next
+      sc_nxt = scale_of(pf);
+      if (!mbar_wait_warp(&tl->w_full[sa], ra & 1, p.cap, abort, p.err)) { ok = false; break; }
+      const uint4 wa = *reinterpret_cast<const uint4*>(wsm + sa * hWStage + row * (hBK / 2));
+      const uint4 wb = *reinterpret_cast<const uint4*>(wsm + sa * hWStage + row * (hBK / 2) + 16);
+      const uint32_t v[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      uint32_t out[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t pq[4], nat[4];
+        int4x8_kperm_f16(v[j], s2, pq);
+        kperm4_to_natural(pq, nat);
+        out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
+        out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
+      }
+      mbar_arrive_warp(&tl->w_empty[sa]);            // packed slab decoded: its stage may be refilled
+      if (ra > 0) {
+        if (!mbar_wait_warp(&tl->a_empty[sa], (ra - 1) & 1, p.cap, abort, p.err)) { ok = false; break; }
+        tc_fence_after();
+      }
+      {
+        const uint32_t (&o0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&out[0]);
+        const uint32_t (&o1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&out[16]);
+        tmem_st16(lane_base + sa * hACols, o0);
+        tmem_st16(lane_base + sa * hACols + 16, o1);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_warp(&tl->a_full[sa]);
+    }
+    while (ok && e_next < ntiles) {
+      if (!(ok = epilogue(e_next))) break;
+      ++e_next;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, hTmemCols);
+  }
+}
+
+// E4M3 codes -> fp16 values (exact), 8 per thread
+__global__ void e4m3_to_f16_kernel(const uint8_t* __restrict__ q, uint16_t* __restrict__ out, long long n8) {
+  const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const uint2 c = __ldg(reinterpret_cast<const uint2*>(q) + i);
+  const uint4 h = make_uint4(e4m3x2_to_f16x2(c.x & 0xFFFFu), e4m3x2_to_f16x2(c.x >> 16),
+                             e4m3x2_to_f16x2(c.y & 0xFFFFu), e4m3x2_to_f16x2(c.y >> 16));
+  reinterpret_cast<uint4*>(out)[i] = h;
+}
+
+}  // namespace
+
+}  // namespace qg
+
+extern "C" qg_status qgemm_w4a8_grouped_f16act(const uint16_t* a_f16, const float* a_s, const int32_t* expert_off,
+                                               const uint8_t* w_q, const uint16_t* w_s, int g, uint16_t* y,
+                                               int R, int E, int N, int K, qg_stream_t stream) {
+  using namespace qg;
+  if (!(a_f16 && a_s && expert_off && w_q && w_s && y))
+    return set_error(QG_ERR_INVALID_ARG, "qgemm_w4a8_grouped_f16act: NULL pointer");
+  if (!(R >= 0 && E >= 1 && N > 0 && K > 0))
+    return set_error(QG_ERR_INVALID_ARG, "qgemm_w4a8_grouped_f16act: bad sizes");
+  if (!(g == 128 && K % 128 == 0 && N % 16 == 0))
+    return set_error(QG_ERR_UNSUPPORTED_SHAPE, "qgemm_w4a8_grouped_f16act: need g == 128, K %% 128 == 0, N %% 16 == 0");
+  if (!(aligned16(a_f16) && aligned16(w_q) && aligned16(y)))
+    return set_error(QG_ERR_MISALIGNED, "qgemm_w4a8_grouped_f16act: misaligned pointer");
+  if (R == 0) return QG_OK;
+  CUtensorMap tmap_a, tmap_w;
+  if (!make_bf16_tmap(&tmap_a, a_f16, R, K, hTT, hBK))     // a 16-bit copy: the element type is not read
+    return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped_f16act: cannot encode the activation tensor map");
+  if (!make_u8_tmap(&tmap_w, w_q, E * N, K / 2, hTW, hBK / 2))
+    return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped_f16act: cannot encode the weight tensor map");
+  unsigned int* err = device_error_word();
+  if (!err) return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped_f16act: no device error word");
+  F16Args a{};
+  a.a_s = a_s; a.off = expert_off; a.ws = w_s; a.y = y;
+  a.R = R; a.E = E; a.N = N; a.K = K;
+  a.tiles_w = (N + hTW - 1) / hTW;
+  a.err = err;
+  a.cap = wait_limit();
+  const int smem = hXStages * hXStage + hSlots * hWStage + (int)sizeof(F16Tail) + 1024;
+  if (!ensure_smem(moe_f16_kernel, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped_f16act: smem attribute");
+  const long long bound = ((long long)(R + hTT - 1) / hTT + E) * a.tiles_w;
+  const int grid = (int)std::min<long long>(bound, (long long)sm_count());
+  moe_f16_kernel<<<grid, hThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tmap_a, tmap_w, a);
+  return check_launch("qgemm_w4a8_grouped_f16act");
+}
+
+extern "C" qg_status qg_e4m3_to_f16(const uint8_t* q, uint16_t* out, long long n, qg_stream_t stream) {
+  using namespace qg;
+  if (!(q && out)) return set_error(QG_ERR_INVALID_ARG, "qg_e4m3_to_f16: NULL pointer");
+  if (n < 0) return set_error(QG_ERR_INVALID_ARG, "qg_e4m3_to_f16: bad size");
+  if (n % 8 != 0) return set_error(QG_ERR_UNSUPPORTED_SHAPE, "qg_e4m3_to_f16: n %% 8 != 0");
+  if (!((reinterpret_cast<uintptr_t>(q) & 7u) == 0 && aligned16(out)))
+    return set_error(QG_ERR_MISALIGNED, "qg_e4m3_to_f16: misaligned pointer");
+  if (n == 0) return QG_OK;
+  const long long n8 = n / 8;
+  e4m3_to_f16_kernel<<<unsigned((n8 + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, out, n8);
+  return check_launch("qg_e4m3_to_f16");
+}

@@ -128,11 +128,6 @@ QG_DEVICE FTile tile_at(const Fp8sArgs& p, int t) {
   return FTile{0, 0, 0, 0};
 }
 
-QG_DEVICE uint32_t f16x2_mul_(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 // two fp16 (low half first) -> two E4M3 codes (low byte first), RNE, satfinite
 QG_DEVICE uint32_t f16x2_to_e4m3x2(uint32_t h2) {
   uint16_t r;
@@ -155,14 +150,14 @@ struct Lut {
   uint32_t p_lo, p_hi, n_lo, n_hi;
 };
 QG_DEVICE Lut lut_build(uint32_t s2) {
-  const uint32_t c0 = f16x2_to_e4m3x2(f16x2_mul_(0x3C000000u, s2));
-  const uint32_t c1 = f16x2_to_e4m3x2(f16x2_mul_(0x42004000u, s2));
-  const uint32_t c2 = f16x2_to_e4m3x2(f16x2_mul_(0x45004400u, s2));
-  const uint32_t c3 = f16x2_to_e4m3x2(f16x2_mul_(0x47004600u, s2));
-  const uint32_t d0 = f16x2_to_e4m3x2(f16x2_mul_(0xC700C800u, s2));
-  const uint32_t d1 = f16x2_to_e4m3x2(f16x2_mul_(0xC500C600u, s2));
-  const uint32_t d2 = f16x2_to_e4m3x2(f16x2_mul_(0xC200C400u, s2));
-  const uint32_t d3 = f16x2_to_e4m3x2(f16x2_mul_(0xBC00C000u, s2));
+  const uint32_t c0 = f16x2_to_e4m3x2(f16x2_mul(0x3C000000u, s2));
+  const uint32_t c1 = f16x2_to_e4m3x2(f16x2_mul(0x42004000u, s2));
+  const uint32_t c2 = f16x2_to_e4m3x2(f16x2_mul(0x45004400u, s2));
+  const uint32_t c3 = f16x2_to_e4m3x2(f16x2_mul(0x47004600u, s2));
+  const uint32_t d0 = f16x2_to_e4m3x2(f16x2_mul(0xC700C800u, s2));
+  const uint32_t d1 = f16x2_to_e4m3x2(f16x2_mul(0xC500C600u, s2));
+  const uint32_t d2 = f16x2_to_e4m3x2(f16x2_mul(0xC200C400u, s2));
+  const uint32_t d3 = f16x2_to_e4m3x2(f16x2_mul(0xBC00C000u, s2));
   return Lut{c0 | (c1 << 16), c2 | (c3 << 16), d0 | (d1 << 16), d2 | (d3 << 16)};
 }
 // Four INT4 codes (the low 4 nibbles of sel; fsel = sel ^ 0x8888) -> four

@@ -246,6 +246,11 @@ QG_DEVICE uint64_t sw128_kmajor_desc(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Instruction descriptor, kind::f16 with fp16 A and B, fp32 D, both K-major.
+QG_HOST_DEVICE uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
 QG_HOST_DEVICE uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);

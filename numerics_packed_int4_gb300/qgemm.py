@@ -19,7 +19,7 @@ STATUS = {0: "QG_OK", 1: "QG_ERR_INVALID_ARG", 2: "QG_ERR_UNSUPPORTED_SHAPE", 3:
 QG_SCALE_E8M0, QG_SCALE_E4M3 = 0, 1
 QG_FMT_INT4, QG_FMT_FP8, QG_FMT_MXFP4, QG_FMT_NVFP4 = 0, 1, 2, 3
 
-P, I, U32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32
+P, I, U32, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_longlong
 
 # name -> argument types (every data pointer and the stream are void*)
 SIGNATURES = {
@@ -32,6 +32,8 @@ SIGNATURES = {
     "qgemm_w4a8_grouped_fp8s": [P, P, P, P, P, P, P, I, I, I, I, P],
     "qg_w4a8_fp8_scales": [P, P, P, I, I, P],
     "qgemm_w4a16_zp": [P, P, P, I, P, P, I, I, I, P],
+    "qgemm_w4a8_grouped_f16act": [P, P, P, P, P, I, P, I, I, I, I, P],
+    "qg_e4m3_to_f16": [P, P, I64, P],
     "qg_quantize_weights_int4_zp": [P, P, P, P, I, I, I, P],
     "qg_dequant_weights_int4_zp": [P, P, P, I, P, I, I, P],
     "qg_quantize_weights_int4": [P, P, P, I, I, I, P],
@@ -140,6 +142,15 @@ def qgemm_w4a8_grouped_fp8s(a_e4m3, a_s, expert_off, w_q, w_s8, w_cs8, y, R, E, 
 
 def qg_w4a8_fp8_scales(w_s, w_s8, w_cs8, rows, G, stream=None):
     return _call("qg_w4a8_fp8_scales", _ptr(w_s), _ptr(w_s8), _ptr(w_cs8), rows, G, stream=stream)
+
+
+def qgemm_w4a8_grouped_f16act(a_f16, a_s, expert_off, w_q, w_s, g, y, R, E, N, K, stream=None):
+    return _call("qgemm_w4a8_grouped_f16act", _ptr(a_f16), _ptr(a_s), _ptr(expert_off), _ptr(w_q),
+                 _ptr(w_s), g, _ptr(y), R, E, N, K, stream=stream)
+
+
+def qg_e4m3_to_f16(q, out, n, stream=None):
+    return _call("qg_e4m3_to_f16", _ptr(q), _ptr(out), int(n), stream=stream)
 
 
 def qgemm_w4a16_zp(w_q, w_s, w_z, g, x, y, M, N, K, stream=None):

@@ -1,0 +1,121 @@
+"""GPU parity of the W4A8 grouped GEMM fed with fp16 copies of the E4M3
+activations (exact re-encoding): the copy itself bit-exact over every code,
+and the GEMM against the same fp64 oracle as the E4M3-input entry point."""
+
+import numpy as np
+import pytest
+import torch
+
+from numerics_packed_int4_gb300 import inputs
+from oracle import formats as OF
+from oracle import gemm as OG
+from oracle import quant as OQ
+from tests.gpu_util import check_gemm, dev, empty, host
+
+pytestmark = pytest.mark.gpu
+
+
+def test_e4m3_to_f16_every_code(qg):
+    codes = np.tile(np.arange(256, dtype=np.uint8), 4)
+    out = empty((codes.size,), torch.int16)
+    qg.qg_e4m3_to_f16(dev(codes), out, codes.size)
+    qg.qg_check_device_error()
+    got = host(out).view(np.float16).astype(np.float64)
+    want = OF.e4m3_decode(codes)
+    nan = np.isnan(want)
+    assert np.all(np.isnan(got[nan]))
+    np.testing.assert_array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))   # signed zero kept
+
+
+def expert_weights(E, N, K, seed):
+    qs, ss = [], []
+    for e in range(E):
+        q, s = OQ.quant_int4_rtn(inputs.weights_f32(N, K, seed=seed + e), 128)
+        qs.append(q)
+        ss.append(s)
+    return np.stack(qs), np.stack(ss)
+
+
+def grouped_f16(qg, a8, a_s, off, wq, ws, N, K):
+    """E4M3 codes -> fp16 copy on the GPU, then the grouped GEMM."""
+    R, E = a8.shape[0], wq.shape[0]
+    y = empty((max(R, 1), N), torch.int16)
+    a16 = empty((max(R, 1), K), torch.int16)
+    if R:
+        qg.qg_e4m3_to_f16(dev(a8), a16, R * K)
+    qg.qgemm_w4a8_grouped_f16act(a16, dev(a_s) if R else empty((1,), torch.float32),
+                                 dev(off.astype(np.int32)), dev(wq), dev(ws), 128, y, R, E, N, K)
+    qg.qg_check_device_error()
+    return OF.bf16_decode(host(y))[:R]
+
+
+@pytest.mark.parametrize("sizes,N,K", [([5, 0, 70, 129], 256, 512), ([1], 128, 128), ([0, 0, 3], 144, 384),
+                                       ([300, 0, 700, 50, 1000], 384, 512), ([512], 272, 1024),
+                                       ([0, 513, 0, 255, 257], 128, 384), ([2048, 2048], 1024, 2048)])
+def test_grouped_f16act(qg, sizes, N, K):
+    E = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R = int(off[-1])
+    x = inputs.activations_bf16(max(R, 1), K, seed=R + K + 3)[:R]
+    a8, a_s = OQ.quant_fp8_block(x, K)
+    wq, ws = expert_weights(E, N, K, seed=150)
+    y = grouped_f16(qg, a8, a_s[:, 0], off, wq, ws, N, K)
+    if R:
+        ref = OF.bf16_decode(OG.to_bf16(OG.w4a8_grouped_f64(a8, a_s[:, 0], off, wq, ws, 128)))
+        check_gemm(y, ref, "f16act %s" % sizes)
+
+
+@pytest.mark.parametrize("sizes,N,K", [([700, 900, 1000], 2048, 384), ([2000, 0, 600], 2560, 1024),
+                                       ([4100], 1200, 512), ([33, 1500, 7, 1100], 1664, 128)])
+def test_grouped_f16act_several_tiles_per_cta(qg, sizes, N, K):
+    E = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R = int(off[-1])
+    x = inputs.activations_bf16(R, K, seed=R + K + 13)
+    a8, a_s = OQ.quant_fp8_block(x, K)
+    wq, ws = expert_weights(E, N, K, seed=160)
+    y = grouped_f16(qg, a8, a_s[:, 0], off, wq, ws, N, K)
+    ref = OF.bf16_decode(OG.to_bf16(OG.w4a8_grouped_f64(a8, a_s[:, 0], off, wq, ws, 128)))
+    check_gemm(y, ref, "f16act multi-tile %s" % sizes)
+
+
+def test_grouped_f16act_matches_e4m3_entry(qg):
+    """Both entry points compute the same exact products in fp32: identical
+    inputs give results equal to within the order of fp32 accumulation."""
+    sizes, N, K = [600, 424], 512, 1024
+    E = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R = int(off[-1])
+    x = inputs.activations_bf16(R, K, seed=91)
+    a8, a_s = OQ.quant_fp8_block(x, K)
+    wq, ws = expert_weights(E, N, K, seed=170)
+    y16 = grouped_f16(qg, a8, a_s[:, 0], off, wq, ws, N, K)
+    y8 = empty((R, N), torch.int16)
+    qg.qgemm_w4a8_grouped(dev(a8), dev(a_s[:, 0]), dev(off), dev(wq), dev(ws), 128, y8, R, E, N, K)
+    qg.qg_check_device_error()
+    y8 = OF.bf16_decode(host(y8))
+    assert np.max(np.abs(y16 - y8)) <= 2.0 ** -7 * np.max(np.abs(y8))
+
+
+def test_grouped_f16act_config_size_sampled(qg):
+    """T=4096 top-2 over E=8: R=8192 rows, gate/up N=2*14336, K=4096."""
+    T, E, H, I = 4096, 8, 4096, 14336
+    rt = inputs.moe_routing(T, E, 2, seed=9)
+    off = rt["expert_off"]
+    x = inputs.activations_bf16(T, H, seed=10)
+    a8, a_s = OQ.quant_fp8_block(x, H)
+    rows = rt["route_rows"]
+    a8r, asr = a8[rows], a_s[rows, 0]
+    wq, ws = expert_weights(E, 2 * I, H, seed=60)
+    y = grouped_f16(qg, a8r, asr, off, wq, ws, 2 * I, H)
+    assert np.all(np.isfinite(y))
+    r = np.random.Generator(np.random.PCG64(6))
+    pick = np.concatenate([r.choice(np.arange(off[e], off[e + 1]), size=min(24, off[e + 1] - off[e]),
+                                    replace=False) for e in range(E)])
+    pick.sort()
+    cols = np.sort(r.choice(2 * I, size=512, replace=False))
+    sub_off = np.searchsorted(pick, off).astype(np.int32)
+    ref = OF.bf16_decode(OG.to_bf16(
+        OG.w4a8_grouped_f64(a8r[pick], asr[pick], sub_off, wq[:, cols], ws[:, cols], 128)))
+    check_gemm(y[pick][:, cols], ref, "f16act config sample")
