@@ -247,11 +247,20 @@ QG_API qg_status qg_quantize_weights_nvfp4(const float* w, uint8_t* w_e2m1, uint
 QG_API qg_status qg_moe_gather_fp8(const uint8_t* src_q, const float* src_s,
                             const int32_t* route_rows, uint8_t* dst_q, float* dst_s,
                             int R, int T, int K, qg_stream_t stream);
+/* qg_moe_gather_fp8 writing the gathered codes' fp16 values (exact) instead
+ * of the codes, for qgemm_w4a8_grouped_f16act.  dst_f16 [R][K] fp16.       */
+QG_API qg_status qg_moe_gather_fp8_f16(const uint8_t* src_q, const float* src_s,
+                                const int32_t* route_rows, uint16_t* dst_f16, float* dst_s,
+                                int R, int T, int K, qg_stream_t stream);
 /* h = SiLU(gate) * up in fp32 from the bf16 projection output [R][2I] (gate
  * columns first), then the per-row FP8 quantizer (block = I).
  *   gate_up [R][2I] bf16 -> q [R][I] E4M3, s [R] fp32.  I % 8 == 0.          */
 QG_API qg_status qg_swiglu_quant_fp8(const uint16_t* gate_up, uint8_t* q, float* s,
                               int R, int I, qg_stream_t stream);
+/* qg_swiglu_quant_fp8 writing the codes' fp16 values (exact) instead of the
+ * codes, for qgemm_w4a8_grouped_f16act.  q_f16 [R][I] fp16.                */
+QG_API qg_status qg_swiglu_quant_fp8_f16(const uint16_t* gate_up, uint16_t* q_f16, float* s,
+                                  int R, int I, qg_stream_t stream);
 /* out[t] = bf16( sum_j weight[t,j] * down[row_of[t,j]] ), j < topk, fp32 sum.
  *   down [R][H] bf16, row_of [T][topk] int32, weight [T][topk] fp32 (DEVICE)
  *   out [T][H] bf16.  H % 8 == 0.                                           */

@@ -6,7 +6,7 @@
 // 4- or 8-byte store per thread.
 #include <cfloat>
 
-#include "qg_common.cuh"
+#include "dequant.cuh"
 
 #define QG_REQUIRE(cond, st, ...) \
   do { if (!(cond)) return qg::set_error(st, __VA_ARGS__); } while (0)
@@ -254,17 +254,42 @@ __global__ void nvfp4_finalize_kernel(float* gs_word) {
 // ===========================================================================
 // MoE harness
 // ===========================================================================
+// 8 E4M3 codes -> their 8 fp16 values (exact)
+QG_DEVICE uint4 e4m3x8_to_f16x8(uint2 c) {
+  return make_uint4(e4m3x2_to_f16x2(c.x & 0xFFFFu), e4m3x2_to_f16x2(c.x >> 16),
+                    e4m3x2_to_f16x2(c.y & 0xFFFFu), e4m3x2_to_f16x2(c.y >> 16));
+}
+
+// Row gather of E4M3 codes and their row scales; F16: the destination takes
+// the codes' fp16 values instead of the codes.
+template <bool F16>
 __global__ void __launch_bounds__(kThreads) gather_fp8_kernel(
     const uint8_t* __restrict__ src_q, const float* __restrict__ src_s,
-    const int32_t* __restrict__ rows, uint8_t* __restrict__ dst_q, float* __restrict__ dst_s,
+    const int32_t* __restrict__ rows, void* __restrict__ dst_v, float* __restrict__ dst_s,
     int T, int K) {
   const int r = blockIdx.x;
   int t = rows[r];
   t = t < 0 ? 0 : (t >= T ? T - 1 : t);
   const uint4* src = reinterpret_cast<const uint4*>(src_q + (long long)t * K);
-  uint4* dst = reinterpret_cast<uint4*>(dst_q + (long long)r * K);
-  for (int i = threadIdx.x; i < K / 16; i += kThreads) dst[i] = src[i];
+  if constexpr (F16) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dst_v) + (long long)r * K);
+    for (int i = threadIdx.x; i < K / 16; i += kThreads) {
+      const uint4 c = src[i];
+      dst[2 * i] = e4m3x8_to_f16x8(make_uint2(c.x, c.y));
+      dst[2 * i + 1] = e4m3x8_to_f16x8(make_uint2(c.z, c.w));
+    }
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dst_v) + (long long)r * K);
+    for (int i = threadIdx.x; i < K / 16; i += kThreads) dst[i] = src[i];
+  }
   if (threadIdx.x == 0) dst_s[r] = src_s[t];
+}
+
+// store of 8 codes, or (F16) of their fp16 values, at element offset o of a row
+template <bool F16>
+QG_DEVICE void store_codes8(void* q, long long o, uint2 codes) {
+  if constexpr (F16) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(q) + o) = e4m3x8_to_f16x8(codes);
+  else *reinterpret_cast<uint2*>(static_cast<uint8_t*>(q) + o) = codes;
 }
 
 // SiLU(g) * u in fp32 with the fast exponential and division intrinsics: the
@@ -281,9 +306,9 @@ QG_DEVICE void swiglu8(const uint16_t* gu, int I, int c, float (&h)[8]) {
 
 // One row per CTA with the row's SwiGLU values kept in registers: one read of
 // gate/up, the per-row absmax, then the E4M3 codes (CPT chunks of 8 per thread).
-template <int CPT>
+template <int CPT, bool F16>
 __global__ void __launch_bounds__(kThreads) swiglu_quant_reg_kernel(
-    const uint16_t* __restrict__ gate_up, uint8_t* __restrict__ q, float* __restrict__ s, int I) {
+    const uint16_t* __restrict__ gate_up, void* __restrict__ q, float* __restrict__ s, int I) {
   __shared__ float red[kThreads / 32];
   const uint16_t* gu = gate_up + (long long)blockIdx.x * 2 * I;
   const int nc = I / 8;
@@ -301,13 +326,14 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_reg_kernel(
 #pragma unroll
   for (int j = 0; j < CPT; ++j) {
     const int c = threadIdx.x + j * kThreads;
-    if (c < nc) *reinterpret_cast<uint2*>(q + (long long)blockIdx.x * I + c * 8) = fp8_codes8(h[j], sc);
+    if (c < nc) store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8(h[j], sc));
   }
   if (threadIdx.x == 0) s[blockIdx.x] = sc;
 }
 
+template <bool F16>
 __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(
-    const uint16_t* __restrict__ gate_up, uint8_t* __restrict__ q, float* __restrict__ s, int I) {
+    const uint16_t* __restrict__ gate_up, void* __restrict__ q, float* __restrict__ s, int I) {
   __shared__ float red[kThreads / 32];
   const uint16_t* gu = gate_up + (long long)blockIdx.x * 2 * I;
   float m = 0.f;
@@ -320,7 +346,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(
   for (int c = threadIdx.x; c < I / 8; c += kThreads) {
     float h[8];
     swiglu8(gu, I, c, h);
-    *reinterpret_cast<uint2*>(q + (long long)blockIdx.x * I + c * 8) = fp8_codes8(h, sc);
+    store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8(h, sc));
   }
   if (threadIdx.x == 0) s[blockIdx.x] = sc;
 }
@@ -536,26 +562,56 @@ qg_status qg_moe_gather_fp8(const uint8_t* src_q, const float* src_s, const int3
   QG_REQUIRE(K % 16 == 0, QG_ERR_UNSUPPORTED_SHAPE, "qg_moe_gather_fp8: K %% 16 != 0");
   QG_REQUIRE(aligned16(src_q) && aligned16(dst_q), QG_ERR_MISALIGNED, "qg_moe_gather_fp8: misaligned");
   if (R == 0) return QG_OK;
-  qg::gather_fp8_kernel<<<R, qg::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+  qg::gather_fp8_kernel<false><<<R, qg::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       src_q, src_s, route_rows, dst_q, dst_s, T, K);
   return qg::check_launch("qg_moe_gather_fp8");
 }
 
-qg_status qg_swiglu_quant_fp8(const uint16_t* gate_up, uint8_t* q, float* s, int R, int I,
-                              qg_stream_t stream) {
-  QG_REQUIRE(gate_up && q && s, QG_ERR_INVALID_ARG, "qg_swiglu_quant_fp8: NULL pointer");
-  QG_REQUIRE(R >= 0 && I > 0, QG_ERR_INVALID_ARG, "qg_swiglu_quant_fp8: bad sizes");
-  QG_REQUIRE(I % 8 == 0, QG_ERR_UNSUPPORTED_SHAPE, "qg_swiglu_quant_fp8: I %% 8 != 0");
-  QG_REQUIRE(aligned16(gate_up) && aligned16(q), QG_ERR_MISALIGNED, "qg_swiglu_quant_fp8: misaligned");
+qg_status qg_moe_gather_fp8_f16(const uint8_t* src_q, const float* src_s, const int32_t* route_rows,
+                                uint16_t* dst_f16, float* dst_s, int R, int T, int K, qg_stream_t stream) {
+  QG_REQUIRE(src_q && src_s && route_rows && dst_f16 && dst_s, QG_ERR_INVALID_ARG,
+             "qg_moe_gather_fp8_f16: NULL pointer");
+  QG_REQUIRE(R >= 0 && T > 0 && K > 0, QG_ERR_INVALID_ARG, "qg_moe_gather_fp8_f16: bad sizes");
+  QG_REQUIRE(K % 16 == 0, QG_ERR_UNSUPPORTED_SHAPE, "qg_moe_gather_fp8_f16: K %% 16 != 0");
+  QG_REQUIRE(aligned16(src_q) && aligned16(dst_f16), QG_ERR_MISALIGNED, "qg_moe_gather_fp8_f16: misaligned");
+  if (R == 0) return QG_OK;
+  qg::gather_fp8_kernel<true><<<R, qg::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      src_q, src_s, route_rows, dst_f16, dst_s, T, K);
+  return qg::check_launch("qg_moe_gather_fp8_f16");
+}
+
+}  // extern "C"
+
+namespace qg {
+template <bool F16>
+qg_status swiglu_quant_launch(const uint16_t* gate_up, void* q, float* s, int R, int I, qg_stream_t stream,
+                              const char* name) {
+  QG_REQUIRE(gate_up && q && s, QG_ERR_INVALID_ARG, "%s: NULL pointer", name);
+  QG_REQUIRE(R >= 0 && I > 0, QG_ERR_INVALID_ARG, "%s: bad sizes", name);
+  QG_REQUIRE(I % 8 == 0, QG_ERR_UNSUPPORTED_SHAPE, "%s: I %% 8 != 0", name);
+  QG_REQUIRE(aligned16(gate_up) && aligned16(q), QG_ERR_MISALIGNED, "%s: misaligned", name);
   if (R == 0) return QG_OK;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int cpt = (I / 8 + qg::kThreads - 1) / qg::kThreads;    // chunks per thread
-  if (cpt <= 1)      qg::swiglu_quant_reg_kernel<1><<<R, qg::kThreads, 0, st>>>(gate_up, q, s, I);
-  else if (cpt <= 2) qg::swiglu_quant_reg_kernel<2><<<R, qg::kThreads, 0, st>>>(gate_up, q, s, I);
-  else if (cpt <= 4) qg::swiglu_quant_reg_kernel<4><<<R, qg::kThreads, 0, st>>>(gate_up, q, s, I);
-  else if (cpt <= 8) qg::swiglu_quant_reg_kernel<8><<<R, qg::kThreads, 0, st>>>(gate_up, q, s, I);
-  else               qg::swiglu_quant_kernel<<<R, qg::kThreads, 0, st>>>(gate_up, q, s, I);
-  return qg::check_launch("qg_swiglu_quant_fp8");
+  const int cpt = (I / 8 + kThreads - 1) / kThreads;    // chunks per thread
+  if (cpt <= 1)      swiglu_quant_reg_kernel<1, F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
+  else if (cpt <= 2) swiglu_quant_reg_kernel<2, F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
+  else if (cpt <= 4) swiglu_quant_reg_kernel<4, F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
+  else if (cpt <= 8) swiglu_quant_reg_kernel<8, F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
+  else               swiglu_quant_kernel<F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
+  return check_launch(name);
+}
+}  // namespace qg
+
+extern "C" {
+
+qg_status qg_swiglu_quant_fp8(const uint16_t* gate_up, uint8_t* q, float* s, int R, int I,
+                              qg_stream_t stream) {
+  return qg::swiglu_quant_launch<false>(gate_up, q, s, R, I, stream, "qg_swiglu_quant_fp8");
+}
+
+qg_status qg_swiglu_quant_fp8_f16(const uint16_t* gate_up, uint16_t* q_f16, float* s, int R, int I,
+                                  qg_stream_t stream) {
+  return qg::swiglu_quant_launch<true>(gate_up, q_f16, s, R, I, stream, "qg_swiglu_quant_fp8_f16");
 }
 
 qg_status qg_moe_combine(const uint16_t* down, const int32_t* row_of, const float* weight,

@@ -34,6 +34,8 @@ SIGNATURES = {
     "qgemm_w4a16_zp": [P, P, P, I, P, P, I, I, I, P],
     "qgemm_w4a8_grouped_f16act": [P, P, P, P, P, I, P, I, I, I, I, P],
     "qg_e4m3_to_f16": [P, P, I64, P],
+    "qg_moe_gather_fp8_f16": [P, P, P, P, P, I, I, I, P],
+    "qg_swiglu_quant_fp8_f16": [P, P, P, I, I, P],
     "qg_quantize_weights_int4_zp": [P, P, P, P, I, I, I, P],
     "qg_dequant_weights_int4_zp": [P, P, P, I, P, I, I, P],
     "qg_quantize_weights_int4": [P, P, P, I, I, I, P],
@@ -147,6 +149,15 @@ def qg_w4a8_fp8_scales(w_s, w_s8, w_cs8, rows, G, stream=None):
 def qgemm_w4a8_grouped_f16act(a_f16, a_s, expert_off, w_q, w_s, g, y, R, E, N, K, stream=None):
     return _call("qgemm_w4a8_grouped_f16act", _ptr(a_f16), _ptr(a_s), _ptr(expert_off), _ptr(w_q),
                  _ptr(w_s), g, _ptr(y), R, E, N, K, stream=stream)
+
+
+def qg_moe_gather_fp8_f16(src_q, src_s, route_rows, dst_f16, dst_s, R, T, K, stream=None):
+    return _call("qg_moe_gather_fp8_f16", _ptr(src_q), _ptr(src_s), _ptr(route_rows), _ptr(dst_f16),
+                 _ptr(dst_s), R, T, K, stream=stream)
+
+
+def qg_swiglu_quant_fp8_f16(gate_up, q_f16, s, R, I, stream=None):
+    return _call("qg_swiglu_quant_fp8_f16", _ptr(gate_up), _ptr(q_f16), _ptr(s), R, I, stream=stream)
 
 
 def qg_e4m3_to_f16(q, out, n, stream=None):

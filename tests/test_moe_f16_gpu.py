@@ -119,3 +119,71 @@ def test_grouped_f16act_config_size_sampled(qg):
     ref = OF.bf16_decode(OG.to_bf16(
         OG.w4a8_grouped_f64(a8r[pick], asr[pick], sub_off, wq[:, cols], ws[:, cols], 128)))
     check_gemm(y[pick][:, cols], ref, "f16act config sample")
+
+
+def test_gather_and_swiglu_f16_outputs_are_the_codes_values(qg):
+    """The fp16-output harness kernels write exactly the fp16 values of the
+    codes (and the same row scales) that their E4M3-output forms write."""
+    T, R, K, I = 50, 97, 1024, 1408
+    r = np.random.Generator(np.random.PCG64(7))
+    x = inputs.activations_bf16(T, K, seed=31)
+    xq, xs = empty((T, K), torch.uint8), empty((T,), torch.float32)
+    qg.quant_act_fp8_block(dev(x), xq, xs, K, T, K)
+    rows = dev(r.integers(0, T, R).astype(np.int32))
+    aq, as8 = empty((R, K), torch.uint8), empty((R,), torch.float32)
+    a16, as16 = empty((R, K), torch.int16), empty((R,), torch.float32)
+    qg.qg_moe_gather_fp8(xq, xs, rows, aq, as8, R, T, K)
+    qg.qg_moe_gather_fp8_f16(xq, xs, rows, a16, as16, R, T, K)
+    ref16 = empty((R, K), torch.int16)
+    qg.qg_e4m3_to_f16(aq, ref16, R * K)
+    gu = OF.bf16_encode((inputs.activations_bf16(R, 2 * I, seed=32).astype(np.uint32) << 16)
+                        .view(np.float32) * np.float32(2.0))
+    hq, hs = empty((R, I), torch.uint8), empty((R,), torch.float32)
+    h16, hs16 = empty((R, I), torch.int16), empty((R,), torch.float32)
+    qg.qg_swiglu_quant_fp8(dev(gu), hq, hs, R, I)
+    qg.qg_swiglu_quant_fp8_f16(dev(gu), h16, hs16, R, I)
+    href16 = empty((R, I), torch.int16)
+    qg.qg_e4m3_to_f16(hq, href16, R * I)
+    qg.qg_check_device_error()
+    np.testing.assert_array_equal(host(a16), host(ref16))
+    np.testing.assert_array_equal(host(as16), host(as8))
+    np.testing.assert_array_equal(host(h16), host(href16))
+    np.testing.assert_array_equal(host(hs16), host(hs))
+
+
+def test_moe_layer_small_f16(qg):
+    """Full layer on the fp16-activation path: per-token FP8 quant, gather to
+    fp16, grouped gate/up, SwiGLU + FP8 requant to fp16, grouped down,
+    weighted combine -- against the oracle layer."""
+    T, E, H, I, topk = 96, 4, 256, 384, 2
+    rt = inputs.moe_routing(T, E, topk, seed=13)
+    off, rows, wts = rt["expert_off"], rt["route_rows"], rt["route_weight"]
+    R = int(off[-1])
+    x = inputs.activations_bf16(T, H, seed=14)
+    w1 = expert_weights(E, 2 * I, H, seed=70)
+    w2 = expert_weights(E, H, I, seed=80)
+    xq, xs = empty((T, H), torch.uint8), empty((T,), torch.float32)
+    qg.quant_act_fp8_block(dev(x), xq, xs, H, T, H)
+    a16, as_ = empty((R, H), torch.int16), empty((R,), torch.float32)
+    qg.qg_moe_gather_fp8_f16(xq, xs, dev(rows), a16, as_, R, T, H)
+    gu = empty((R, 2 * I), torch.int16)
+    d_off = dev(off)
+    qg.qgemm_w4a8_grouped_f16act(a16, as_, d_off, dev(w1[0]), dev(w1[1]), 128, gu, R, E, 2 * I, H)
+    h16, hs = empty((R, I), torch.int16), empty((R,), torch.float32)
+    qg.qg_swiglu_quant_fp8_f16(gu, h16, hs, R, I)
+    down = empty((R, H), torch.int16)
+    qg.qgemm_w4a8_grouped_f16act(h16, hs, d_off, dev(w2[0]), dev(w2[1]), 128, down, R, E, H, I)
+    row_of = np.full((T, topk), -1, np.int32)
+    wt = np.zeros((T, topk), np.float32)
+    fill = np.zeros(T, np.int64)
+    for r_, t_ in enumerate(rows):
+        row_of[t_, fill[t_]] = r_
+        wt[t_, fill[t_]] = wts[r_]
+        fill[t_] += 1
+    out = empty((T, H), torch.int16)
+    qg.qg_moe_combine(down, dev(row_of), dev(wt), out, T, topk, R, H)
+    qg.qg_check_device_error()
+    down_ref, gu_ref = OG.moe_layer(x, rows, off, w1, w2, 128, I)
+    out_ref = OG.moe_combine(down_ref, rows, wts, T)
+    check_gemm(OF.bf16_decode(host(gu)), OF.bf16_decode(gu_ref), "gate/up")
+    check_gemm(OF.bf16_decode(host(out)), OF.bf16_decode(out_ref), "moe out")
