@@ -350,10 +350,12 @@ moe_fp8s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         tmem_wait_ld();
         const float as = i ? as_hi : as_lo;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float lo = __uint_as_float(v[2 * c]) * __shfl_sync(0xffffffffu, as, 2 * c) * cs;
-          const float hi = __uint_as_float(v[2 * c + 1]) * __shfl_sync(0xffffffffu, as, 2 * c + 1) * cs;
-          packed[16 * i + c] = f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+        for (int c = 0; c < 16; ++c) {        // (acc * token scale) * channel scale, a pair at a time
+          float lo, hi;
+          fmul2(lo, hi, __uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]),
+                __shfl_sync(0xffffffffu, as, 2 * c), __shfl_sync(0xffffffffu, as, 2 * c + 1));
+          fmul2(lo, hi, lo, hi, cs, cs);
+          packed[16 * i + c] = f32x2_to_bf16x2(lo, hi);
         }
       }
       tc_fence_before();
@@ -361,11 +363,13 @@ moe_fp8s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
       const bool odd = lane & 1;
       const uint32_t sel = odd ? 0x3276u : 0x5410u;
       const int n2 = nn & ~1;                        // N is even: a pair is in range or out as a whole
+      const int m0 = mb + (odd ? 1 : 0);
+      const bool full = mb + 64 <= t.r_end && n2 < p.N;
+      uint32_t* yp = reinterpret_cast<uint32_t*>(p.y + (size_t)m0 * p.N + n2);   // rows m0, m0 + 2, ...
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const uint32_t w = prmt(packed[c], __shfl_xor_sync(0xffffffffu, packed[c], 1), sel);
-        const int m = mb + 2 * c + (odd ? 1 : 0);
-        if (n2 < p.N && m < t.r_end) *reinterpret_cast<uint32_t*>(p.y + (size_t)m * p.N + n2) = w;
+        if (full || (n2 < p.N && m0 + 2 * c < t.r_end)) yp[(size_t)c * p.N] = w;
       }
       return true;
     };

@@ -246,6 +246,20 @@ QG_DEVICE uint64_t sw128_kmajor_desc(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// ---- epilogue arithmetic --------------------------------------------------
+// (a0, a1) * (b0, b1), two IEEE round-to-nearest fp32 products in one packed op
+QG_DEVICE void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// two fp32 -> bf16x2 (lo in the low half), round to nearest even
+QG_DEVICE uint32_t f32x2_to_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
 // Instruction descriptor, kind::f16 with fp16 A and B, fp32 D, both K-major.
 QG_HOST_DEVICE uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
