@@ -45,12 +45,35 @@ QG_DEVICE void int4x8_kperm(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {
   for (int i = 0; i < 4; ++i) p[i] = bf16x2_mul(bf16x2_sub(p[i], kBf16x2_136), s2);
 }
 
+// Natural k order straight from the nibbles, for operands stored to tensor
+// memory: byte b of v holds (k_2b, k_2b+1) and byte b of v >> 4 has k_2b+1 in
+// its low nibble, so one prmt puts k_2b under the low half's magic and k_2b+1
+// under the high half's; then the same (u | 0x4300) - 136 and one multiply by
+// the scale as int4x8_kperm.  p[b] = (k_2b, k_2b+1) for b = 0..3.
+QG_DEVICE void int4x8_nat(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {
+  const uint32_t v4 = v >> 4;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t t = prmt(v, v4, (uint32_t)(b | ((4 + b) << 8)));
+    p[b] = bf16x2_mul(bf16x2_sub(lop3<kLutAndXor>(t, 0x000F000Fu, 0x43084308u), kBf16x2_136), s2);
+  }
+}
+
 // ---- INT4 with a zero point -----------------------------------------------------
 // Unsigned nibble u, group zero point z and scale s: (u | 0x4300) is the exact
 // bf16 128 + u; subtracting zb2 = bf16x2(128 + z) leaves the exact integer
 // u - z in [-15, 15], and one bf16 multiply by s rounds (u - z) * s once --
 // the canonical bf16_RNE((q - z) * s), at the cost of the symmetric decode.
 QG_DEVICE uint32_t bf16x2_zero128(uint32_t z) { return (0x4300u | (z & 0xFu)) * 0x00010001u; }
+// Natural-order form (see int4x8_nat) with a zero point: zb2 = bf16x2(128 + z).
+QG_DEVICE void int4zp_x8_nat(uint32_t v, uint32_t s2, uint32_t zb2, uint32_t (&p)[4]) {
+  const uint32_t v4 = v >> 4;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t t = prmt(v, v4, (uint32_t)(b | ((4 + b) << 8)));
+    p[b] = bf16x2_mul(bf16x2_sub(lop3<kLutAndOr>(t, 0x000F000Fu, 0x43004300u), zb2), s2);
+  }
+}
 // p[i] = (k_i, k_{i+4}) for i = 0..3
 QG_DEVICE void int4zp_x8_kperm(uint32_t v, uint32_t s2, uint32_t zb2, uint32_t (&p)[4]) {
   p[0] = lop3<kLutAndOr>(v, 0x000F000Fu, 0x43004300u);      // 0x4300 | nibble = 128 + u
@@ -85,6 +108,15 @@ QG_DEVICE uint16_t f32_to_f16_bits(float f) {
   return r;
 }
 
+// Natural-order fp16 form (see int4x8_nat): p[b] = (k_2b, k_2b+1) * scale.
+QG_DEVICE void int4x8_nat_f16(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {
+  const uint32_t v4 = v >> 4;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t t = prmt(v, v4, (uint32_t)(b | ((4 + b) << 8)));
+    p[b] = f16x2_mul(f16x2_sub(lop3<kLutAndXor>(t, 0x000F000Fu, 0x64086408u), 0x64086408u), s2);
+  }
+}
 // INT4 nibbles -> fp16 pairs (k_i, k_{i+4}) = q * scale: (1024 + (nib ^ 8)) - 1032
 // is the exact integer q, one fp16 multiply forms the exact product.
 QG_DEVICE void int4x8_kperm_f16(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {

@@ -333,12 +333,11 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       uint32_t out[32];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        uint32_t pq[4], nat[4];
+        uint32_t nat[4];
         if constexpr (ZP)
-          int4zp_x8_kperm(v[j], j < 4 ? s2a : s2b, j < 4 ? z2a : z2b, pq);
+          int4zp_x8_nat(v[j], j < 4 ? s2a : s2b, j < 4 ? z2a : z2b, nat);
         else
-          int4x8_kperm(v[j], j < 4 ? s2a : s2b, pq);
-        kperm4_to_natural(pq, nat);
+          int4x8_nat(v[j], j < 4 ? s2a : s2b, nat);
         out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
         out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
       }

@@ -331,9 +331,8 @@ moe_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_cons
       uint32_t out[32];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        uint32_t pq[4], nat[4];
-        int4x8_kperm_f16(v[j], s2, pq);
-        kperm4_to_natural(pq, nat);
+        uint32_t nat[4];
+        int4x8_nat_f16(v[j], s2, nat);
         out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
         out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
       }
