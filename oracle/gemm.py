@@ -93,6 +93,24 @@ def gemm_bf16_f64(x_bits, w_bits, col_scale=None):
     return y
 
 
+def w8a8_f64(a_codes, a_s, w_codes, cs, g):
+    """FP8 weights with per-channel scales times activations quantized to E4M3
+    per 1 x g block (the activation quantizer of the FP8 GEMV prologue in
+    FreeToken PR #805's list of native casts; here the a7 block rule):
+    y64[m, n] = cs[n] * sum_b a_s[m, b] * sum_{k in block b} e4m3(a[m,k]) * e4m3(w[n,k]),
+    everything in float64 (the block partial sums are exact products summed).
+    a_codes [M, K], a_s [M, K/g], w_codes [N, K], cs [N]."""
+    a = F.e4m3_decode(a_codes)
+    w = F.e4m3_decode(w_codes)
+    M, K = a.shape
+    nb = K // g
+    y = np.zeros((M, w.shape[0]))
+    s = np.asarray(a_s, np.float64).reshape(M, nb)
+    for b in range(nb):
+        y += (a[:, b * g:(b + 1) * g] @ w[:, b * g:(b + 1) * g].T) * s[:, b:b + 1]
+    return y * np.asarray(cs, np.float64)[None, :]
+
+
 def qgemm_w4a16(x_bits, packed, s_bits, g):
     return gemm_bf16_f64(x_bits, dequant_int4(packed, s_bits, g))
 

@@ -474,6 +474,29 @@ def test_gemm_f64_matches_exact_brute_force():
             assert Fraction(float(y[m, n])) == ref * Fraction(float(cs[n]))
 
 
+def test_w8a8_matches_exact_brute_force():
+    """E4M3 codes on both sides, per-block activation scales and per-channel
+    weight scales that are powers of two: every term is exact, so the fp64
+    oracle must equal a Fraction sum; swapping the block index, a transposed
+    operand or a scale on the wrong axis fails (M != N, 3 blocks)."""
+    r = np.random.Generator(np.random.PCG64(23))
+    M, N, g, nb = 2, 3, 16, 3
+    K = g * nb
+    a = r.integers(0, 0x7F, (M, K)).astype(np.uint8) | (r.integers(0, 2, (M, K)) << 7).astype(np.uint8)
+    w = r.integers(0, 0x7F, (N, K)).astype(np.uint8)
+    a_s = 2.0 ** r.integers(-4, 4, (M, nb)).astype(np.float64)
+    cs = 2.0 ** r.integers(-3, 3, N).astype(np.float64)
+    y = G.w8a8_f64(a, a_s, w, cs, g)
+    for m in range(M):
+        for n in range(N):
+            ref = Fraction(0)
+            for b in range(nb):
+                part = sum(Fraction(float(F.e4m3_decode(a[m, k]))) * Fraction(float(F.e4m3_decode(w[n, k])))
+                           for k in range(b * g, (b + 1) * g))
+                ref += part * Fraction(float(a_s[m, b]))
+            assert Fraction(float(y[m, n])) == ref * Fraction(float(cs[n]))
+
+
 def test_w4a8_grouped_matches_exact_brute_force():
     r = np.random.Generator(np.random.PCG64(18))
     E, N, K, g = 3, 4, 256, 128
