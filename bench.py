@@ -11,6 +11,8 @@ One step = one pass over every row of the hot path at its workload size:
                  tensor-core GEMMs; roofline against the FP8 dense peak)
   zero points    asymmetric INT4 (zero point per group of 64): M = 1 GEMVs and
                  M = 8192 prefill over the same three (N, K)
+  W8A8 GEMV      FP8 weights, activations quantized per 1 x 128 block inside the
+                 GEMV prologue: M = 1 over the same three (N, K)
 Each row is one CUDA graph; CUDA events between the graphs time every row
 inside the timed region.  The headline value is the metric's first quantity:
 effective HBM GB/s of the M = 1 GEMVs (algorithmic bytes / time); the
@@ -367,6 +369,10 @@ class Workload:
             for N, K in SHAPES:
                 W = self.W[("int4", N, K)]
                 qg.qgemm_w4a16(W["q"], W["s"], 128, self.XP[K], self.YP[N], 8192, N, K)
+        elif name == "decode_w8a8":
+            for N, K in SHAPES:
+                W = self.W[("fp8", N, K)]
+                qg.qgemm_w8a8(W["q"], W["s"], self.X[(1, K)], self.Y[(1, N)], 1, N, K)
         elif name == "decode_zp":
             for N, K in SHAPES:
                 W = self.W[("int4zp", N, K)]
@@ -411,6 +417,9 @@ class Workload:
             self.flops["prefill"] = sum(2.0 * 8192 * N * K for N, K in SHAPES)
         if "prefill_zp" in self.rows:
             self.flops["prefill_zp"] = sum(2.0 * 8192 * N * K for N, K in SHAPES)
+        if "decode_w8a8" in self.rows:
+            self.bytes["decode_w8a8"] = sum(N * K + 4 * N + 2 * K + 2 * N for N, K in SHAPES)
+            self.launches["decode_w8a8"] = None
         if "decode_zp" in self.rows:
             self.bytes["decode_zp"] = sum(N * K * (0.5 + 3.0 / ZP_G) + 2 * K + 2 * N for N, K in SHAPES)
             self.launches["decode_zp"] = None
@@ -494,7 +503,7 @@ def bench_config(rows, world):
     return {"workload": "decode sweep M in {1,4,16} x {4096^2, 14336x4096, 4096x14336} x "
                         "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill W4A16 M=8192 + "
                         "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2 (bf16 group scales; "
-                        "FP8 group scales) + asymmetric INT4 g64 M=1 and M=8192",
+                        "FP8 group scales) + asymmetric INT4 g64 M=1 and M=8192 + W8A8 GEMV M=1",
             "rows": rows, "l2": "inputs larger than L2: every weight matrix read once per step; "
                                 "step working set > 1 GB vs 129 MB L2",
             "parallelism": "replicas" if world > 1 else "single"}
@@ -725,7 +734,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe,moe_fp8s,"
-                                      "decode_zp,prefill_zp")
+                                      "decode_zp,prefill_zp,decode_w8a8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)

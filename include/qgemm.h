@@ -107,6 +107,17 @@ QG_API qg_status qgemm_w8a16(const uint8_t* w_e4m3, const float* w_cs,
                       const uint16_t* x, uint16_t* y, int M, int N, int K,
                       qg_stream_t stream);
 
+/* W8A8 with the activation quantization inside the GEMV prologue (the
+ * in-kernel act quant of an FP8 GEMV, FreeToken PR #805's list of native
+ * E4M3 casts; the quantizer is quant_act_fp8_block's, 1 x 128 blocks):
+ * y[m,n] = w_cs[n] * sum_b s[m,b] * sum_{k in b} e4m3(a[m,k]) * e4m3(w[n,k])
+ * with (a, s) = the E4M3 block quantization of x (s = absmax/448, IEEE
+ * division, RNE satfinite), fp32 accumulation, one bf16 rounding.
+ *   w_e4m3 [N][K] u8   w_cs [N] fp32   x [M][K] bf16   y [M][N] bf16.
+ * K % 128 == 0, N % 8 == 0; the decode GEMV (M is processed 16 rows at a time). */
+QG_API qg_status qgemm_w8a8(const uint8_t* w_e4m3, const float* w_cs, const uint16_t* x,
+                     uint16_t* y, int M, int N, int K, qg_stream_t stream);
+
 /* FP4 E2M1 weights with block scales.
  *  scale_fmt QG_SCALE_E8M0: MXFP4, g == 32, w_bs [N][K/32] E8M0 codes,
  *     canonical weight e2m1 * 2^(c-127) (exact); global_scale must be NULL.

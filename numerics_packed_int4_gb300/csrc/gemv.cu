@@ -23,6 +23,10 @@
 //     kernel's output -- stated in the header).
 //   * fp32 accumulation; the FP8 channel scale / NVFP4 global scale is
 //     applied to the reduced row; one bf16 rounding at the store.
+//   * W8A8 (FP8 weights, activations quantized here): the prologue quantizes
+//     the CTA's activation slice per 1 x 128 block with the quant_act_fp8_block
+//     rule and stages the codes' exact bf16 values; each block's partial sums
+//     are scaled into the accumulator by the block scale at the block's end.
 #include <algorithm>
 
 #include "dequant.cuh"
@@ -33,7 +37,10 @@
 namespace qg {
 namespace {
 
-enum Fmt { F_INT4 = 0, F_FP8 = 1, F_MXFP4 = 2, F_NVFP4 = 3, F_INT4Z = 4 };
+enum Fmt { F_INT4 = 0, F_FP8 = 1, F_MXFP4 = 2, F_NVFP4 = 3, F_INT4Z = 4, F_FP8A8 = 5 };
+// FP8 weights (one byte per weight)
+constexpr bool fp8_weights(int f) { return f == F_FP8 || f == F_FP8A8; }
+constexpr int kActBlock = 128;         // F_FP8A8: activation quantization block (1 x 128)
 
 constexpr int kWarps = 8;
 constexpr int kRing = 6;               // weight segments in flight per warp (cp.async ring)
@@ -46,6 +53,7 @@ template <> struct FmtTraits<F_INT4Z> { static constexpr int KSEG = 128, CPL = 4
 template <> struct FmtTraits<F_MXFP4> { static constexpr int KSEG = 128, CPL = 4; };
 template <> struct FmtTraits<F_NVFP4> { static constexpr int KSEG = 128, CPL = 4; };
 template <> struct FmtTraits<F_FP8>   { static constexpr int KSEG = 64,  CPL = 2; };
+template <> struct FmtTraits<F_FP8A8> { static constexpr int KSEG = 64,  CPL = 2; };
 
 struct GemvArgs {
   const uint8_t* w;        // packed weights [N][row_bytes]
@@ -139,7 +147,7 @@ QG_DEVICE void decode_chunk(const uint4& w, const Scale& s, int j, uint32_t (&a)
 // X chunk permutation matching decode_chunk's pair order
 template <int FMT>
 QG_DEVICE uint4 perm_x(const uint4& u) {
-  if constexpr (FMT == F_FP8)   // (0,2,1,3,4,6,5,7)
+  if constexpr (fp8_weights(FMT))   // (0,2,1,3,4,6,5,7)
     return make_uint4(prmt(u.x, u.y, 0x5410u), prmt(u.x, u.y, 0x7632u),
                       prmt(u.z, u.w, 0x5410u), prmt(u.z, u.w, 0x7632u));
   else                          // (0,4,1,5,2,6,3,7)
@@ -181,6 +189,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   uint4* xs = smem + (size_t)kWarps * kRing * 64;                           // [M][ncp]
   float* red = reinterpret_cast<float*>(xs + (size_t)M * p.ncp);            // [kWarps][16][MP]
   float* rsum = red + kWarps * 16 * MP;                                     // [rows_cta][MP]
+  float* xsc = rsum + 16 * RG * MP;          // F_FP8A8: activation block scales [M][nblk]
 
   // k range of this CTA (cluster split) and of this warp (warp split)
   const int ks = gridDim.x, kr = blockIdx.x;
@@ -189,7 +198,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   const int nseg_cta = seg_hi - seg_lo;
   const int k0 = seg_lo * Tr::KSEG;
   const int nchunk = nseg_cta * Tr::KSEG / 8;
-  const size_t row_bytes = (FMT == F_FP8) ? (size_t)p.K : (size_t)p.K / 2;
+  const size_t row_bytes = fp8_weights(FMT) ? (size_t)p.K : (size_t)p.K / 2;
   const int row0 = blockIdx.y * rows_cta;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -241,16 +250,71 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   // ---- previous kernel done: its outputs (our activations) are visible ------
   pdl_wait();
   // ---- stage the activation slice, permuted and swizzled -------------------
+  // F_FP8A8 then quantizes it in place, per 1 x 128 block of the whole row
+  // (the quant_act_fp8_block rule: s = absmax / 448, code = E4M3_RNE_sat(x /
+  // s)), keeping the codes' exact bf16 values; the block maxima are gathered
+  // while staging (a partly covered block's maximum includes its elements
+  // outside this CTA's k range) and the scales go to xsc.
+  const int blk0 = k0 / kActBlock;
+  const int nblk = (k0 + nchunk * 8 + kActBlock - 1) / kActBlock - blk0;
+  unsigned int* xmax = reinterpret_cast<unsigned int*>(xsc + M * nblk);     // [M][nblk] |x| maxima (bits)
+  if constexpr (FMT == F_FP8A8) {
+    for (int i = threadIdx.x; i < M * nblk; i += kWarps * 32) xmax[i] = 0u;
+    __syncthreads();
+  }
   for (int i = threadIdx.x; i < M * nchunk; i += kWarps * 32) {
     const int m = i / nchunk, c = i - m * nchunk;
     const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * p.K + k0 + 8 * c));
     xs[m * p.ncp + swz(c)] = perm_x<FMT>(u);
+    if constexpr (FMT == F_FP8A8) {
+      const float a = fmaxf(fmaxf(fmaxf(fabsf(bf16_lo_to_f32(u.x)), fabsf(bf16_hi_to_f32(u.x))),
+                                  fmaxf(fabsf(bf16_lo_to_f32(u.y)), fabsf(bf16_hi_to_f32(u.y)))),
+                            fmaxf(fmaxf(fabsf(bf16_lo_to_f32(u.z)), fabsf(bf16_hi_to_f32(u.z))),
+                                  fmaxf(fabsf(bf16_lo_to_f32(u.w)), fabsf(bf16_hi_to_f32(u.w)))));
+      atomicMax(&xmax[m * nblk + (k0 + 8 * c) / kActBlock - blk0], __float_as_uint(a));   // a >= 0
+    }
+  }
+  if constexpr (FMT == F_FP8A8) {
+    // the parts of the first and last blocks outside this CTA's k range
+    const int kend = k0 + nchunk * 8;
+    const int head = k0 - blk0 * kActBlock, tail = (blk0 + nblk) * kActBlock - kend;
+    for (int i = threadIdx.x; i < M * (head + tail) / 8; i += kWarps * 32) {
+      const int per = (head + tail) / 8, m = i / per, c = i - m * per;
+      const int k = c < head / 8 ? blk0 * kActBlock + 8 * c : kend + 8 * (c - head / 8);
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * p.K + k));
+      const float a = fmaxf(fmaxf(fmaxf(fabsf(bf16_lo_to_f32(u.x)), fabsf(bf16_hi_to_f32(u.x))),
+                                  fmaxf(fabsf(bf16_lo_to_f32(u.y)), fabsf(bf16_hi_to_f32(u.y)))),
+                            fmaxf(fmaxf(fabsf(bf16_lo_to_f32(u.z)), fabsf(bf16_hi_to_f32(u.z))),
+                                  fmaxf(fabsf(bf16_lo_to_f32(u.w)), fabsf(bf16_hi_to_f32(u.w)))));
+      atomicMax(&xmax[m * nblk + k / kActBlock - blk0], __float_as_uint(a));
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < M * nblk; i += kWarps * 32) xsc[i] = fp8_scale(__uint_as_float(xmax[i]));
+    __syncthreads();
+    for (int i = threadIdx.x; i < M * nchunk; i += kWarps * 32) {
+      const int m = i / nchunk, c = i - m * nchunk;
+      const float sc = xsc[m * nblk + (k0 + 8 * c) / kActBlock - blk0];
+      uint4& xv = xs[m * p.ncp + swz(c)];
+      uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {          // elementwise, so the staged (permuted) order is fine
+        const uint32_t code = f32x2_to_e4m3x2(__fdiv_rn(bf16_hi_to_f32(w[j]), sc), __fdiv_rn(bf16_lo_to_f32(w[j]), sc));
+        w[j] = (__float_as_uint(e4m3_to_f32(code & 0xFFu)) >> 16) | (__float_as_uint(e4m3_to_f32(code >> 8)) & 0xFFFF0000u);
+      }
+      xv = make_uint4(w[0], w[1], w[2], w[3]);
+    }
   }
   __syncthreads();
 
   float acc[MT][4];
 #pragma unroll
   for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  // F_FP8A8: the current activation block's partial sums, scaled into acc at
+  // each block boundary (the products inside a block are exact in fp32)
+  float accb[MT][4];
+#pragma unroll
+  for (int i = 0; i < MT; ++i) accb[i][0] = accb[i][1] = accb[i][2] = accb[i][3] = 0.f;
+  float (&acc_mma)[MT][4] = (FMT == F_FP8A8) ? accb : acc;
 
   for (int s0 = 0; s0 < nseg; s0 += kRing) {
 #pragma unroll
@@ -281,13 +345,29 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
           const int c = swz(cbase + j);
           {
             const uint4 xf = xr0[c];
-            mma_bf16(acc[0], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
-            mma_bf16(acc[0], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
+            mma_bf16(acc_mma[0], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
+            mma_bf16(acc_mma[0], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
           }
           if constexpr (MT == 2) {
             const uint4 xf = xr1[c];
-            mma_bf16(acc[1], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
-            mma_bf16(acc[1], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
+            mma_bf16(acc_mma[1], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
+            mma_bf16(acc_mma[1], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
+          }
+        }
+        if constexpr (FMT == F_FP8A8) {
+          // block boundary (two 64-k segments per block) or the end of this
+          // warp's range: acc += partial * block scale of each column m
+          const int gseg = seg_lo + s_lo + s;
+          if ((gseg & 1) || s == nseg - 1) {
+            const int bl = (gseg >> 1) - blk0;
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+              const float x0 = xsc[min(8 * i + 2 * t, M - 1) * nblk + bl];
+              const float x1 = xsc[min(8 * i + 2 * t + 1, M - 1) * nblk + bl];
+              acc[i][0] = fmaf(accb[i][0], x0, acc[i][0]); acc[i][1] = fmaf(accb[i][1], x1, acc[i][1]);
+              acc[i][2] = fmaf(accb[i][2], x0, acc[i][2]); acc[i][3] = fmaf(accb[i][3], x1, acc[i][3]);
+              accb[i][0] = accb[i][1] = accb[i][2] = accb[i][3] = 0.f;
+            }
           }
         }
       }
@@ -332,7 +412,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
       v = rsum[r * MP + m];
     }
     if (n < p.N) {
-      if constexpr (FMT == F_FP8) v *= __ldg(static_cast<const float*>(p.scales) + n);
+      if constexpr (fp8_weights(FMT)) v *= __ldg(static_cast<const float*>(p.scales) + n);
       if constexpr (FMT == F_NVFP4) v *= __ldg(p.gscale);
       p.y[(size_t)m * p.N + n] = f32_to_bf16_bits(v);
     }
@@ -354,7 +434,7 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ w, const void* __rest
   const long long total = (long long)N * nseg;
   if (lane_id >= total) return;
   const int n = int(lane_id / nseg), seg = int(lane_id % nseg);
-  const size_t row_bytes = (FMT == F_FP8) ? (size_t)K : (size_t)K / 2;
+  const size_t row_bytes = fp8_weights(FMT) ? (size_t)K : (size_t)K / 2;
   const uint4 wv = *reinterpret_cast<const uint4*>(w + (size_t)n * row_bytes + seg * 64 + 16 * t);
   GemvArgs p{};
   p.scales = scales; p.zeros = zeros; p.K = K; p.g = g; p.lg = 31 - __clz(g);
@@ -387,11 +467,12 @@ qg_status launch_gemv_t(const GemvArgs& a0, cudaStream_t st, const char* name) {
   auto smem_for = [&](int ks, int rg) {
     const int nseg_max = (a.nseg + ks - 1) / ks;
     int ncp = nseg_max * Tr::KSEG / 8;
-    const int want = (FMT == F_FP8) ? 1 : 2;          // bank-conflict-free pitch (mod 8)
+    const int want = fp8_weights(FMT) ? 1 : 2;        // bank-conflict-free pitch (mod 8)
     while ((ncp & 7) != want) ++ncp;
     a.ncp = ncp;
+    const size_t xsc_bytes = FMT == F_FP8A8 ? (size_t)a.M * (nseg_max * Tr::KSEG / kActBlock + 2) * 8 : 0;
     return (size_t)kWarps * kRing * 64 * 16 + (size_t)a.M * ncp * 16 +
-           (size_t)(kWarps * 16 + 16 * rg) * MT * 8 * 4;
+           (size_t)(kWarps * 16 + 16 * rg) * MT * 8 * 4 + xsc_bytes;
   };
   // K split over a cluster only when the activation slice does not fit
   int ks = 1;
@@ -535,6 +616,17 @@ qg_status qgemm_w8a16(const uint8_t* w_e4m3, const float* w_cs, const uint16_t* 
   qg::GemvArgs a{};
   a.w = w_e4m3; a.scales = w_cs; a.x = x; a.y = y; a.M = M; a.N = N; a.K = K; a.g = K;
   return qg::run_weight_only<qg::F_FP8>(a, reinterpret_cast<cudaStream_t>(stream), "qgemm_w8a16");
+}
+
+qg_status qgemm_w8a8(const uint8_t* w_e4m3, const float* w_cs, const uint16_t* x, uint16_t* y,
+                     int M, int N, int K, qg_stream_t stream) {
+  qg_status r = qg::check_common(w_e4m3, x, y, M, N, K, "qgemm_w8a8");
+  if (r != QG_OK) return r;
+  QG_REQUIRE(w_cs, QG_ERR_INVALID_ARG, "qgemm_w8a8: NULL channel scales");
+  if (M == 0) return QG_OK;
+  qg::GemvArgs a{};
+  a.w = w_e4m3; a.scales = w_cs; a.x = x; a.y = y; a.M = M; a.N = N; a.K = K; a.g = K;
+  return qg::run_weight_only<qg::F_FP8A8>(a, reinterpret_cast<cudaStream_t>(stream), "qgemm_w8a8");
 }
 
 qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt, int g,

@@ -72,6 +72,9 @@ QG_DEVICE uint32_t f32x2_to_e2m1x2(float hi, float lo) {
 }
 
 // E4M3 code -> exact fp32 value (finite codes; 0x7F/0xFF give NaN)
+// FP8 E4M3 block scale: absmax / 448 in IEEE fp32 (an all-zero block gets 1)
+QG_DEVICE float fp8_scale(float amax) { return amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f); }
+
 QG_DEVICE float e4m3_to_f32(uint32_t c) {
   const uint32_t s = (c & 0x80u) << 24, E = (c >> 3) & 0xFu, Mn = c & 7u;
   if ((c & 0x7Fu) == 0x7Fu) return __uint_as_float(0x7FC00000u);

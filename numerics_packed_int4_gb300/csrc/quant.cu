@@ -42,7 +42,6 @@ QG_DEVICE float absmax8(const float (&v)[8]) {
 }
 
 // ---- E4M3 block step: s = amax/448 (zero -> 1), codes of x/s ---------------
-QG_DEVICE float fp8_scale(float amax) { return amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f); }
 
 QG_DEVICE uint2 fp8_codes8(const float (&v)[8], float s) {
   uint32_t c[4];

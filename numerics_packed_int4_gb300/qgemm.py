@@ -25,6 +25,7 @@ P, I, U32, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_longlo
 SIGNATURES = {
     "qgemm_w4a16": [P, P, I, P, P, I, I, I, P],
     "qgemm_w8a16": [P, P, P, P, I, I, I, P],
+    "qgemm_w8a8": [P, P, P, P, I, I, I, P],
     "qgemm_fp4a16": [P, P, I, I, P, P, P, I, I, I, P],
     "quant_act_mxfp4": [P, P, P, I, I, I, P],
     "quant_act_fp8_block": [P, P, P, I, I, I, P],
@@ -117,6 +118,10 @@ def qgemm_w4a16(w_q, w_s, g, x, y, M, N, K, stream=None):
 
 def qgemm_w8a16(w_e4m3, w_cs, x, y, M, N, K, stream=None):
     return _call("qgemm_w8a16", _ptr(w_e4m3), _ptr(w_cs), _ptr(x), _ptr(y), M, N, K, stream=stream)
+
+
+def qgemm_w8a8(w_e4m3, w_cs, x, y, M, N, K, stream=None):
+    return _call("qgemm_w8a8", _ptr(w_e4m3), _ptr(w_cs), _ptr(x), _ptr(y), M, N, K, stream=stream)
 
 
 def qgemm_fp4a16(w_e2m1, w_bs, scale_fmt, g, global_scale, x, y, M, N, K, stream=None):
