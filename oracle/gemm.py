@@ -45,7 +45,8 @@ F32 = np.float32
 def dequant_int4(packed, s_bits, g):
     q = F.int4_decode(Q.unpack_nibbles(packed)).astype(F32)
     s = F.bf16_decode(s_bits).astype(F32)
-    prod = (q.reshape(q.shape[:-1] + (-1, g)) * s[..., None]).astype(F32)   # exact
+    with np.errstate(over="ignore"):       # beyond fp32's range: inf, as RNE to bf16 gives
+        prod = (q.reshape(q.shape[:-1] + (-1, g)) * s[..., None]).astype(F32)   # exact
     return F.bf16_encode(prod.reshape(q.shape))
 
 

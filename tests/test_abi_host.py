@@ -83,6 +83,34 @@ def test_misaligned_pointers(lib):
     assert _rc(lib, "quant_act_fp8_block", FAKE, FAKE_MIS, FAKE, 128, 1, 128) == 3
 
 
+def test_validation_of_the_widened_entry_points(lib):
+    """The entry points beyond the six of the path reject bad arguments
+    before touching the GPU."""
+    # asymmetric INT4
+    assert _rc(lib, "qgemm_w4a16_zp", FAKE, FAKE, None, 64, FAKE, FAKE, 1, 128, 128) == 1
+    assert _rc(lib, "qgemm_w4a16_zp", FAKE, FAKE, FAKE, 48, FAKE, FAKE, 1, 128, 384) == 2
+    assert _rc(lib, "qg_quantize_weights_int4_zp", FAKE, FAKE, FAKE, FAKE, 12, 8, 96) == 2
+    assert _rc(lib, "qg_dequant_weights_int4_zp", FAKE, FAKE, FAKE, 16, FAKE, 8, 128) == 2
+    # W8A8 GEMV
+    assert _rc(lib, "qgemm_w8a8", FAKE, None, FAKE, FAKE, 1, 128, 128) == 1
+    assert _rc(lib, "qgemm_w8a8", FAKE, FAKE, FAKE, FAKE, 1, 12, 128) == 2
+    assert _rc(lib, "qgemm_w8a8", FAKE, FAKE, FAKE_MIS, FAKE, 1, 128, 128) == 3
+    # W4A8 on fp16 activation copies, and its harness kernels
+    assert _rc(lib, "qgemm_w4a8_grouped_f16act", None, FAKE, FAKE, FAKE, FAKE, 128, FAKE, 1, 1, 16, 128) == 1
+    assert _rc(lib, "qgemm_w4a8_grouped_f16act", FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, 1, 1, 16, 128) == 2
+    assert _rc(lib, "qgemm_w4a8_grouped_f16act", FAKE, FAKE, FAKE, FAKE, FAKE, 128, FAKE, 1, 1, 24, 128) == 2
+    assert _rc(lib, "qgemm_w4a8_grouped_f16act", FAKE_MIS, FAKE, FAKE, FAKE, FAKE, 128, FAKE, 1, 1, 16, 128) == 3
+    assert _rc(lib, "qg_e4m3_to_f16", FAKE, FAKE, 12) == 2
+    assert _rc(lib, "qg_e4m3_to_f16", FAKE, FAKE_MIS, 16) == 3
+    assert _rc(lib, "qg_moe_gather_fp8_f16", FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 24) == 2
+    assert _rc(lib, "qg_swiglu_quant_fp8_f16", FAKE, FAKE, FAKE, 4, 12) == 2
+    # W4A8 with FP8 group scales
+    assert _rc(lib, "qgemm_w4a8_grouped_fp8s", FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 1, 1, 16, 128) == 1
+    assert _rc(lib, "qgemm_w4a8_grouped_fp8s", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 96) == 2
+    assert _rc(lib, "qg_w4a8_fp8_scales", FAKE, FAKE, None, 4, 8) == 1
+    assert _rc(lib, "qg_w4a8_fp8_scales", FAKE, FAKE, FAKE, 4, 0) == 1
+
+
 def test_wait_limit_setter_is_callable(lib):
     lib.qg_set_wait_limit(5)
     lib.qg_set_wait_limit(0)
