@@ -264,7 +264,10 @@ QG_API qg_status qg_moe_gather_fp8_f16(const uint8_t* src_q, const float* src_s,
                                 const int32_t* route_rows, uint16_t* dst_f16, float* dst_s,
                                 int R, int T, int K, qg_stream_t stream);
 /* h = SiLU(gate) * up in fp32 from the bf16 projection output [R][2I] (gate
- * columns first), then the per-row FP8 quantizer (block = I).
+ * columns first), then the per-row FP8 quantizer (block = I): s as
+ * quant_act_fp8_block, codes of h * (1/s).  SiLU uses the fast exponential
+ * and division, so h is good to a few fp32 ulps and the codes to one E4M3
+ * step where h / s lies that close to a rounding boundary.
  *   gate_up [R][2I] bf16 -> q [R][I] E4M3, s [R] fp32.  I % 8 == 0.          */
 QG_API qg_status qg_swiglu_quant_fp8(const uint16_t* gate_up, uint8_t* q, float* s,
                               int R, int I, qg_stream_t stream);

@@ -50,6 +50,16 @@ QG_DEVICE uint2 fp8_codes8(const float (&v)[8], float s) {
     c[i] = f32x2_to_e4m3x2(__fdiv_rn(v[2 * i + 1], s), __fdiv_rn(v[2 * i], s));
   return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
+// The same codes of v * rs with rs = 1/s: within an fp32 ulp of v / s, which
+// moves a code only when v / s sits that close to an E4M3 rounding boundary.
+// For values that are themselves only good to a few ulps (the fast-SiLU
+// output of the MoE harness) this is as exact as the division.
+QG_DEVICE uint2 fp8_codes8_rcp(const float (&v)[8], float rs) {
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = f32x2_to_e4m3x2(v[2 * i + 1] * rs, v[2 * i] * rs);
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
 
 // ---- MXFP4 block step -----------------------------------------------------------
 // Exponent-first 0.75-threshold rule (vLLM PR #43557, "Fix").
@@ -322,10 +332,11 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_reg_kernel(
     }
   }
   const float sc = fp8_scale(cta_max(m, red));
+  const float rs = __frcp_rn(sc);
 #pragma unroll
   for (int j = 0; j < CPT; ++j) {
     const int c = threadIdx.x + j * kThreads;
-    if (c < nc) store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8(h[j], sc));
+    if (c < nc) store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8_rcp(h[j], rs));
   }
   if (threadIdx.x == 0) s[blockIdx.x] = sc;
 }
@@ -342,10 +353,11 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(
     m = fmaxf(m, absmax8(h));
   }
   const float sc = fp8_scale(cta_max(m, red));
+  const float rs = __frcp_rn(sc);
   for (int c = threadIdx.x; c < I / 8; c += kThreads) {
     float h[8];
     swiglu8(gu, I, c, h);
-    store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8(h, sc));
+    store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8_rcp(h, rs));
   }
   if (threadIdx.x == 0) s[blockIdx.x] = sc;
 }
