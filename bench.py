@@ -338,6 +338,10 @@ class Workload:
             self.qg.qg_quantize_weights_int4(w, w2q[e], w2s[e], 128, H, I)
             del w
         m.update(w1q=w1q, w1s=w1s, w2q=w2q, w2s=w2s)
+        m["w1e"] = t.empty((E * 2 * I,), dtype=t.int8, device=dev)    # load-time row shifts
+        m["w2e"] = t.empty((E * H,), dtype=t.int8, device=dev)
+        self.qg.qg_w4a8_row_shifts(w1s, m["w1e"], E * 2 * I, H // 128)
+        self.qg.qg_w4a8_row_shifts(w2s, m["w2e"], E * H, I // 128)
         if "moe_fp8s" in self.rows:                       # load-time scale preparation
             m["w1s8"] = t.empty((H // 128, E * 2 * I), dtype=t.uint8, device=dev)      # group-major
             m["w1cs8"] = t.empty((E, 2 * I), dtype=t.float32, device=dev)
@@ -389,10 +393,10 @@ class Workload:
             T, E, H, I, R, topk = m["T"], m["E"], m["H"], m["I"], m["R"], m["topk"]
             qg.quant_act_fp8_block(m["x"], m["xq"], m["xs"], H, T, H)
             qg.qg_moe_gather_fp8_f16(m["xq"], m["xs"], m["rows"], m["aq16"], m["as"], R, T, H)
-            qg.qgemm_w4a8_grouped_f16act(m["aq16"], m["as"], m["off"], m["w1q"], m["w1s"], 128, m["gu"],
+            qg.qgemm_w4a8_grouped_f16act(m["aq16"], m["as"], m["off"], m["w1q"], m["w1s"], m["w1e"], 128, m["gu"],
                                          R, E, 2 * I, H)
             qg.qg_swiglu_quant_fp8_f16(m["gu"], m["hq16"], m["hs"], R, I)
-            qg.qgemm_w4a8_grouped_f16act(m["hq16"], m["hs"], m["off"], m["w2q"], m["w2s"], 128, m["down"],
+            qg.qgemm_w4a8_grouped_f16act(m["hq16"], m["hs"], m["off"], m["w2q"], m["w2s"], m["w2e"], 128, m["down"],
                                          R, E, H, I)
             qg.qg_moe_combine(m["down"], m["row_of"], m["wt"], m["out"], T, topk, R, H)
         elif name == "moe_fp8s":

@@ -175,12 +175,22 @@ QG_API qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,
  * copy, or a producer writes it directly).  With the activations in HBM as
  * fp16 they reach the tensor cores by TMA with no restaging in the kernel
  * (one CTA per SM, tcgen05 kind::f16), for one more read of R*K*2 bytes.
- *   a_f16 [R][K] fp16; the other arguments as qgemm_w4a8_grouped.
+ *   a_f16 [R][K] fp16; w_e [E*N] int8 row shifts from qg_w4a8_row_shifts
+ *   (or NULL); the other arguments as qgemm_w4a8_grouped.
  * Rules: g == 128, K % 128 == 0, N % 16 == 0, R >= 0, E >= 1.               */
 QG_API qg_status qgemm_w4a8_grouped_f16act(const uint16_t* a_f16, const float* a_s,
                                     const int32_t* expert_off, const uint8_t* w_q,
-                                    const uint16_t* w_s, int g, uint16_t* y, int R, int E,
-                                    int N, int K, qg_stream_t stream);
+                                    const uint16_t* w_s, const int8_t* w_e, int g, uint16_t* y,
+                                    int R, int E, int N, int K, qg_stream_t stream);
+
+/* Load-time companion of qgemm_w4a8_grouped_f16act: each weight row's power
+ * of two e (the row's largest |scale| times 2^e lies in [2^11, 2^12), which
+ * keeps every fp16 product q * s * 2^e exact and in range), so the GEMM need
+ * not scan the row's scales on every tile.  Pass the result as w_e, or NULL
+ * to have the GEMM compute it.
+ *   w_s [rows][G] bf16 -> w_e [rows] int8 (rows = E*N, G = K/128).          */
+QG_API qg_status qg_w4a8_row_shifts(const uint16_t* w_s, int8_t* w_e, int rows, int G,
+                             qg_stream_t stream);
 
 /* E4M3 codes -> their values as fp16 (exact; NaN codes give fp16 NaN).
  *   q [n] u8 (8-byte aligned) -> out [n] fp16 (16-byte aligned).  n % 8 == 0. */

@@ -64,6 +64,7 @@ struct F16Args {
   const float* a_s;
   const int32_t* off;
   const uint16_t* ws;                    // [E*N][K/128] bf16
+  const int8_t* we;                      // [E*N] row exponent shifts (qg_w4a8_row_shifts) or nullptr
   uint16_t* y;
   int R, E, N, K;
   int tiles_w;
@@ -275,8 +276,9 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     auto set_row = [&](Cur& c) {
       if (c.i < ntiles) {
         const HTile t = tile_of(c.i);
-        c.srow = p.ws + ((size_t)t.e * p.N + min(t.n0 + row, p.N - 1)) * ng;
-        c.up = ldexpf(1.f, row_exponent(c.srow, ng));
+        const size_t r = (size_t)t.e * p.N + min(t.n0 + row, p.N - 1);
+        c.srow = p.ws + r * ng;
+        c.up = ldexpf(1.f, p.we ? (int)__ldg(p.we + r) : row_exponent(c.srow, ng));
       }
     };
     auto advance = [&](Cur& c, int by) {
@@ -294,7 +296,8 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       const HTile t = tile_of(e);
       const int nn = t.n0 + row;
       const int mb = t.r0 + 64 * cq;
-      const float down = ldexpf(1.f, -row_exponent(p.ws + ((size_t)t.e * p.N + min(nn, p.N - 1)) * ng, ng));
+      const size_t rr = (size_t)t.e * p.N + min(nn, p.N - 1);
+      const float down = ldexpf(1.f, -(p.we ? (int)__ldg(p.we + rr) : row_exponent(p.ws + rr * ng, ng)));
       const float as_lo = mb + lane < t.r_end ? __ldg(p.a_s + mb + lane) : 0.f;
       const float as_hi = mb + 32 + lane < t.r_end ? __ldg(p.a_s + mb + 32 + lane) : 0.f;
       uint32_t packed[32];
@@ -385,6 +388,27 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   }
 }
 
+// Row exponent shifts for qgemm_w4a8_grouped_f16act, one warp per row.
+__global__ void row_shifts_kernel(const uint16_t* __restrict__ ws, int8_t* __restrict__ we, int rows, int G) {
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint16_t* src = ws + row * G;
+  float m = 0.f;
+  for (int g = lane; g < G; g += 32) m = fmaxf(m, fabsf(bf16_bits_to_f32(src[g])));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) {
+    int ex = 0;
+    if (m > 0.f) {
+      int e2;
+      frexpf(m, &e2);
+      ex = min(max(12 - e2, -100), 100);
+    }
+    we[row] = (int8_t)ex;
+  }
+}
+
 // E4M3 codes -> fp16 values (exact), 8 per thread
 __global__ void e4m3_to_f16_kernel(const uint8_t* __restrict__ q, uint16_t* __restrict__ out, long long n8) {
   const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -400,8 +424,8 @@ __global__ void e4m3_to_f16_kernel(const uint8_t* __restrict__ q, uint16_t* __re
 }  // namespace qg
 
 extern "C" qg_status qgemm_w4a8_grouped_f16act(const uint16_t* a_f16, const float* a_s, const int32_t* expert_off,
-                                               const uint8_t* w_q, const uint16_t* w_s, int g, uint16_t* y,
-                                               int R, int E, int N, int K, qg_stream_t stream) {
+                                               const uint8_t* w_q, const uint16_t* w_s, const int8_t* w_e, int g,
+                                               uint16_t* y, int R, int E, int N, int K, qg_stream_t stream) {
   using namespace qg;
   if (!(a_f16 && a_s && expert_off && w_q && w_s && y))
     return set_error(QG_ERR_INVALID_ARG, "qgemm_w4a8_grouped_f16act: NULL pointer");
@@ -420,7 +444,7 @@ extern "C" qg_status qgemm_w4a8_grouped_f16act(const uint16_t* a_f16, const floa
   unsigned int* err = device_error_word();
   if (!err) return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped_f16act: no device error word");
   F16Args a{};
-  a.a_s = a_s; a.off = expert_off; a.ws = w_s; a.y = y;
+  a.a_s = a_s; a.off = expert_off; a.ws = w_s; a.we = w_e; a.y = y;
   a.R = R; a.E = E; a.N = N; a.K = K;
   a.tiles_w = (N + hTW - 1) / hTW;
   a.err = err;
@@ -431,6 +455,17 @@ extern "C" qg_status qgemm_w4a8_grouped_f16act(const uint16_t* a_f16, const floa
   const int grid = (int)std::min<long long>(bound, (long long)sm_count());
   moe_f16_kernel<<<grid, hThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tmap_a, tmap_w, a);
   return check_launch("qgemm_w4a8_grouped_f16act");
+}
+
+extern "C" qg_status qg_w4a8_row_shifts(const uint16_t* w_s, int8_t* w_e, int rows, int G, qg_stream_t stream) {
+  using namespace qg;
+  if (!(w_s && w_e)) return set_error(QG_ERR_INVALID_ARG, "qg_w4a8_row_shifts: NULL pointer");
+  if (!(rows >= 0 && G > 0)) return set_error(QG_ERR_INVALID_ARG, "qg_w4a8_row_shifts: bad sizes");
+  if (rows == 0) return QG_OK;
+  const long long threads = (long long)rows * 32;
+  row_shifts_kernel<<<unsigned((threads + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      w_s, w_e, rows, G);
+  return check_launch("qg_w4a8_row_shifts");
 }
 
 extern "C" qg_status qg_e4m3_to_f16(const uint8_t* q, uint16_t* out, long long n, qg_stream_t stream) {

@@ -33,7 +33,8 @@ SIGNATURES = {
     "qgemm_w4a8_grouped_fp8s": [P, P, P, P, P, P, P, I, I, I, I, P],
     "qg_w4a8_fp8_scales": [P, P, P, I, I, P],
     "qgemm_w4a16_zp": [P, P, P, I, P, P, I, I, I, P],
-    "qgemm_w4a8_grouped_f16act": [P, P, P, P, P, I, P, I, I, I, I, P],
+    "qgemm_w4a8_grouped_f16act": [P, P, P, P, P, P, I, P, I, I, I, I, P],
+    "qg_w4a8_row_shifts": [P, P, I, I, P],
     "qg_e4m3_to_f16": [P, P, I64, P],
     "qg_moe_gather_fp8_f16": [P, P, P, P, P, I, I, I, P],
     "qg_swiglu_quant_fp8_f16": [P, P, P, I, I, P],
@@ -151,9 +152,13 @@ def qg_w4a8_fp8_scales(w_s, w_s8, w_cs8, rows, G, stream=None):
     return _call("qg_w4a8_fp8_scales", _ptr(w_s), _ptr(w_s8), _ptr(w_cs8), rows, G, stream=stream)
 
 
-def qgemm_w4a8_grouped_f16act(a_f16, a_s, expert_off, w_q, w_s, g, y, R, E, N, K, stream=None):
+def qgemm_w4a8_grouped_f16act(a_f16, a_s, expert_off, w_q, w_s, w_e, g, y, R, E, N, K, stream=None):
     return _call("qgemm_w4a8_grouped_f16act", _ptr(a_f16), _ptr(a_s), _ptr(expert_off), _ptr(w_q),
-                 _ptr(w_s), g, _ptr(y), R, E, N, K, stream=stream)
+                 _ptr(w_s), _ptr(w_e), g, _ptr(y), R, E, N, K, stream=stream)
+
+
+def qg_w4a8_row_shifts(w_s, w_e, rows, G, stream=None):
+    return _call("qg_w4a8_row_shifts", _ptr(w_s), _ptr(w_e), rows, G, stream=stream)
 
 
 def qg_moe_gather_fp8_f16(src_q, src_s, route_rows, dst_f16, dst_s, R, T, K, stream=None):

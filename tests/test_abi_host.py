@@ -96,10 +96,11 @@ def test_validation_of_the_widened_entry_points(lib):
     assert _rc(lib, "qgemm_w8a8", FAKE, FAKE, FAKE, FAKE, 1, 12, 128) == 2
     assert _rc(lib, "qgemm_w8a8", FAKE, FAKE, FAKE_MIS, FAKE, 1, 128, 128) == 3
     # W4A8 on fp16 activation copies, and its harness kernels
-    assert _rc(lib, "qgemm_w4a8_grouped_f16act", None, FAKE, FAKE, FAKE, FAKE, 128, FAKE, 1, 1, 16, 128) == 1
-    assert _rc(lib, "qgemm_w4a8_grouped_f16act", FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, 1, 1, 16, 128) == 2
-    assert _rc(lib, "qgemm_w4a8_grouped_f16act", FAKE, FAKE, FAKE, FAKE, FAKE, 128, FAKE, 1, 1, 24, 128) == 2
-    assert _rc(lib, "qgemm_w4a8_grouped_f16act", FAKE_MIS, FAKE, FAKE, FAKE, FAKE, 128, FAKE, 1, 1, 16, 128) == 3
+    assert _rc(lib, "qgemm_w4a8_grouped_f16act", None, FAKE, FAKE, FAKE, FAKE, None, 128, FAKE, 1, 1, 16, 128) == 1
+    assert _rc(lib, "qgemm_w4a8_grouped_f16act", FAKE, FAKE, FAKE, FAKE, FAKE, None, 64, FAKE, 1, 1, 16, 128) == 2
+    assert _rc(lib, "qgemm_w4a8_grouped_f16act", FAKE, FAKE, FAKE, FAKE, FAKE, None, 128, FAKE, 1, 1, 24, 128) == 2
+    assert _rc(lib, "qgemm_w4a8_grouped_f16act", FAKE_MIS, FAKE, FAKE, FAKE, FAKE, None, 128, FAKE, 1, 1, 16, 128) == 3
+    assert _rc(lib, "qg_w4a8_row_shifts", FAKE, None, 4, 8) == 1
     assert _rc(lib, "qg_e4m3_to_f16", FAKE, FAKE, 12) == 2
     assert _rc(lib, "qg_e4m3_to_f16", FAKE, FAKE_MIS, 16) == 3
     assert _rc(lib, "qg_moe_gather_fp8_f16", FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 24) == 2

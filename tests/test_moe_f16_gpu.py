@@ -37,15 +37,21 @@ def expert_weights(E, N, K, seed):
     return np.stack(qs), np.stack(ss)
 
 
-def grouped_f16(qg, a8, a_s, off, wq, ws, N, K):
-    """E4M3 codes -> fp16 copy on the GPU, then the grouped GEMM."""
+def grouped_f16(qg, a8, a_s, off, wq, ws, N, K, shifts=True):
+    """E4M3 codes -> fp16 copy on the GPU, then the grouped GEMM (with the
+    row shifts prepared by qg_w4a8_row_shifts, or computed in the kernel)."""
     R, E = a8.shape[0], wq.shape[0]
     y = empty((max(R, 1), N), torch.int16)
     a16 = empty((max(R, 1), K), torch.int16)
     if R:
         qg.qg_e4m3_to_f16(dev(a8), a16, R * K)
+    dws = dev(ws)
+    we = None
+    if shifts:
+        we = empty((E * N,), torch.int8)
+        qg.qg_w4a8_row_shifts(dws, we, E * N, K // 128)
     qg.qgemm_w4a8_grouped_f16act(a16, dev(a_s) if R else empty((1,), torch.float32),
-                                 dev(off.astype(np.int32)), dev(wq), dev(ws), 128, y, R, E, N, K)
+                                 dev(off.astype(np.int32)), dev(wq), dws, we, 128, y, R, E, N, K)
     qg.qg_check_device_error()
     return OF.bf16_decode(host(y))[:R]
 
@@ -78,6 +84,26 @@ def test_grouped_f16act_several_tiles_per_cta(qg, sizes, N, K):
     y = grouped_f16(qg, a8, a_s[:, 0], off, wq, ws, N, K)
     ref = OF.bf16_decode(OG.to_bf16(OG.w4a8_grouped_f64(a8, a_s[:, 0], off, wq, ws, 128)))
     check_gemm(y, ref, "f16act multi-tile %s" % sizes)
+
+
+def test_row_shifts_given_or_computed_give_the_same_bits(qg):
+    """The load-time row shifts are the ones the kernel would compute: both
+    modes produce identical outputs, including a row whose scales span a wide
+    range and an all-zero expert row."""
+    sizes, N, K = [300, 700], 256, 1024
+    E = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R = int(off[-1])
+    x = inputs.activations_bf16(R, K, seed=93)
+    a8, a_s = OQ.quant_fp8_block(x, K)
+    w = np.stack([inputs.weights_f32(N, K, seed=180 + e) for e in range(E)])
+    w[0, 5] *= np.float32(2.0 ** -12)
+    w[1, 7] = 0.0
+    qs, ss = zip(*[OQ.quant_int4_rtn(w[e], 128) for e in range(E)])
+    wq, ws = np.stack(qs), np.stack(ss)
+    y1 = grouped_f16(qg, a8, a_s[:, 0], off, wq, ws, N, K, shifts=True)
+    y0 = grouped_f16(qg, a8, a_s[:, 0], off, wq, ws, N, K, shifts=False)
+    np.testing.assert_array_equal(OF.bf16_encode(y1), OF.bf16_encode(y0))
 
 
 def test_grouped_f16act_matches_e4m3_entry(qg):
@@ -168,11 +194,11 @@ def test_moe_layer_small_f16(qg):
     qg.qg_moe_gather_fp8_f16(xq, xs, dev(rows), a16, as_, R, T, H)
     gu = empty((R, 2 * I), torch.int16)
     d_off = dev(off)
-    qg.qgemm_w4a8_grouped_f16act(a16, as_, d_off, dev(w1[0]), dev(w1[1]), 128, gu, R, E, 2 * I, H)
+    qg.qgemm_w4a8_grouped_f16act(a16, as_, d_off, dev(w1[0]), dev(w1[1]), None, 128, gu, R, E, 2 * I, H)
     h16, hs = empty((R, I), torch.int16), empty((R,), torch.float32)
     qg.qg_swiglu_quant_fp8_f16(gu, h16, hs, R, I)
     down = empty((R, H), torch.int16)
-    qg.qgemm_w4a8_grouped_f16act(h16, hs, d_off, dev(w2[0]), dev(w2[1]), 128, down, R, E, H, I)
+    qg.qgemm_w4a8_grouped_f16act(h16, hs, d_off, dev(w2[0]), dev(w2[1]), None, 128, down, R, E, H, I)
     row_of = np.full((T, topk), -1, np.int32)
     wt = np.zeros((T, topk), np.float32)
     fill = np.zeros(T, np.int64)
