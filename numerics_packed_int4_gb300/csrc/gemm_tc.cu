@@ -64,7 +64,15 @@ constexpr int kDeq0 = 3;                            // first dequant warp
 constexpr int kSchedWarp = kDeq0 + kDeqWarps;       // scheduler warp
 constexpr int kThreadsTc = (kSchedWarp + 1) * 32;
 constexpr int kXStageBytes = kTileT * kBK * 2;      // 32 KB activations
-constexpr int kWStageBytes = kTileW * kBK / 2;      // 4 KB packed INT4 weights
+
+// Weight formats of the kernel.  Per format: packed bytes per weight row per
+// 64-k slab, activation stages (FP8's 8 KB weight stages leave room for 5).
+enum WFmt { WF_INT4 = 0, WF_INT4Z = 1, WF_FP8 = 2, WF_MXFP4 = 3, WF_NVFP4 = 4 };
+template <int WF> struct PfTraits {
+  static constexpr int WROW = WF == WF_FP8 ? kBK : kBK / 2;
+  static constexpr int STAGES = WF == WF_FP8 ? 5 : 6;
+  static constexpr int WSTAGE = kTileW * WROW;        // packed-weight stage bytes
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACol0 = 256;                    // A slots follow the accumulator
 constexpr uint32_t kACols = kBK / 2;                // 32 columns (2 bf16 per column)
@@ -72,8 +80,10 @@ constexpr uint32_t kDrainCap = 1u << 21;            // waits on work already iss
 
 struct TcArgs {
   const uint8_t* wq;
-  const uint16_t* ws;
+  const void* ws;                      // INT4: [N][K/g] bf16; MXFP4: [N][K/32] E8M0; NVFP4: [N][K/16] E4M3
   const uint8_t* wz;                   // zero points [N][K/g] (asymmetric INT4) or nullptr
+  const float* cs;                     // FP8: per-channel scales [N]
+  const float* gs;                     // NVFP4: global scale (device scalar)
   uint16_t* y;
   int M, N, K, g, lg;
   int tiles_t, tiles_w, group_t;
@@ -106,15 +116,18 @@ QG_DEVICE void tile_origin(const TcArgs& p, int tile, int& m0, int& n0) {
   n0 = (within / gsize) * kTileW;
 }
 
-template <bool ZP>
+template <int WF>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                 const TcArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* xs = smem;                                                     // [kStages][32 KB]
-  uint8_t* wsm = smem + kStages * kXStageBytes;                           // [kASlots][4 KB]
-  TcSmemTail* tl = reinterpret_cast<TcSmemTail*>(wsm + kASlots * kWStageBytes);
+  using Tr = PfTraits<WF>;
+  constexpr bool ZP = WF == WF_INT4Z;
+  constexpr int kSt = Tr::STAGES;
+  uint8_t* xs = smem;                                                     // [kSt][32 KB]
+  uint8_t* wsm = smem + kSt * kXStageBytes;                               // [kASlots][Tr::WSTAGE]
+  TcSmemTail* tl = reinterpret_cast<TcSmemTail*>(wsm + kASlots * Tr::WSTAGE);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -128,7 +141,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   auto tile_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       mbar_init(&tl->x_full[s], 1);
     }
     for (int s = 0; s < kASlots; ++s) {
@@ -160,15 +173,15 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       if (total > 0) tile_origin(p, tile_of(0), m0, n0);
       for (int g = 0; g < total; ++g, ++s) {
         if (s == nslab) { s = 0; tile_origin(p, tile_of(++i), m0, n0); }
-        const int st = g % kStages, gp = g - kStages;   // stage last held slab gp
+        const int st = g % kSt, gp = g - kSt;           // stage last held slab gp
         if (gp >= 0 && !mbar_wait(&tl->a_empty[gp % kASlots], (gp / kASlots) & 1, p.cap, abort, p.err)) break;
         mbar_arrive_expect_tx(&tl->x_full[st], kXStageBytes);
         tma_load_2d(xs + st * kXStageBytes, &tmap_x, &tl->x_full[st], s * kBK, m0);
         issued = g + 1;
       }
       if (*abort) {     // let every copy already issued land before the CTA exits
-        for (int g = max(0, issued - kStages); g < issued; ++g)
-          mbar_wait(&tl->x_full[g % kStages], (g / kStages) & 1, kDrainCap, abort, nullptr);
+        for (int g = max(0, issued - kSt); g < issued; ++g)
+          mbar_wait(&tl->x_full[g % kSt], (g / kSt) & 1, kDrainCap, abort, nullptr);
       }
     }
   } else if (warp == 2) {
@@ -180,8 +193,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         if (s == nslab) { s = 0; tile_origin(p, tile_of(++i), m0, n0); }
         const int st = g % kASlots, r = g / kASlots;
         if (r > 0 && !mbar_wait(&tl->w_empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
-        mbar_arrive_expect_tx(&tl->w_full[st], kWStageBytes);
-        tma_load_2d(wsm + st * kWStageBytes, &tmap_w, &tl->w_full[st], s * (kBK / 2), n0);
+        mbar_arrive_expect_tx(&tl->w_full[st], Tr::WSTAGE);
+        tma_load_2d(wsm + st * Tr::WSTAGE, &tmap_w, &tl->w_full[st], s * Tr::WROW, n0);
         issued = g + 1;
       }
       if (*abort) {
@@ -204,7 +217,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         }
         bool ok = true;
         for (int s = 0; s < nslab; ++s, ++g) {
-          const int st = g % kStages, sa = g % kASlots;
+          const int st = g % kSt, sa = g % kASlots;
           if (!wait_count(&tl->ready, (unsigned)g, ready, p.cap * 4, abort, p.err)) { ok = false; break; }
           tc_fence_after();
           const uint64_t bdesc = sw128_kmajor_desc(smem_addr(xs + st * kXStageBytes));
@@ -227,7 +240,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     if (lane == 0) {
       for (int g = 0; g < total; ++g) {
         if (!mbar_wait(&tl->a_full[g % kASlots], (g / kASlots) & 1, p.cap, abort, p.err)) break;
-        if (!mbar_wait(&tl->x_full[g % kStages], (g / kStages) & 1, p.cap, abort, p.err)) break;
+        if (!mbar_wait(&tl->x_full[g % kSt], (g / kSt) & 1, p.cap, abort, p.err)) break;
         publish_count(&tl->ready, (unsigned)(g + 1));
       }
     }
@@ -249,14 +262,22 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + kACol0;
     // scale cursor: tile index, slab in the tile, this thread's scale row
     // (and, with zero points, its zero-point row)
-    struct Cur { int i, s; const uint16_t* srow; const uint8_t* zrow; };
+    struct Cur { int i, s; const uint8_t* srow; const uint8_t* zrow; };
     auto set_row = [&](Cur& c) {
       if (c.i < ntiles) {
         int m0, n0;
         tile_origin(p, tile_of(c.i), m0, n0);
-        const size_t r = (size_t)min(n0 + row, p.N - 1) * (p.K >> p.lg);
-        c.srow = p.ws + r;
-        if constexpr (ZP) c.zrow = p.wz + r;
+        const size_t n = (size_t)min(n0 + row, p.N - 1);
+        const uint8_t* wsb = static_cast<const uint8_t*>(p.ws);
+        if constexpr (WF == WF_INT4 || WF == WF_INT4Z) {
+          const size_t r = n * (p.K >> p.lg);
+          c.srow = wsb + 2 * r;
+          if constexpr (ZP) c.zrow = p.wz + r;
+        } else if constexpr (WF == WF_MXFP4) {
+          c.srow = wsb + n * (p.K / 32);
+        } else if constexpr (WF == WF_NVFP4) {
+          c.srow = wsb + n * (p.K / 16);
+        }
       }
     };
     auto advance = [&](Cur& c, int by) {
@@ -266,17 +287,25 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     // group scales of the slab's two 32-k halves (bits 0-15) and, with zero
     // points, their zero points (bits 16-19); one load when both halves lie
     // in one group (g >= 64)
+    // FP4 formats: the slab's block-scale codes (MXFP4: two, NVFP4: four) in v0
     auto scales_of = [&](const Cur& c, uint32_t& v0, uint32_t& v1) {
       v0 = v1 = 0u;
       if (c.i >= ntiles) return;
-      const int g0 = (c.s * kBK) >> p.lg, g1 = (c.s * kBK + 32) >> p.lg;
-      v0 = __ldg(c.srow + g0);
-      if constexpr (ZP) v0 |= (uint32_t)__ldg(c.zrow + g0) << 16;
-      if (g1 == g0) {
-        v1 = v0;
-      } else {
-        v1 = __ldg(c.srow + g1);
-        if constexpr (ZP) v1 |= (uint32_t)__ldg(c.zrow + g1) << 16;
+      if constexpr (WF == WF_INT4 || WF == WF_INT4Z) {
+        const uint16_t* sr = reinterpret_cast<const uint16_t*>(c.srow);
+        const int g0 = (c.s * kBK) >> p.lg, g1 = (c.s * kBK + 32) >> p.lg;
+        v0 = __ldg(sr + g0);
+        if constexpr (ZP) v0 |= (uint32_t)__ldg(c.zrow + g0) << 16;
+        if (g1 == g0) {
+          v1 = v0;
+        } else {
+          v1 = __ldg(sr + g1);
+          if constexpr (ZP) v1 |= (uint32_t)__ldg(c.zrow + g1) << 16;
+        }
+      } else if constexpr (WF == WF_MXFP4) {
+        v0 = __ldg(reinterpret_cast<const uint16_t*>(c.srow) + c.s);
+      } else if constexpr (WF == WF_NVFP4) {
+        v0 = __ldg(reinterpret_cast<const uint32_t*>(c.srow) + c.s);
       }
     };
     // epilogue of tile e: TMEM -> registers -> (accumulator free) -> bf16 -> Y
@@ -298,9 +327,16 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       const int nn = n0 + row;
       const int mb = m0 + 64 * cq;
       if (nn < p.N) {
+        // epilogue scale: FP8 per channel, NVFP4 global, none for INT4 / MXFP4
+        float es = 1.f;
+        if constexpr (WF == WF_FP8) es = __ldg(p.cs + nn);
+        if constexpr (WF == WF_NVFP4) es = __ldg(p.gs);
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (mb + c < p.M) p.y[(size_t)(mb + c) * p.N + nn] = f32_to_bf16_bits(__uint_as_float(v[c]));
+        for (int c = 0; c < 64; ++c) {
+          float val = __uint_as_float(v[c]);
+          if constexpr (WF == WF_FP8 || WF == WF_NVFP4) val *= es;
+          if (mb + c < p.M) p.y[(size_t)(mb + c) * p.N + nn] = f32_to_bf16_bits(val);
+        }
       }
       return true;
     };
@@ -322,24 +358,51 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       const int sa = g % kASlots, ra = g / kASlots;
       const uint32_t s2a = bf16x2_splat(sc_cur0), s2b = bf16x2_splat(sc_cur1);
       const uint32_t z2a = bf16x2_zero128(sc_cur0 >> 16), z2b = bf16x2_zero128(sc_cur1 >> 16);
+      const uint32_t fb = sc_cur0;                  // FP4 formats: the slab's block-scale codes
       sc_cur0 = sc_nxt0;
       sc_cur1 = sc_nxt1;
       advance(pf, kDeqSets);                        // pf now at this set's slab after the next
       scales_of(pf, sc_nxt0, sc_nxt1);
       if (!mbar_wait_warp(&tl->w_full[sa], ra & 1, p.cap, abort, p.err)) { ok = false; break; }
-      const uint4 wa = *reinterpret_cast<const uint4*>(wsm + sa * kWStageBytes + row * (kBK / 2));
-      const uint4 wb = *reinterpret_cast<const uint4*>(wsm + sa * kWStageBytes + row * (kBK / 2) + 16);
-      const uint32_t v[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
       uint32_t out[32];
+      if constexpr (WF == WF_FP8) {
+        // 64 E4M3 codes of this row; 64-byte swizzled stage: chunk c at c ^ ((row >> 1) & 3)
+        const uint8_t* wrow = wsm + sa * Tr::WSTAGE + row * Tr::WROW;
+        const int wsw = (row >> 1) & 3;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t nat[4];
-        if constexpr (ZP)
-          int4zp_x8_nat(v[j], j < 4 ? s2a : s2b, j < 4 ? z2a : z2b, nat);
-        else
-          int4x8_nat(v[j], j < 4 ? s2a : s2b, nat);
-        out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
-        out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
+        for (int c = 0; c < 4; ++c) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(wrow + 16 * (c ^ wsw));
+          const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {             // bytes k0..k3 -> (k0, k1), (k2, k3), exact
+            uint32_t p02, p13;
+            e4m3x4_kperm(ww[i], p02, p13);
+            out[8 * c + 2 * i] = prmt(p02, p13, 0x5410u);
+            out[8 * c + 2 * i + 1] = prmt(p02, p13, 0x7632u);
+          }
+        }
+      } else {
+        const uint4 wa = *reinterpret_cast<const uint4*>(wsm + sa * Tr::WSTAGE + row * Tr::WROW);
+        const uint4 wb = *reinterpret_cast<const uint4*>(wsm + sa * Tr::WSTAGE + row * Tr::WROW + 16);
+        const uint32_t v[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t nat[4];
+          if constexpr (WF == WF_INT4Z) {
+            int4zp_x8_nat(v[j], j < 4 ? s2a : s2b, j < 4 ? z2a : z2b, nat);
+          } else if constexpr (WF == WF_INT4) {
+            int4x8_nat(v[j], j < 4 ? s2a : s2b, nat);
+          } else {
+            // E2M1 words of 8 codes; block scale: MXFP4 per 32 k (words j/4), NVFP4 per 16 (j/2)
+            const uint32_t sc = WF == WF_MXFP4 ? e8m0_to_bf16x2((fb >> (8 * (j >> 2))) & 0xFFu)
+                                               : e4m3_to_bf16x2((fb >> (8 * (j >> 1))) & 0xFFu);
+            uint32_t pq[4];
+            e2m1x8_kperm(v[j], sc, pq);
+            kperm4_to_natural(pq, nat);
+          }
+          out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
+          out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
+        }
       }
       mbar_arrive_warp(&tl->w_empty[sa]);           // packed slab decoded: its stage may be refilled
       if (ra > 0) {
@@ -432,20 +495,31 @@ bool make_bf16_tmap(CUtensorMap* m, const void* base, int rows, int cols, int bo
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g, const uint16_t* x,
-                        uint16_t* y, int M, int N, int K, cudaStream_t st, bool* handled, const char* name) {
+// The prefill dispatcher.  wf is a WFmt; w_s is the format's scale array
+// (INT4 bf16 per group, MXFP4 E8M0 per 32, NVFP4 E4M3 per 16, unused for
+// FP8), w_z the zero points (INT4Z), cs the FP8 channel scales, gs the NVFP4
+// global scale.  Declines (handled = false) shapes for the decode kernel.
+qg_status prefill_tc(int wf, const uint8_t* w_q, const void* w_s, const uint8_t* w_z, const float* cs,
+                     const float* gs, int g, const uint16_t* x, uint16_t* y, int M, int N, int K,
+                     cudaStream_t st, bool* handled, const char* name) {
   *handled = false;
-  if (M <= 16 || K % kBK != 0 || g < 32 || (g & (g - 1)) != 0 || K % g != 0) return QG_OK;   // decode path
+  if (M <= 16 || K % kBK != 0) return QG_OK;
+  if ((wf == WF_INT4 || wf == WF_INT4Z) && (g < 32 || (g & (g - 1)) != 0 || K % g != 0)) return QG_OK;
+  // the FP4 block scales are read two (MXFP4) or four (NVFP4) codes at a time
+  if (wf == WF_MXFP4 && (reinterpret_cast<uintptr_t>(w_s) & 1)) return QG_OK;
+  if (wf == WF_NVFP4 && (reinterpret_cast<uintptr_t>(w_s) & 3)) return QG_OK;
   *handled = true;
+  const int wrow = wf == WF_FP8 ? kBK : kBK / 2;        // packed bytes per row per slab
   CUtensorMap tmap, tmap_w;
   if (!make_bf16_tmap(&tmap, x, M, K, kTileT, kBK))
     return set_error(QG_ERR_CUDA, "%s: cannot encode the activation tensor map", name);
-  if (!make_u8_tmap(&tmap_w, w_q, N, K / 2, kTileW, kBK / 2))
-    return set_error(QG_ERR_CUDA, "%s: cannot encode the weight tensor map", name);
+  const bool wok = wf == WF_FP8 ? make_u8_tmap_swizzled(&tmap_w, w_q, N, K, kTileW, wrow)
+                                : make_u8_tmap(&tmap_w, w_q, N, K / 2, kTileW, wrow);
+  if (!wok) return set_error(QG_ERR_CUDA, "%s: cannot encode the weight tensor map", name);
   unsigned int* err = device_error_word();
   if (!err) return set_error(QG_ERR_CUDA, "%s: no device error word", name);
   TcArgs a{};
-  a.wq = w_q; a.ws = w_s; a.wz = w_z; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
+  a.wq = w_q; a.ws = w_s; a.wz = w_z; a.cs = cs; a.gs = gs; a.y = y; a.M = M; a.N = N; a.K = K; a.g = g;
   a.lg = 0;
   while ((1 << a.lg) < g) ++a.lg;
   a.tiles_t = (M + kTileT - 1) / kTileT;
@@ -453,8 +527,17 @@ qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* 
   a.group_t = 8;
   a.err = err;
   a.cap = wait_limit();
-  const int smem = kStages * kXStageBytes + kASlots * kWStageBytes + (int)sizeof(TcSmemTail) + 1024;
-  auto kern = w_z ? w4a16_tc_kernel<true> : w4a16_tc_kernel<false>;
+  const int stages = wf == WF_FP8 ? PfTraits<WF_FP8>::STAGES : PfTraits<WF_INT4>::STAGES;
+  const int smem = stages * kXStageBytes + kASlots * kTileW * wrow + (int)sizeof(TcSmemTail) + 1024;
+  void (*kern)(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap, const TcArgs) = nullptr;
+  switch (wf) {
+    case WF_INT4: kern = w4a16_tc_kernel<WF_INT4>; break;
+    case WF_INT4Z: kern = w4a16_tc_kernel<WF_INT4Z>; break;
+    case WF_FP8: kern = w4a16_tc_kernel<WF_FP8>; break;
+    case WF_MXFP4: kern = w4a16_tc_kernel<WF_MXFP4>; break;
+    case WF_NVFP4: kern = w4a16_tc_kernel<WF_NVFP4>; break;
+    default: return set_error(QG_ERR_INVALID_ARG, "%s: unknown prefill format %d", name, wf);
+  }
   if (!ensure_smem(kern, smem)) return set_error(QG_ERR_CUDA, "%s: smem attribute", name);
   const long long tiles = (long long)a.tiles_t * a.tiles_w;
   const int grid = (int)std::min<long long>(tiles, (long long)sm_count());   // persistent: one CTA per SM

@@ -565,10 +565,11 @@ qg_status gemv_w4a16_any_m(const uint8_t* w_q, const uint16_t* w_s, const uint8_
 
 using qg::aligned16;
 
-// prefill dispatcher lives in gemm_tc.cu
+// prefill dispatcher lives in gemm_tc.cu (wf: 0 INT4, 1 INT4 with zero points, 2 FP8, 3 MXFP4, 4 NVFP4)
 namespace qg {
-qg_status prefill_w4a16(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g, const uint16_t* x,
-                        uint16_t* y, int M, int N, int K, cudaStream_t st, bool* handled, const char* name);
+qg_status prefill_tc(int wf, const uint8_t* w_q, const void* w_s, const uint8_t* w_z, const float* cs,
+                     const float* gs, int g, const uint16_t* x, uint16_t* y, int M, int N, int K,
+                     cudaStream_t st, bool* handled, const char* name);
 }
 
 extern "C" {
@@ -584,7 +585,7 @@ qg_status qgemm_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (M > 16) {
     bool handled = false;
-    r = qg::prefill_w4a16(w_q, w_s, nullptr, g, x, y, M, N, K, st, &handled, "qgemm_w4a16");
+    r = qg::prefill_tc(0, w_q, w_s, nullptr, nullptr, nullptr, g, x, y, M, N, K, st, &handled, "qgemm_w4a16");
     if (handled) return r;
   }
   return qg::gemv_w4a16_any_m(w_q, w_s, nullptr, g, x, y, M, N, K, st, "qgemm_w4a16");
@@ -601,7 +602,7 @@ qg_status qgemm_w4a16_zp(const uint8_t* w_q, const uint16_t* w_s, const uint8_t*
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (M > 16) {
     bool handled = false;
-    r = qg::prefill_w4a16(w_q, w_s, w_z, g, x, y, M, N, K, st, &handled, "qgemm_w4a16_zp");
+    r = qg::prefill_tc(1, w_q, w_s, w_z, nullptr, nullptr, g, x, y, M, N, K, st, &handled, "qgemm_w4a16_zp");
     if (handled) return r;
   }
   return qg::gemv_w4a16_any_m(w_q, w_s, w_z, g, x, y, M, N, K, st, "qgemm_w4a16_zp");
@@ -613,9 +614,15 @@ qg_status qgemm_w8a16(const uint8_t* w_e4m3, const float* w_cs, const uint16_t* 
   if (r != QG_OK) return r;
   QG_REQUIRE(w_cs, QG_ERR_INVALID_ARG, "qgemm_w8a16: NULL channel scales");
   if (M == 0) return QG_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (M > 16) {
+    bool handled = false;
+    r = qg::prefill_tc(2, w_e4m3, nullptr, nullptr, w_cs, nullptr, K, x, y, M, N, K, st, &handled, "qgemm_w8a16");
+    if (handled) return r;
+  }
   qg::GemvArgs a{};
   a.w = w_e4m3; a.scales = w_cs; a.x = x; a.y = y; a.M = M; a.N = N; a.K = K; a.g = K;
-  return qg::run_weight_only<qg::F_FP8>(a, reinterpret_cast<cudaStream_t>(stream), "qgemm_w8a16");
+  return qg::run_weight_only<qg::F_FP8>(a, st, "qgemm_w8a16");
 }
 
 qg_status qgemm_w8a8(const uint8_t* w_e4m3, const float* w_cs, const uint16_t* x, uint16_t* y,
@@ -642,6 +649,11 @@ qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt
     QG_REQUIRE(g == 32, QG_ERR_UNSUPPORTED_SHAPE, "qgemm_fp4a16: MXFP4 needs g == 32");
     QG_REQUIRE(global_scale == nullptr, QG_ERR_INVALID_ARG, "qgemm_fp4a16: MXFP4 takes no global scale");
     if (M == 0) return QG_OK;
+    if (M > 16) {
+      bool handled = false;
+      r = qg::prefill_tc(3, w_e2m1, w_bs, nullptr, nullptr, nullptr, g, x, y, M, N, K, st, &handled, "qgemm_fp4a16");
+      if (handled) return r;
+    }
     return qg::run_weight_only<qg::F_MXFP4>(a, st, "qgemm_fp4a16");
   }
   if (scale_fmt == QG_SCALE_E4M3) {
@@ -651,6 +663,12 @@ qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt
                "qgemm_fp4a16: misaligned global scale");
     a.gscale = global_scale;
     if (M == 0) return QG_OK;
+    if (M > 16) {
+      bool handled = false;
+      r = qg::prefill_tc(4, w_e2m1, w_bs, nullptr, nullptr, global_scale, g, x, y, M, N, K, st, &handled,
+                         "qgemm_fp4a16");
+      if (handled) return r;
+    }
     return qg::run_weight_only<qg::F_NVFP4>(a, st, "qgemm_fp4a16");
   }
   return qg::set_error(QG_ERR_INVALID_ARG, "qgemm_fp4a16: unknown scale format %d", scale_fmt);

@@ -1,4 +1,5 @@
-"""GPU parity of the tcgen05 prefill W4A16 GEMM (M > 16) against the fp64 oracle."""
+"""GPU parity of the tcgen05 prefill GEMM (M > 16) against the fp64 oracle: INT4
+with group scales, and the FP8 per-channel, MXFP4 and NVFP4 weight formats."""
 
 import numpy as np
 import pytest
@@ -76,3 +77,44 @@ def test_prefill_deterministic(qg):
     x = inputs.activations_bf16(M, K, seed=2)
     q, s = OQ.quant_int4_rtn(w, 128)
     assert np.array_equal(run(qg, x, q, s, M, N, K), run(qg, x, q, s, M, N, K))
+
+
+# ---- the other weight formats on the same tcgen05 kernel (M > 16) ----
+from tests.test_gemv_gpu import quantized, reference as wo_reference, run_gpu  # noqa: E402
+
+OTHER_FORMATS = ["fp8", "mxfp4", "nvfp4"]
+
+
+@pytest.mark.parametrize("fmt", OTHER_FORMATS)
+@pytest.mark.parametrize("M,N,K", [(17, 128, 128), (300, 264, 512), (1024, 1000, 640), (2000, 2600, 384),
+                                   (4100, 1200, 256)])
+def test_prefill_formats(qg, fmt, M, N, K):
+    """FP8 per-channel, MXFP4 and NVFP4 weights: single-tile, ragged, and
+    more tiles than SMs (several tiles per persistent CTA)."""
+    Wd = quantized(fmt, N, K, seed=M + N)
+    x = inputs.activations_bf16(M, K, seed=K + 13, outlier_frac=0.01, outlier_scale=50.0)
+    y = run_gpu(qg, fmt, Wd, x, M, N, K)
+    ref, _ = wo_reference(Wd, x)
+    check_gemm(y, ref, "%s prefill M=%d N=%d K=%d" % (fmt, M, N, K))
+
+
+@pytest.mark.parametrize("fmt", OTHER_FORMATS)
+def test_prefill_formats_config_sampled(qg, fmt):
+    """M = 8192, N = 14336, K = 4096: parity on a seeded sample of 128 rows,
+    every output finite."""
+    M, N, K = 8192, 14336, 4096
+    Wd = quantized(fmt, N, K, seed=500)
+    x = inputs.activations_bf16(M, K, seed=501, outlier_frac=0.01, outlier_scale=50.0)
+    y = run_gpu(qg, fmt, Wd, x, M, N, K)
+    assert np.all(np.isfinite(y))
+    rows = np.sort(np.random.Generator(np.random.PCG64(7)).choice(M, 128, replace=False))
+    ref, _ = wo_reference(Wd, x, rows)
+    check_gemm(y[rows], ref, "%s prefill config sample" % fmt)
+
+
+@pytest.mark.parametrize("fmt", OTHER_FORMATS)
+def test_prefill_formats_deterministic(qg, fmt):
+    M, N, K = 600, 512, 1024
+    Wd = quantized(fmt, N, K, seed=9)
+    x = inputs.activations_bf16(M, K, seed=10)
+    assert np.array_equal(run_gpu(qg, fmt, Wd, x, M, N, K), run_gpu(qg, fmt, Wd, x, M, N, K))
