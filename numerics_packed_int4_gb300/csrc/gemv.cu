@@ -69,7 +69,10 @@ struct GemvArgs {
   int rg;                  // 16-row groups per CTA (warps split K by kWarps / rg)
 };
 
-QG_DEVICE int swz(int c) { return c ^ ((c >> 3) & 1); }
+// Staged activation chunk c (16 bytes) sits at c + c / 8: one pad chunk per
+// 8 keeps the lanes' 16-byte reads bank-conflict free, and a lane's chunks
+// for one segment are consecutive, so they are addressed from one base.
+QG_DEVICE int xpad(int c) { return c + (c >> 3); }
 
 QG_DEVICE void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                         uint32_t b0, uint32_t b1) {
@@ -100,10 +103,17 @@ QG_DEVICE const uint8_t* zero_row(const GemvArgs& p, int n) {
   return nullptr;
 }
 
-template <int FMT>
+// G1: INT4 with g == 128, one group per segment: the group index is the
+// segment index.
+template <int FMT, bool G1>
 QG_DEVICE Scale load_scale(const GemvArgs& p, const uint8_t* srow, const uint8_t* zrow, int seg, int t) {
   Scale s{0u, 0u};
-  if constexpr (FMT == F_INT4) {
+  if constexpr (G1 && FMT == F_INT4) {
+    s.a = bf16x2_splat(__ldg(reinterpret_cast<const uint16_t*>(srow) + seg));
+  } else if constexpr (G1 && FMT == F_INT4Z) {
+    s.a = bf16x2_splat(__ldg(reinterpret_cast<const uint16_t*>(srow) + seg));
+    s.b = bf16x2_zero128(__ldg(zrow + seg));
+  } else if constexpr (FMT == F_INT4) {
     const int grp = (seg * 128 + 32 * t) >> p.lg;
     s.a = bf16x2_splat(__ldg(reinterpret_cast<const uint16_t*>(srow) + grp));
   } else if constexpr (FMT == F_INT4Z) {
@@ -177,7 +187,7 @@ QG_DEVICE float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
   return v;
 }
 
-template <int FMT, int MT>
+template <int FMT, int MT, bool G1>
 __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   using Tr = FmtTraits<FMT>;
   extern __shared__ __align__(16) uint4 smem[];
@@ -217,8 +227,12 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   const uint8_t* w1 = p.w + (size_t)n1 * row_bytes + (size_t)(seg_lo + s_lo) * 64 + 16 * t;
 
   const int col0 = min(g, M - 1), col1 = min(8 + g, M - 1);
-  const uint4* xr0 = xs + col0 * p.ncp;
-  const uint4* xr1 = xs + col1 * p.ncp;
+  // this lane's activation chunks: segment s, chunk j at xq0[s * kPadSeg + j]
+  // (KSEG / 8 is a multiple of 8, so the pad count of a segment is KSEG / 64)
+  constexpr int kPadSeg = Tr::KSEG / 8 + Tr::KSEG / 64;
+  const int lane_chunk = t * Tr::CPL;
+  const uint4* xq0 = xs + col0 * p.ncp + s_lo * kPadSeg + xpad(lane_chunk);
+  const uint4* xq1 = xs + col1 * p.ncp + s_lo * kPadSeg + xpad(lane_chunk);
 
   // Start the next kernel in the stream now.  This grid's weight stream is
   // issued before waiting for the previous kernel (qgemm.h: weights are never
@@ -242,8 +256,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
 #pragma unroll
   for (int u = 0; u < kPFS; ++u) {
     if (u < nseg) {
-      sa[u] = load_scale<FMT>(p, sr0, zr0, seg_lo + s_lo + u, t);
-      sb[u] = load_scale<FMT>(p, sr1, zr1, seg_lo + s_lo + u, t);
+      sa[u] = load_scale<FMT, G1>(p, sr0, zr0, seg_lo + s_lo + u, t);
+      sb[u] = load_scale<FMT, G1>(p, sr1, zr1, seg_lo + s_lo + u, t);
     }
   }
 
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   for (int i = threadIdx.x; i < M * nchunk; i += kWarps * 32) {
     const int m = i / nchunk, c = i - m * nchunk;
     const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * p.K + k0 + 8 * c));
-    xs[m * p.ncp + swz(c)] = perm_x<FMT>(u);
+    xs[m * p.ncp + xpad(c)] = perm_x<FMT>(u);
     if constexpr (FMT == F_FP8A8) {
       const float a = fmaxf(fmaxf(fmaxf(fabsf(bf16_lo_to_f32(u.x)), fabsf(bf16_hi_to_f32(u.x))),
                                   fmaxf(fabsf(bf16_lo_to_f32(u.y)), fabsf(bf16_hi_to_f32(u.y)))),
@@ -294,7 +308,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
     for (int i = threadIdx.x; i < M * nchunk; i += kWarps * 32) {
       const int m = i / nchunk, c = i - m * nchunk;
       const float sc = xsc[m * nblk + (k0 + 8 * c) / kActBlock - blk0];
-      uint4& xv = xs[m * p.ncp + swz(c)];
+      uint4& xv = xs[m * p.ncp + xpad(c)];
       uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {          // elementwise, so the staged (permuted) order is fine
@@ -333,23 +347,24 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
         const int us = u % kPFS;
         const Scale s_a = sa[us], s_b = sb[us];
         if (s + kPFS < nseg) {
-          sa[us] = load_scale<FMT>(p, sr0, zr0, seg_lo + s_lo + s + kPFS, t);
-          sb[us] = load_scale<FMT>(p, sr1, zr1, seg_lo + s_lo + s + kPFS, t);
+          sa[us] = load_scale<FMT, G1>(p, sr0, zr0, seg_lo + s_lo + s + kPFS, t);
+          sb[us] = load_scale<FMT, G1>(p, sr1, zr1, seg_lo + s_lo + s + kPFS, t);
         }
-        const int cbase = (s_lo + s) * (Tr::KSEG / 8) + t * Tr::CPL;
+        const uint4* xs0 = xq0 + s * kPadSeg;
+        const uint4* xs1 = xq1 + s * kPadSeg;
 #pragma unroll
         for (int j = 0; j < Tr::CPL; ++j) {
           uint32_t ag[4], ah[4];
           decode_chunk<FMT>(wa, s_a, j, ag);
           decode_chunk<FMT>(wb, s_b, j, ah);
-          const int c = swz(cbase + j);
+
           {
-            const uint4 xf = xr0[c];
+            const uint4 xf = xs0[j];
             mma_bf16(acc_mma[0], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
             mma_bf16(acc_mma[0], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
           }
           if constexpr (MT == 2) {
-            const uint4 xf = xr1[c];
+            const uint4 xf = xs1[j];
             mma_bf16(acc_mma[1], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
             mma_bf16(acc_mma[1], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
           }
@@ -438,7 +453,7 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ w, const void* __rest
   const uint4 wv = *reinterpret_cast<const uint4*>(w + (size_t)n * row_bytes + seg * 64 + 16 * t);
   GemvArgs p{};
   p.scales = scales; p.zeros = zeros; p.K = K; p.g = g; p.lg = 31 - __clz(g);
-  const Scale s = load_scale<FMT>(p, scale_row<FMT>(p, n), zero_row<FMT>(p, n), seg, t);
+  const Scale s = load_scale<FMT, false>(p, scale_row<FMT>(p, n), zero_row<FMT>(p, n), seg, t);
   uint16_t* o = out + (size_t)n * K + (size_t)seg * Tr::KSEG + t * Tr::CPL * 8;
 #pragma unroll
   for (int j = 0; j < Tr::CPL; ++j) {
@@ -463,10 +478,12 @@ qg_status launch_gemv_t(const GemvArgs& a0, cudaStream_t st, const char* name) {
   GemvArgs a = a0;
   a.nseg = a.K / Tr::KSEG;
   const int row_groups = (a.N + 15) / 16;
-  auto kern = gemv_kernel<FMT, MT>;
+  constexpr bool kInt4 = FMT == F_INT4 || FMT == F_INT4Z;
+  auto kern = (kInt4 && a.g == 128) ? gemv_kernel<FMT, MT, kInt4> : gemv_kernel<FMT, MT, false>;
   auto smem_for = [&](int ks, int rg) {
     const int nseg_max = (a.nseg + ks - 1) / ks;
-    int ncp = nseg_max * Tr::KSEG / 8;
+    const int nch = nseg_max * Tr::KSEG / 8;
+    int ncp = nch + nch / 8;                          // padded row (one pad chunk per 8)
     const int want = fp8_weights(FMT) ? 1 : 2;        // bank-conflict-free pitch (mod 8)
     while ((ncp & 7) != want) ++ncp;
     a.ncp = ncp;
@@ -672,6 +689,21 @@ qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt
     return qg::run_weight_only<qg::F_NVFP4>(a, st, "qgemm_fp4a16");
   }
   return qg::set_error(QG_ERR_INVALID_ARG, "qgemm_fp4a16: unknown scale format %d", scale_fmt);
+}
+
+// W4A4 numerics on bf16 tensor cores: the MXFP4 activations are expanded to
+// bf16 (exact) into a_work, then the MXFP4-weight GEMM runs on them.
+qg_status qgemm_w4a4_mxfp4(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint8_t* a_e2m1,
+                           const uint8_t* a_e8m0, uint16_t* a_work, uint16_t* y, int M, int N, int K,
+                           qg_stream_t stream) {
+  QG_REQUIRE(a_e2m1 && a_e8m0 && a_work && w_e8m0, QG_ERR_INVALID_ARG, "qgemm_w4a4_mxfp4: NULL pointer");
+  qg_status r = qg::check_common(w_e2m1, a_work, y, M, N, K, "qgemm_w4a4_mxfp4");
+  if (r != QG_OK) return r;
+  QG_REQUIRE(aligned16(a_e2m1), QG_ERR_MISALIGNED, "qgemm_w4a4_mxfp4: misaligned activation codes");
+  if (M == 0) return QG_OK;
+  r = qg_dequant_weights(QG_FMT_MXFP4, a_e2m1, a_e8m0, 32, a_work, M, K, stream);
+  if (r != QG_OK) return r;
+  return qgemm_fp4a16(w_e2m1, w_e8m0, QG_SCALE_E8M0, 32, nullptr, a_work, y, M, N, K, stream);
 }
 
 qg_status qg_dequant_weights(int fmt, const uint8_t* w, const void* scales, int g, uint16_t* w_out,
