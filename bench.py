@@ -273,11 +273,14 @@ class Workload:
         t = self.t
         from numerics_packed_int4_gb300 import inputs
         self.W = {}
-        if any(r.startswith("decode") or r in ("prefill", "prefill_zp") for r in self.rows):
+        prefill_rows = [r for r in self.rows if r.startswith("prefill")]
+        if any(r.startswith("decode") for r in self.rows) or prefill_rows:
             for i, (N, K) in enumerate(SHAPES):
                 w = self._randn((N, K), seed=1000 + i, std=0.02)
                 for fmt in FORMATS:
-                    if fmt != "int4" and not any(r.startswith("decode") for r in self.rows):
+                    if (fmt != "int4" and not any(r.startswith("decode") for r in self.rows)
+                            and "prefill_" + fmt not in self.rows
+                            and not (fmt == "mxfp4" and "prefill_w4a4" in self.rows)):
                         continue
                     self.W[(fmt, N, K)] = self._weights(fmt, w)
                 if "decode_zp" in self.rows or "prefill_zp" in self.rows:
@@ -289,7 +292,7 @@ class Workload:
                 self.X[(M, K)] = self._bf16(self._randn((M, K), seed=2000 + M * 7 + K))
             for N in sorted({n for n, _ in SHAPES}):
                 self.Y[(M, N)] = t.empty((M, N), dtype=t.int16, device=self.dev)
-        if "prefill" in self.rows or "prefill_zp" in self.rows:
+        if prefill_rows:
             self.XP = {}
             for K in sorted({k for _, k in SHAPES}):
                 x = self._randn((8192, K), seed=3000 + K)
@@ -298,6 +301,11 @@ class Workload:
                 x[:, ch] *= 50.0                               # 1 % outlier channels x50
                 self.XP[K] = self._bf16(x)
             self.YP = {N: t.empty((8192, N), dtype=t.int16, device=self.dev) for N, _ in SHAPES}
+        if "prefill_w4a4" in self.rows:                     # MXFP4 activation codes, scales, bf16 expansion
+            ks = sorted({k for _, k in SHAPES})
+            self.A4 = {K: t.empty((8192, K // 2), dtype=t.uint8, device=self.dev) for K in ks}
+            self.A4s = {K: t.empty((8192, K // 32), dtype=t.uint8, device=self.dev) for K in ks}
+            self.A4w = {K: t.empty((8192, K), dtype=t.int16, device=self.dev) for K in ks}
         if "quant" in self.rows:
             xq = inputs.quantizer_activations_bf16(4096, 7168, seed=0)
             self.XQ = t.from_numpy(xq.view(np.int16)).to(self.dev)
@@ -373,6 +381,15 @@ class Workload:
             for N, K in SHAPES:
                 W = self.W[("int4", N, K)]
                 qg.qgemm_w4a16(W["q"], W["s"], 128, self.XP[K], self.YP[N], 8192, N, K)
+        elif name == "prefill_w4a4":
+            for N, K in SHAPES:                             # MXFP4 activations x MXFP4 weights
+                qg.quant_act_mxfp4(self.XP[K], self.A4[K], self.A4s[K], 32, 8192, K)
+                qg.qgemm_w4a4_mxfp4(self.W[("mxfp4", N, K)]["q"], self.W[("mxfp4", N, K)]["s"], self.A4[K],
+                                    self.A4s[K], self.A4w[K], self.YP[N], 8192, N, K)
+        elif name.startswith("prefill_") and name[len("prefill_"):] in FORMATS:
+            fmt = name[len("prefill_"):]                    # FP8 / MXFP4 / NVFP4 weights, same kernel
+            for N, K in SHAPES:
+                self.gemv(fmt, self.W[(fmt, N, K)], self.XP[K], self.YP[N], 8192, N, K)
         elif name == "decode_w8a8":
             for N, K in SHAPES:
                 W = self.W[("fp8", N, K)]
@@ -419,8 +436,9 @@ class Workload:
                 self.launches[name] = None
         if "prefill" in self.rows:
             self.flops["prefill"] = sum(2.0 * 8192 * N * K for N, K in SHAPES)
-        if "prefill_zp" in self.rows:
-            self.flops["prefill_zp"] = sum(2.0 * 8192 * N * K for N, K in SHAPES)
+        for r in ("prefill_zp", "prefill_fp8", "prefill_mxfp4", "prefill_nvfp4", "prefill_w4a4"):
+            if r in self.rows:
+                self.flops[r] = sum(2.0 * 8192 * N * K for N, K in SHAPES)
         if "decode_w8a8" in self.rows:
             self.bytes["decode_w8a8"] = sum(N * K + 4 * N + 2 * K + 2 * N for N, K in SHAPES)
             self.launches["decode_w8a8"] = None
@@ -505,7 +523,8 @@ def cpu_cores():
 def bench_config(rows, world):
     """The workload of the bench line (shared by both arms)."""
     return {"workload": "decode sweep M in {1,4,16} x {4096^2, 14336x4096, 4096x14336} x "
-                        "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill W4A16 M=8192 + "
+                        "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill M=8192 (W4A16; FP8, MXFP4, NVFP4 weights; "
+                        "W4A4 MXFP4 with online activation quant) + "
                         "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2 (bf16 group scales; "
                         "FP8 group scales) + asymmetric INT4 g64 M=1 and M=8192 + W8A8 GEMV M=1",
             "rows": rows, "l2": "inputs larger than L2: every weight matrix read once per step; "
@@ -738,7 +757,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe,moe_fp8s,"
-                                      "decode_zp,prefill_zp,decode_w8a8")
+                                      "decode_zp,prefill_zp,decode_w8a8,prefill_fp8,prefill_mxfp4,prefill_nvfp4,prefill_w4a4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)

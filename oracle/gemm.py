@@ -129,6 +129,20 @@ def qgemm_nvfp4a16(x_bits, packed, sb, gs):
     return gemm_bf16_f64(x_bits, dequant_nvfp4(packed, sb), np.full(n, float(gs)))
 
 
+def w4a4_mxfp4_f64(x_bits, packed, se, g_act=32):
+    """W4A4 with MXFP4 on both sides (the MXFP4 W4A4 MoE GEMM of vLLM PR
+    #43557): the activations are quantized by the a6 rule (exponent-first
+    0.75-threshold E8M0 scale, E2M1 RNE with saturation) per block of g_act,
+    both operands decoded to their exact values, the product summed in
+    float64.  Returns (y64, activation codes, activation scale codes)."""
+    aq, ase = Q.quant_mxfp4(np.asarray(x_bits, np.uint16), g_act)
+    a = F.e2m1_decode(Q.unpack_nibbles(aq))
+    a = (a.reshape(a.shape[:-1] + (-1, g_act)) * F.e8m0_decode(ase)[..., None]).reshape(a.shape)
+    w = F.e2m1_decode(Q.unpack_nibbles(packed))
+    w = (w.reshape(w.shape[:-1] + (-1, 32)) * F.e8m0_decode(se)[..., None]).reshape(w.shape)
+    return a.astype(np.float64) @ w.astype(np.float64).T, aq, ase
+
+
 def to_bf16(y64):
     """The path's narrowing store: one round-to-nearest-even to bf16."""
     return F.bf16_encode(y64)

@@ -135,3 +135,13 @@ def test_quantizer_workload_injects_edges():
     v = (x.astype(np.uint32) << 16).view(np.float32)
     anchors = np.abs(v[0, ::128][::3])
     assert np.all(np.log2(anchors / 448.0) == np.round(np.log2(anchors / 448.0)))
+
+
+def test_w4a4_argument_validation(lib):
+    # (w_e2m1, w_e8m0, a_e2m1, a_e8m0, a_work, y, M, N, K, stream)
+    assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, None, FAKE, FAKE, FAKE, 1, 128, 128) == 1
+    assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, None, FAKE, FAKE, FAKE, FAKE, 1, 128, 128) == 1
+    assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 12, 128) == 2     # N % 8
+    assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 96) == 2     # K % 128
+    assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE_MIS, FAKE, FAKE, FAKE, 1, 128, 128) == 3
+    assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 128, 128) == 0    # M = 0

@@ -628,3 +628,82 @@ def test_fp8_group_scale_recipe_stays_close_to_exact_w4a8():
     recipe = G.w4a8_fp8s_grouped_f64(a, a_s[:, 0], off, w8[None], cs8[None])
     rel = np.linalg.norm(recipe - exact) / np.linalg.norm(exact)
     assert 1e-3 < rel < 5e-2
+
+
+# ----------------------------------------------------------------------------
+# W4A4 MXFP4 x MXFP4 (vLLM PR #43557's W4A4 GEMM, activations by the a6 rule)
+# ----------------------------------------------------------------------------
+
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]     # the E2M1 magnitudes the pages list
+
+
+def _e2m1_value(code):
+    v = Fraction(E2M1_TABLE[code & 7]).limit_denominator(2)
+    return -v if code & 8 else v
+
+
+def _nibble(packed_row, k):
+    b = int(packed_row[k // 2])
+    return b & 0xF if k % 2 == 0 else b >> 4
+
+
+def _mxfp4_weights(N, K, seed):
+    r = np.random.Generator(np.random.PCG64(seed))
+    w = (r.standard_normal((N, K)) * 0.02).astype(np.float32)
+    return Q.quant_mxfp4_weights(w)
+
+
+def test_w4a4_matches_exact_brute_force():
+    """Both operands decoded by hand (E2M1 table, 2^(c-127) scales, nibble
+    order even-k low) and summed as Fractions: the fp64 oracle must agree
+    exactly (every term is a dyadic rational well inside fp64).  Two
+    activation blocks per row, M != N, so a swapped block index or a
+    transposed operand fails."""
+    r = np.random.Generator(np.random.PCG64(31))
+    M, N, K = 3, 4, 64
+    x = F.bf16_encode((r.standard_normal((M, K)) * np.exp2(r.integers(-6, 6, (M, 1)))).astype(np.float32))
+    wq, wse = _mxfp4_weights(N, K, 32)
+    y, aq, ase = G.w4a4_mxfp4_f64(x, wq, wse)
+    for m in range(M):
+        for n in range(N):
+            ref = Fraction(0)
+            for k in range(K):
+                a = _e2m1_value(_nibble(aq[m], k)) * Fraction(2) ** (int(ase[m, k // 32]) - 127)
+                w = _e2m1_value(_nibble(wq[n], k)) * Fraction(2) ** (int(wse[n, k // 32]) - 127)
+                ref += a * w
+            assert Fraction(float(y[m, n])) == ref
+
+
+def test_w4a4_on_representable_activations_is_the_w4a16_product():
+    """Activations that already are MXFP4 values, each 32-block holding a
+    6 * 2^e element (the rule's vecMax 6 * 2^e gives scale exponent e, so the
+    quantizer returns them unchanged): W4A4 must equal the weight-only MXFP4
+    product of the same bf16 activations, bit for bit in fp64."""
+    r = np.random.Generator(np.random.PCG64(37))
+    M, N, K = 5, 6, 128
+    codes = r.integers(0, 16, (M, K)).astype(np.uint8)
+    codes[:, ::32] = 7                                          # +6 in every block
+    e = r.integers(-20, 10, (M, K // 32))
+    vals = F.e2m1_decode(codes) * np.exp2(np.repeat(e, 32, axis=1))
+    x = F.bf16_encode(vals.astype(np.float32))
+    assert np.array_equal(F.bf16_decode(x), vals)               # representable in bf16
+    wq, wse = _mxfp4_weights(N, K, 38)
+    y, aq, ase = G.w4a4_mxfp4_f64(x, wq, wse)
+    np.testing.assert_array_equal(ase, (e + 127).astype(np.uint8))
+    np.testing.assert_array_equal(Q.unpack_nibbles(aq), codes)   # -0 keeps its sign code
+    np.testing.assert_array_equal(y, G.qgemm_mxfp4a16(x, wq, wse))
+
+
+@pytest.mark.parametrize("j", [-9, -1, 3, 12])
+def test_w4a4_commutes_with_power_of_two_activation_scaling(j):
+    """Scaling the activations by 2^j moves every block scale by j and leaves
+    the E2M1 codes alone, so the product scales by exactly 2^j."""
+    r = np.random.Generator(np.random.PCG64(41))
+    M, N, K = 4, 3, 96
+    xf = r.standard_normal((M, K)).astype(np.float32)
+    wq, wse = _mxfp4_weights(N, K, 42)
+    y0, aq0, ase0 = G.w4a4_mxfp4_f64(F.bf16_encode(xf), wq, wse)
+    y1, aq1, ase1 = G.w4a4_mxfp4_f64(F.bf16_encode(np.ldexp(xf, j)), wq, wse)
+    np.testing.assert_array_equal(aq1, aq0)
+    np.testing.assert_array_equal(ase1.astype(int), ase0.astype(int) + j)
+    np.testing.assert_array_equal(y1, np.ldexp(y0, j))
