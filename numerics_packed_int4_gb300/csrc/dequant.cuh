@@ -130,14 +130,26 @@ QG_DEVICE void int4x8_kperm_f16(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {
 
 // ---- E2M1 -------------------------------------------------------------------
 // p[i] = (k_i, k_{i+4}) for i = 0..3, each e2m1 * scale (exact)
-QG_DEVICE void e2m1x8_kperm(uint32_t v, uint32_t scale2, uint32_t (&p)[4]) {
+// The E2M1 bit patterns only: p[i] = (k_i, k_{i+4}) * 2^-126 (exact, the
+// 0.5 code a bf16 subnormal).
+QG_DEVICE void e2m1x8_kperm_raw(uint32_t v, uint32_t (&p)[4]) {
   const uint32_t MAG = 0x01C001C0u, SGN = 0x80008000u;
   p[0] = lop3<kLutAndOr>(v << 6, MAG, (v << 12) & SGN);
   p[1] = lop3<kLutAndOr>(v << 2, MAG, (v << 8) & SGN);
   p[2] = lop3<kLutAndOr>(v >> 2, MAG, (v << 4) & SGN);
   p[3] = lop3<kLutAndOr>(v >> 6, MAG, v & SGN);
+}
+QG_DEVICE void e2m1x8_kperm(uint32_t v, uint32_t scale2, uint32_t (&p)[4]) {
+  e2m1x8_kperm_raw(v, p);
 #pragma unroll
   for (int i = 0; i < 4; ++i) p[i] = bf16x2_mul(bf16x2_mul(p[i], kBf16x2_2p126), scale2);
+}
+// One multiply by a folded factor f2 = 2^126 * (block scale) * 2^-j: the caller
+// guarantees f2 is a normal bf16 and undoes 2^-j on the accumulated row.
+QG_DEVICE void e2m1x8_kperm_folded(uint32_t v, uint32_t f2, uint32_t (&p)[4]) {
+  e2m1x8_kperm_raw(v, p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = bf16x2_mul(p[i], f2);
 }
 
 // ---- E4M3 -------------------------------------------------------------------

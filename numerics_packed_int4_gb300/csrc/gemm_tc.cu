@@ -1,4 +1,7 @@
-// Prefill (M > 16) W4A16 GEMM on the 5th-generation tensor cores (tcgen05).
+// Prefill (M > 16) weight-only GEMM on the 5th-generation tensor cores
+// (tcgen05), one kernel template per weight format (slab.cuh): INT4 with group
+// scales (symmetric or with zero points), FP8 E4M3 with channel scales, MXFP4
+// and NVFP4.
 //
 // Orientation: the MMA computes Y^T tiles, D[n, m] = sum_k W[n,k] X[m,k].
 //   * A operand = dequantized weights, 128 output channels x 16 k per MMA,
@@ -46,7 +49,7 @@
 // and returns.
 #include <algorithm>
 
-#include "dequant.cuh"
+#include "slab.cuh"
 #include "tc_common.cuh"
 
 namespace qg {
@@ -65,12 +68,12 @@ constexpr int kSchedWarp = kDeq0 + kDeqWarps;       // scheduler warp
 constexpr int kThreadsTc = (kSchedWarp + 1) * 32;
 constexpr int kXStageBytes = kTileT * kBK * 2;      // 32 KB activations
 
-// Weight formats of the kernel.  Per format: packed bytes per weight row per
-// 64-k slab, activation stages (FP8's 8 KB weight stages leave room for 5).
-enum WFmt { WF_INT4 = 0, WF_INT4Z = 1, WF_FP8 = 2, WF_MXFP4 = 3, WF_NVFP4 = 4 };
+// Per weight format (SlabFmt): packed bytes per weight row per 64-k slab and
+// activation stages (FP8's 8 KB weight stages leave room for 5).
+static_assert(kBK == kSlabK, "one k-slab of the pipeline is one decoded slab");
 template <int WF> struct PfTraits {
-  static constexpr int WROW = WF == WF_FP8 ? kBK : kBK / 2;
-  static constexpr int STAGES = WF == WF_FP8 ? 5 : 6;
+  static constexpr int WROW = SlabTraits<WF>::WROW;
+  static constexpr int STAGES = WF == SF_FP8 ? 5 : 6;
   static constexpr int WSTAGE = kTileW * WROW;        // packed-weight stage bytes
 };
 constexpr uint32_t kTmemCols = 512;
@@ -123,7 +126,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using Tr = PfTraits<WF>;
-  constexpr bool ZP = WF == WF_INT4Z;
   constexpr int kSt = Tr::STAGES;
   uint8_t* xs = smem;                                                     // [kSt][32 KB]
   uint8_t* wsm = smem + kSt * kXStageBytes;                               // [kASlots][Tr::WSTAGE]
@@ -267,46 +269,16 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       if (c.i < ntiles) {
         int m0, n0;
         tile_origin(p, tile_of(c.i), m0, n0);
-        const size_t n = (size_t)min(n0 + row, p.N - 1);
-        const uint8_t* wsb = static_cast<const uint8_t*>(p.ws);
-        if constexpr (WF == WF_INT4 || WF == WF_INT4Z) {
-          const size_t r = n * (p.K >> p.lg);
-          c.srow = wsb + 2 * r;
-          if constexpr (ZP) c.zrow = p.wz + r;
-        } else if constexpr (WF == WF_MXFP4) {
-          c.srow = wsb + n * (p.K / 32);
-        } else if constexpr (WF == WF_NVFP4) {
-          c.srow = wsb + n * (p.K / 16);
-        }
+        slab_rows<WF>(p.ws, p.wz, p.K, p.lg, (size_t)min(n0 + row, p.N - 1), c.srow, c.zrow);
       }
     };
     auto advance = [&](Cur& c, int by) {
       c.s += by;
       while (c.s >= nslab) { c.s -= nslab; ++c.i; set_row(c); }
     };
-    // group scales of the slab's two 32-k halves (bits 0-15) and, with zero
-    // points, their zero points (bits 16-19); one load when both halves lie
-    // in one group (g >= 64)
-    // FP4 formats: the slab's block-scale codes (MXFP4: two, NVFP4: four) in v0
     auto scales_of = [&](const Cur& c, uint32_t& v0, uint32_t& v1) {
       v0 = v1 = 0u;
-      if (c.i >= ntiles) return;
-      if constexpr (WF == WF_INT4 || WF == WF_INT4Z) {
-        const uint16_t* sr = reinterpret_cast<const uint16_t*>(c.srow);
-        const int g0 = (c.s * kBK) >> p.lg, g1 = (c.s * kBK + 32) >> p.lg;
-        v0 = __ldg(sr + g0);
-        if constexpr (ZP) v0 |= (uint32_t)__ldg(c.zrow + g0) << 16;
-        if (g1 == g0) {
-          v1 = v0;
-        } else {
-          v1 = __ldg(sr + g1);
-          if constexpr (ZP) v1 |= (uint32_t)__ldg(c.zrow + g1) << 16;
-        }
-      } else if constexpr (WF == WF_MXFP4) {
-        v0 = __ldg(reinterpret_cast<const uint16_t*>(c.srow) + c.s);
-      } else if constexpr (WF == WF_NVFP4) {
-        v0 = __ldg(reinterpret_cast<const uint32_t*>(c.srow) + c.s);
-      }
+      if (c.i < ntiles) slab_scales<WF>(c.srow, c.zrow, c.s, p.lg, v0, v1);
     };
     // epilogue of tile e: TMEM -> registers -> (accumulator free) -> bf16 -> Y
     auto epilogue = [&](int e) -> bool {
@@ -329,12 +301,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       if (nn < p.N) {
         // epilogue scale: FP8 per channel, NVFP4 global, none for INT4 / MXFP4
         float es = 1.f;
-        if constexpr (WF == WF_FP8) es = __ldg(p.cs + nn);
-        if constexpr (WF == WF_NVFP4) es = __ldg(p.gs);
+        if constexpr (WF == SF_FP8) es = __ldg(p.cs + nn);
+        if constexpr (WF == SF_NVFP4) es = __ldg(p.gs);
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           float val = __uint_as_float(v[c]);
-          if constexpr (WF == WF_FP8 || WF == WF_NVFP4) val *= es;
+          if constexpr (SlabTraits<WF>::EPI_SCALE) val *= es;
           if (mb + c < p.M) p.y[(size_t)(mb + c) * p.N + nn] = f32_to_bf16_bits(val);
         }
       }
@@ -356,54 +328,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       }
       if (!ok) break;
       const int sa = g % kASlots, ra = g / kASlots;
-      const uint32_t s2a = bf16x2_splat(sc_cur0), s2b = bf16x2_splat(sc_cur1);
-      const uint32_t z2a = bf16x2_zero128(sc_cur0 >> 16), z2b = bf16x2_zero128(sc_cur1 >> 16);
-      const uint32_t fb = sc_cur0;                  // FP4 formats: the slab's block-scale codes
+      const uint32_t v0 = sc_cur0, v1 = sc_cur1;
       sc_cur0 = sc_nxt0;
       sc_cur1 = sc_nxt1;
       advance(pf, kDeqSets);                        // pf now at this set's slab after the next
       scales_of(pf, sc_nxt0, sc_nxt1);
       if (!mbar_wait_warp(&tl->w_full[sa], ra & 1, p.cap, abort, p.err)) { ok = false; break; }
       uint32_t out[32];
-      if constexpr (WF == WF_FP8) {
-        // 64 E4M3 codes of this row; 64-byte swizzled stage: chunk c at c ^ ((row >> 1) & 3)
-        const uint8_t* wrow = wsm + sa * Tr::WSTAGE + row * Tr::WROW;
-        const int wsw = (row >> 1) & 3;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 w4 = *reinterpret_cast<const uint4*>(wrow + 16 * (c ^ wsw));
-          const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {             // bytes k0..k3 -> (k0, k1), (k2, k3), exact
-            uint32_t p02, p13;
-            e4m3x4_kperm(ww[i], p02, p13);
-            out[8 * c + 2 * i] = prmt(p02, p13, 0x5410u);
-            out[8 * c + 2 * i + 1] = prmt(p02, p13, 0x7632u);
-          }
-        }
-      } else {
-        const uint4 wa = *reinterpret_cast<const uint4*>(wsm + sa * Tr::WSTAGE + row * Tr::WROW);
-        const uint4 wb = *reinterpret_cast<const uint4*>(wsm + sa * Tr::WSTAGE + row * Tr::WROW + 16);
-        const uint32_t v[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint32_t nat[4];
-          if constexpr (WF == WF_INT4Z) {
-            int4zp_x8_nat(v[j], j < 4 ? s2a : s2b, j < 4 ? z2a : z2b, nat);
-          } else if constexpr (WF == WF_INT4) {
-            int4x8_nat(v[j], j < 4 ? s2a : s2b, nat);
-          } else {
-            // E2M1 words of 8 codes; block scale: MXFP4 per 32 k (words j/4), NVFP4 per 16 (j/2)
-            const uint32_t sc = WF == WF_MXFP4 ? e8m0_to_bf16x2((fb >> (8 * (j >> 2))) & 0xFFu)
-                                               : e4m3_to_bf16x2((fb >> (8 * (j >> 1))) & 0xFFu);
-            uint32_t pq[4];
-            e2m1x8_kperm(v[j], sc, pq);
-            kperm4_to_natural(pq, nat);
-          }
-          out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
-          out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
-        }
-      }
+      decode_slab<WF>(wsm + sa * Tr::WSTAGE + row * Tr::WROW, row, v0, v1, out);
       mbar_arrive_warp(&tl->w_empty[sa]);           // packed slab decoded: its stage may be refilled
       if (ra > 0) {
         if (!mbar_wait_warp(&tl->a_empty[sa], (ra - 1) & 1, p.cap, abort, p.err)) { ok = false; break; }
@@ -504,16 +436,16 @@ qg_status prefill_tc(int wf, const uint8_t* w_q, const void* w_s, const uint8_t*
                      cudaStream_t st, bool* handled, const char* name) {
   *handled = false;
   if (M <= 16 || K % kBK != 0) return QG_OK;
-  if ((wf == WF_INT4 || wf == WF_INT4Z) && (g < 32 || (g & (g - 1)) != 0 || K % g != 0)) return QG_OK;
+  if ((wf == SF_INT4 || wf == SF_INT4Z) && (g < 32 || (g & (g - 1)) != 0 || K % g != 0)) return QG_OK;
   // the FP4 block scales are read two (MXFP4) or four (NVFP4) codes at a time
-  if (wf == WF_MXFP4 && (reinterpret_cast<uintptr_t>(w_s) & 1)) return QG_OK;
-  if (wf == WF_NVFP4 && (reinterpret_cast<uintptr_t>(w_s) & 3)) return QG_OK;
+  if (wf == SF_MXFP4 && (reinterpret_cast<uintptr_t>(w_s) & 1)) return QG_OK;
+  if (wf == SF_NVFP4 && (reinterpret_cast<uintptr_t>(w_s) & 3)) return QG_OK;
   *handled = true;
-  const int wrow = wf == WF_FP8 ? kBK : kBK / 2;        // packed bytes per row per slab
+  const int wrow = wf == SF_FP8 ? kBK : kBK / 2;        // packed bytes per row per slab
   CUtensorMap tmap, tmap_w;
   if (!make_bf16_tmap(&tmap, x, M, K, kTileT, kBK))
     return set_error(QG_ERR_CUDA, "%s: cannot encode the activation tensor map", name);
-  const bool wok = wf == WF_FP8 ? make_u8_tmap_swizzled(&tmap_w, w_q, N, K, kTileW, wrow)
+  const bool wok = wf == SF_FP8 ? make_u8_tmap_swizzled(&tmap_w, w_q, N, K, kTileW, wrow)
                                 : make_u8_tmap(&tmap_w, w_q, N, K / 2, kTileW, wrow);
   if (!wok) return set_error(QG_ERR_CUDA, "%s: cannot encode the weight tensor map", name);
   unsigned int* err = device_error_word();
@@ -527,15 +459,15 @@ qg_status prefill_tc(int wf, const uint8_t* w_q, const void* w_s, const uint8_t*
   a.group_t = 8;
   a.err = err;
   a.cap = wait_limit();
-  const int stages = wf == WF_FP8 ? PfTraits<WF_FP8>::STAGES : PfTraits<WF_INT4>::STAGES;
+  const int stages = wf == SF_FP8 ? PfTraits<SF_FP8>::STAGES : PfTraits<SF_INT4>::STAGES;
   const int smem = stages * kXStageBytes + kASlots * kTileW * wrow + (int)sizeof(TcSmemTail) + 1024;
   void (*kern)(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap, const TcArgs) = nullptr;
   switch (wf) {
-    case WF_INT4: kern = w4a16_tc_kernel<WF_INT4>; break;
-    case WF_INT4Z: kern = w4a16_tc_kernel<WF_INT4Z>; break;
-    case WF_FP8: kern = w4a16_tc_kernel<WF_FP8>; break;
-    case WF_MXFP4: kern = w4a16_tc_kernel<WF_MXFP4>; break;
-    case WF_NVFP4: kern = w4a16_tc_kernel<WF_NVFP4>; break;
+    case SF_INT4: kern = w4a16_tc_kernel<SF_INT4>; break;
+    case SF_INT4Z: kern = w4a16_tc_kernel<SF_INT4Z>; break;
+    case SF_FP8: kern = w4a16_tc_kernel<SF_FP8>; break;
+    case SF_MXFP4: kern = w4a16_tc_kernel<SF_MXFP4>; break;
+    case SF_NVFP4: kern = w4a16_tc_kernel<SF_NVFP4>; break;
     default: return set_error(QG_ERR_INVALID_ARG, "%s: unknown prefill format %d", name, wf);
   }
   if (!ensure_smem(kern, smem)) return set_error(QG_ERR_CUDA, "%s: smem attribute", name);

@@ -103,9 +103,34 @@ QG_DEVICE const uint8_t* zero_row(const GemvArgs& p, int n) {
   return nullptr;
 }
 
+// FP4 block scales folded into the E2M1 decode, so that each weight pair
+// costs one bf16 multiply instead of two (the E2M1 bit pattern is the value
+// times 2^-126):
+//  * MXFP4: f = 2^126 * 2^(c-127) = 2^(c-1), a normal bf16 for codes c <= 128
+//    (blocks with magnitudes below 12 -- every code a weight block of unit
+//    order gets); a warp whose rows hold a larger code takes the two-multiply
+//    decode for that segment.  Exact either way.
+//  * NVFP4: f = 2^126 * e4m3(sb) * 2^-9 (at most 448 * 2^117 < 2^126), the
+//    weight comes out times 2^-9 exactly (never below 2^-19, so normal) and
+//    the epilogue multiplies the row by 2^9 with the global scale.
+constexpr float kNvfp4Unfold = 512.f;
+QG_DEVICE uint32_t mxfp4_fold(uint32_t c) { return c <= 128u ? bf16x2_splat((c + 126u) << 7) : 0u; }
+QG_DEVICE uint32_t nvfp4_fold_x2(uint32_t two_codes) {     // (lo code, hi code) -> bf16x2 folded factors
+  const uint32_t h = e4m3x2_to_f16x2(two_codes);         // exact
+  float lo, hi;
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.f32.f16 %0, a;\n cvt.f32.f16 %1, b;\n}"
+      : "=f"(lo), "=f"(hi) : "r"(h));
+  const float k = 1.6615349947311448e35f;                 // 2^117
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi * k), "f"(lo * k));   // exact products
+  return d;
+}
+
 // G1: INT4 with g == 128, one group per segment: the group index is the
-// segment index.
-template <int FMT, bool G1>
+// segment index.  FOLD: the GEMV's folded FP4 factors in s.b (MXFP4; 0 when
+// the code is above 128) and s.a (NVFP4, both codes of the segment); without
+// FOLD the raw codes (the canonical dequant export).
+template <int FMT, bool G1, bool FOLD = false>
 QG_DEVICE Scale load_scale(const GemvArgs& p, const uint8_t* srow, const uint8_t* zrow, int seg, int t) {
   Scale s{0u, 0u};
   if constexpr (G1 && FMT == F_INT4) {
@@ -122,8 +147,10 @@ QG_DEVICE Scale load_scale(const GemvArgs& p, const uint8_t* srow, const uint8_t
     s.b = bf16x2_zero128(__ldg(zrow + grp));
   } else if constexpr (FMT == F_MXFP4) {
     s.a = __ldg(srow + seg * 4 + t);
+    if constexpr (FOLD) s.b = mxfp4_fold(s.a);
   } else if constexpr (FMT == F_NVFP4) {
     s.a = __ldg(reinterpret_cast<const uint16_t*>(srow + seg * 8 + 2 * t));
+    if constexpr (FOLD) s.a = nvfp4_fold_x2(s.a);
   }
   return s;
 }
@@ -137,15 +164,21 @@ QG_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Decode chunk j (8 k-values) of the lane's 16-byte word into A pairs:
 // a[0], a[1] for the first mma (lo / hi k-slots), a[2], a[3] for the second.
-template <int FMT>
+// FOLD (FP4 formats, scales from load_scale<..., true>): MXFP4 with
+// FAST = every row of the warp has its folded factor, NVFP4 always.
+template <int FMT, bool FOLD = false, bool FAST = false>
 QG_DEVICE void decode_chunk(const uint4& w, const Scale& s, int j, uint32_t (&a)[4]) {
   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
   if constexpr (FMT == F_INT4) {
     int4x8_kperm(ww[j], s.a, a);
   } else if constexpr (FMT == F_INT4Z) {
     int4zp_x8_kperm(ww[j], s.a, s.b, a);
+  } else if constexpr (FMT == F_MXFP4 && FOLD && FAST) {
+    e2m1x8_kperm_folded(ww[j], s.b, a);
   } else if constexpr (FMT == F_MXFP4) {
     e2m1x8_kperm(ww[j], e8m0_to_bf16x2(s.a), a);
+  } else if constexpr (FMT == F_NVFP4 && FOLD) {
+    e2m1x8_kperm_folded(ww[j], prmt(s.a, s.a, j < 2 ? 0x1010u : 0x3232u), a);
   } else if constexpr (FMT == F_NVFP4) {
     e2m1x8_kperm(ww[j], e4m3_to_bf16x2(j < 2 ? (s.a & 0xFFu) : (s.a >> 8)), a);
   } else {
@@ -256,8 +289,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
 #pragma unroll
   for (int u = 0; u < kPFS; ++u) {
     if (u < nseg) {
-      sa[u] = load_scale<FMT, G1>(p, sr0, zr0, seg_lo + s_lo + u, t);
-      sb[u] = load_scale<FMT, G1>(p, sr1, zr1, seg_lo + s_lo + u, t);
+      sa[u] = load_scale<FMT, G1, true>(p, sr0, zr0, seg_lo + s_lo + u, t);
+      sb[u] = load_scale<FMT, G1, true>(p, sr1, zr1, seg_lo + s_lo + u, t);
     }
   }
 
@@ -347,27 +380,37 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
         const int us = u % kPFS;
         const Scale s_a = sa[us], s_b = sb[us];
         if (s + kPFS < nseg) {
-          sa[us] = load_scale<FMT, G1>(p, sr0, zr0, seg_lo + s_lo + s + kPFS, t);
-          sb[us] = load_scale<FMT, G1>(p, sr1, zr1, seg_lo + s_lo + s + kPFS, t);
+          sa[us] = load_scale<FMT, G1, true>(p, sr0, zr0, seg_lo + s_lo + s + kPFS, t);
+          sb[us] = load_scale<FMT, G1, true>(p, sr1, zr1, seg_lo + s_lo + s + kPFS, t);
         }
         const uint4* xs0 = xq0 + s * kPadSeg;
         const uint4* xs1 = xq1 + s * kPadSeg;
+        auto chunks = [&](auto fast) {
 #pragma unroll
-        for (int j = 0; j < Tr::CPL; ++j) {
-          uint32_t ag[4], ah[4];
-          decode_chunk<FMT>(wa, s_a, j, ag);
-          decode_chunk<FMT>(wb, s_b, j, ah);
-
-          {
-            const uint4 xf = xs0[j];
-            mma_bf16(acc_mma[0], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
-            mma_bf16(acc_mma[0], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
+          for (int j = 0; j < Tr::CPL; ++j) {
+            uint32_t ag[4], ah[4];
+            decode_chunk<FMT, true, decltype(fast)::value>(wa, s_a, j, ag);
+            decode_chunk<FMT, true, decltype(fast)::value>(wb, s_b, j, ah);
+            {
+              const uint4 xf = xs0[j];
+              mma_bf16(acc_mma[0], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
+              mma_bf16(acc_mma[0], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
+            }
+            if constexpr (MT == 2) {
+              const uint4 xf = xs1[j];
+              mma_bf16(acc_mma[1], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
+              mma_bf16(acc_mma[1], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
+            }
           }
-          if constexpr (MT == 2) {
-            const uint4 xf = xs1[j];
-            mma_bf16(acc_mma[1], ag[0], ah[0], ag[1], ah[1], xf.x, xf.y);
-            mma_bf16(acc_mma[1], ag[2], ah[2], ag[3], ah[3], xf.z, xf.w);
-          }
+        };
+        if constexpr (FMT == F_MXFP4) {
+          // one multiply per pair when every row of the warp has its folded factor
+          if (__all_sync(0xffffffffu, (s_a.b != 0u) && (s_b.b != 0u)))
+            chunks(std::true_type{});
+          else
+            chunks(std::false_type{});
+        } else {
+          chunks(std::false_type{});
         }
         if constexpr (FMT == F_FP8A8) {
           // block boundary (two 64-k segments per block) or the end of this
@@ -428,7 +471,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
     }
     if (n < p.N) {
       if constexpr (fp8_weights(FMT)) v *= __ldg(static_cast<const float*>(p.scales) + n);
-      if constexpr (FMT == F_NVFP4) v *= __ldg(p.gscale);
+      if constexpr (FMT == F_NVFP4) v *= __ldg(p.gscale) * kNvfp4Unfold;   // 2^9 exactly (folded decode)
       p.y[(size_t)m * p.N + n] = f32_to_bf16_bits(v);
     }
   }

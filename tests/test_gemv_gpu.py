@@ -123,3 +123,45 @@ def test_chained_gemvs_wait_for_the_previous_output(qg):
         ref = OG.to_bf16(OG.gemm_bf16_f64(ref, W["deq"], W["epi"]))
     y = OF.bf16_decode(host(d[3]))
     check_gemm(y, OF.bf16_decode(ref), "chained")
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_mxfp4_block_scales_across_the_code_range(qg, M):
+    """MXFP4 rows whose block scales span the E8M0 range: codes above 128
+    (magnitudes of 12 and more) take the decode with two multiplies for the
+    warp that holds them, the others the folded single multiply; both must
+    give the canonical weights."""
+    N, K = 256, 1024
+    r = np.random.Generator(np.random.PCG64(M + 70))
+    w = inputs.weights_f32(N, K, seed=M + 71)
+    row_exp = r.integers(-60, 1, N).astype(np.float32)
+    row_exp[:16] = 40.0                      # the first warp's rows: every code > 128
+    row_exp[40] = 20.0                       # one row in another warp
+    w = (w * np.exp2(row_exp)[:, None]).astype(np.float32)
+    q, se = OQ.quant_mxfp4_weights(w)
+    assert (se > 128).any() and (se <= 128).any()
+    Wd = dict(q=q, s=se, deq=OG.dequant_mxfp4(q, se), epi=None)
+    x = inputs.activations_bf16(M, K, seed=M + 72)
+    y = run_gpu(qg, "mxfp4", Wd, x, M, N, K)
+    ref, _ = reference(Wd, x)
+    unit = np.exp2(-row_exp)[None, :]        # every row back to unit order (exact)
+    check_gemm(y * unit, ref * unit, "mxfp4 scale range M=%d" % M)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_nvfp4_every_finite_block_scale_code(qg, M):
+    """NVFP4 block scales over every finite E4M3 code (subnormals and 448
+    included) and random E2M1 codes: the folded decode (factor 2^117 times
+    the scale, the row multiplied by 2^9 at the end) must give the product of
+    the canonical weights."""
+    N, K = 128, 2048
+    r = np.random.Generator(np.random.PCG64(80 + M))
+    q = r.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    sb = r.integers(0, 0x7F, (N, K // 16)).astype(np.uint8)      # 0x00 .. 0x7E, all finite
+    sb[0, :0x7F] = np.arange(0x7F, dtype=np.uint8)
+    gs = np.float32(0.75)
+    Wd = dict(q=q, s=sb, gs=gs, deq=OG.dequant_nvfp4(q, sb), epi=np.full(N, float(gs)))
+    x = inputs.activations_bf16(M, K, seed=81 + M)
+    y = run_gpu(qg, "nvfp4", Wd, x, M, N, K)
+    ref, _ = reference(Wd, x)
+    check_gemm(y, ref, "nvfp4 all scale codes M=%d" % M)
