@@ -51,9 +51,9 @@ BYTES_PER_PARAM = {"int4": 0.5 + 2 / 128, "fp8": 1.0, "mxfp4": 0.5 + 1 / 32, "nv
 # on and that launch's algorithmic bytes.  The summaries and the commands are
 # under profiles/.  An entry goes back to None whenever its kernel changes.
 PROFILED_TRAFFIC = {
-    "decode_m1": {"bytes": 30.32e6, "launch": "gemv_kernel INT4 M=1 N=14336 K=4096",
+    "decode_m1": {"bytes": 30.32e6, "launch": "gemv_kernel<0, 1, 1> INT4 M=1 N=14336 K=4096",
                   "algorithmic_bytes": 30.30e6, "profile": "profiles/gemv_int4_m1_n14336_k4096.md"},
-    "prefill": {"bytes": 381.1e6, "launch": "w4a16_tc_kernel M=8192 N=14336 K=4096",
+    "prefill": {"bytes": 380.3e6, "launch": "w4a16_tc_kernel<0> M=8192 N=14336 K=4096",
                 "algorithmic_bytes": 332.3e6, "profile": "profiles/prefill_w4a16_tc_m8192_n14336_k4096.md"},
     "moe": {"bytes": 985.3e6, "launch": "moe_f16_kernel gate/up R=8192 N=28672 K=4096",
             "algorithmic_bytes": 1021.4e6, "profile": "profiles/moe_w4a8_f16act_t4096_e8.md"},
@@ -523,8 +523,7 @@ def cpu_cores():
 def bench_config(rows, world):
     """The workload of the bench line (shared by both arms)."""
     return {"workload": "decode sweep M in {1,4,16} x {4096^2, 14336x4096, 4096x14336} x "
-                        "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill M=8192 (W4A16; FP8, MXFP4, NVFP4 weights; "
-                        "W4A4 MXFP4 with online activation quant) + "
+                        "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill M=8192 (W4A16; FP8, MXFP4, NVFP4 weights) + "
                         "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2 (bf16 group scales; "
                         "FP8 group scales) + asymmetric INT4 g64 M=1 and M=8192 + W8A8 GEMV M=1",
             "rows": rows, "l2": "inputs larger than L2: every weight matrix read once per step; "
@@ -757,7 +756,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe,moe_fp8s,"
-                                      "decode_zp,prefill_zp,decode_w8a8,prefill_fp8,prefill_mxfp4,prefill_nvfp4,prefill_w4a4")
+                                      "decode_zp,prefill_zp,decode_w8a8,prefill_fp8,prefill_mxfp4,prefill_nvfp4",
+                    help="segments to time; prefill_w4a4 (MXFP4 activations x MXFP4 weights) is available too")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
