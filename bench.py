@@ -655,6 +655,10 @@ def run_ours(args):
     value = aggregate(world * wl.bytes.get("decode_m1", 0.0), seg_ms_max.get("decode_m1", 1.0) * 1e-3) / 1e9
 
     e2e = e2e_decode_m1(torch, qg, wl, dev, steps=max(2, min(args.steps, 5))) if "decode_m1" in rows else None
+    if "decode_m1" in rows:
+        rc = read_ceiling(torch, qg, wl, dev)
+        rc["gemv_row_over_read_time"] = seg_ms_max["decode_m1"] / rc["ms"]
+        row_out["decode_m1"]["single_launch_read"] = rc
     clocks = clk.summary(t_region0, t_region1)
     launches_per_step = sum((wl.launches[r] or 0) for r in rows)
 
@@ -684,6 +688,41 @@ def run_ours(args):
                                 "sample": "M=1 GEMVs (oracle dequant + fp64 product): %s; %.1f s" % (desc, spent)}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def read_ceiling(torch, qg, wl, dev, reps=5):
+    """A plain streaming read of each of the decode row's 12 packed weight
+    matrices, one launch each, in the row's order and under the same L2
+    conditions: what one launch of that many bytes reaches on this GPU.
+    Measured outside the timed step (it is not part of the path)."""
+    bufs = [wl.W[(f, N, K)]["q"] for f in FORMATS for N, K in SHAPES]
+    nbytes = sum(b.numel() * b.element_size() for b in bufs)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def seg():
+        for b in bufs:
+            qg.qg_stream_read(b, b.numel() * b.element_size(), sink)
+
+    seg()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream(device=dev)):
+        seg()
+    for _ in range(3):
+        g.replay()
+    ts = []
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = sorted(ts)[len(ts) // 2]
+    qg.qg_check_device_error()
+    return {"what": "qg_stream_read of each decode weight matrix, one launch each", "bytes": nbytes,
+            "launches": len(bufs), "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9}
 
 
 def e2e_decode_m1(torch, qg, wl, dev, steps):

@@ -337,6 +337,15 @@ QG_API const char* qg_last_error_string(void);
  * Intended for tests that exercise the timeout path.                        */
 QG_API void qg_set_wait_limit(uint32_t iterations);
 
+/* Measurement aid, not part of the method: a plain streaming read of `bytes`
+ * bytes at p (16-byte non-allocating loads, grid-stride over 8 CTAs per SM),
+ * the rate one launch of that size reaches on this GPU -- the ceiling against
+ * which a single decode launch of the same bytes is judged.  p 16-byte
+ * aligned, bytes a positive multiple of 16, sink one 4-byte device word that
+ * the kernel may write.                                                      */
+QG_API qg_status qg_stream_read(const void* p, long long bytes, unsigned int* sink,
+                         qg_stream_t stream);
+
 /* Failure-path self-test; the method has no counterpart.  Launches one CTA
  * whose thread waits on an mbarrier that nothing arrives at, giving up after
  * `polls` bounded polls (each suspends for at most about 1 us).  The kernel

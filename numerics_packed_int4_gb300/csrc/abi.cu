@@ -1,4 +1,5 @@
 // Status, error reporting and device error word shared by every entry point.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -106,9 +107,39 @@ __global__ void selftest_wait_kernel(uint32_t polls, unsigned int* err) {
   __syncthreads();
 }
 
+// Plain streaming read: 16-byte non-allocating loads, grid-stride, xor-reduced
+// so that the loads stay; the sink is written only on a value no real data
+// gives in practice (it must still be a valid word).
+__global__ void stream_read_kernel(const uint4* __restrict__ p, long long n16, unsigned int* sink) {
+  uint32_t acc = 0;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+#pragma unroll 4
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16; i += stride) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p + i));
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  if (acc == 0x9E3779B9u) atomicOr(sink, acc);
+}
+
 extern "C" {
 
 const char* qg_last_error_string(void) { return g_msg; }
+
+qg_status qg_stream_read(const void* p, long long bytes, unsigned int* sink, qg_stream_t stream) {
+  if (!p || !sink) return qg::set_error(QG_ERR_INVALID_ARG, "qg_stream_read: NULL pointer");
+  if (bytes <= 0 || bytes % 16 != 0)
+    return qg::set_error(QG_ERR_UNSUPPORTED_SHAPE, "qg_stream_read: bytes must be a positive multiple of 16");
+  if ((reinterpret_cast<uintptr_t>(p) & 15) != 0 || (reinterpret_cast<uintptr_t>(sink) & 3) != 0)
+    return qg::set_error(QG_ERR_MISALIGNED, "qg_stream_read: misaligned pointer");
+  const long long n16 = bytes / 16;
+  const long long want = (n16 + 255) / 256;
+  const int grid = (int)std::min<long long>(want, 8LL * qg::sm_count());     // 8 CTAs of 256 threads per SM
+  stream_read_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(p), n16, sink);
+  return qg::check_launch("qg_stream_read");
+}
 
 void qg_set_wait_limit(uint32_t iterations) {
   g_wait_limit = iterations ? iterations : kDefaultWaitLimit;

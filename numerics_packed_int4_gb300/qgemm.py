@@ -28,6 +28,7 @@ SIGNATURES = {
     "qgemm_w8a8": [P, P, P, P, I, I, I, P],
     "qgemm_fp4a16": [P, P, I, I, P, P, P, I, I, I, P],
     "qgemm_w4a4_mxfp4": [P, P, P, P, P, P, I, I, I, P],
+    "qg_stream_read": [P, I64, P, P],
     "quant_act_mxfp4": [P, P, P, I, I, I, P],
     "quant_act_fp8_block": [P, P, P, I, I, I, P],
     "qgemm_w4a8_grouped": [P, P, P, P, P, I, P, I, I, I, I, P],
@@ -129,6 +130,10 @@ def qgemm_w8a8(w_e4m3, w_cs, x, y, M, N, K, stream=None):
 def qgemm_fp4a16(w_e2m1, w_bs, scale_fmt, g, global_scale, x, y, M, N, K, stream=None):
     return _call("qgemm_fp4a16", _ptr(w_e2m1), _ptr(w_bs), scale_fmt, g, _ptr(global_scale),
                  _ptr(x), _ptr(y), M, N, K, stream=stream)
+
+
+def qg_stream_read(p, nbytes, sink, stream=None):
+    return _call("qg_stream_read", _ptr(p), nbytes, _ptr(sink), stream=stream)
 
 
 def qgemm_w4a4_mxfp4(w_e2m1, w_e8m0, a_e2m1, a_e8m0, a_work, y, M, N, K, stream=None):

@@ -145,3 +145,12 @@ def test_w4a4_argument_validation(lib):
     assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 96) == 2     # K % 128
     assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE_MIS, FAKE, FAKE, FAKE, 1, 128, 128) == 3
     assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 128, 128) == 0    # M = 0
+
+
+def test_stream_read_argument_validation(lib):
+    # (p, bytes, sink, stream)
+    assert _rc(lib, "qg_stream_read", None, 1024, FAKE) == 1
+    assert _rc(lib, "qg_stream_read", FAKE, 1024, None) == 1
+    assert _rc(lib, "qg_stream_read", FAKE, 1000, FAKE) == 2
+    assert _rc(lib, "qg_stream_read", FAKE, 0, FAKE) == 2
+    assert _rc(lib, "qg_stream_read", FAKE_MIS, 1024, FAKE) == 3

@@ -165,3 +165,14 @@ def test_nvfp4_every_finite_block_scale_code(qg, M):
     y = run_gpu(qg, "nvfp4", Wd, x, M, N, K)
     ref, _ = reference(Wd, x)
     check_gemm(y, ref, "nvfp4 all scale codes M=%d" % M)
+
+
+def test_stream_read_measurement_aid(qg):
+    """The bench's read-ceiling probe runs on any 16-byte multiple, leaves no
+    device error and writes its sink only on the one sentinel value."""
+    buf = torch.arange(1 << 20, dtype=torch.int32, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for nbytes in (16, 4096, 4 << 20):
+        qg.qg_stream_read(buf, nbytes, sink)
+    qg.qg_check_device_error()
+    assert int(sink.item()) == 0
