@@ -177,6 +177,29 @@ QG_DEVICE uint32_t e4m3_to_bf16x2(uint32_t c) {
   return bf16x2_splat(__float_as_uint(e4m3_to_f32(c & 0xFFu)) >> 16);
 }
 
+// FP4 block scales folded into the E2M1 decode, so that each weight pair
+// costs one bf16 multiply instead of two (the E2M1 bit pattern is the value
+// times 2^-126):
+//  * MXFP4: f = 2^126 * 2^(c-127) = 2^(c-1), a normal bf16 for codes c <= 128
+//    (blocks with magnitudes below 12 -- every code a weight block of unit
+//    order gets); a warp whose rows hold a larger code takes the two-multiply
+//    decode for that slab or segment.  Exact either way.
+//  * NVFP4: f = 2^126 * e4m3(sb) * 2^-9 (at most 448 * 2^117 < 2^126), the
+//    weight comes out times 2^-9 exactly (never below 2^-19, so normal) and
+//    the epilogue multiplies the row by 2^9 with the global scale.
+constexpr float kNvfp4Unfold = 512.f;
+QG_DEVICE uint32_t mxfp4_fold(uint32_t c) { return c <= 128u ? bf16x2_splat((c + 126u) << 7) : 0u; }
+QG_DEVICE uint32_t nvfp4_fold_x2(uint32_t two_codes) {     // (lo code, hi code) -> bf16x2 folded factors
+  const uint32_t h = e4m3x2_to_f16x2(two_codes);         // exact
+  float lo, hi;
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.f32.f16 %0, a;\n cvt.f32.f16 %1, b;\n}"
+      : "=f"(lo), "=f"(hi) : "r"(h));
+  const float k = 1.6615349947311448e35f;                 // 2^117
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi * k), "f"(lo * k));   // exact products
+  return d;
+}
+
 // ---- natural order ---------------------------------------------------------
 // (k0,k1),(k2,k3),(k4,k5),(k6,k7) from the (k_i, k_{i+4}) pairs
 QG_DEVICE void kperm4_to_natural(const uint32_t (&p)[4], uint32_t (&o)[4]) {

@@ -302,7 +302,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         // epilogue scale: FP8 per channel, NVFP4 global, none for INT4 / MXFP4
         float es = 1.f;
         if constexpr (WF == SF_FP8) es = __ldg(p.cs + nn);
-        if constexpr (WF == SF_NVFP4) es = __ldg(p.gs);
+        if constexpr (WF == SF_NVFP4) es = __ldg(p.gs) * kNvfp4Unfold;   // the slab decode's 2^-9 undone
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           float val = __uint_as_float(v[c]);

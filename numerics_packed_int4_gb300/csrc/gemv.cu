@@ -103,29 +103,6 @@ QG_DEVICE const uint8_t* zero_row(const GemvArgs& p, int n) {
   return nullptr;
 }
 
-// FP4 block scales folded into the E2M1 decode, so that each weight pair
-// costs one bf16 multiply instead of two (the E2M1 bit pattern is the value
-// times 2^-126):
-//  * MXFP4: f = 2^126 * 2^(c-127) = 2^(c-1), a normal bf16 for codes c <= 128
-//    (blocks with magnitudes below 12 -- every code a weight block of unit
-//    order gets); a warp whose rows hold a larger code takes the two-multiply
-//    decode for that segment.  Exact either way.
-//  * NVFP4: f = 2^126 * e4m3(sb) * 2^-9 (at most 448 * 2^117 < 2^126), the
-//    weight comes out times 2^-9 exactly (never below 2^-19, so normal) and
-//    the epilogue multiplies the row by 2^9 with the global scale.
-constexpr float kNvfp4Unfold = 512.f;
-QG_DEVICE uint32_t mxfp4_fold(uint32_t c) { return c <= 128u ? bf16x2_splat((c + 126u) << 7) : 0u; }
-QG_DEVICE uint32_t nvfp4_fold_x2(uint32_t two_codes) {     // (lo code, hi code) -> bf16x2 folded factors
-  const uint32_t h = e4m3x2_to_f16x2(two_codes);         // exact
-  float lo, hi;
-  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.f32.f16 %0, a;\n cvt.f32.f16 %1, b;\n}"
-      : "=f"(lo), "=f"(hi) : "r"(h));
-  const float k = 1.6615349947311448e35f;                 // 2^117
-  uint32_t d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi * k), "f"(lo * k));   // exact products
-  return d;
-}
-
 // G1: INT4 with g == 128, one group per segment: the group index is the
 // segment index.  FOLD: the GEMV's folded FP4 factors in s.b (MXFP4; 0 when
 // the code is above 128) and s.a (NVFP4, both codes of the segment); without

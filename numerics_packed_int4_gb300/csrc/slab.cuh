@@ -108,7 +108,11 @@ QG_DEVICE void load_slab_words_sw128(const uint8_t* row128, int row, int sub, Sl
   }
 }
 
-// Decode a slab's words: out[i] = (k_2i, k_2i+1) in bf16.
+// Decode a slab's words: out[i] = (k_2i, k_2i+1) in bf16.  The FP4 block
+// scales are folded into the E2M1 decode (dequant.cuh): NVFP4 weights come out
+// times 2^-9 exactly (the caller multiplies the accumulated row by
+// kNvfp4Unfold), MXFP4 weights exactly, with one multiply per pair when every
+// row of the warp has block codes <= 128.  Warp-collective for MXFP4.
 template <int WF>
 QG_DEVICE void decode_slab_words(const SlabWords<WF>& sw, uint32_t v0, uint32_t v1, uint32_t (&out)[32]) {
   if constexpr (WF == SF_FP8) {
@@ -119,26 +123,56 @@ QG_DEVICE void decode_slab_words(const SlabWords<WF>& sw, uint32_t v0, uint32_t 
       out[2 * i] = prmt(p02, p13, 0x5410u);
       out[2 * i + 1] = prmt(p02, p13, 0x7632u);
     }
-  } else {
+  } else if constexpr (WF == SF_INT4 || WF == SF_INT4Z) {
     const uint32_t s2a = bf16x2_splat(v0), s2b = bf16x2_splat(v1);
     const uint32_t z2a = bf16x2_zero128(v0 >> 16), z2b = bf16x2_zero128(v1 >> 16);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       uint32_t nat[4];
-      if constexpr (WF == SF_INT4Z) {
+      if constexpr (WF == SF_INT4Z)
         int4zp_x8_nat(sw.w[j], j < 4 ? s2a : s2b, j < 4 ? z2a : z2b, nat);
-      } else if constexpr (WF == SF_INT4) {
+      else
         int4x8_nat(sw.w[j], j < 4 ? s2a : s2b, nat);
-      } else {
-        // words of 8 E2M1 codes; block scale: MXFP4 per 32 k (words j / 4), NVFP4 per 16 (j / 2)
-        const uint32_t sc = WF == SF_MXFP4 ? e8m0_to_bf16x2((v0 >> (8 * (j >> 2))) & 0xFFu)
-                                           : e4m3_to_bf16x2((v0 >> (8 * (j >> 1))) & 0xFFu);
-        uint32_t pq[4];
-        e2m1x8_kperm(sw.w[j], sc, pq);
-        kperm4_to_natural(pq, nat);
-      }
       out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
       out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
+    }
+  } else {
+    // words of 8 E2M1 codes; block scale: MXFP4 per 32 k (words j / 4), NVFP4 per 16 (j / 2)
+    auto put = [&](int j, const uint32_t (&pq)[4]) {
+      uint32_t nat[4];
+      kperm4_to_natural(pq, nat);
+      out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
+      out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
+    };
+    if constexpr (WF == SF_NVFP4) {
+      const uint32_t f01 = nvfp4_fold_x2(v0 & 0xFFFFu), f23 = nvfp4_fold_x2(v0 >> 16);
+      const uint32_t f[4] = {prmt(f01, f01, 0x1010u), prmt(f01, f01, 0x3232u),
+                             prmt(f23, f23, 0x1010u), prmt(f23, f23, 0x3232u)};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t pq[4];
+        e2m1x8_kperm_folded(sw.w[j], f[j >> 1], pq);
+        put(j, pq);
+      }
+    } else {
+      const uint32_t c0 = v0 & 0xFFu, c1 = (v0 >> 8) & 0xFFu;
+      if (__all_sync(0xffffffffu, c0 <= 128u && c1 <= 128u)) {
+        const uint32_t f0 = mxfp4_fold(c0), f1 = mxfp4_fold(c1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t pq[4];
+          e2m1x8_kperm_folded(sw.w[j], j < 4 ? f0 : f1, pq);
+          put(j, pq);
+        }
+      } else {
+        const uint32_t s0 = e8m0_to_bf16x2(c0), s1 = e8m0_to_bf16x2(c1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t pq[4];
+          e2m1x8_kperm(sw.w[j], j < 4 ? s0 : s1, pq);
+          put(j, pq);
+        }
+      }
     }
   }
 }

@@ -118,3 +118,42 @@ def test_prefill_formats_deterministic(qg, fmt):
     Wd = quantized(fmt, N, K, seed=9)
     x = inputs.activations_bf16(M, K, seed=10)
     assert np.array_equal(run_gpu(qg, fmt, Wd, x, M, N, K), run_gpu(qg, fmt, Wd, x, M, N, K))
+
+
+@pytest.mark.parametrize("M", [40, 600])
+def test_prefill_mxfp4_block_scales_across_the_code_range(qg, M):
+    """MXFP4 rows whose block codes exceed 128 (the dequant warp holding them
+    takes the two-multiply decode for the slab) next to rows of small codes
+    (the folded single multiply): both give the canonical weights."""
+    N, K = 384, 1024
+    r = np.random.Generator(np.random.PCG64(M + 90))
+    w = inputs.weights_f32(N, K, seed=M + 91)
+    row_exp = r.integers(-60, 1, N).astype(np.float32)
+    row_exp[:32] = 40.0                      # one dequant warp's 32 rows: every code > 128
+    row_exp[200] = 20.0                      # one row of another warp
+    w = (w * np.exp2(row_exp)[:, None]).astype(np.float32)
+    q, se = OQ.quant_mxfp4_weights(w)
+    Wd = dict(q=q, s=se, deq=OG.dequant_mxfp4(q, se), epi=None)
+    x = inputs.activations_bf16(M, K, seed=M + 92)
+    y = run_gpu(qg, "mxfp4", Wd, x, M, N, K)
+    ref, _ = wo_reference(Wd, x)
+    unit = np.exp2(-row_exp)[None, :]
+    check_gemm(y * unit, ref * unit, "mxfp4 prefill scale range M=%d" % M)
+
+
+@pytest.mark.parametrize("M", [40, 600])
+def test_prefill_nvfp4_every_finite_block_scale_code(qg, M):
+    """NVFP4 with block scales over every finite E4M3 code: the folded decode
+    (weights times 2^-9, the row times 2^9 with the global scale) against the
+    canonical product."""
+    N, K = 256, 2048
+    r = np.random.Generator(np.random.PCG64(M + 93))
+    q = r.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    sb = r.integers(0, 0x7F, (N, K // 16)).astype(np.uint8)
+    sb[0, :0x7F] = np.arange(0x7F, dtype=np.uint8)
+    gs = np.float32(1.5)
+    Wd = dict(q=q, s=sb, gs=gs, deq=OG.dequant_nvfp4(q, sb), epi=np.full(N, float(gs)))
+    x = inputs.activations_bf16(M, K, seed=M + 94)
+    y = run_gpu(qg, "nvfp4", Wd, x, M, N, K)
+    ref, _ = wo_reference(Wd, x)
+    check_gemm(y, ref, "nvfp4 prefill all scale codes M=%d" % M)
