@@ -339,8 +339,8 @@ QG_API void qg_set_wait_limit(uint32_t iterations);
 
 /* Measurement aid, not part of the method: a plain streaming read of `bytes`
  * bytes at p (16-byte non-allocating loads, grid-stride over 8 CTAs per SM),
- * the rate one launch of that size reaches on this GPU -- the ceiling against
- * which a single decode launch of the same bytes is judged.  p 16-byte
+ * the rate one launch of that size reaches on this GPU -- the ceiling a
+ * single decode launch of the same bytes is compared with.  p 16-byte
  * aligned, bytes a positive multiple of 16, sink one 4-byte device word that
  * the kernel may write.                                                      */
 QG_API qg_status qg_stream_read(const void* p, long long bytes, unsigned int* sink,
