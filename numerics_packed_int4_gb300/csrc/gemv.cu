@@ -11,12 +11,12 @@
 //     reduced through distributed shared memory -- no global scratch, no
 //     atomics, deterministic.
 //   * Each warp streams the packed words of its two rows per lane (g and g+8
-//     of the mma group) through a private kRing-deep cp.async.cg ring in
+//     of the mma group) through a private 4- to 6-deep cp.async.cg ring in
 //     shared memory (16-byte, L1-bypassing), and decodes them in registers
 //     into mma.sync m16n8k16 A fragments (weights are the M = 16 side,
 //     activations the N = 8 side, so one mma covers 256 weights).
 //   * The activation slice is staged once per CTA in shared memory with the k
-//     order permuted to match the decode's pair order and a bank swizzle.
+//     order permuted to match the decode's pair order, one pad chunk per 8.
 //   * Programmatic dependent launch: a CTA triggers its dependent at once,
 //     issues its weight prologue, and waits for the previous kernel only
 //     before it reads X (weights and scales must not be the previous decode
@@ -43,9 +43,16 @@ constexpr bool fp8_weights(int f) { return f == F_FP8 || f == F_FP8A8; }
 constexpr int kActBlock = 128;         // F_FP8A8: activation quantization block (1 x 128)
 
 constexpr int kWarps = 8;
-constexpr int kRing = 6;               // weight segments in flight per warp (cp.async ring)
-constexpr int kPFS = 3;                // scale prefetch distance (segments); divides kRing
-static_assert(kRing % kPFS == 0, "the scale ring index u % kPFS must equal s % kPFS");
+// Weight segments in flight per warp (cp.async ring) and the scale prefetch
+// distance, per activation-tile count: with two 8-column tiles (M > 8) the
+// activation slice takes much of the shared memory, and a 4-deep ring leaves
+// room for more CTAs per SM (M = 16, INT4 14336x4096: 25.8 -> 18.5 us;
+// a 4-deep ring at M = 1 costs 10.0 -> 11.4 us).
+template <int MT> struct RingCfg {
+  static constexpr int RING = MT == 2 ? 4 : 6;
+  static constexpr int PFS = MT == 2 ? 2 : 3;   // divides RING
+  static_assert(RING % PFS == 0, "the scale ring index u % PFS must equal s % PFS");
+};
 
 template <int FMT> struct FmtTraits;
 template <> struct FmtTraits<F_INT4>  { static constexpr int KSEG = 128, CPL = 4; };
@@ -200,6 +207,7 @@ QG_DEVICE float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
 template <int FMT, int MT, bool G1>
 __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
   using Tr = FmtTraits<FMT>;
+  constexpr int kRing = RingCfg<MT>::RING, kPFS = RingCfg<MT>::PFS;
   extern __shared__ __align__(16) uint4 smem[];
   const int M = p.M;
   const int MP = MT * 8;
@@ -508,7 +516,7 @@ qg_status launch_gemv_t(const GemvArgs& a0, cudaStream_t st, const char* name) {
     while ((ncp & 7) != want) ++ncp;
     a.ncp = ncp;
     const size_t xsc_bytes = FMT == F_FP8A8 ? (size_t)a.M * (nseg_max * Tr::KSEG / kActBlock + 2) * 8 : 0;
-    return (size_t)kWarps * kRing * 64 * 16 + (size_t)a.M * ncp * 16 +
+    return (size_t)kWarps * RingCfg<MT>::RING * 64 * 16 + (size_t)a.M * ncp * 16 +
            (size_t)(kWarps * 16 + 16 * rg) * MT * 8 * 4 + xsc_bytes;
   };
   // K split over a cluster only when the activation slice does not fit
