@@ -519,9 +519,14 @@ qg_status launch_gemv_t(const GemvArgs& a0, cudaStream_t st, const char* name) {
     return (size_t)kWarps * RingCfg<MT>::RING * 64 * 16 + (size_t)a.M * ncp * 16 +
            (size_t)(kWarps * 16 + 16 * rg) * MT * 8 * 4 + xsc_bytes;
   };
-  // K split over a cluster only when the activation slice does not fit
+  // K split over a cluster when the activation slice would leave room for
+  // only one CTA per SM: for one activation tile (M <= 8) above 96 KB of
+  // shared memory (M = 4, K = 14336: 13.7 -> 12.6 us INT4, 16.8 -> 14.8 us
+  // FP8), for two tiles only when it does not fit (a split there costs more
+  // than it gains: M = 16 14336x4096 25.9 -> 38.1 us at a 96 KB target)
   int ks = 1;
-  while (smem_for(ks, 8) > 200 * 1024 && ks < 8) ks *= 2;
+  const size_t smem_target = MT == 1 ? 96 * 1024 : 200 * 1024;
+  while (smem_for(ks, 8) > smem_target && ks < 8) ks *= 2;
   if (smem_for(ks, 8) > 220 * 1024)
     return set_error(QG_ERR_UNSUPPORTED_SHAPE, "%s: activation slice too large for one CTA", name);
   // rows per CTA: the fewest that keep every CTA resident in one wave
