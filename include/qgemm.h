@@ -100,8 +100,8 @@ QG_API qg_status qgemm_w4a16_zp(const uint8_t* w_q, const uint16_t* w_s, const u
 
 /* FP8 E4M3 weights with one fp32 scale per output channel.
  * y[m,n] = w_cs[n] * sum_k x[m,k] * e4m3(w[n,k]); the E4M3 -> bf16 decode is
- * exact ("Every E4M3 and E2M1 value is exactly representable in FP16/BF16",
- * "Your 3090 Isn't Missing Anything...", section 4.1).
+ * exact: every E4M3 (and E2M1) value has an exact 16-bit float form
+ * ("Your 3090 Isn't Missing Anything...", section 4.1).
  *   w_e4m3 [N][K] u8    w_cs [N] fp32                                      */
 QG_API qg_status qgemm_w8a16(const uint8_t* w_e4m3, const float* w_cs,
                       const uint16_t* x, uint16_t* y, int M, int N, int K,
@@ -247,8 +247,9 @@ QG_API qg_status qg_w4a8_fp8_scales(const uint16_t* w_s, uint8_t* w_s8, float* w
 
 /* INT4 round-to-nearest, s = bf16_RNE(absmax/7) per group (fp32 division),
  * q = clamp(rint(w/s), -8, 7); an all-zero group (or a scale that rounds to
- * zero) gets s = 1, q = 0 ("Numerics": symmetric scale from a live amax,
- * "Define an all-zero-group policy such as s=1").  K % g == 0, g % 8 == 0. */
+ * zero) gets s = 1, q = 0 ("Numerics": symmetric scale from a live amax;
+ * the page asks for an explicit all-zero-group rule and names s = 1).
+ * K % g == 0, g % 8 == 0.                                                    */
 QG_API qg_status qg_quantize_weights_int4(const float* w, uint8_t* w_q, uint16_t* w_s, int g,
                                    int N, int K, qg_stream_t stream);
 /* Asymmetric INT4 with zero points, one per group of g (the reading of

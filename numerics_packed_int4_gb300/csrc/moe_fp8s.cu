@@ -16,7 +16,7 @@
 // prmt(N, nibble ^ 8) is N[j] or 0xFF; a third permute of the constant 0x55
 // times 3 gives the 0xFF byte mask of the negative nibbles, and one lop3
 // merges.  fp32 accumulation; the per-token and per-channel scales are
-// applied in the epilogue ("outer vector scaling").
+// applied in the epilogue (the page's outer-vector scaling step).
 //
 // tcgen05.mma.cta_group::1.kind::f8f6f4, E4M3 x E4M3, M = 128 channels,
 // N = 256 activation rows, K = 32:

@@ -9,9 +9,9 @@ elements per byte along K, even k in the low nibble.
 Canonical dequantized weights (bf16 bit patterns, the bit-exact targets):
 * INT4:  bf16_RNE(q * s).  The fp32 product is exact (a 4-bit integer times
   an 8-bit significand), so there is exactly one rounding.  This is the
-  "dequantize INT4 weights to BF16, then run the matmul in BF16" recipe of
-  the Cohere W4A8 article and the in-register dequant of the 3090 article
-  (section 4.1).
+  Cohere W4A8 article's recipe (INT4 weights turned into BF16 on the CUDA
+  cores, the product taken in BF16) and the in-register dequant of the 3090
+  article (section 4.1).
 * FP8:   the E4M3 value in bf16 (exact; "Every E4M3 and E2M1 value is exactly
   representable in FP16/BF16").  The fp32 channel scale is applied to the
   accumulated row in the epilogue.

@@ -134,7 +134,7 @@ def fp8_block_scale(amax):
     """scale = amax / 448 in fp32; an all-zero block gets scale 1.0.
 
     "Numerics" page, fp8 linear walk-through step 1 (amax -> fp32 -> / 448),
-    and "Define an all-zero-group policy such as s=1".  The unstated minimum
+    which asks for an explicit all-zero-group rule and names s = 1.  The unstated minimum
     clamp (_FP8_MIN_SCALING_FACTOR) is not applied.
     """
     a = np.asarray(amax, dtype=F32)
@@ -187,7 +187,7 @@ def fp8_group_scales(s_bits):
 def fp8_lut_weights(packed, s8_codes, g=128):
     """Weights of the W4A8 FP8 matmul: E4M3(q * s8) for every INT4 value q
     and its group's FP8 scale -- the contents of the page's per-scale lookup
-    table ("there are only 16 possible values of s * w"), one E4M3
+    table (a 4-bit q gives just 16 products s * w per scale), one E4M3
     round-to-nearest-even of the exact product.  Returns E4M3 codes [N, K]."""
     q = F.int4_decode(unpack_nibbles(packed)).astype(np.float64)
     s8 = F.e4m3_decode(s8_codes).astype(np.float64)
@@ -256,7 +256,7 @@ def quant_fp8_channel(w):
     """FP8 E4M3 with one fp32 scale per output channel (row of W [N, K]).
 
     Same arithmetic as the block quantizer with the block equal to the row
-    ("per-channel ... one scale per output column of the weight").
+    (per-channel: a single scale for each output channel of the weight).
     Returns (codes [N, K] uint8, cs [N] float32).
     """
     w = np.asarray(w, dtype=F32)

@@ -189,7 +189,8 @@ def test_e4m3_cast_page_values():
 
 
 def test_double_rounding_bug_is_not_reproduced():
-    """FreeToken PR #805: fp32 -RTZ-> fp16 -RNE-> e4m3 gives 192 for 200.04."""
+    """FreeToken PR #805: going through fp16 with truncation first, then E4M3
+    rounding, turns 200.04 into 192 (the double-rounding bug)."""
     x = np.float32(200.04)
     h = np.float16(x)
     rtz = h if abs(float(h)) <= float(x) else np.nextafter(h, np.float16(0))
