@@ -125,8 +125,8 @@ QG_API qg_status qgemm_w8a8(const uint8_t* w_e4m3, const float* w_cs, const uint
  *     power-of-two scale.)
  *  scale_fmt QG_SCALE_E4M3: NVFP4, g == 16, w_bs [N][K/16] E4M3 codes,
  *     canonical weight e2m1 * e4m3(sb) (exact); global_scale is a DEVICE
- *     pointer to one fp32 applied to the accumulated row ("decodes each
- *     16-value E2M1 weight block and its E4M3 scale to BF16", 3090 article
+ *     pointer to one fp32 applied to the accumulated row (each 16-value
+ *     E2M1 block and its E4M3 scale become BF16 before the MMA: 3090 article
  *     section 2.1).
  *   w_e2m1 [N][K/2] packed E2M1                                            */
 QG_API qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt,
@@ -140,8 +140,8 @@ QG_API qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int sc
  * exact in bf16 and every product exact in fp32, so the result is the one a
  * block-scaled FP4 MMA computes, up to the order of the fp32 additions.  The
  * activations are expanded into a_work (caller-owned bf16 [M][K]); the
- * product runs on the bf16 tensor-core path of qgemm_fp4a16 ("FP4 has 4x
- * [the BF16 ceiling]", 3090 article section 5, is not reached this way).
+ * product runs on the bf16 tensor-core path of qgemm_fp4a16, so the FP4
+ * tensor rate (four times bf16's, 3090 article section 5) is not reached.
  *   w_e2m1 [N][K/2]  w_e8m0 [N][K/32]  a_e2m1 [M][K/2]  a_e8m0 [M][K/32]
  *   a_work [M][K] bf16 (written)  y [M][N] bf16.  Rules as qgemm_fp4a16.     */
 QG_API qg_status qgemm_w4a4_mxfp4(const uint8_t* w_e2m1, const uint8_t* w_e8m0,
