@@ -176,3 +176,42 @@ def test_stream_read_measurement_aid(qg):
         qg.qg_stream_read(buf, nbytes, sink)
     qg.qg_check_device_error()
     assert int(sink.item()) == 0
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_decode_large_n_sampled_rows(qg, fmt):
+    """N = 65536, K = 4096 (well past one wave of CTAs) at M = 1 and 16:
+    seeded random codes and scales of each format (no quantizer needed at
+    this size), parity on a seeded sample of 256 output channels, every
+    output finite."""
+    N, K = 65536, 4096
+    r = np.random.Generator(np.random.PCG64(123))
+    if fmt == "fp8":
+        q = r.integers(0, 0x7F, (N, K)).astype(np.uint8) | (r.integers(0, 2, (N, K)) << 7).astype(np.uint8)
+        q[(q & 0x7F) == 0x7F] = 0x30                                  # no NaN codes
+    else:
+        q = r.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    if fmt == "int4":
+        s = OF.bf16_encode((r.uniform(0.5, 2.0, (N, K // 128)) * 0.003).astype(np.float32))
+    elif fmt == "fp8":
+        s = (r.uniform(0.5, 2.0, N) * 0.001).astype(np.float32)
+    elif fmt == "mxfp4":
+        s = r.integers(117, 124, (N, K // 32)).astype(np.uint8)
+    else:
+        s = r.integers(0x20, 0x50, (N, K // 16)).astype(np.uint8)
+    cols = np.sort(r.choice(N, 256, replace=False))
+    if fmt == "int4":
+        Wd = dict(q=q, s=s, deq=OG.dequant_int4(q[cols], s[cols], 128), epi=None)
+    elif fmt == "fp8":
+        Wd = dict(q=q, s=s, deq=OG.dequant_fp8(q[cols]), epi=s[cols].astype(np.float64))
+    elif fmt == "mxfp4":
+        Wd = dict(q=q, s=s, deq=OG.dequant_mxfp4(q[cols], s[cols]), epi=None)
+    else:
+        gs = np.float32(0.01)
+        Wd = dict(q=q, s=s, gs=gs, deq=OG.dequant_nvfp4(q[cols], s[cols]), epi=np.full(len(cols), float(gs)))
+    for M in (1, 16):
+        x = inputs.activations_bf16(M, K, seed=125 + M)
+        y = run_gpu(qg, fmt, Wd, x, M, N, K)
+        assert np.all(np.isfinite(y))
+        ref, _ = reference(Wd, x)
+        check_gemm(y[:, cols], ref, "%s large N M=%d" % (fmt, M))
