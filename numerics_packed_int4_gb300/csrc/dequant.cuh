@@ -117,16 +117,6 @@ QG_DEVICE void int4x8_nat_f16(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {
     p[b] = f16x2_mul(f16x2_sub(lop3<kLutAndXor>(t, 0x000F000Fu, 0x64086408u), 0x64086408u), s2);
   }
 }
-// INT4 nibbles -> fp16 pairs (k_i, k_{i+4}) = q * scale: (1024 + (nib ^ 8)) - 1032
-// is the exact integer q, one fp16 multiply forms the exact product.
-QG_DEVICE void int4x8_kperm_f16(uint32_t v, uint32_t s2, uint32_t (&p)[4]) {
-  p[0] = lop3<kLutAndXor>(v, 0x000F000Fu, 0x64086408u);
-  p[1] = lop3<kLutAndXor>(v >> 4, 0x000F000Fu, 0x64086408u);
-  p[2] = lop3<kLutAndXor>(v >> 8, 0x000F000Fu, 0x64086408u);
-  p[3] = lop3<kLutAndXor>(v >> 12, 0x000F000Fu, 0x64086408u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = f16x2_mul(f16x2_sub(p[i], 0x64086408u), s2);
-}
 
 // ---- E2M1 -------------------------------------------------------------------
 // p[i] = (k_i, k_{i+4}) for i = 0..3, each e2m1 * scale (exact)

@@ -94,20 +94,6 @@ QG_DEVICE void load_slab_words(const uint8_t* wrow, int row, SlabWords<WF>& sw) 
   }
 }
 
-// Slab words from a stage of 128-byte rows in the 128-byte swizzle (16-byte
-// chunk c of row r at c ^ (r & 7)) that holds 128 / (slab bytes) consecutive
-// slabs per row; 'sub' selects the slab.
-template <int WF>
-QG_DEVICE void load_slab_words_sw128(const uint8_t* row128, int row, int sub, SlabWords<WF>& sw) {
-  constexpr int kChunks = WF == SF_FP8 ? 4 : 2;               // 16-byte chunks per slab
-  const int x = row & 7;
-#pragma unroll
-  for (int c = 0; c < kChunks; ++c) {
-    const uint4 w4 = *reinterpret_cast<const uint4*>(row128 + 16 * ((sub * kChunks + c) ^ x));
-    sw.w[4 * c] = w4.x; sw.w[4 * c + 1] = w4.y; sw.w[4 * c + 2] = w4.z; sw.w[4 * c + 3] = w4.w;
-  }
-}
-
 // Decode a slab's words: out[i] = (k_2i, k_2i+1) in bf16.  The FP4 block
 // scales are folded into the E2M1 decode (dequant.cuh): NVFP4 weights come out
 // times 2^-9 exactly (the caller multiplies the accumulated row by
