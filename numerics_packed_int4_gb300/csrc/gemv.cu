@@ -6,10 +6,10 @@
 //   * A CTA of 8 warps owns rg 16-row groups (16 * rg output channels); the
 //     kWarps / rg warps of a row group take interleaved K segments and their
 //     partial sums are reduced through shared memory.  The grid is sized to
-//     a single wave.  When the activation slice would not fit in shared
-//     memory, the K range is split over a thread-block cluster (1..8 CTAs)
-//     reduced through distributed shared memory -- no global scratch, no
-//     atomics, deterministic.
+//     a single wave.  When the activation slice would leave room for only one
+//     CTA per SM (M <= 8) or would not fit (M > 8), the K range is split over
+//     a thread-block cluster (1..8 CTAs) reduced through distributed shared
+//     memory -- no global scratch, no atomics, deterministic.
 //   * Each warp streams the packed words of its two rows per lane (g and g+8
 //     of the mma group) through a private 4- to 6-deep cp.async.cg ring in
 //     shared memory (16-byte, L1-bypassing), and decodes them in registers
@@ -21,6 +21,9 @@
 //     issues its weight prologue, and waits for the previous kernel only
 //     before it reads X (weights and scales must not be the previous decode
 //     kernel's output -- stated in the header).
+//   * FP4 block scales are folded into the E2M1 decode (one multiply per
+//     pair; dequant.cuh), the NVFP4 weights then carrying 2^-9, undone with
+//     the global scale.
 //   * fp32 accumulation; the FP8 channel scale / NVFP4 global scale is
 //     applied to the reduced row; one bf16 rounding at the store.
 //   * W8A8 (FP8 weights, activations quantized here): the prologue quantizes
