@@ -154,3 +154,34 @@ def test_stream_read_argument_validation(lib):
     assert _rc(lib, "qg_stream_read", FAKE, 1000, FAKE) == 2
     assert _rc(lib, "qg_stream_read", FAKE, 0, FAKE) == 2
     assert _rc(lib, "qg_stream_read", FAKE_MIS, 1024, FAKE) == 3
+
+
+def _bf16_round(x):
+    """float64 -> nearest bf16 value (ties to even), as float64."""
+    from oracle import formats as F
+    return F.bf16_decode(F.bf16_encode(np.asarray(x, np.float32)))
+
+
+def test_folded_fp4_decode_is_exact_for_every_code():
+    """The decode kernels form an E2M1 weight with one bf16 multiply of its
+    bit pattern (value x 2^-126, the 0.5 code a bf16 subnormal) by a folded
+    factor: NVFP4 2^117 x e4m3(sb), MXFP4 2^(c-1) for E8M0 codes c <= 128.
+    Emulated here with IEEE arithmetic over every E2M1 code and every finite
+    scale code: the one rounding never changes the value, so the NVFP4 weight
+    is exactly 2^-9 times the canonical one and the MXFP4 weight is exact."""
+    from oracle import formats as F
+    e2m1 = F.e2m1_decode(np.arange(16)).astype(np.float64)
+    raw = e2m1 * 2.0 ** -126                               # the bit pattern's value
+    assert np.array_equal(_bf16_round(raw), raw)           # representable (subnormal for 0.5)
+    sb = np.array([c for c in range(256) if (c & 0x7F) != 0x7F])
+    e4m3 = F.e4m3_decode(sb).astype(np.float64)
+    fold = _bf16_round(e4m3 * 2.0 ** 117)
+    assert np.array_equal(fold, e4m3 * 2.0 ** 117)          # the factor is exact
+    assert np.all(np.abs(fold[fold != 0]) >= 2.0 ** -126)  # and normal
+    prod = _bf16_round(raw[:, None] * fold[None, :])
+    assert np.array_equal(prod, e2m1[:, None] * e4m3[None, :] * 2.0 ** -9)
+    c = np.arange(0, 129)
+    f = _bf16_round(2.0 ** (c - 1.0))
+    assert np.array_equal(f, 2.0 ** (c - 1.0))
+    prod = _bf16_round(raw[:, None] * f[None, :])
+    assert np.array_equal(prod, e2m1[:, None] * 2.0 ** (c[None, :] - 127.0))
