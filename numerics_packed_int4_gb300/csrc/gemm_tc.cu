@@ -16,7 +16,7 @@
 //     shared memory in the 128-byte swizzled K-major layout.
 //   * D = fp32 accumulator in tensor memory, 128 lanes x 256 columns.
 // Persistent: one CTA per SM walks the tiles blockIdx.x, + gridDim.x, ... of
-// 256 tokens x 128 channels (grouped raster: 2 token tiles per group), and
+// 256 tokens x 128 channels (raster: every channel tile of a token tile in turn), and
 // every role counts the k-slabs of all its tiles in one sequence, so the
 // rings simply continue from one tile into the next.
 //   warp 0      TMA producer for the activations (one elected lane)
@@ -456,7 +456,7 @@ qg_status prefill_tc(int wf, const uint8_t* w_q, const void* w_s, const uint8_t*
   while ((1 << a.lg) < g) ++a.lg;
   a.tiles_t = (M + kTileT - 1) / kTileT;
   a.tiles_w = (N + kTileW - 1) / kTileW;
-  a.group_t = 2;          // token tiles per raster group (8 / 4 / 2 measured 1673 / 1690 / 1705 TFLOP/s)
+  a.group_t = 1;          // token tiles per raster group (8 / 4 / 2 / 1: 1673 / 1690 / 1705 / 1705+ TFLOP/s)
   a.err = err;
   a.cap = wait_limit();
   const int stages = wf == SF_FP8 ? PfTraits<SF_FP8>::STAGES : PfTraits<SF_INT4>::STAGES;
