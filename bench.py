@@ -13,8 +13,14 @@ One step = one pass over every row of the hot path at its workload size:
                  M = 8192 prefill over the same three (N, K)
   W8A8 GEMV      FP8 weights, activations quantized per 1 x 128 block inside the
                  GEMV prologue: M = 1 over the same three (N, K)
-Each row is one CUDA graph; CUDA events between the graphs time every row
-inside the timed region.  The headline value is the metric's first quantity:
+  prefill, other weights  M = 8192 over the same three (N, K) with FP8
+                 per-channel, MXFP4 and NVFP4 weights
+  (opt-in) W4A4  MXFP4 activations (quantized in the step) x MXFP4 weights
+Each row is one CUDA graph (the MoE rows five, so that their grouped GEMMs --
+the step's dominant kernel -- are timed on their own); CUDA events between
+the graphs time every row inside the timed region.  After the timed region the
+M = 1 row's single-launch read ceiling is measured (a plain streaming read of
+the same 12 weight matrices, one launch each).  The headline value is the metric's first quantity:
 effective HBM GB/s of the M = 1 GEMVs (algorithmic bytes / time); the
 M = 8192 TFLOP/s is reported beside it.  Inputs are seeded synthetic data
 (weights N(0, 0.02), activations N(0, 1)), resident in HBM before timing; the
