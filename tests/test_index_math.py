@@ -61,3 +61,42 @@ def tile_origin(tile, tiles_t, tiles_w, group_t):
 def test_prefill_raster_covers_every_tile_once(group_t, tiles_t, tiles_w):
     seen = {tile_origin(i, tiles_t, tiles_w, group_t) for i in range(tiles_t * tiles_w)}
     assert seen == {(a, b) for a in range(tiles_t) for b in range(tiles_w)}
+
+
+@pytest.mark.parametrize("nseg", [1, 4, 7, 8, 32, 112, 224])
+@pytest.mark.parametrize("ks", [1, 2, 4, 8])
+@pytest.mark.parametrize("kw", [1, 2, 4, 8])
+def test_gemv_k_split_partitions_the_segments(nseg, ks, kw):
+    """K segments split over the ks CTAs of a cluster, then over the kw warps
+    of a row group (the GEMV's seg_lo/seg_hi and s_lo/s_hi): every segment
+    exactly once, in order."""
+    got = []
+    for kr in range(ks):
+        seg_lo, seg_hi = nseg * kr // ks, nseg * (kr + 1) // ks
+        n_cta = seg_hi - seg_lo
+        for w in range(kw):
+            s_lo, s_hi = n_cta * w // kw, n_cta * (w + 1) // kw
+            got.extend(seg_lo + s for s in range(s_lo, s_hi))
+    assert got == list(range(nseg))
+
+
+@pytest.mark.parametrize("rows_cta", [16, 32, 64, 128])
+@pytest.mark.parametrize("ks", [1, 2, 4, 8])
+def test_gemv_cluster_epilogue_rows(rows_cta, ks):
+    """Each CTA of a cluster finishes rows_cta / ks rows of the shared tile:
+    together every row once."""
+    rows_per = rows_cta // ks
+    got = sorted(kr * rows_per + r for kr in range(ks) for r in range(rows_per))
+    assert got == list(range(rows_cta))
+
+
+@pytest.mark.parametrize("ntiles_total", [1, 112, 151, 152, 153, 448, 1024])
+def test_persistent_tile_lists_cover_every_tile(ntiles_total):
+    """Persistent kernels: CTA b of a grid of min(tiles, 152) takes tiles
+    b, b + grid, ...; the count each CTA computes for itself adds up."""
+    grid = min(ntiles_total, 152)
+    got = []
+    for b in range(grid):
+        ntiles = (ntiles_total - b + grid - 1) // grid
+        got.extend(b + i * grid for i in range(ntiles))
+    assert sorted(got) == list(range(ntiles_total))
