@@ -59,3 +59,21 @@ def test_single_process_defaults():
     import bench
     assert bench.dist_max(3.5, 1) == 3.5
     assert bench.aggregate(10.0, 4.0) == 2.5
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    """bench.py --impl reference runs the CPU oracle (no GPU needed) and
+    prints one JSON line with the contract's keys."""
+    import json
+
+    import bench
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "1"]) in (0, None)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "config", "impl", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "GB/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
