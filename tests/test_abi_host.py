@@ -185,3 +185,15 @@ def test_folded_fp4_decode_is_exact_for_every_code():
     assert np.array_equal(f, 2.0 ** (c - 1.0))
     prod = _bf16_round(raw[:, None] * f[None, :])
     assert np.array_equal(prod, e2m1[:, None] * 2.0 ** (c[None, :] - 127.0))
+
+
+def test_binding_argument_counts_match_the_header():
+    """Every ctypes signature in the binding has as many arguments as the
+    prototype in include/qgemm.h (a dropped or extra argument would shift
+    every pointer after it)."""
+    from numerics_packed_int4_gb300 import qgemm
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = dict(re.findall(r"QG_API\s+(?:const\s+char\s*\*|qg_status|void)\s+(\w+)\s*\(([^)]*)\)", src))
+    for name, argtypes in qgemm.SIGNATURES.items():
+        params = [p for p in protos[name].split(",") if p.strip() and p.strip() != "void"]
+        assert len(params) == len(argtypes), (name, len(params), len(argtypes))
