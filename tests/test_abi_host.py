@@ -194,6 +194,20 @@ def test_binding_argument_counts_match_the_header():
     from numerics_packed_int4_gb300 import qgemm
     src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
     protos = dict(re.findall(r"QG_API\s+(?:const\s+char\s*\*|qg_status|void)\s+(\w+)\s*\(([^)]*)\)", src))
+    def ctype_of(param):
+        p = param.strip()
+        if "*" in p or p.startswith("qg_stream_t"):
+            return ctypes.c_void_p
+        if p.startswith("long long"):
+            return ctypes.c_longlong
+        if p.startswith("uint32_t"):
+            return ctypes.c_uint32
+        if p.startswith("int "):
+            return ctypes.c_int
+        raise AssertionError("unexpected parameter type: " + p)
+
     for name, argtypes in qgemm.SIGNATURES.items():
         params = [p for p in protos[name].split(",") if p.strip() and p.strip() != "void"]
         assert len(params) == len(argtypes), (name, len(params), len(argtypes))
+        for prm, at in zip(params, argtypes):
+            assert ctype_of(prm) == at, (name, prm, at)
