@@ -149,6 +149,30 @@ QG_API qg_status qgemm_w4a4_mxfp4(const uint8_t* w_e2m1, const uint8_t* w_e8m0,
                            uint16_t* a_work, uint16_t* y, int M, int N, int K,
                            qg_stream_t stream);
 
+/* qgemm_w4a4_mxfp4 for callers that cannot allocate device memory; the pages
+ * have no counterpart of this entry point.  Plugin-style host interfaces that
+ * hand an op only its inputs and outputs, and runtimes that committed all
+ * device memory to their own pool (where cudaMalloc would fail, and where
+ * cudaMalloc/cudaFree could synchronise the device mid-loop), have no way to
+ * pass the a_work buffer.  Here the bf16 expansion of the activations goes to
+ * a fixed 16 MiB array compiled into the library (every GPU that loads the
+ * library holds it until the process exits), so the call allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *   Arguments and result as qgemm_w4a4_mxfp4, without a_work.
+ *   Limit: M * K <= 8388608 (16 MiB of bf16); larger sizes return
+ *   QG_ERR_UNSUPPORTED_SHAPE and launch nothing.
+ *   Set-up: the first call made with a given device current looks up the
+ *   array's device address (cudaGetSymbolAddress) and caches it; make that
+ *   first call before any stream capture.  A failed lookup returns QG_ERR_CUDA.
+ *   Sharing: every call on a device uses the same array, and it keeps the last
+ *   call's contents.  Nothing needs clearing (each call writes all the
+ *   elements it reads), but calls whose kernels overlap on the GPU -- e.g. on
+ *   two streams without an event between them -- race on the array and give
+ *   wrong results.  Calls on one stream are ordered and safe.                */
+QG_API qg_status qgemm_w4a4_mxfp4_noalloc(const uint8_t* w_e2m1, const uint8_t* w_e8m0,
+                                   const uint8_t* a_e2m1, const uint8_t* a_e8m0,
+                                   uint16_t* y, int M, int N, int K, qg_stream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * Online activation quantizers.  Rules: M >= 1, K % g == 0, K % 8 == 0.
  * ------------------------------------------------------------------------ */

@@ -211,3 +211,12 @@ def test_binding_argument_counts_match_the_header():
         assert len(params) == len(argtypes), (name, len(params), len(argtypes))
         for prm, at in zip(params, argtypes):
             assert ctype_of(prm) == at, (name, prm, at)
+
+
+def test_w4a4_noalloc_argument_validation(lib):
+    # (w_e2m1, w_e8m0, a_e2m1, a_e8m0, y, M, N, K, stream): sizes are checked
+    # before the work array is touched, so none of these needs a GPU
+    assert _rc(lib, "qgemm_w4a4_mxfp4_noalloc", FAKE, FAKE, FAKE, FAKE, FAKE, -1, 128, 128) == 1
+    assert _rc(lib, "qgemm_w4a4_mxfp4_noalloc", FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 0) == 1
+    assert _rc(lib, "qgemm_w4a4_mxfp4_noalloc", FAKE, FAKE, FAKE, FAKE, FAKE, 4097, 128, 2048) == 2
+    assert "static work area" in lib.qg_last_error_string().decode()
