@@ -12,9 +12,9 @@ Canonical dequantized weights (bf16 bit patterns, the bit-exact targets):
   Cohere W4A8 article's recipe (INT4 weights turned into BF16 on the CUDA
   cores, the product taken in BF16) and the in-register dequant of the 3090
   article (section 4.1).
-* FP8:   the E4M3 value in bf16 (exact; "Every E4M3 and E2M1 value is exactly
-  representable in FP16/BF16").  The fp32 channel scale is applied to the
-  accumulated row in the epilogue.
+* FP8:   the E4M3 value in bf16 (exact: the 3090 article, section 4.1, notes
+  that every E4M3 and E2M1 value has an exact 16-bit float form).  The fp32
+  channel scale is applied to the accumulated row in the epilogue.
 * MXFP4: bf16(e2m1 * 2**(c - 127)) -- exact for every code the quantizer
   emits (c <= 252).
 * NVFP4: bf16(e2m1 * e4m3(sb)) -- exact; the fp32 global scale is applied in
@@ -26,8 +26,11 @@ bf16_RNE(y64).  ("Numerics": accumulate wide, narrow once at the store.)
 
 Parity: the product is pinned by exact-arithmetic brute force on tiny inputs
 (fractions), the dequantizers by the format pins and brute force over codes.
-The MoE harness (routing use, SwiGLU, combine) is parity unpinned beyond the
-GEMM checks: its semantics are readings, not page facts.
+The MoE harness functions are readings (the pages name the steps but print no
+formulas); ``swiglu_f32`` and ``moe_combine`` are pinned by mathematics:
+SiLU(0) = 0, SiLU(v) - SiLU(-v) = v, the limits at +-inf, the Taylor value
+near 0, agreement with a library logistic routine, the gate/up order, and an
+exact-rational brute force of the weighted combine.
 """
 
 import numpy as np
@@ -202,6 +205,9 @@ def swiglu_f32(gate_up_bits, inter):
     ``_swiglu_kernel``, but give no formula): the first ``inter`` columns are
     the gate, the next ``inter`` the up projection; SiLU(v) = v / (1 + e^-v).
     Evaluated in float64 and rounded once to float32.
+    Pinned by mathematics: SiLU(0) = 0; SiLU(v) - SiLU(-v) = v (sigmoid(v) +
+    sigmoid(-v) = 1); SiLU(v) -> v and -> 0 at +-inf; the series x/2 + x^2/4
+    near 0; v * expit(v) from a library logistic routine; the gate half first.
     """
     gu = F.bf16_decode(gate_up_bits)
     gate, up = gu[:, :inter], gu[:, inter:2 * inter]
@@ -230,7 +236,13 @@ def moe_layer(x_bits, route_rows, expert_off, w1, w2, g, inter):
 
 
 def moe_combine(down_bits, route_rows, route_weight, T):
-    """out[t] = sum over t's rows of p * down (float64), one bf16 rounding."""
+    """out[t] = sum over t's rows of p * down (float64), one bf16 rounding.
+
+    Reading of the MoE harness: each token's output is the sum of its routed
+    rows' down projections weighted by their (not renormalised) routing
+    probabilities.  Pinned by an exact-rational brute force on dyadic inputs
+    (every product and partial sum exact), rounded once to bf16.
+    """
     d = F.bf16_decode(down_bits)
     out = np.zeros((T, d.shape[1]))
     np.add.at(out, np.asarray(route_rows), d * np.asarray(route_weight, np.float64)[:, None])

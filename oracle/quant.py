@@ -13,7 +13,8 @@ Parity status
   worked table of vLLM PR #43557 ("Root Cause": vecMax 2.7/5.5/1.2 -> 126/127/
   125) and by the clip-zone table ("Why This Helps Precision").
 * ``quant_mxfp4``: the scale rule above + the E2M1 cast (pinned in formats) +
-  the saturation statement "ratio in [6.0, 7.0) ... clips to 6.0".
+  the PR's saturation statement (a scaled element between 6 and 7 is clipped
+  to E2M1's largest value, 6).
 * ``quant_fp8_block``: the scale example "amax 22.4 -> scale 0.05 -> 448" and
   the E4M3 cast pins (200.04 -> 208, subnormal edges).
 * ``quant_int4_rtn``, ``quant_nvfp4``: parity unpinned beyond invariants (the
@@ -62,15 +63,20 @@ def unpack_nibbles(packed):
 def e8m0_scale_exp(vecMax):
     """Scale exponent for one MX block from the fp32 block maximum.
 
-    vLLM PR #43557, "Fix: Exponent-First with 0.75-Threshold Rounding": take
-    the fp32 bit pattern of vecMax, add 1<<21 (half of the top mantissa bit
-    after the two that E2M1 keeps), keep sign+exponent, read the biased
-    exponent, and subtract 2 (E2M1's largest binade is 2**2), clamping at 0.
+    vLLM PR #43557, "Fix: Exponent-First with 0.75-Threshold Rounding".  The
+    rule works on vecMax's binade: write vecMax = f * 2**E with the
+    significand f in [1, 2).  The exponent is rounded up to E + 1 when the
+    fraction part of f is at least 0.75 (f >= 1.75 -- the point where
+    adding half a unit of the third mantissa bit carries into the exponent),
+    and the scale is the biased result minus 2 (E2M1 tops out in the 2**2
+    binade), never below 0.  Formulated here with frexp in float64: frexp
+    gives vecMax = m * 2**e with m in [0.5, 1), so f = 2m and E = e - 1.
+    Subnormal and zero maxima have biased exponents <= 2 and clamp to 0.
     """
-    max_bits = F.bits_from_f32(np.asarray(vecMax, dtype=F32)).astype(np.uint64)
-    rounded_bits = (max_bits + (1 << 21)) & 0xFF800000
-    biased_exp = ((rounded_bits >> 23) & 0xFF).astype(np.int64)
-    return np.where(biased_exp > 2, biased_exp - 2, 0).astype(np.uint8)
+    v = np.asarray(vecMax, dtype=F32).astype(np.float64)
+    m, e = np.frexp(v)
+    biased = (e.astype(np.int64) - 1) + 127 + (2.0 * m >= 1.75)
+    return np.where((v > 0) & (biased > 2), biased - 2, 0).astype(np.uint8)
 
 
 def e8m0_scale_exp_old(vecMax):

@@ -708,3 +708,113 @@ def test_w4a4_commutes_with_power_of_two_activation_scaling(j):
     np.testing.assert_array_equal(aq1, aq0)
     np.testing.assert_array_equal(ase1.astype(int), ase0.astype(int) + j)
     np.testing.assert_array_equal(y1, np.ldexp(y0, j))
+
+
+# ----------------------------------------------------------------------------
+# MoE harness between the projections: SwiGLU and the weighted combine.
+# The pages name a fused SwiGLU kernel (FreeToken PR #805's list of native
+# kernels) but print no formula; these pins come from the mathematics of
+# SiLU(v) = v * sigmoid(v) and of an exact weighted sum.
+# ----------------------------------------------------------------------------
+
+def _gate_up(gate, up):
+    """[R, 2I] bf16 bit patterns with the gate columns first."""
+    return F.bf16_encode(np.concatenate([np.asarray(gate, np.float32), np.asarray(up, np.float32)], 1))
+
+
+def _bf16_grid(lo, hi):
+    """Every finite bf16 value in [lo, hi] (as float32)."""
+    v = F.bf16_decode(np.arange(65536, dtype=np.uint32)).astype(np.float64)
+    v = v[np.isfinite(v) & (v >= lo) & (v <= hi)]
+    return np.unique(v).astype(np.float32)
+
+
+def test_silu_at_zero_is_zero():
+    """SiLU(0) = 0 whatever the up value, and up = 0 zeroes any gate."""
+    up = np.array([[1.0, -3.0, 250.0, 2.0 ** -20]], np.float32)
+    h = G.swiglu_f32(_gate_up(np.zeros_like(up), up), 4)
+    assert np.all(h == 0)
+    h = G.swiglu_f32(_gate_up(np.array([[5.0, -5.0, 0.5, 100.0]], np.float32), np.zeros_like(up)), 4)
+    assert np.all(h == 0)
+
+
+def test_silu_odd_part_is_the_identity():
+    """sigmoid(v) + sigmoid(-v) = 1, so SiLU(v) - SiLU(-v) = v exactly.  Each
+    side is one fp32 rounding of the true value, so the fp32 difference is v
+    within half an ulp of each side, over every bf16 value in [-30, 30]."""
+    v = _bf16_grid(-30.0, 30.0)
+    ones = np.ones((1, v.size), np.float32)
+    hp = G.swiglu_f32(_gate_up(v[None, :], ones), v.size).astype(np.float64)[0]
+    hn = G.swiglu_f32(_gate_up(-v[None, :], ones), v.size).astype(np.float64)[0]
+    ulp = lambda a: np.spacing(np.abs(a).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs((hp - hn) - v) <= 0.5 * (ulp(hp) + ulp(hn)) * 1.0001)
+
+
+def test_silu_limits():
+    """SiLU(v) -> v as v -> +inf and -> 0 as v -> -inf: for v >= 40, e^-v <
+    2^-57 and the fp32 result is v itself; for v <= -40, |SiLU(v)| <= |v| e^v."""
+    v = _bf16_grid(40.0, 3.0e38)
+    v = v[:: max(1, v.size // 400)]
+    h = G.swiglu_f32(_gate_up(v[None, :], np.ones((1, v.size), np.float32)), v.size)[0]
+    assert np.array_equal(h, v)
+    n = -v[v <= 80.0]
+    h = G.swiglu_f32(_gate_up(n[None, :], np.ones((1, n.size), np.float32)), n.size)[0].astype(np.float64)
+    assert np.all(h <= 0) and np.all(np.abs(h) <= np.abs(n) * np.exp(n.astype(np.float64)) * 1.0001)
+
+
+@pytest.mark.parametrize("j", [10, 12, 16])
+def test_silu_taylor_point(j):
+    """Near 0, SiLU(x) = x/2 + x^2/4 - x^4/48 + ...  For x = 2^-j the quartic
+    term is below half an fp32 ulp of x/2, so the fp32 result is exactly
+    2^-(j+1) + 2^-(2j+2).  A sign error in the exponent gives x/2 - x^2/4, a
+    GELU-style gate x/2 + 0.399 x^2: both miss this value."""
+    x = np.float32(2.0 ** -j)
+    h = G.swiglu_f32(_gate_up([[x]], [[1.0]]), 1)[0, 0]
+    assert h == np.float32(2.0 ** -(j + 1) + 2.0 ** -(2 * j + 2))
+
+
+def test_silu_matches_the_logistic_routine():
+    """SiLU(v) = v * expit(v), with scipy's logistic function as the
+    independent routine (every bf16 value in [-60, 60], unit up)."""
+    special = pytest.importorskip("scipy.special")
+    v = _bf16_grid(-60.0, 60.0)
+    h = G.swiglu_f32(_gate_up(v[None, :], np.ones((1, v.size), np.float32)), v.size)[0]
+    ref = (v.astype(np.float64) * special.expit(v.astype(np.float64))).astype(np.float32)
+    assert np.array_equal(h, ref)
+
+
+def test_swiglu_takes_the_gate_from_the_first_half():
+    """gate = [50, 0], up = [3, 7]: SiLU(50) * 3 = 150 and SiLU(0) * 7 = 0.
+    With the halves swapped the row would be [SiLU(3) * 50, SiLU(7) * 0] =
+    [142.88.., 0]; with the up projection ignored, [50, 0]."""
+    h = G.swiglu_f32(_gate_up([[50.0, 0.0]], [[3.0, 7.0]]), 2)
+    assert h.tolist() == [[150.0, 0.0]]
+    # the product is formed in wide precision and rounded once: SiLU(v) * u
+    # with u = 3 for v where the fp32 SiLU times 3 would round differently
+    v = _bf16_grid(0.5, 8.0)
+    h = G.swiglu_f32(_gate_up(v[None, :], np.full((1, v.size), 3.0, np.float32)), v.size)[0]
+    ref = [float(Fraction(float(x)) * 3 / (1 + Fraction(np.exp(-np.float64(x))))) for x in v]
+    assert np.array_equal(h, np.array(ref, np.float64).astype(np.float32))
+
+
+def test_moe_combine_matches_exact_brute_force():
+    """out[t] = bf16(sum over the rows routed from t of p * down[row]): dyadic
+    rows and weights (every product and sum exact as a Fraction), rows in a
+    scrambled order, one token with no rows, weights not renormalised.  The
+    exact sum rounded once to bf16 (nearest, ties to even, by search) must be
+    the oracle's output; a dropped weight, a wrong row index or a second
+    rounding fails it."""
+    r = np.random.Generator(np.random.PCG64(23))
+    T, H, R = 5, 24, 8
+    route_rows = np.array([3, 0, 1, 3, 0, 4, 1, 3])           # token 2 gets no row
+    weight = r.integers(1, 64, R) / 64.0                       # dyadic, not summing to 1
+    down = F.bf16_encode((r.integers(-512, 512, (R, H)) / 8.0).astype(np.float32) +
+                         np.float32(2.0 ** -9))                # 13-bit values: bf16 rounds some
+    out = F.bf16_decode(G.moe_combine(down, route_rows, weight, T))
+    dv = F.bf16_decode(down)
+    for t in range(T):
+        for h in range(H):
+            acc = sum((Fraction(float(weight[i])) * Fraction(float(dv[i, h]))
+                       for i in range(R) if route_rows[i] == t), Fraction(0))
+            assert Fraction(float(out[t, h])) == _nearest_bf16_fraction(acc)
+    assert np.all(out[2] == 0)
