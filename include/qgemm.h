@@ -63,20 +63,27 @@ enum { QG_FMT_INT4 = 0, QG_FMT_FP8 = 1, QG_FMT_MXFP4 = 2, QG_FMT_NVFP4 = 3 };
  * Weight-only GEMM/GEMV (W x A16): Y = X . dequant(W)^T, fp32 accumulate.
  * M <= 16 runs the HBM-streaming decode kernel; larger M the prefill kernel.
  * Shape rules: M >= 1, N >= 1, N % 8 == 0, K % 128 == 0.
- * Stream overlap: the decode kernel is launched with programmatic dependent
- * launch.  It starts streaming its weights and scales while the previous
- * kernel in the stream may still be running, and waits for that kernel before
- * it reads X or writes Y.  Only the decode kernels allow this early start,
- * and they write nothing but Y, so the one rule for callers is: the weights
- * or scales of a decode call must not be the Y of the decode call enqueued
- * just before it.
+ * Stream overlap: the decode kernel (M <= 16) is launched with programmatic
+ * dependent launch.  It may start while kernels enqueued before it on the
+ * stream are still running or have not yet made their writes visible, and it
+ * reads its weights and scales (and the NVFP4 global scale) right away; only
+ * X is read after it has waited for the previous kernel to complete.  A decode
+ * kernel also lets the kernel after it start early, so in a chain of decode
+ * calls the early reads can reach back past several kernels.  Rule for
+ * callers: the weight, scale and global-scale buffers of a decode call must
+ * not be written by any kernel that is still queued or running when the call
+ * is enqueued.  Write them (weight quantizers, casts, copies by kernels), then
+ * synchronise the stream or device -- or have the host wait for an event
+ * recorded after the writes -- before the first decode call that reads them.
+ * Weights written once at load time satisfy this.  X may be the Y of the
+ * call just before (the wait covers it).
  * ------------------------------------------------------------------------ */
 
 /* INT4 weights with one bf16 scale per group of g along K.
- * Canonical weight: bf16_RNE(q * s) (one rounding of the exact product):
- * "Dequantize INT4 weights to BF16 using CUDA cores ... run the matrix
- * multiplication in BF16" (Production-Ready W4A8, "High-Performance W4A8
- * GEMM Kernel"); symmetric affine map with zero-point 0 ("Numerics", integer
+ * Canonical weight: bf16_RNE(q * s) (one rounding of the exact product): the
+ * W4A16 baseline of Production-Ready W4A8 ("High-Performance W4A8 GEMM
+ * Kernel") turns the INT4 weights into BF16 on the CUDA cores and multiplies
+ * in BF16; symmetric affine map with zero-point 0 ("Numerics", integer
  * formats paragraph).
  *   w_q [N][K/2]  packed INT4        w_s [N][K/g] bf16
  *   x   [M][K]    bf16               y   [M][N]   bf16 (written)
@@ -315,10 +322,14 @@ QG_API qg_status qg_moe_gather_fp8_f16(const uint8_t* src_q, const float* src_s,
                                 const int32_t* route_rows, uint16_t* dst_f16, float* dst_s,
                                 int R, int T, int K, qg_stream_t stream);
 /* h = SiLU(gate) * up in fp32 from the bf16 projection output [R][2I] (gate
- * columns first), then the per-row FP8 quantizer (block = I): s as
- * quant_act_fp8_block, codes of h * (1/s).  SiLU uses the fast exponential
- * and division, so h is good to a few fp32 ulps and the codes to one E4M3
- * step where h / s lies that close to a rounding boundary.
+ * columns first), then the per-row FP8 quantizer of quant_act_fp8_block
+ * (block = I: s = amax/448, codes E4M3_RNE_satfinite(h / s) with IEEE
+ * division).  h = (gate * up) / (1 + exp(-gate)) with the exact bf16 product,
+ * CUDA's accurate expf, the sum 1 + e kept in two floats and one remainder
+ * correction of the quotient, so h is within a few fp32 ulps of the exact
+ * value (about half an ulp where expf's error does not reach it): a code can
+ * differ from the correctly rounded h's code only where h / s lies that close
+ * to an E4M3 rounding boundary.
  *   gate_up [R][2I] bf16 -> q [R][I] E4M3, s [R] fp32.  I % 8 == 0.          */
 QG_API qg_status qg_swiglu_quant_fp8(const uint16_t* gate_up, uint8_t* q, float* s,
                               int R, int I, qg_stream_t stream);

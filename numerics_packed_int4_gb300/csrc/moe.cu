@@ -109,7 +109,9 @@ __global__ void __launch_bounds__(kThreadsMoe) moe_w4a8_kernel(const MoeArgs p) 
   // ---- which expert / row tile is this CTA? ---------------------------------
   int tile = blockIdx.x, e = -1, r0 = 0, r_end = 0;
   for (int i = 0; i < p.E; ++i) {
-    const int a = p.off[i], b = p.off[i + 1];
+    // offsets come from device memory: clamp them into [0, R] (and b >= a)
+    // so that a malformed expert_off can never move a row outside A or y
+    const int a = min(max(p.off[i], 0), p.R), b = min(max(p.off[i + 1], a), p.R);
     const int nt = b > a ? (b - a + BM - 1) / BM : 0;
     if (tile < nt) { e = i; r0 = a + tile * BM; r_end = b; break; }
     tile -= nt;
@@ -213,14 +215,6 @@ __global__ void __launch_bounds__(kThreadsMoe) moe_w4a8_kernel(const MoeArgs p) 
 }  // namespace
 }  // namespace qg
 
-namespace qg {
-qg_status moe_w4a8_tc(const uint8_t* a_e4m3, const float* a_s, const int32_t* expert_off, const uint8_t* w_q,
-                      const uint16_t* w_s, uint16_t* y, int R, int E, int N, int K, cudaStream_t st);
-// rows at which the tensor-core kernel (256-row tiles) takes over from the
-// 64-row mma.sync tiles
-constexpr int kMoeTcMinRows = 512;
-}  // namespace qg
-
 extern "C" qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s, const int32_t* expert_off,
                                         const uint8_t* w_q, const uint16_t* w_s, int g, uint16_t* y, int R,
                                         int E, int N, int K, qg_stream_t stream) {
@@ -232,9 +226,6 @@ extern "C" qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,
   QG_REQUIRE(qg::aligned16(a_e4m3) && qg::aligned16(w_q) && qg::aligned16(y) && qg::aligned16(w_s),
              QG_ERR_MISALIGNED, "qgemm_w4a8_grouped: misaligned pointer");
   if (R == 0) return QG_OK;
-  if (R >= qg::kMoeTcMinRows)
-    return qg::moe_w4a8_tc(a_e4m3, a_s, expert_off, w_q, w_s, y, R, E, N, K,
-                           reinterpret_cast<cudaStream_t>(stream));
   qg::MoeArgs p{a_e4m3, a_s, expert_off, w_q, w_s, y, R, E, N, K};
   const size_t smem = (size_t)(2 * qg::BM + 2 * qg::BN) * qg::LDS * 2;
   if (!qg::ensure_smem(qg::moe_w4a8_kernel, (int)smem))

@@ -50,24 +50,15 @@ QG_DEVICE uint2 fp8_codes8(const float (&v)[8], float s) {
     c[i] = f32x2_to_e4m3x2(__fdiv_rn(v[2 * i + 1], s), __fdiv_rn(v[2 * i], s));
   return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
-// The same codes of v * rs with rs = 1/s: within an fp32 ulp of v / s, which
-// moves a code only when v / s sits that close to an E4M3 rounding boundary.
-// For values that are themselves only good to a few ulps (the fast-SiLU
-// output of the MoE harness) this is as exact as the division.
-QG_DEVICE uint2 fp8_codes8_rcp(const float (&v)[8], float rs) {
-  uint32_t c[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) c[i] = f32x2_to_e4m3x2(v[2 * i + 1] * rs, v[2 * i] * rs);
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
-
 // ---- MXFP4 block step -----------------------------------------------------------
-// Exponent-first 0.75-threshold rule (vLLM PR #43557, "Fix").
+// Exponent-first 0.75-threshold rule (vLLM PR #43557, "Fix"): take vecMax's
+// exponent field, step it up by one when the significand is at least 1.75
+// (its two leading fraction bits both set), then subtract E2M1's top binade
+// (2) and clamp at 0.  vecMax >= 0 here (a maximum of magnitudes).
 QG_DEVICE uint32_t e8m0_scale_exp(float vecMax) {
-  const uint32_t max_bits = __float_as_uint(vecMax);
-  const uint32_t rounded_bits = (max_bits + (1u << 21)) & 0xFF800000u;
-  const uint32_t biased_exp = (rounded_bits >> 23) & 0xFFu;
-  return biased_exp > 2u ? biased_exp - 2u : 0u;
+  const uint32_t u = __float_as_uint(vecMax);
+  const uint32_t e = ((u >> 23) & 0xFFu) + (((u >> 21) & 3u) == 3u ? 1u : 0u);
+  return e > 2u ? e - 2u : 0u;
 }
 
 QG_DEVICE uint32_t e2m1_codes8(const float (&v)[8], float mul) {
@@ -328,16 +319,36 @@ QG_DEVICE void store_codes8(void* q, long long o, uint2 codes) {
   else *reinterpret_cast<uint2*>(static_cast<uint8_t*>(q) + o) = codes;
 }
 
-// SiLU(g) * u in fp32 with the fast exponential and division intrinsics: the
-// value is quantized to E4M3 (3 mantissa bits) right after, so their few-ulp
-// error is far below the code spacing.  g -> -inf gives 1 + e^-g = inf and
-// g / inf = 0; g -> +inf gives g / 1.
+// h = SiLU(g) * u = (g * u) / (1 + e^-g) in fp32.  g and u are bf16, so
+// p = g * u (16 significant bits) is exact.  The exponential is CUDA's accurate
+// expf (not the fast intrinsic).  d = 1 + e is kept as an unevaluated sum
+// d + dl (Knuth's TwoSum), and the quotient gets one Newton-style correction
+// from its exact remainder p - q*d (an FMA), so h is p / (d + dl) to about
+// half an ulp: the only error left beyond one rounding is expf's, scaled by
+// e / (1 + e) -- negligible where g is large and positive, which is where a
+// row's largest |h| (and so its scale) usually comes from.  A code can still
+// differ from the correctly rounded h's code where h / s lies within a few
+// ulps of an E4M3 rounding boundary.  g -> -inf gives d = inf and h = +-0
+// (the correction is skipped there); g -> +inf gives p / 1.
+QG_DEVICE float silu_mul(float g, float u) {
+  const float p = __fmul_rn(g, u);
+  const float e = expf(-g);
+  const float d = __fadd_rn(1.f, e);
+  const float q = __fdiv_rn(p, d);
+  if (isinf(d)) return q;
+  const float bv = __fsub_rn(d, 1.f);
+  const float dl = __fadd_rn(__fsub_rn(1.f, __fsub_rn(d, bv)), __fsub_rn(e, bv));   // (1 + e) - d, exact
+  float r = __fmaf_rn(-q, d, p);          // p - q*d, exact
+  r = __fmaf_rn(-q, dl, r);               // minus q*dl
+  return __fadd_rn(q, __fdiv_rn(r, d));
+}
+
 QG_DEVICE void swiglu8(const uint16_t* gu, int I, int c, float (&h)[8]) {
   float gv[8], uv[8];
   Load8<uint16_t>::run(gu + c * 8, gv);
   Load8<uint16_t>::run(gu + I + c * 8, uv);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) h[i] = __fdividef(gv[i], 1.f + __expf(-gv[i])) * uv[i];
+  for (int i = 0; i < 8; ++i) h[i] = silu_mul(gv[i], uv[i]);
 }
 
 // One row per CTA with the row's SwiGLU values kept in registers: one read of
@@ -359,11 +370,10 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_reg_kernel(
     }
   }
   const float sc = fp8_scale(cta_max(m, red));
-  const float rs = __frcp_rn(sc);
 #pragma unroll
   for (int j = 0; j < CPT; ++j) {
     const int c = threadIdx.x + j * kThreads;
-    if (c < nc) store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8_rcp(h[j], rs));
+    if (c < nc) store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8(h[j], sc));
   }
   if (threadIdx.x == 0) s[blockIdx.x] = sc;
 }
@@ -380,11 +390,10 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(
     m = fmaxf(m, absmax8(h));
   }
   const float sc = fp8_scale(cta_max(m, red));
-  const float rs = __frcp_rn(sc);
   for (int c = threadIdx.x; c < I / 8; c += kThreads) {
     float h[8];
     swiglu8(gu, I, c, h);
-    store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8_rcp(h, rs));
+    store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8(h, sc));
   }
   if (threadIdx.x == 0) s[blockIdx.x] = sc;
 }

@@ -235,6 +235,24 @@ def moe_layer(x_bits, route_rows, expert_off, w1, w2, g, inter):
     return down, gu
 
 
+def moe_layer_fp8s(x_bits, route_rows, expert_off, w1, w2, inter):
+    """The MoE layer of ``moe_layer`` with both projections on the FP8
+    group-scale recipe ("Production-Ready W4A8", "Accurate W4A8 Kernel"):
+    w1 = (w8 codes [E, 2I, H], cs8 [E, 2I]) and w2 = (w8 [E, H, I], cs8 [E, H])
+    as prepared by ``quant.fp8_group_scales`` and ``quant.fp8_lut_weights``.
+    Same steps in the same order: per-token FP8 quant of x (block = H) ->
+    gather -> grouped gate/up -> bf16 -> SwiGLU (fp32) -> per-row FP8 quant
+    (block = I) -> grouped down -> bf16.  Returns (down_bits, gate_up_bits)."""
+    H = np.asarray(x_bits).shape[1]
+    a8, a_s = Q.quant_fp8_block(x_bits, H)
+    rows = np.asarray(route_rows)
+    gu = to_bf16(w4a8_fp8s_grouped_f64(a8[rows], a_s[rows, 0], expert_off, w1[0], w1[1]))
+    h = swiglu_f32(gu, inter)
+    h8, h_s = Q.quant_fp8_block(h, inter)
+    down = to_bf16(w4a8_fp8s_grouped_f64(h8, h_s[:, 0], expert_off, w2[0], w2[1]))
+    return down, gu
+
+
 def moe_combine(down_bits, route_rows, route_weight, T):
     """out[t] = sum over t's rows of p * down (float64), one bf16 rounding.
 

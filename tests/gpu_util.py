@@ -1,5 +1,7 @@
 """Host<->device helpers for the GPU parity tests (no arithmetic of the method)."""
 
+import functools
+
 import numpy as np
 import torch
 
@@ -39,3 +41,19 @@ def check_gemm(y, ref, tag=""):
     assert fro <= 2e-3, "%s: rel Frobenius %.3e > 2e-3" % (tag, fro)
     assert mx <= bound, "%s: max abs err %.3e > %.3e" % (tag, mx, bound)
     return fro
+
+
+@functools.lru_cache(maxsize=2)
+def config_expert_weights(E, N, K, seed):
+    """INT4 g128 expert weights [E][N][K/2] and bf16 scales [E][N][K/128] from
+    N(0, 0.02) weights (the oracle's RTN quantizer), generated once per
+    process: the config-size MoE tests of several files share them (callers
+    must not modify the arrays)."""
+    from numerics_packed_int4_gb300 import inputs
+    from oracle import quant as OQ
+    qs, ss = [], []
+    for e in range(E):
+        q, s = OQ.quant_int4_rtn(inputs.weights_f32(N, K, seed=seed + e), 128)
+        qs.append(q)
+        ss.append(s)
+    return np.stack(qs), np.stack(ss)

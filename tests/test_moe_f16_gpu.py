@@ -10,7 +10,7 @@ from numerics_packed_int4_gb300 import inputs
 from oracle import formats as OF
 from oracle import gemm as OG
 from oracle import quant as OQ
-from tests.gpu_util import check_gemm, dev, empty, host
+from tests.gpu_util import check_gemm, config_expert_weights, dev, empty, host
 
 pytestmark = pytest.mark.gpu
 
@@ -133,7 +133,7 @@ def test_grouped_f16act_config_size_sampled(qg):
     a8, a_s = OQ.quant_fp8_block(x, H)
     rows = rt["route_rows"]
     a8r, asr = a8[rows], a_s[rows, 0]
-    wq, ws = expert_weights(E, 2 * I, H, seed=60)
+    wq, ws = config_expert_weights(E, 2 * I, H, 60)
     y = grouped_f16(qg, a8r, asr, off, wq, ws, 2 * I, H)
     assert np.all(np.isfinite(y))
     r = np.random.Generator(np.random.PCG64(6))

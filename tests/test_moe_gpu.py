@@ -8,7 +8,7 @@ from numerics_packed_int4_gb300 import inputs
 from oracle import formats as OF
 from oracle import gemm as OG
 from oracle import quant as OQ
-from tests.gpu_util import check_gemm, dev, empty, host
+from tests.gpu_util import check_gemm, config_expert_weights, dev, empty, host
 
 pytestmark = pytest.mark.gpu
 
@@ -49,8 +49,8 @@ def test_grouped_small(qg, sizes, N, K):
 @pytest.mark.parametrize("sizes,N,K", [([300, 0, 700, 50, 1000], 384, 512), ([512], 272, 1024),
                                        ([0, 513, 0, 255, 257], 128, 384), ([2048, 2048], 1024, 2048)])
 def test_grouped_tensor_core_path(qg, sizes, N, K):
-    """R >= 512 takes the tcgen05 kernel: uneven experts, empty experts, partial
-    row tiles and a partial channel tile."""
+    """Larger R: uneven experts, empty experts, partial row tiles and a partial
+    channel tile, with many tiles per expert."""
     E = len(sizes)
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     R = int(off[-1])
@@ -73,7 +73,7 @@ def test_grouped_config_size_sampled(qg):
     a8, a_s = OQ.quant_fp8_block(x, H)
     rows = rt["route_rows"]
     a8r, asr = a8[rows], a_s[rows, 0]
-    wq, ws = expert_weights(E, 2 * I, H, seed=60)
+    wq, ws = config_expert_weights(E, 2 * I, H, 60)
     y = grouped(qg, a8r, asr, off, wq, ws, 2 * I, H)
     assert np.all(np.isfinite(y))
     r = np.random.Generator(np.random.PCG64(3))
@@ -129,24 +129,120 @@ def test_moe_layer_small(qg):
     check_gemm(OF.bf16_decode(host(out)), OF.bf16_decode(out_ref), "moe out")
 
 
+# Error budget of the kernel's h = (g * u) / (1 + expf(-g)) against the
+# oracle's fp64 SiLU rounded once to fp32: g * u is exact, expf is within 2
+# ulps (CUDA's documented bound), the add and the division round once each, so
+# h is within 3 * 2^-23 relative of the exact value; with the oracle's half
+# ulp, EPS_H = 2^-21 covers both sides with margin.
+EPS_H = 2.0 ** -21
+
+
+def _e4m3_midpoints():
+    v = np.unique(np.abs(OF.e4m3_decode(np.arange(256, dtype=np.uint8))))
+    v = v[np.isfinite(v)]
+    return (v[:-1] + v[1:]) / 2.0                 # 0 .. 448 in steps; nothing above 448 is a boundary
+
+
+def check_swiglu_codes(q, s, gu, I):
+    """Row scales within EPS_H relative plus one ulp of the oracle's; codes
+    identical wherever the oracle's h / s lies farther than the combined
+    relative error from every E4M3 rounding boundary, at most one step apart
+    elsewhere.  Returns (fraction of elements near a boundary, max scale ulps)."""
+    h = OG.swiglu_f32(gu, I)
+    ref_q, ref_s = OQ.quant_fp8_block(h, I)
+    ref_s = ref_s[:, 0].astype(np.float64)
+    ulp = np.spacing(ref_s.astype(np.float32)).astype(np.float64)
+    ds = np.abs(s.astype(np.float64) - ref_s)
+    assert np.all(ds <= EPS_H * ref_s + ulp), (ds / ulp).max()
+    t = np.abs(h.astype(np.float64) / ref_s[:, None])
+    delta = 2 * EPS_H + 4 * 2.0 ** -24           # h and s errors plus the quotient's rounding
+    mid = _e4m3_midpoints()
+    near = np.searchsorted(mid, t * (1 + delta), side="right") != np.searchsorted(mid, t * (1 - delta),
+                                                                                 side="left")
+    ordv = lambda c: np.where(c & 0x80, -(c.astype(np.int32) & 0x7F), c.astype(np.int32) & 0x7F)
+    d = np.abs(ordv(q) - ordv(ref_q))
+    assert np.all(d[~near] == 0), int(np.count_nonzero(d[~near]))
+    assert d.max() <= 1, d.max()
+    return float(np.mean(near)), float((ds / ulp).max())
+
+
+def _swiglu_inputs(R, I, scale=3.0):
+    return OF.bf16_encode((inputs.activations_bf16(R, 2 * I, seed=R + I).astype(np.uint32) << 16)
+                          .view(np.float32) * np.float32(scale))
+
+
 @pytest.mark.parametrize("R,I", [(1, 8), (37, 384), (300, 1408), (64, 14336)])
 def test_swiglu_quant_vs_oracle(qg, R, I):
     """SwiGLU + per-row FP8 requantization against the oracle's fp64 SwiGLU
-    (rounded once to fp32) and FP8 quantizer.  The kernel evaluates SiLU with
-    the fast exponential and division, so h carries a few fp32 ulps of error:
-    a code may differ by one E4M3 step where h / s lies within those ulps of a
-    rounding midpoint, the row scale by a few ulps, and nothing more."""
-    gu = OF.bf16_encode((inputs.activations_bf16(R, 2 * I, seed=R + I).astype(np.uint32) << 16)
-                        .view(np.float32) * np.float32(3.0))
+    (rounded once to fp32) and its FP8 quantizer (IEEE h / s, one E4M3
+    rounding).  The kernel's h carries the few-ulp error of expf: codes must
+    match exactly except where h / s lies within that error of an E4M3
+    rounding boundary."""
+    gu = _swiglu_inputs(R, I)
     hq, hs = empty((R, I), torch.uint8), empty((R,), torch.float32)
     qg.qg_swiglu_quant_fp8(dev(gu), hq, hs, R, I)
     qg.qg_check_device_error()
-    ref_q, ref_s = OQ.quant_fp8_block(OG.swiglu_f32(gu, I), I)
-    q, s = host(hq), host(hs)
-    assert np.allclose(s, ref_s[:, 0], rtol=4 * 2.0 ** -23, atol=0)
-    # compare by E4M3 grid position: sign-magnitude code -> ordinal
-    ordv = lambda c: np.where(c & 0x80, -(c.astype(np.int32) & 0x7F), c.astype(np.int32) & 0x7F)
-    d = np.abs(ordv(q) - ordv(ref_q))
-    assert d.max() <= 1, d.max()
-    assert np.mean(d != 0) < 1e-3, np.mean(d != 0)
+    near, _ = check_swiglu_codes(host(hq), host(hs), gu, I)
+    assert near < 1e-3, near
 
+
+@pytest.mark.parametrize("R,I", [(5, 136), (64, 14336)])
+def test_swiglu_quant_f16_values_vs_oracle(qg, R, I):
+    """The fp16-value output of the same kernel: each value must be exactly the
+    E4M3 value of the code the E4M3-output kernel writes, and pass the same
+    comparison with the oracle."""
+    gu = _swiglu_inputs(R, I, scale=5.0)
+    d_gu = dev(gu)
+    hq, hs = empty((R, I), torch.uint8), empty((R,), torch.float32)
+    qg.qg_swiglu_quant_fp8(d_gu, hq, hs, R, I)
+    hv, hs2 = empty((R, I), torch.int16), empty((R,), torch.float32)
+    qg.qg_swiglu_quant_fp8_f16(d_gu, hv, hs2, R, I)
+    qg.qg_check_device_error()
+    q = host(hq)
+    np.testing.assert_array_equal(host(hs2), host(hs))
+    vals = OF.fp16_decode(host(hv).view(np.uint16))
+    np.testing.assert_array_equal(vals, OF.e4m3_decode(q))
+    check_swiglu_codes(q, host(hs), gu, I)
+
+
+@pytest.mark.parametrize("entry", ["grouped", "f16act", "fp8s"])
+@pytest.mark.parametrize("R", [200, 640])
+def test_malformed_expert_offsets_stay_inside_the_buffers(qg, entry, R):
+    """expert_off comes from device memory and is not validated on the host:
+    a last offset past R (R + 64) and a decreasing entry must still keep every
+    access inside A and y.  y is the head of a larger allocation whose tail
+    holds a sentinel; the tail must be untouched, and with only the last
+    offset too large the rows are those of the clamped offsets."""
+    E, N, K = 3, 256, 512
+    x = inputs.activations_bf16(R, K, seed=R + 5)
+    a8, a_s = OQ.quant_fp8_block(x, K)
+    wq, ws = expert_weights(E, N, K, seed=33)
+    d_a8, d_as, d_wq, d_ws = dev(a8), dev(a_s[:, 0].copy()), dev(wq), dev(ws)
+    d_s8 = d_cs8 = d_a16 = None
+    if entry == "fp8s":
+        d_s8 = empty((K // 128, E * N), torch.uint8)
+        d_cs8 = empty((E * N,), torch.float32)
+        qg.qg_w4a8_fp8_scales(d_ws, d_s8, d_cs8, E * N, K // 128)
+    if entry == "f16act":
+        d_a16 = empty((R, K), torch.int16)
+        qg.qg_e4m3_to_f16(d_a8, d_a16, R * K)
+    sentinel = -12345
+    cases = {"past_end": np.array([0, R // 3, R // 2, R + 64], np.int32),
+             "decreasing": np.array([0, (2 * R) // 3, R // 4, R + 64], np.int32)}
+    for name, off in cases.items():
+        buf = torch.full((R + 96, N), sentinel, dtype=torch.int16, device="cuda")
+        y = buf[:R]
+        d_off = dev(off)
+        if entry == "grouped":
+            qg.qgemm_w4a8_grouped(d_a8, d_as, d_off, d_wq, d_ws, 128, y, R, E, N, K)
+        elif entry == "f16act":
+            qg.qgemm_w4a8_grouped_f16act(d_a16, d_as, d_off, d_wq, d_ws, None, 128, y, R, E, N, K)
+        else:
+            qg.qgemm_w4a8_grouped_fp8s(d_a8, d_as, d_off, d_wq, d_s8, d_cs8, y, R, E, N, K)
+        qg.qg_check_device_error()
+        tail = host(buf[R:]).view(np.int16)
+        assert np.all(tail == sentinel), "%s %s: rows past R written" % (entry, name)
+        if name == "past_end" and entry != "fp8s":
+            clamped = np.minimum(off, R).astype(np.int32)
+            ref = OF.bf16_decode(OG.to_bf16(OG.w4a8_grouped_f64(a8, a_s[:, 0], clamped, wq, ws, 128)))
+            check_gemm(OF.bf16_decode(host(y)), ref, "%s clamped offsets" % entry)
