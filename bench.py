@@ -9,6 +9,8 @@ One step = one pass over every row of the hot path at its workload size:
                  (E4M3 activations handed to the GEMMs as exact fp16 copies)
   MoE, FP8 scales  the same layer on the FP8-group-scale recipe (E4M3 x E4M3
                  tensor-core GEMMs; roofline against the FP8 dense peak)
+  MoE, E4M3 entry  the same layer through qgemm_w4a8_grouped (E4M3 activations
+                 handed over as codes, exact bf16 group scales)
   zero points    asymmetric INT4 (zero point per group of 64): M = 1 GEMVs and
                  M = 8192 prefill over the same three (N, K)
   W8A8 GEMV      FP8 weights, activations quantized per 1 x 128 block inside the
@@ -18,9 +20,13 @@ One step = one pass over every row of the hot path at its workload size:
   (opt-in) W4A4  MXFP4 activations (quantized in the step) x MXFP4 weights
 Each row is one CUDA graph (the MoE rows five, so that their grouped GEMMs --
 the step's dominant kernel -- are timed on their own); CUDA events between
-the graphs time every row inside the timed region.  After the timed region the
-M = 1 row's single-launch read ceiling is measured (a plain streaming read of
-the same 12 weight matrices, one launch each).  The headline value is the metric's first quantity:
+the graphs time every row inside the timed region.  Measured beside the step,
+outside the timed region: the M = 1 row's single-launch read ceiling (a plain
+streaming read of the same 12 weight matrices, one launch each), the dense
+FP8 rate of this GPU (the FP8 rows' roofline denominator), a bf16 dense GEMM
+(cuBLAS) on the prefill's own data, the 1 x 1024 x 1024 GEMV as latency, the
+pinned host link, and the oracle on the host cores.  The first output line
+holds every row in full; the last is the contract line.  The headline value is the metric's first quantity:
 effective HBM GB/s of the M = 1 GEMVs (algorithmic bytes / time); the
 M = 8192 TFLOP/s is reported beside it.  Inputs are seeded synthetic data
 (weights N(0, 0.02), activations N(0, 1)), resident in HBM before timing; the
@@ -70,7 +76,9 @@ PROFILED_TRAFFIC = {
 
 # the main kernel of rows timed in parts
 MAIN_KERNEL = {"moe": "moe_f16_kernel (gate/up + down launches)",
-               "moe_fp8s": "moe_fp8s_kernel (gate/up + down launches)"}
+               "moe_fp8s": "moe_fp8s_kernel (gate/up + down launches)",
+               "moe_e4m3": "qgemm_w4a8_grouped kernel (gate/up + down launches)"}
+MOE_ROWS = ("moe", "moe_fp8s", "moe_e4m3")
 
 
 def gemv_bytes(fmt, M, N, K):
@@ -324,7 +332,7 @@ class Workload:
             self.QFs = t.empty((4096, 56), dtype=t.float32, device=self.dev)
             self.QM = t.empty((4096, 3584), dtype=t.uint8, device=self.dev)
             self.QMs = t.empty((4096, 448), dtype=t.uint8, device=self.dev)
-        if "moe" in self.rows or "moe_fp8s" in self.rows:
+        if any(r in self.rows for r in MOE_ROWS):
             self._build_moe(inputs)
 
     def _build_moe(self, inputs):
@@ -416,7 +424,7 @@ class Workload:
         elif name == "quant":
             qg.quant_act_fp8_block(self.XQ, self.QF, self.QFs, 128, 4096, 7168)
             qg.quant_act_mxfp4(self.XQ, self.QM, self.QMs, 16, 4096, 7168)
-        elif name in ("moe", "moe_fp8s"):
+        elif name in MOE_ROWS:
             for _, fn, _ in self.parts(name):
                 fn()
 
@@ -424,7 +432,7 @@ class Workload:
     # layer's main kernel, timed on their own inside the step.
     def parts(self, name):
         qg = self.qg
-        if name not in ("moe", "moe_fp8s"):
+        if name not in MOE_ROWS:
             return [(name, lambda: self.run_segment(name), False)]
         m = self.moe
         T, E, H, I, R, topk = m["T"], m["E"], m["H"], m["I"], m["R"], m["topk"]
@@ -443,6 +451,19 @@ class Workload:
             def gemm2():
                 qg.qgemm_w4a8_grouped_f16act(m["hq16"], m["hs"], m["off"], m["w2q"], m["w2s"], m["w2e"], 128,
                                              m["down"], R, E, H, I)
+        elif name == "moe_e4m3":            # the E4M3-input entry with exact bf16 group scales
+            def pre():
+                qg.quant_act_fp8_block(m["x"], m["xq"], m["xs"], H, T, H)
+                qg.qg_moe_gather_fp8(m["xq"], m["xs"], m["rows"], m["aq"], m["as"], R, T, H)
+
+            def gemm1():
+                qg.qgemm_w4a8_grouped(m["aq"], m["as"], m["off"], m["w1q"], m["w1s"], 128, m["gu"], R, E, 2 * I, H)
+
+            def mid():
+                qg.qg_swiglu_quant_fp8(m["gu"], m["hq"], m["hs"], R, I)
+
+            def gemm2():
+                qg.qgemm_w4a8_grouped(m["hq"], m["hs"], m["off"], m["w2q"], m["w2s"], 128, m["down"], R, E, H, I)
         else:
             def pre():
                 qg.quant_act_fp8_block(m["x"], m["xq"], m["xs"], H, T, H)
@@ -485,7 +506,7 @@ class Workload:
         if "quant" in self.rows:
             M, K = 4096, 7168
             self.bytes["quant"] = M * K * (2 + 1) + M * K // 128 * 4 + M * K * 2 + M * K // 2 + M * K // 16
-        for r in ("moe", "moe_fp8s"):
+        for r in MOE_ROWS:
             if r in self.rows:
                 m = self.moe
                 self.flops[r] = 2.0 * m["R"] * (2 * m["I"] * m["H"] + m["H"] * m["I"])
@@ -546,6 +567,52 @@ def oracle_gemv_sample(seconds_budget=15.0, max_items=None):
     return done_bytes / spent / 1e9, spent, ", ".join(items)
 
 
+def oracle_other_rows():
+    """The oracle beside the other rows, on the host cores: both activation
+    quantizers at full size (4096 x 7168), and 256-row samples of the M=8192
+    prefill (INT4, 14336 x 4096) and of the MoE layer (256 rows of one expert:
+    gate/up, SwiGLU + requant, down), the latter two reported as the rate of
+    the sample (extrapolated linearly to the full row count).  Returns
+    {row: {"value", "unit", "seconds", "sample"}}."""
+    from numerics_packed_int4_gb300 import inputs
+    from oracle import gemm as OG
+    from oracle import quant as OQ
+    out = {}
+    M, K = 4096, 7168
+    x = inputs.quantizer_activations_bf16(M, K, seed=0)
+    t0 = time.perf_counter()
+    OQ.quant_fp8_block(x, 128)
+    t1 = time.perf_counter()
+    OQ.quant_mxfp4(x, 16)
+    t2 = time.perf_counter()
+    fp8_bytes = M * K * 3 + M * K // 128 * 4
+    mx_bytes = M * K * 2 + M * K // 2 + M * K // 16
+    out["quant"] = {"value": (fp8_bytes + mx_bytes) / (t2 - t0) / 1e9, "unit": "GB/s", "seconds": t2 - t0,
+                    "sample": "full size: FP8 1x128 %.1f s, MXFP4 g16 %.1f s" % (t1 - t0, t2 - t1)}
+    N, K = 14336, 4096
+    q, sc = OQ.quant_int4_rtn(inputs.weights_f32(N, K, seed=1001), 128)
+    xa = inputs.activations_bf16(256, K, seed=3001, outlier_frac=0.01, outlier_scale=50.0)
+    t0 = time.perf_counter()
+    OG.to_bf16(OG.qgemm_w4a16(xa, q, sc, 128))
+    dt = time.perf_counter() - t0
+    out["prefill"] = {"value": 2.0 * 256 * N * K / dt / 1e12, "unit": "TFLOP/s", "seconds": dt,
+                      "sample": "256 of 8192 rows, INT4 14336x4096 (dequant + fp64 product); "
+                                "extrapolated linearly"}
+    H, I = 4096, 14336
+    w1 = OQ.quant_int4_rtn(inputs.weights_f32(2 * I, H, seed=5000), 128)
+    w2 = OQ.quant_int4_rtn(inputs.weights_f32(H, I, seed=6000), 128)
+    xm = inputs.activations_bf16(256, H, seed=4000)
+    w1 = (w1[0][None], w1[1][None])
+    w2 = (w2[0][None], w2[1][None])
+    t0 = time.perf_counter()
+    OG.moe_layer(xm, np.arange(256), np.array([0, 256], np.int32), w1, w2, 128, I)
+    dt = time.perf_counter() - t0
+    out["moe"] = {"value": 2.0 * 256 * (2 * I * H + H * I) / dt / 1e12, "unit": "TFLOP/s", "seconds": dt,
+                  "sample": "256 of 8192 rows, one expert (gate/up, SwiGLU + FP8 requant, down); "
+                            "extrapolated linearly"}
+    return out
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -561,8 +628,8 @@ def bench_config(rows, world):
     """The workload of the bench line (shared by both arms)."""
     return {"workload": "decode sweep M in {1,4,16} x {4096^2, 14336x4096, 4096x14336} x "
                         "{INT4-g128, FP8-channel, MXFP4, NVFP4} + prefill M=8192 (W4A16; FP8, MXFP4, NVFP4 weights) + "
-                        "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2 (bf16 group scales; "
-                        "FP8 group scales) + asymmetric INT4 g64 M=1 and M=8192 + W8A8 GEMV M=1",
+                        "act quantizers 4096x7168 + W4A8 MoE T=4096 E=8 top-2 (bf16 group scales on fp16 copies; "
+                        "FP8 group scales; E4M3 entry) + asymmetric INT4 g64 M=1 and M=8192 + W8A8 GEMV M=1",
             "rows": rows, "l2": "inputs larger than L2: every weight matrix read once per step; "
                                 "step working set > 1 GB vs 129 MB L2",
             "parallelism": "replicas" if world > 1 else "single"}
@@ -680,6 +747,17 @@ def run_ours(args):
             t = sum(sum(m[i].elapsed_time(m[i + 1]) for i in idx) for m in ev[r]) / args.steps
             kern_ms[r] = (dist_max(t, world, dev), len(idx))
 
+    # ---- measurements beside the step (not part of it) --------------------------
+    fp8_meas = measure_fp8_peak(torch, dev) if "moe_fp8s" in rows else None
+    if fp8_meas is not None:
+        peaks["fp8"], peaks["fp8_src"] = fp8_meas, "measured in this run (torch._scaled_mm E4M3 8192^3, best of 10)"
+    else:
+        peaks["fp8_src"] = "measured bf16 x 2 (nominal fp8/bf16 ratio)"
+    side = {}
+    if "prefill" in rows:
+        side["prefill_vs_bf16"] = bf16_comparator(torch, qg, wl, dev)
+    side["gemv_1x1024x1024"] = gemv_1k_latency(torch, qg, dev)
+
     # ---- per-row throughput and rooflines ----------------------------------------
     row_out = {}
     for r in rows:
@@ -698,7 +776,7 @@ def run_ours(args):
                           "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                                        "frac": tf / peak, "traffic": traffic_of(r), **traffic_info(r)}}
             if fp8:
-                row_out[r]["roofline"]["peak_kind"] = "fp8 dense = measured bf16 x 2 (nominal ratio)"
+                row_out[r]["roofline"]["peak_kind"] = "fp8 dense: " + peaks["fp8_src"]
             if r in kern_ms:
                 kms, nl = kern_ms[r]
                 ktf = wl.flops[r] / (kms * 1e-3) / 1e12
@@ -710,6 +788,8 @@ def run_ours(args):
     value = aggregate(world * wl.bytes.get("decode_m1", 0.0), seg_ms_max.get("decode_m1", 1.0) * 1e-3) / 1e9
 
     e2e = e2e_decode_m1(torch, qg, wl, dev, steps=max(2, min(args.steps, 5))) if "decode_m1" in rows else None
+    if e2e is not None:
+        e2e["host_link"] = h2d_link(torch, dev)
     if "decode_m1" in rows:
         rc = read_ceiling(torch, qg, wl, dev)
         rc["gemv_row_over_read_time"] = seg_ms_max["decode_m1"] / rc["ms"]
@@ -719,6 +799,27 @@ def run_ours(args):
 
     if rank != 0:
         return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, spent, desc = oracle_gemv_sample(seconds_budget=args.cpu_seconds)
+        other = {} if args.cpu_seconds <= 0 else oracle_other_rows()
+        cpu = {"value": v, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": "M=1 GEMVs (oracle dequant + fp64 product), %d matrices, %.1f s; other rows below"
+                         % (len(desc.split(", ")), spent),
+               "rows": {k: {"value": o["value"], "unit": o["unit"], "s": round(o["seconds"], 1)}
+                        for k, o in other.items()}}
+        side["cpu_baseline_detail"] = {"decode_m1": desc, **{k: o["sample"] for k, o in other.items()}}
+
+    # line 1: every row in full, the side measurements and the peaks used
+    detail = {"detail": "per-row results of the step below", "rows": row_out, "side": side,
+              "peaks": peaks, "wall_s": t_wall}
+    print(json.dumps(detail), flush=True)
+
+    # line 2: the contract line, kept short
+    summary = {}
+    for r, o in row_out.items():
+        ach = o.get("GB/s", o.get("TFLOP/s"))
+        summary[r] = [round(o["ms"], 4), round(ach, 1), round(o["roofline"]["frac"], 3)]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -729,20 +830,29 @@ def run_ours(args):
         "roofline": (dict(row_out[dominant]["kernel"]["roofline"], kernel=row_out[dominant]["kernel"]["name"],
                           row=dominant) if "kernel" in row_out[dominant]
                      else dict(row_out[dominant]["roofline"], kernel=dominant)),
-        "roofline_value": dict(row_out["decode_m1"]["roofline"], kernel="decode_m1") if "decode_m1" in row_out else None,
-        "rows": row_out, "peaks_source": peaks["src"], "clocks": clocks,
-        "gpu_launches": launches_per_step * args.steps, "e2e": e2e,
-        "wall_s": t_wall,
+        "rows": {"columns": ["ms", "GB/s or TFLOP/s", "frac of measured peak"], **summary},
+        "clocks": clocks, "gpu_launches": launches_per_step * args.steps, "e2e": e2e,
     }
+    if "decode_m1" in row_out:
+        rc = row_out["decode_m1"]["single_launch_read"]
+        line["roofline_value"] = {"kernel": "decode_m1 (12 GEMVs)", "achieved": value, "peak": peaks["hbm"],
+                                  "frac": value / peaks["hbm"], "single_launch_read_GB/s": rc["GB/s"],
+                                  "frac_of_single_launch_read": value / rc["GB/s"]}
     if "prefill" in row_out:
         p = row_out["prefill"]
         line["secondary"] = {"metric": "M=8192 TFLOP/s", "value": p["TFLOP/s"], "unit": "TFLOP/s",
                              "frac_of_bf16_peak": p["TFLOP/s"] / peaks["bf16"],
                              "frac_of_bf16_sustained": p["TFLOP/s"] / peaks["bf16_sus"]}
-    if not args.no_cpu_baseline and world == 1:
-        v, spent, desc = oracle_gemv_sample(seconds_budget=args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-                                "sample": "M=1 GEMVs (oracle dequant + fp64 product): %s; %.1f s" % (desc, spent)}
+        if "prefill_vs_bf16" in side:
+            c = side["prefill_vs_bf16"]
+            line["secondary"]["bf16_dense_same_data_TFLOP/s"] = c["bf16_TFLOP/s"]
+            line["secondary"]["w4a16_over_bf16_speed"] = c["w4a16_over_bf16_speed"]
+    g1 = side["gemv_1x1024x1024"]
+    line["gemv_1x1024x1024"] = {"us": g1["graph_us_per_launch"], "GB/s": g1["graph_GB/s"],
+                                "single_call_us": g1["single_call_us_median"]}
+    line["peaks"] = {"hbm": peaks["hbm"], "bf16": peaks["bf16"], "fp8": peaks["fp8"], "src": peaks["src"]}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     return 0
 
@@ -780,6 +890,153 @@ def read_ceiling(torch, qg, wl, dev, reps=5):
     qg.qg_check_device_error()
     return {"what": "qg_stream_read of each decode weight matrix, one launch each", "bytes": nbytes,
             "launches": len(bufs), "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9}
+
+
+def _time_graph(torch, dev, fn, reps=10, warm=3):
+    """Capture fn in a CUDA graph and return (median, best) replay times in ms."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream(device=dev)):
+        fn()
+    for _ in range(warm):
+        g.replay()
+    stream = torch.cuda.current_stream(dev)
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return sorted(ts)[len(ts) // 2], min(ts)
+
+
+def measure_fp8_peak(torch, dev, n=8192, reps=10):
+    """Dense E4M3 x E4M3 (fp32 accumulate, bf16 out) rate of this GPU through
+    the vendor library (torch._scaled_mm, 8192^3, best of `reps`): the
+    denominator of the FP8 tensor-core rows, measured in the same run.  A
+    measurement of the library, not part of the path.  None if unavailable."""
+    try:
+        a = (torch.randn((n, n), device=dev) * 0.5).to(torch.float8_e4m3fn)
+        b = (torch.randn((n, n), device=dev) * 0.5).to(torch.float8_e4m3fn).t()     # column-major
+        one = torch.ones((), device=dev, dtype=torch.float32)
+        out = torch.empty((n, n), device=dev, dtype=torch.bfloat16)
+
+        def f():
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16, out=out)
+
+        _, best = _time_graph(torch, dev, f, reps=reps)
+        del a, b, out
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:
+        return None
+
+
+def bf16_comparator(torch, qg, wl, dev, reps=10):
+    """The prefill config's comparison: a bf16 dense GEMM (torch.matmul,
+    cuBLAS) on the same data -- the same outlier activations times the
+    canonical dequantized INT4 weights -- over the three (N, K), against the
+    W4A16 prefill on the same inputs.  Reports both times, the ratio, and how
+    far apart the two outputs are (relative Frobenius).  Outside the timed step."""
+    Wd, out = {}, {}
+    for N, K in SHAPES:
+        W = wl.W[("int4", N, K)]
+        wd = torch.empty((N, K), dtype=torch.int16, device=dev)
+        qg.qg_dequant_weights(qg.QG_FMT_INT4, W["q"], W["s"], 128, wd, N, K)
+        Wd[(N, K)] = wd.view(torch.bfloat16)
+        out[N] = torch.empty((8192, N), dtype=torch.bfloat16, device=dev)
+    qg.qg_check_device_error()
+
+    def dense():
+        for N, K in SHAPES:
+            torch.matmul(wl.XP[K].view(torch.bfloat16), Wd[(N, K)].t(), out=out[N])
+
+    def ours():
+        for N, K in SHAPES:
+            W = wl.W[("int4", N, K)]
+            qg.qgemm_w4a16(W["q"], W["s"], 128, wl.XP[K], wl.YP[N], 8192, N, K)
+
+    flops = sum(2.0 * 8192 * N * K for N, K in SHAPES)
+    d_ms, d_best = _time_graph(torch, dev, dense, reps=reps)
+    o_ms, o_best = _time_graph(torch, dev, ours, reps=reps)
+    ours()
+    torch.cuda.synchronize()
+    diff = []
+    for N, _ in SHAPES:
+        y = wl.YP[N].view(torch.bfloat16).float()
+        r = out[N].float()
+        diff.append(float(torch.linalg.vector_norm(y - r) / torch.linalg.vector_norm(r)))
+    qg.qg_check_device_error()
+    return {"what": "torch.matmul bf16 (cuBLAS) on the dequantized INT4 weights and the same outlier "
+                    "activations, M=8192 over the three (N,K)",
+            "bf16_ms": d_ms, "bf16_TFLOP/s": flops / (d_ms * 1e-3) / 1e12,
+            "w4a16_ms": o_ms, "w4a16_TFLOP/s": flops / (o_ms * 1e-3) / 1e12,
+            "w4a16_over_bf16_speed": d_ms / o_ms, "rel_fro_vs_bf16": max(diff)}
+
+
+def gemv_1k_latency(torch, qg, dev, copies=512, calls=200):
+    """The 1 x 1024 x 1024 W4A16 GEMV (INT4 g128): launch-bound at 0.54 MB,
+    so it is reported as latency plus effective GB/s.  (a) a CUDA graph of one
+    GEMV per weight copy, `copies` copies (277 MB, more than L2) so every
+    launch streams its weights from HBM: time per launch; (b) single calls
+    through the C ABI from Python, each timed with events on the stream."""
+    N = K = 1024
+    g = torch.Generator(device=dev)
+    g.manual_seed(7000)
+    w = torch.randn((copies * N, K), generator=g, device=dev) * 0.02
+    q = torch.empty((copies * N, K // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((copies * N, K // 128), dtype=torch.int16, device=dev)
+    qg.qg_quantize_weights_int4(w, q, s, 128, copies * N, K)
+    del w
+    x = torch.randn((1, K), generator=g, device=dev).to(torch.bfloat16).view(torch.int16)
+    y = torch.empty((1, N), dtype=torch.int16, device=dev)
+    torch.cuda.synchronize()
+    nbytes = gemv_bytes("int4", 1, N, K)
+
+    def sweep():
+        for i in range(copies):
+            qg.qgemm_w4a16(q[i * N:(i + 1) * N], s[i * N:(i + 1) * N], 128, x, y, 1, N, K)
+
+    ms, _ = _time_graph(torch, dev, sweep, reps=5)
+    per = ms / copies
+    stream = torch.cuda.current_stream(dev)
+    single = []
+    for c in range(calls):
+        i = (c * 97) % copies
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        qg.qgemm_w4a16(q[i * N:(i + 1) * N], s[i * N:(i + 1) * N], 128, x, y, 1, N, K)
+        b.record(stream)
+        torch.cuda.synchronize()
+        single.append(a.elapsed_time(b))
+    single.sort()
+    qg.qg_check_device_error()
+    return {"what": "W4A16 GEMV M=1 N=1024 K=1024 INT4 g128", "bytes": nbytes,
+            "graph_us_per_launch": per * 1e3, "graph_GB/s": nbytes / (per * 1e-3) / 1e9,
+            "single_call_us_median": single[len(single) // 2] * 1e3,
+            "single_call_GB/s": nbytes / (single[len(single) // 2] * 1e-3) / 1e9,
+            "weight_copies": copies}
+
+
+def h2d_link(torch, dev, nbytes=1 << 30, reps=5):
+    """One pinned host-to-device copy of 1 GiB (a single cudaMemcpyAsync),
+    best of `reps`: the host link's rate, the ceiling of the end-to-end figure."""
+    h = torch.empty((nbytes,), dtype=torch.uint8).pin_memory()
+    d = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ts = []
+    for _ in range(reps + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        d.copy_(h, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    best = min(ts[1:])
+    del h, d
+    return {"bytes": nbytes, "ms": best, "GB/s": nbytes / (best * 1e-3) / 1e9}
 
 
 def e2e_decode_m1(torch, qg, wl, dev, steps):
@@ -851,7 +1108,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe,moe_fp8s,"
+    ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe,moe_fp8s,moe_e4m3,"
                                       "decode_zp,prefill_zp,decode_w8a8,prefill_fp8,prefill_mxfp4,prefill_nvfp4",
                     help="segments to time; prefill_w4a4 (MXFP4 activations x MXFP4 weights) is available too")
     ap.add_argument("--no-cpu-baseline", action="store_true")

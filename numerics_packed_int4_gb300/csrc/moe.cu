@@ -215,6 +215,14 @@ __global__ void __launch_bounds__(kThreadsMoe) moe_w4a8_kernel(const MoeArgs p) 
 }  // namespace
 }  // namespace qg
 
+namespace qg {
+qg_status moe_w4a8_fp8p(const uint8_t* a_e4m3, const float* a_s, const int32_t* expert_off, const uint8_t* w_q,
+                        const uint16_t* w_s, uint16_t* y, int R, int E, int N, int K, cudaStream_t st);
+// rows from which the FP8 tensor-core kernel (128-row tiles, per-group
+// promotion) takes over from the 64-row mma.sync tiles
+constexpr int kFp8pMinRows = 256;
+}  // namespace qg
+
 extern "C" qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s, const int32_t* expert_off,
                                         const uint8_t* w_q, const uint16_t* w_s, int g, uint16_t* y, int R,
                                         int E, int N, int K, qg_stream_t stream) {
@@ -226,6 +234,9 @@ extern "C" qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,
   QG_REQUIRE(qg::aligned16(a_e4m3) && qg::aligned16(w_q) && qg::aligned16(y) && qg::aligned16(w_s),
              QG_ERR_MISALIGNED, "qgemm_w4a8_grouped: misaligned pointer");
   if (R == 0) return QG_OK;
+  if (R >= qg::kFp8pMinRows)
+    return qg::moe_w4a8_fp8p(a_e4m3, a_s, expert_off, w_q, w_s, y, R, E, N, K,
+                             reinterpret_cast<cudaStream_t>(stream));
   qg::MoeArgs p{a_e4m3, a_s, expert_off, w_q, w_s, y, R, E, N, K};
   const size_t smem = (size_t)(2 * qg::BM + 2 * qg::BN) * qg::LDS * 2;
   if (!qg::ensure_smem(qg::moe_w4a8_kernel, (int)smem))

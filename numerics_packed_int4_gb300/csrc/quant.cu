@@ -322,25 +322,32 @@ QG_DEVICE void store_codes8(void* q, long long o, uint2 codes) {
 // h = SiLU(g) * u = (g * u) / (1 + e^-g) in fp32.  g and u are bf16, so
 // p = g * u (16 significant bits) is exact.  The exponential is CUDA's accurate
 // expf (not the fast intrinsic).  d = 1 + e is kept as an unevaluated sum
-// d + dl (Knuth's TwoSum), and the quotient gets one Newton-style correction
-// from its exact remainder p - q*d (an FMA), so h is p / (d + dl) to about
-// half an ulp: the only error left beyond one rounding is expf's, scaled by
-// e / (1 + e) -- negligible where g is large and positive, which is where a
-// row's largest |h| (and so its scale) usually comes from.  A code can still
-// differ from the correctly rounded h's code where h / s lies within a few
-// ulps of an E4M3 rounding boundary.  g -> -inf gives d = inf and h = +-0
+// d + dl (Knuth's TwoSum), and the quotient p / (d + dl) is formed from an
+// approximate reciprocal with one correction from the exact remainder p - q*d
+// (an FMA) -- the classic Newton/Markstein step -- so h is p / (d + dl) to
+// about half an ulp: the only error left beyond one rounding is expf's, scaled
+// by e / (1 + e) -- negligible where g is large and positive, which is where
+// a row's largest |h| (and so its scale) usually comes from.  A code can
+// still differ from the correctly rounded h's code where h / s lies within a
+// few ulps of an E4M3 rounding boundary.  g -> -inf gives d = inf and h = +-0
 // (the correction is skipped there); g -> +inf gives p / 1.
+QG_DEVICE float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 QG_DEVICE float silu_mul(float g, float u) {
   const float p = __fmul_rn(g, u);
   const float e = expf(-g);
   const float d = __fadd_rn(1.f, e);
-  const float q = __fdiv_rn(p, d);
-  if (isinf(d)) return q;
+  const float rc = rcp_approx(d);
+  const float q = __fmul_rn(p, rc);
+  if (isinf(d)) return q;                 // +-0
   const float bv = __fsub_rn(d, 1.f);
   const float dl = __fadd_rn(__fsub_rn(1.f, __fsub_rn(d, bv)), __fsub_rn(e, bv));   // (1 + e) - d, exact
   float r = __fmaf_rn(-q, d, p);          // p - q*d, exact
   r = __fmaf_rn(-q, dl, r);               // minus q*dl
-  return __fadd_rn(q, __fdiv_rn(r, d));
+  return __fmaf_rn(r, rc, q);
 }
 
 QG_DEVICE void swiglu8(const uint16_t* gu, int I, int c, float (&h)[8]) {
@@ -352,27 +359,43 @@ QG_DEVICE void swiglu8(const uint16_t* gu, int I, int c, float (&h)[8]) {
 }
 
 // One row per CTA with the row's SwiGLU values kept in registers: one read of
-// gate/up, the per-row absmax, then the E4M3 codes (CPT chunks of 8 per thread).
-template <int CPT, bool F16>
-__global__ void __launch_bounds__(kThreads) swiglu_quant_reg_kernel(
+// gate/up, the per-row absmax, then the E4M3 codes (CPT chunks of 8 per thread,
+// NT threads).
+template <int NT>
+QG_DEVICE float cta_max_nt(float v, float* red) {
+  v = group_max<32>(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < NT / 32 ? red[lane] : 0.f;
+    v = group_max<32>(v);
+    if (lane == 0) red[0] = v;
+  }
+  __syncthreads();
+  return red[0];
+}
+
+template <int CPT, int NT, bool F16>
+__global__ void __launch_bounds__(NT) swiglu_quant_reg_kernel(
     const uint16_t* __restrict__ gate_up, void* __restrict__ q, float* __restrict__ s, int I) {
-  __shared__ float red[kThreads / 32];
+  __shared__ float red[NT / 32];
   const uint16_t* gu = gate_up + (long long)blockIdx.x * 2 * I;
   const int nc = I / 8;
   float h[CPT][8];
   float m = 0.f;
 #pragma unroll
   for (int j = 0; j < CPT; ++j) {
-    const int c = threadIdx.x + j * kThreads;
+    const int c = threadIdx.x + j * NT;
     if (c < nc) {
       swiglu8(gu, I, c, h[j]);
       m = fmaxf(m, absmax8(h[j]));
     }
   }
-  const float sc = fp8_scale(cta_max(m, red));
+  const float sc = fp8_scale(cta_max_nt<NT>(m, red));
 #pragma unroll
   for (int j = 0; j < CPT; ++j) {
-    const int c = threadIdx.x + j * kThreads;
+    const int c = threadIdx.x + j * NT;
     if (c < nc) store_codes8<F16>(q, (long long)blockIdx.x * I + c * 8, fp8_codes8(h[j], sc));
   }
   if (threadIdx.x == 0) s[blockIdx.x] = sc;
@@ -646,10 +669,11 @@ qg_status swiglu_quant_launch(const uint16_t* gate_up, void* q, float* s, int R,
   if (R == 0) return QG_OK;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int cpt = (I / 8 + kThreads - 1) / kThreads;    // chunks per thread
-  if (cpt <= 1)      swiglu_quant_reg_kernel<1, F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
-  else if (cpt <= 2) swiglu_quant_reg_kernel<2, F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
-  else if (cpt <= 4) swiglu_quant_reg_kernel<4, F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
-  else if (cpt <= 8) swiglu_quant_reg_kernel<8, F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
+  const int cpt512 = (I / 8 + 511) / 512;
+  if (cpt <= 1)         swiglu_quant_reg_kernel<1, kThreads, F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
+  else if (cpt <= 2)    swiglu_quant_reg_kernel<2, kThreads, F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
+  else if (cpt512 <= 2) swiglu_quant_reg_kernel<2, 512, F16><<<R, 512, 0, st>>>(gate_up, q, s, I);
+  else if (cpt512 <= 4) swiglu_quant_reg_kernel<4, 512, F16><<<R, 512, 0, st>>>(gate_up, q, s, I);
   else               swiglu_quant_kernel<F16><<<R, kThreads, 0, st>>>(gate_up, q, s, I);
   return check_launch(name);
 }

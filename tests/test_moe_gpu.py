@@ -246,3 +246,31 @@ def test_malformed_expert_offsets_stay_inside_the_buffers(qg, entry, R):
             clamped = np.minimum(off, R).astype(np.int32)
             ref = OF.bf16_decode(OG.to_bf16(OG.w4a8_grouped_f64(a8, a_s[:, 0], clamped, wq, ws, 128)))
             check_gemm(OF.bf16_decode(host(y)), ref, "%s clamped offsets" % entry)
+
+
+def test_grouped_long_k_config_size_repeatable(qg):
+    """The down projection of the config layer (R = 8192 rows over E = 8
+    experts, N = 4096, K = 14336 -- 112 scale groups) three times over: the
+    outputs must be bit-identical run to run (the kernel is deterministic, so
+    any difference is a race) and match the oracle on sampled rows."""
+    T, E, H, I = 4096, 8, 4096, 14336
+    rt = inputs.moe_routing(T, E, 2, seed=9)
+    off = rt["expert_off"]
+    R = int(off[-1])
+    h = inputs.activations_bf16(R, I, seed=31)
+    a8, a_s = OQ.quant_fp8_block(h, I)
+    wq, ws = config_expert_weights(E, H, I, 61)
+    d_a8, d_as, d_off, d_wq, d_ws = dev(a8), dev(a_s[:, 0].copy()), dev(off), dev(wq), dev(ws)
+    outs = []
+    for _ in range(3):
+        y = torch.zeros((R, H), dtype=torch.int16, device="cuda")
+        qg.qgemm_w4a8_grouped(d_a8, d_as, d_off, d_wq, d_ws, 128, y, R, E, H, I)
+        qg.qg_check_device_error()
+        outs.append(host(y))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2]), "nondeterministic output"
+    r = np.random.Generator(np.random.PCG64(8))
+    pick = np.sort(np.concatenate([r.choice(np.arange(off[e], off[e + 1]), size=6, replace=False)
+                                   for e in range(E)]))
+    sub_off = np.searchsorted(pick, off).astype(np.int32)
+    ref = OF.bf16_decode(OG.to_bf16(OG.w4a8_grouped_f64(a8[pick], a_s[pick, 0], sub_off, wq, ws, 128)))
+    check_gemm(OF.bf16_decode(outs[0][pick]), ref, "grouped K=14336 sampled rows")
