@@ -77,8 +77,9 @@ PROFILED_TRAFFIC = {
 # the main kernel of rows timed in parts
 MAIN_KERNEL = {"moe": "moe_f16_kernel (gate/up + down launches)",
                "moe_fp8s": "moe_fp8s_kernel (gate/up + down launches)",
-               "moe_e4m3": "qgemm_w4a8_grouped kernel (gate/up + down launches)"}
+               "moe_e4m3": "moe_fp8p_kernel (gate/up + down launches)"}
 MOE_ROWS = ("moe", "moe_fp8s", "moe_e4m3")
+FP8_ROWS = ("moe_fp8s", "moe_e4m3")          # FP8 tensor-core contractions: roofline against the FP8 peak
 
 
 def gemv_bytes(fmt, M, N, K):
@@ -748,7 +749,7 @@ def run_ours(args):
             kern_ms[r] = (dist_max(t, world, dev), len(idx))
 
     # ---- measurements beside the step (not part of it) --------------------------
-    fp8_meas = measure_fp8_peak(torch, dev) if "moe_fp8s" in rows else None
+    fp8_meas = measure_fp8_peak(torch, dev) if any(r in FP8_ROWS for r in rows) else None
     if fp8_meas is not None:
         peaks["fp8"], peaks["fp8_src"] = fp8_meas, "measured in this run (torch._scaled_mm E4M3 8192^3, best of 10)"
     else:
@@ -770,7 +771,7 @@ def run_ours(args):
                                        "traffic": traffic_of(r), **traffic_info(r)}}
         else:
             tf = wl.flops[r] / (ms * 1e-3) / 1e12
-            fp8 = r == "moe_fp8s"
+            fp8 = r in FP8_ROWS
             peak = peaks["fp8"] if fp8 else peaks["bf16"]
             row_out[r] = {"ms": ms, "TFLOP/s": tf, "launches": wl.launches[r],
                           "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",

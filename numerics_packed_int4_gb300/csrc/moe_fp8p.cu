@@ -33,17 +33,25 @@
 //   warp 0      TMA for the packed weights (8 stages, 64-byte swizzled)
 //   warp 1      TMEM allocation and MMA issuer (one lane)
 //   warp 2      TMA for the activations (8 stages)
-//   warps 3-18  for every group, promotion of its lane quarter x 32 of the
-//               128 rows (at a tile's last group they apply the token scale
-//               and store), then dequant (set = (warp - 3) / 4 takes the slabs
-//               g = set mod 4, four ahead, into weight slot set; lane quarter
-//               = warp % 4)
-//   warp 19     scheduler: waits for each slab's operands and for the group
+//   warps 3-10  dequant: two sets of 4 (one warp per TMEM lane quarter), set
+//               s taking the slabs g = s mod 2 into weight slot g mod 4, as far
+//               ahead of the MMAs as the slots allow
+//   warps 11-26 promotion: lane quarter x 32 of the 128 rows each, for every
+//               group; at a tile's last group they apply the token scale and
+//               store.  They do nothing else, so a group accumulator is
+//               released as soon as its MMAs complete
+//   warp 27     scheduler: waits for each slab's operands and for the group
 //               accumulator it will overwrite to be promoted, and publishes
 //               the ready count the issuer polls (the issuer waits on no
 //               mbarrier while its MMAs are in flight)
 // Every wait is bounded; on expiry the CTA records a timeout in the device
 // error word, drains what it issued, frees its tensor memory and returns.
+// Measured on GB300 (MoE config, R = 8192): about 1 PFLOP/s.  What bounds it
+// is the per-group round trip -- MMA completion, promotion, release of the
+// accumulator, re-issue -- against only three accumulators of tensor memory:
+// removing every promotion load and weight-slot store gained about 10 %, and
+// 192-row tiles (two accumulators) or one commit instead of three per slab
+// changed nothing.
 #include <algorithm>
 
 #include "dequant.cuh"
@@ -62,20 +70,31 @@ constexpr int pXStages = 8;              // activation stages
 constexpr int pWStages = 8;              // packed-weight stages
 constexpr int pSlots = 4;                // weight slots in tensor memory (one per dequant set)
 constexpr int pBufs = 3;                 // group accumulators in tensor memory
-constexpr int pDeqWarps = 16;
+constexpr int pDone = 8;                 // slab-completion barriers (>= pXStages, even)
+constexpr int pDeqWarps = 8;             // two sets of 4 (one warp per TMEM lane quarter)
 constexpr int pDeqSet = 4;
 constexpr int pDeqSets = pDeqWarps / pDeqSet;
+constexpr int pProWarps = 16;            // promotion: 4 lane quarters x 4 column groups
+constexpr int pProCols = pTT / 4;        // accumulator columns (activation rows) per promotion warp
 constexpr int pDeq0 = 3;
-constexpr int pSchedWarp = pDeq0 + pDeqWarps;
+constexpr int pPro0 = pDeq0 + pDeqWarps;
+constexpr int pSchedWarp = pPro0 + pProWarps;
 constexpr int pThreads = (pSchedWarp + 1) * 32;
 constexpr int pXStage = pTT * pBK;       // 16 KB E4M3 activations
 constexpr int pWStage = pTW * pBK / 2;   // 8 KB packed INT4
 constexpr uint32_t pTmemCols = 512;
-constexpr uint32_t pACol0 = pBufs * pTT; // 384: weight slots after the accumulators
+constexpr uint32_t pACol0 = pBufs * pTT; // weight slots after the accumulators
 constexpr uint32_t pACols = pBK / 4;     // 32 columns: 128 E4M3 codes per lane
 constexpr uint32_t pDrainCap = 1u << 21;
-static_assert(pSlots == pDeqSets, "each dequant set owns one weight slot");
+static_assert(pSlots % pDeqSets == 0, "a slot is always written by the same dequant set");
+static_assert(pProCols % 16 == 0 && pProCols <= 64, "promotion columns per warp");
 static_assert(pACol0 + pSlots * pACols <= pTmemCols, "tensor memory budget");
+// Waiters of the done ring: the activation producer (slab g - pXStages, every
+// slab in order), each dequant set (slab g - pSlots for its own slabs: with
+// pDone and pDeqSets even a set only ever waits on its own entries, each of
+// their phases in order) and the promotion warps (every slab in order, never
+// more than pBufs behind the MMAs) -- none can fall a whole ring behind.
+static_assert(pDone >= pXStages && pDone % pDeqSets == 0 && pSlots % pDeqSets == 0, "done ring");
 
 struct Fp8pArgs {
   const float* a_s;
@@ -90,12 +109,10 @@ struct Fp8pArgs {
 
 struct __align__(8) Fp8pTail {
   uint64_t x_full[pXStages];
-  uint64_t x_empty[pXStages];
   uint64_t w_full[pWStages];
   uint64_t w_empty[pWStages];
   uint64_t a_full[pSlots];
-  uint64_t a_empty[pSlots];
-  uint64_t g_full[pBufs];                // the group's MMAs completed
+  uint64_t done[pDone];                  // slab g's MMAs completed (one commit per slab, entry g % pDone)
   uint64_t g_empty[pBufs];               // every promoting warp has read the group's accumulator
   uint64_t drain;
   uint32_t tmem_base;
@@ -153,6 +170,15 @@ QG_DEVICE uint32_t int4x4_to_e4m3(uint32_t sel, uint32_t fsel) {
   return lop3<0xF8>(a, b, m);
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane
+QG_DEVICE void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr) : "memory");
+}
+
 __global__ void __launch_bounds__(pThreads, 1)
 moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                 const Fp8pArgs p) {
@@ -174,7 +200,6 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
   if (threadIdx.x == 0) {
     for (int s = 0; s < pXStages; ++s) {
       mbar_init(&tl->x_full[s], 1);
-      mbar_init(&tl->x_empty[s], 1);
     }
     for (int s = 0; s < pWStages; ++s) {
       mbar_init(&tl->w_full[s], 1);
@@ -182,11 +207,10 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
     }
     for (int s = 0; s < pSlots; ++s) {
       mbar_init(&tl->a_full[s], pDeqSet);
-      mbar_init(&tl->a_empty[s], 1);
     }
+    for (int d = 0; d < pDone; ++d) mbar_init(&tl->done[d], 1);
     for (int b = 0; b < pBufs; ++b) {
-      mbar_init(&tl->g_full[b], 1);
-      mbar_init(&tl->g_empty[b], pDeqWarps);
+      mbar_init(&tl->g_empty[b], pProWarps);
     }
     mbar_init(&tl->drain, 1);
     tl->abort = 0;
@@ -227,8 +251,9 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
       PTile t = tile_of(0);
       for (int g = 0; g < total; ++g, ++s) {
         if (s == nslab) { s = 0; t = tile_of(++i); }
-        const int st = g % pXStages, r = g / pXStages;
-        if (r > 0 && !mbar_wait(&tl->x_empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+        const int st = g % pXStages;
+        const int gp = g - pXStages;                     // the stage last held slab gp
+        if (gp >= 0 && !mbar_wait(&tl->done[gp % pDone], (gp / pDone) & 1, p.cap, abort, p.err)) break;
         mbar_arrive_expect_tx(&tl->x_full[st], pXStage);
         tma_load_2d(xs + st * pXStage, &tmap_a, &tl->x_full[st], s * pBK, t.r0);
         issued = g + 1;
@@ -259,9 +284,9 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
               :: "r"(d), "r"(tmem + pACol0 + sa * pACols + 8 * j), "l"(bdesc + 2 * j), "r"(idesc),
                  "r"(j != 0 ? 1u : 0u)
               : "memory");
-        tc_commit(&tl->a_empty[sa]);                     // the weight slot may be rewritten
-        tc_commit(&tl->x_empty[st]);                     // the activation stage may be refilled
-        tc_commit(&tl->g_full[b]);                       // the group's partial is complete
+        // one commit per slab: its completion frees the weight slot and the
+        // activation stage and makes the group's partial readable
+        tc_commit(&tl->done[g % pDone]);
         any = true;
       }
       if (*abort && any) {
@@ -280,20 +305,21 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         publish_count(&tl->ready, (unsigned)(g + 1));
       }
     }
-  } else {
-    // ---------------- dequant, promotion and the epilogue ----------------
+  } else if (warp < pPro0) {
+    // ---------------- dequant: set s takes the slabs g = s mod 2 ----------------
+    // Thread = one weight row (TMEM lane) of a 128-k slab.  The sets run ahead
+    // of the MMAs as far as the weight slots allow (slot g mod 4, freed by the
+    // MMAs of slab g - 4), never waiting on the promotion.
     const int dw = warp - pDeq0;
     const int q = warp & 3, set = dw >> 2;
-    const int row = 32 * q + lane;                       // channel within the tile (TMEM lane)
+    const int row = 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
     const int wsw = (row >> 1) & 3;
-    const int ng = p.K / pBK;                            // scale groups per row
-
-    // dequant of slab gs into this set's weight slot
-    auto dequant = [&](int gs, const PTile& t) -> bool {
-      (void)t;
-      const int sw = gs % pWStages, rw = gs / pWStages, ra = gs / pSlots;
-      if (!mbar_wait_warp(&tl->w_full[sw], rw & 1, p.cap, abort, p.err)) return false;
+    for (int g = set; g < total; g += pDeqSets) {
+      const int sw = g % pWStages, rw = g / pWStages, sa = g % pSlots, ra = g / pSlots;
+      if (!mbar_wait_warp(&tl->w_full[sw], rw & 1, p.cap, abort, p.err)) break;
+      // this row's 64 packed bytes; 64-byte swizzled stage: 16-byte chunk c
+      // of the row sits at chunk c ^ ((row >> 1) & 3)
       const uint8_t* wrow = wsm + sw * pWStage + row * (pBK / 2);
       uint32_t v[16];
 #pragma unroll
@@ -301,42 +327,47 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         const uint4 w4 = *reinterpret_cast<const uint4*>(wrow + 16 * (c ^ wsw));
         v[4 * c] = w4.x; v[4 * c + 1] = w4.y; v[4 * c + 2] = w4.z; v[4 * c + 3] = w4.w;
       }
-      uint32_t out[32];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {                     // 8 INT4 codes (k0..k7, k0 lowest) -> 8 E4M3 codes
-        const uint32_t f = v[j] ^ 0x88888888u;
-        out[2 * j] = int4x4_to_e4m3(v[j], f);
-        out[2 * j + 1] = int4x4_to_e4m3(v[j] >> 16, f >> 16);
-      }
       mbar_arrive_warp(&tl->w_empty[sw]);                // packed slab read: its stage may be refilled
       if (ra > 0) {
-        if (!mbar_wait_warp(&tl->a_empty[set], (ra - 1) & 1, p.cap, abort, p.err)) return false;
+        const int gp = g - pSlots;                       // the slot last held slab gp
+        if (!mbar_wait_warp(&tl->done[gp % pDone], (gp / pDone) & 1, p.cap, abort, p.err)) break;
         tc_fence_after();
       }
-      {
-        const uint32_t (&o0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&out[0]);
-        const uint32_t (&o1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&out[16]);
-        const uint32_t a = tmem + lane_addr + pACol0 + (uint32_t)(set * pACols);
-        tmem_st16(a, o0);
-        tmem_st16(a + 16, o1);
+      const uint32_t at = tmem + lane_addr + pACol0 + (uint32_t)(sa * pACols);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {                      // 64 k at a time: 16 columns
+        uint32_t out[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {                    // 8 INT4 codes (k0..k7, k0 lowest) -> 8 E4M3 codes
+          const uint32_t w = v[8 * h + j], f = w ^ 0x88888888u;
+          out[2 * j] = int4x4_to_e4m3(w, f);
+          out[2 * j + 1] = int4x4_to_e4m3(w >> 16, f >> 16);
+        }
+        tmem_st16(at + 16 * h, out);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(&tl->a_full[set]);
-      return true;
-    };
-
-    float sum[32];
+      mbar_arrive_warp(&tl->a_full[sa]);
+    }
+  } else {
+    // ---------------- promotion and the epilogue ----------------
+    // Warp = lane quarter q (32 channels) x column group cq (32 of the 128
+    // rows).  For every group: read the group's accumulator, release it, add
+    // s[n, g] times it into the running sums; at a tile's last group apply
+    // the token scale and store.
+    const int pw = warp - pPro0;
+    const int q = warp & 3, cq = pw >> 2;
+    const int row = 32 * q + lane;                       // channel within the tile (TMEM lane)
+    const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
+    const int ng = p.K / pBK;                            // scale groups per row
+    float sum[pProCols];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) sum[c] = 0.f;
-    // the group scale of this thread's channel, one group ahead
-    int ti = 0, s = 0;                                   // tile index and slab of the promoted group
+    for (int c = 0; c < pProCols; ++c) sum[c] = 0.f;
+    int ti = 0, s = 0;                                   // tile index and slab of the group promoted next
     PTile t = tile_of(0);
     const uint16_t* srow = p.ws + ((size_t)t.e * p.N + min(t.n0 + row, p.N - 1)) * ng;
     float sc = bf16_bits_to_f32(__ldg(srow));
-    bool ok = true;
-    if (set < total) ok = dequant(set, t);
-    for (int g = 0; ok && g < total; ++g) {
+    for (int g = 0; g < total; ++g) {
       // next group's scale (the next tile's first when this group ends the tile)
       float sc_next = 0.f;
       PTile t_next = t;
@@ -348,26 +379,29 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         srow_next = p.ws + ((size_t)t_next.e * p.N + min(t_next.n0 + row, p.N - 1)) * ng;
         sc_next = bf16_bits_to_f32(__ldg(srow_next));
       }
-      // promote group g: sum += s[n, g] * D_g (this warp's 32 of the 128 rows)
       const int b = g % pBufs;
-      if (!(ok = mbar_wait_warp(&tl->g_full[b], (g / pBufs) & 1, p.cap, abort, p.err))) break;
+      if (!mbar_wait_warp(&tl->done[g % pDone], (g / pDone) & 1, p.cap, abort, p.err)) break;
       tc_fence_after();
-      uint32_t v[32];
-      tmem_ld32(tmem + lane_addr + (uint32_t)(b * pTT + 32 * set), v);
-      tmem_wait_ld();
+#pragma unroll
+      for (int h = 0; h < pProCols / 16; ++h) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_addr + (uint32_t)(b * pTT + pProCols * cq + 16 * h), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) sum[16 * h + c] = __fmaf_rn(sc, __uint_as_float(v[c]), sum[16 * h + c]);
+      }
       tc_fence_before();
       mbar_arrive_warp(&tl->g_empty[b]);                 // the accumulator may take group g + 3
-#pragma unroll
-      for (int c = 0; c < 32; ++c) sum[c] = __fmaf_rn(sc, __uint_as_float(v[c]), sum[c]);
       if (s + 1 == nslab) {
         // tile done: token scale, one bf16 rounding, store; lane l fetches the
-        // token scale of row 32 * set + l, the others come by shuffle
-        const int mb = t.r0 + 32 * set;
+        // token scales of rows pProCols * cq + l (+ 32), the others come by shuffle
+        const int mb = t.r0 + pProCols * cq;
         const int nn = t.n0 + row;
-        const float as = mb + lane < t.r_end ? __ldg(p.a_s + mb + lane) : 0.f;
+        const float as0 = mb + lane < t.r_end ? __ldg(p.a_s + mb + lane) : 0.f;
+        const float as1 = lane + 32 < pProCols && mb + 32 + lane < t.r_end ? __ldg(p.a_s + mb + 32 + lane) : 0.f;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float a_sc = __shfl_sync(0xffffffffu, as, c);
+        for (int c = 0; c < pProCols; ++c) {
+          const float a_sc = __shfl_sync(0xffffffffu, c < 32 ? as0 : as1, c & 31);
           if (nn < p.N && mb + c < t.r_end)
             p.y[(size_t)(mb + c) * p.N + nn] = f32_to_bf16_bits(__fmul_rn(sum[c], a_sc));
           sum[c] = 0.f;
@@ -380,13 +414,6 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         ++s;
       }
       sc = sc_next;
-      // then the next slab of this set, four ahead (its weight slot was freed
-      // by group g's MMAs, which the promotion above has already seen finish):
-      // promoting first keeps the dequant off the path that releases the
-      // group accumulators
-      if ((g % pDeqSets) == set && g + pDeqSets < total) {
-        if (!(ok = dequant(g + pDeqSets, t))) break;
-      }
     }
   }
 
