@@ -17,7 +17,8 @@ One step = one pass over every row of the hot path at its workload size:
                  GEMV prologue: M = 1 over the same three (N, K)
   prefill, other weights  M = 8192 over the same three (N, K) with FP8
                  per-channel, MXFP4 and NVFP4 weights
-  (opt-in) W4A4  MXFP4 activations (quantized in the step) x MXFP4 weights
+  W4A4           MXFP4 activations (quantized in the step) x MXFP4 weights on
+                 the block-scaled FP4 tensor cores, M = 8192 over the three (N, K)
 Each row is one CUDA graph (the MoE rows five, so that their grouped GEMMs --
 the step's dominant kernel -- are timed on their own); CUDA events between
 the graphs time every row inside the timed region.  Measured beside the step,
@@ -80,6 +81,7 @@ MAIN_KERNEL = {"moe": "moe_f16_kernel (gate/up + down launches)",
                "moe_e4m3": "moe_fp8p_kernel (gate/up + down launches)"}
 MOE_ROWS = ("moe", "moe_fp8s", "moe_e4m3")
 FP8_ROWS = ("moe_fp8s", "moe_e4m3")          # FP8 tensor-core contractions: roofline against the FP8 peak
+FP4_ROWS = ("prefill_w4a4",)                  # block-scaled FP4 contractions: 2 x the FP8 peak (nominal ratio)
 
 
 def gemv_bytes(fmt, M, N, K):
@@ -749,7 +751,7 @@ def run_ours(args):
             kern_ms[r] = (dist_max(t, world, dev), len(idx))
 
     # ---- measurements beside the step (not part of it) --------------------------
-    fp8_meas = measure_fp8_peak(torch, dev) if any(r in FP8_ROWS for r in rows) else None
+    fp8_meas = measure_fp8_peak(torch, dev) if any(r in FP8_ROWS + FP4_ROWS for r in rows) else None
     if fp8_meas is not None:
         peaks["fp8"], peaks["fp8_src"] = fp8_meas, "measured in this run (torch._scaled_mm E4M3 8192^3, best of 10)"
     else:
@@ -772,12 +774,14 @@ def run_ours(args):
         else:
             tf = wl.flops[r] / (ms * 1e-3) / 1e12
             fp8 = r in FP8_ROWS
-            peak = peaks["fp8"] if fp8 else peaks["bf16"]
+            peak = 2.0 * peaks["fp8"] if r in FP4_ROWS else (peaks["fp8"] if fp8 else peaks["bf16"])
             row_out[r] = {"ms": ms, "TFLOP/s": tf, "launches": wl.launches[r],
                           "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                                        "frac": tf / peak, "traffic": traffic_of(r), **traffic_info(r)}}
             if fp8:
                 row_out[r]["roofline"]["peak_kind"] = "fp8 dense: " + peaks["fp8_src"]
+            if r in FP4_ROWS:
+                row_out[r]["roofline"]["peak_kind"] = "fp4 dense: 2 x the fp8 peak (" + peaks["fp8_src"] + ")"
             if r in kern_ms:
                 kms, nl = kern_ms[r]
                 ktf = wl.flops[r] / (kms * 1e-3) / 1e12
@@ -1110,8 +1114,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="decode_m1,decode_m4,decode_m16,prefill,quant,moe,moe_fp8s,moe_e4m3,"
-                                      "decode_zp,prefill_zp,decode_w8a8,prefill_fp8,prefill_mxfp4,prefill_nvfp4",
-                    help="segments to time; prefill_w4a4 (MXFP4 activations x MXFP4 weights) is available too")
+                                      "decode_zp,prefill_zp,decode_w8a8,prefill_fp8,prefill_mxfp4,prefill_nvfp4,"
+                                      "prefill_w4a4",
+                    help="segments to time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)

@@ -143,14 +143,18 @@ QG_API qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int sc
 /* W4A4 with MXFP4 on both operands (the MXFP4 W4A4 MoE GEMM of vLLM PR
  * #43557; activations from quant_act_mxfp4 with g = 32, weights MXFP4):
  * y[m,n] = sum_k (e2m1(a[m,k]) * 2^(sa[m,k/32]-127)) * (e2m1(w[n,k]) *
- * 2^(sw[n,k/32]-127)), fp32 accumulation, one bf16 rounding.  Every factor is
- * exact in bf16 and every product exact in fp32, so the result is the one a
- * block-scaled FP4 MMA computes, up to the order of the fp32 additions.  The
- * activations are expanded into a_work (caller-owned bf16 [M][K]); the
- * product runs on the bf16 tensor-core path of qgemm_fp4a16, so the FP4
- * tensor rate (four times bf16's, 3090 article section 5) is not reached.
+ * 2^(sw[n,k/32]-127)), fp32 accumulation, one bf16 rounding.  Every product is
+ * exact in fp32, so the result is the exact-product sum up to the order of
+ * the fp32 additions.
+ * For M > 16 with K % 256 == 0 and both scale arrays 8-byte aligned the
+ * product runs on the block-scaled FP4 tensor cores (tcgen05 kind::mxf4 with
+ * the E8M0 scales applied inside the MMA; the FP4 tensor rate of the 3090
+ * article, section 5) and a_work is not touched.  Otherwise the activations
+ * are expanded exactly to bf16 into a_work and multiplied on the bf16 path of
+ * qgemm_fp4a16.  a_work is caller-owned scratch; its contents afterwards are
+ * unspecified.
  *   w_e2m1 [N][K/2]  w_e8m0 [N][K/32]  a_e2m1 [M][K/2]  a_e8m0 [M][K/32]
- *   a_work [M][K] bf16 (written)  y [M][N] bf16.  Rules as qgemm_fp4a16.     */
+ *   a_work [M][K] bf16 (scratch)  y [M][N] bf16.  Rules as qgemm_fp4a16.     */
 QG_API qg_status qgemm_w4a4_mxfp4(const uint8_t* w_e2m1, const uint8_t* w_e8m0,
                            const uint8_t* a_e2m1, const uint8_t* a_e8m0,
                            uint16_t* a_work, uint16_t* y, int M, int N, int K,

@@ -602,6 +602,10 @@ qg_status check_common(const void* w, const void* x, const void* y, int M, int N
 
 }  // namespace
 
+// block-scaled FP4 W4A4 (gemm_fp4.cu)
+qg_status w4a4_mxfp4_bs(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint8_t* a_e2m1,
+                        const uint8_t* a_e8m0, uint16_t* y, int M, int N, int K, cudaStream_t st, bool* handled);
+
 // entry for the prefill path (gemm_tc.cu) when it declines a shape; w_z
 // (zero points) selects the asymmetric format
 qg_status gemv_w4a16_any_m(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g,
@@ -727,8 +731,10 @@ qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt
   return qg::set_error(QG_ERR_INVALID_ARG, "qgemm_fp4a16: unknown scale format %d", scale_fmt);
 }
 
-// W4A4 numerics on bf16 tensor cores: the MXFP4 activations are expanded to
-// bf16 (exact) into a_work, then the MXFP4-weight GEMM runs on them.
+// W4A4: for M > 16 the block-scaled FP4 tensor cores (gemm_fp4.cu), when K
+// is a multiple of 256 and both scale arrays are 8-byte aligned; otherwise
+// the MXFP4 activations are expanded to bf16 (exact) into a_work and the
+// MXFP4-weight GEMM runs on them.
 qg_status qgemm_w4a4_mxfp4(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint8_t* a_e2m1,
                            const uint8_t* a_e8m0, uint16_t* a_work, uint16_t* y, int M, int N, int K,
                            qg_stream_t stream) {
@@ -737,6 +743,12 @@ qg_status qgemm_w4a4_mxfp4(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const u
   if (r != QG_OK) return r;
   QG_REQUIRE(aligned16(a_e2m1), QG_ERR_MISALIGNED, "qgemm_w4a4_mxfp4: misaligned activation codes");
   if (M == 0) return QG_OK;
+  if (M > 16) {
+    bool handled = false;
+    r = qg::w4a4_mxfp4_bs(w_e2m1, w_e8m0, a_e2m1, a_e8m0, y, M, N, K, reinterpret_cast<cudaStream_t>(stream),
+                          &handled);
+    if (handled) return r;
+  }
   r = qg_dequant_weights(QG_FMT_MXFP4, a_e2m1, a_e8m0, 32, a_work, M, K, stream);
   if (r != QG_OK) return r;
   return qgemm_fp4a16(w_e2m1, w_e8m0, QG_SCALE_E8M0, 32, nullptr, a_work, y, M, N, K, stream);

@@ -1,7 +1,10 @@
 """GPU parity of the W4A4 MXFP4 path (vLLM PR #43557's W4A4 GEMM): the
-activation quantizer's codes, the exact bf16 expansion of the activations and
-the GEMM against the fp64 oracle, which quantizes the same bf16 activations
-by the exponent-first 0.75-threshold rule and multiplies the exact values."""
+activation quantizer's codes and the GEMM against the fp64 oracle, which
+quantizes the same bf16 activations by the exponent-first 0.75-threshold rule
+and multiplies the exact values.  For M > 16 with K a multiple of 256 the
+product runs on the block-scaled FP4 tensor cores (scales applied inside the
+MMA); otherwise the activations are expanded exactly to bf16 in the work
+buffer, which is then checked too."""
 
 import numpy as np
 import pytest
@@ -38,8 +41,15 @@ def expanded(aq, ase):
     return OF.bf16_encode(v.astype(np.float32))
 
 
+def block_scaled(M, K):
+    """The cases qgemm_w4a4_mxfp4 runs on the block-scaled FP4 tensor cores
+    (the test's scale arrays are fresh allocations, 8-byte aligned)."""
+    return M > 16 and K % 256 == 0
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 1024, 1024), (5, 264, 384), (16, 512, 2048), (17, 128, 256),
-                                   (300, 264, 512), (2000, 2600, 384)])
+                                   (300, 264, 512), (2000, 2600, 384), (129, 136, 256), (128, 128, 1280),
+                                   (1000, 1032, 2048), (4096, 384, 768)])
 def test_w4a4(qg, M, N, K):
     x = inputs.activations_bf16(M, K, seed=M + K, outlier_frac=0.01, outlier_scale=50.0)
     wq, wse = weights(N, K, seed=N + 3)
@@ -47,7 +57,8 @@ def test_w4a4(qg, M, N, K):
     y64, aq, ase = OG.w4a4_mxfp4_f64(x, wq, wse)
     np.testing.assert_array_equal(gaq, aq)
     np.testing.assert_array_equal(gase, ase)
-    np.testing.assert_array_equal(work.view(np.uint16), expanded(aq, ase))
+    if not block_scaled(M, K):
+        np.testing.assert_array_equal(work.view(np.uint16), expanded(aq, ase))
     check_gemm(y, OF.bf16_decode(OG.to_bf16(y64)), "w4a4 M=%d N=%d K=%d" % (M, N, K))
 
 
@@ -77,7 +88,8 @@ def test_w4a4_extreme_block_scales(qg, band):
     np.testing.assert_array_equal(gase, ase)
     if band == "low":
         assert ase[:8].min() == 0
-    np.testing.assert_array_equal(work.view(np.uint16), expanded(aq, ase))
+    if not block_scaled(M, K):
+        np.testing.assert_array_equal(work.view(np.uint16), expanded(aq, ase))
     ref = OF.bf16_decode(OG.to_bf16(y64))
     for rows in (slice(0, 8), slice(8, 12), slice(12, M)):      # each magnitude band on its own
         check_gemm(y[rows], ref[rows], "w4a4 %s rows %s" % (band, rows))
@@ -93,3 +105,16 @@ def test_w4a4_config_sampled(qg):
     rows = np.sort(np.random.Generator(np.random.PCG64(11)).choice(M, 96, replace=False))
     y64, _, _ = OG.w4a4_mxfp4_f64(x[rows], wq, wse)
     check_gemm(y[rows], OF.bf16_decode(OG.to_bf16(y64)), "w4a4 config sample")
+
+
+def test_w4a4_block_scaled_matches_the_expansion_path(qg):
+    """The block-scaled product (M = 64, K = 1024) against the bf16-expansion
+    product of the same codes (taken with M = 16 slices, which always expand):
+    both sum the same exact products in fp32, so they agree to within the
+    bf16 output rounding."""
+    M, N, K = 64, 512, 1024
+    x = inputs.activations_bf16(M, K, seed=41, outlier_frac=0.01, outlier_scale=50.0)
+    wq, wse = weights(N, K, seed=42)
+    _, _, _, y = run(qg, x, wq, wse, M, N, K)
+    parts = [run(qg, x[i:i + 16], wq, wse, 16, N, K)[3] for i in range(0, M, 16)]
+    check_gemm(y, np.concatenate(parts), "block-scaled vs expansion")
