@@ -15,28 +15,32 @@
 //   A operand = packed E2M1 weights, 128 channels x 256 k per stage (128-byte
 //               rows), TMA-loaded straight into the 128-byte swizzled K-major
 //               layout;
-//   B operand = packed E2M1 activations, 128 tokens x 256 k, the same way;
+//   B operand = packed E2M1 activations, 256 tokens x 256 k, the same way;
 //   scale factors = E8M0 codes in tensor memory, written from registers
 //               (tcgen05.st) by four warps: for the MMA of k-quarter j (64 k,
-//               two 32-k blocks) a 128-row operand's codes fill a group of
-//               four columns, row 32c + l in column c, lane l (all four lane
-//               quarters hold the same words), bytes 0 and 1 (scale-factor ID
-//               0); A's group is column 8j of the slab's slot, B's 8j + 4, so
-//               every scale-factor address is 4-column aligned;
-//   D         = fp32, two 128-column accumulators (the epilogue of tile i
-//               overlaps the MMAs of tile i + 1).
+//               two 32-k blocks) an operand's codes fill a group of columns,
+//               row 32c + l in column c, lane l (all four lane quarters hold
+//               the same words), bytes 0 and 1 (scale-factor ID 0): four
+//               columns for the 128 weight rows at slot column 4j, eight for
+//               the 256 token rows at slot column 16 + 8j;
+//   D         = fp32, one 128 x 256 accumulator (256 columns): the epilogue
+//               packs it to bf16 in registers and releases it before storing.
+// One MMA instruction covers 128 x 256 x 64: an issue costs about the same
+// at N = 256 as at N = 128, so the wide tile halves the instructions per flop.
 // Persistent: one CTA per SM walks the tiles blockIdx.x, + gridDim.x, ... of
-// 128 tokens x 128 channels (every channel tile of a token tile in turn, so a
+// 256 tokens x 128 channels (every channel tile of a token tile in turn, so a
 // token tile's activations are read once).  Every role counts the k-slabs of
 // all its tiles in one sequence g.
-//   warp 0      TMA for both operands (one elected lane; 6 stages of 32 KB)
+//   warp 0      TMA for both operands (one elected lane; 4 stages of 48 KB)
 //   warp 1      TMEM allocation and MMA issuer (one lane)
 //   warp 2      scheduler: waits for each slab's operands and scale factors,
 //               publishes the ready count the issuer polls
-//   warps 3-10  scale factors: two sets of 4 (lane quarter = warp % 4) taking
-//               alternate slabs, each loading its next slab's codes while it
-//               stores the current one
-//   warps 11-14 epilogue: lane quarter = warp % 4, TMEM -> bf16 -> Y
+//   warps 3-6   scale factors (lane quarter = warp % 4): copy the codes of 2
+//               slabs at a time into shared memory with cp.async, 16
+//               contiguous bytes per row (one row per lane straight from
+//               global memory would cost a wavefront per row), and store each
+//               slab's words into their lane quarter
+//   warps 7-14  epilogue: lane quarter = warp % 4, token half = (warp - 7) / 4
 // Every wait is bounded; on expiry the CTA records a timeout in the device
 // error word, drains what it issued, frees its tensor memory and returns.
 #include <algorithm>
@@ -45,27 +49,40 @@
 
 namespace qg {
 
+bool make_u8_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols);
 bool make_u8_tmap_swizzled(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols);
 
 namespace {
 
 constexpr int bTW = 128;                 // channels per tile (MMA M)
-constexpr int bTT = 128;                 // tokens per tile (MMA N)
+constexpr int bTT = 256;                 // tokens per tile (MMA N)
 constexpr int bBK = 256;                 // k per slab: 128 packed bytes per row
-constexpr int bStages = 6;               // operand stages (A + B)
-constexpr int bSfSlots = 8;              // scale-factor slots in tensor memory
+constexpr int bStages = 4;               // operand stages (A + B)
+constexpr int bSfSlots = 5;              // scale-factor slots in tensor memory
 constexpr int bDone = 8;                 // slab-completion barriers
-constexpr int bOpBytes = bTW * bBK / 2;  // 16 KB per operand per stage
-constexpr int bStageBytes = 2 * bOpBytes;
-constexpr int bSfWarp0 = 3, bSfSets = 2, bEpiWarp0 = bSfWarp0 + 4 * bSfSets;
-constexpr int bThreads = (bEpiWarp0 + 4) * 32;
+constexpr int bABytes = bTW * bBK / 2;   // 16 KB of weights per stage
+constexpr int bBBytes = bTT * bBK / 2;   // 32 KB of activations per stage
+constexpr int bStageBytes = bABytes + bBBytes;
+constexpr int bSfWarp0 = 3, bSfWarps = 4, bEpiWarp0 = bSfWarp0 + bSfWarps, bEpiWarps = 8;
+constexpr int bThreads = (bEpiWarp0 + bEpiWarps) * 32;
 constexpr uint32_t bTmemCols = 512;
-constexpr uint32_t bSfCol0 = 2 * bTT;    // scale-factor slots follow the two accumulators
-constexpr uint32_t bSfCols = 32;         // per slot: MMA j reads A at +8j, B at +8j+4 (4-column aligned)
+constexpr uint32_t bSfCol0 = bTT;        // scale-factor slots follow the accumulator
+constexpr uint32_t bSfCols = 48;         // per slot: MMA j reads A at +4j (4 columns), B at +16+8j (8 columns)
+constexpr uint32_t bSfUsed = 48;         // columns a slot's codes fill
+static_assert(bSfCol0 % 8 == 0 && bSfCols % 8 == 0, "every 8-column group of token codes is 8-column aligned");
+constexpr int bChunk = 2;                // slabs of codes per shared-memory chunk (16 bytes per row)
+constexpr int bSfRows = bTW + bTT;       // code rows per chunk: weights, then tokens
+constexpr int bSfRowBytes = 8 * bChunk;
+constexpr int bSfBufBytes = bSfRows * bSfRowBytes;
+constexpr int bXchBytes = 2 * bSfBufBytes;                   // two chunk buffers
+constexpr int bPieceTok = 16;            // tokens per staged output piece (TMA store box: 128 channels x 16 tokens)
+constexpr int bPieceBytes = bPieceTok * bTW * 2;
+constexpr int bStgBytes = 2 * 2 * bPieceBytes;               // per token half, two pieces in flight
+static_assert(bSfRows * bChunk % (bSfWarps * 32) == 0, "chunk copy divides over the scale-factor threads");
 constexpr uint32_t bDrainCap = 1u << 21;
 static_assert(bDone >= bStages && bDone >= bSfSlots, "slab-completion ring covers every reuse distance");
 static_assert(bSfCol0 + bSfSlots * bSfCols <= bTmemCols, "tensor memory budget");
-static_assert(bSfSlots % bSfSets == 0 && bDone % bSfSets == 0, "a set waits only on its own done entries, in order");
+static_assert(bEpiWarps * 32 * 128 == bTW * bTT, "each epilogue thread owns 128 outputs");
 
 struct Fp4Args {
   const uint8_t* w_sf;                   // [N][K/32] E8M0
@@ -81,8 +98,9 @@ struct __align__(8) Fp4Tail {
   uint64_t full[bStages];                // both operands of the stage landed (TMA bytes)
   uint64_t sf_full[bSfSlots];            // the slot's scale factors stored (4 warps)
   uint64_t done[bDone];                  // slab g's MMAs completed (entry g % bDone)
-  uint64_t acc_full[2];                  // the tile's MMAs completed (one phase per use)
-  uint64_t acc_empty[2];                 // the epilogue has read the accumulator (4 warps)
+  uint64_t sf_tma[2];                    // a chunk of scale-factor codes landed (TMA bytes)
+  uint64_t acc_full;                     // the tile's MMAs completed (one phase per tile)
+  uint64_t acc_empty;                    // the epilogue has read the accumulator (8 warps)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -109,17 +127,49 @@ QG_DEVICE void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint3
       : "memory");
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane
+QG_DEVICE void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr) : "memory");
+}
+
+QG_DEVICE void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;"
+               :: "r"(smem_addr(dst)), "l"(__cvta_generic_to_global(src)) : "memory");
+}
+QG_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+QG_DEVICE void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+QG_DEVICE void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+QG_DEVICE void tma_store_2d(const CUtensorMap* m, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+               :: "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_addr(src)), "r"(x), "r"(y) : "memory");
+}
+QG_DEVICE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+QG_DEVICE void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory"); }
+QG_DEVICE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+QG_DEVICE void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 QG_DEVICE void tile_origin(const Fp4Args& p, int tile, int& m0, int& n0) {
   m0 = (tile / p.tiles_w) * bTT;         // every channel tile of a token tile in turn
   n0 = (tile % p.tiles_w) * bTW;
 }
 
+template <bool kTmaSf>
 __global__ void __launch_bounds__(bThreads, 1)
 w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
-               const Fp4Args p) {
+               const __grid_constant__ CUtensorMap tmap_y, const __grid_constant__ CUtensorMap tmap_wsf,
+               const __grid_constant__ CUtensorMap tmap_asf, const Fp4Args p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Fp4Tail* tl = reinterpret_cast<Fp4Tail*>(smem + bStages * bStageBytes);
+  Fp4Tail* tl = reinterpret_cast<Fp4Tail*>(smem + bStages * bStageBytes + bXchBytes + bStgBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int nslab = p.K / bBK;
@@ -132,18 +182,19 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < bStages; ++s) mbar_init(&tl->full[s], 1);
-    for (int s = 0; s < bSfSlots; ++s) mbar_init(&tl->sf_full[s], 4);     // the 4 warps of the slot's set
+    for (int s = 0; s < bSfSlots; ++s) mbar_init(&tl->sf_full[s], bSfWarps);
     for (int d = 0; d < bDone; ++d) mbar_init(&tl->done[d], 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tl->acc_full[b], 1);
-      mbar_init(&tl->acc_empty[b], 4);
-    }
+    mbar_init(&tl->sf_tma[0], 1);
+    mbar_init(&tl->sf_tma[1], 1);
+    mbar_init(&tl->acc_full, 1);
+    mbar_init(&tl->acc_empty, bEpiWarps);
     mbar_init(&tl->drain, 1);
     tl->abort = 0;
     tl->ready = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tmap_w);
     tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_y);
   }
   if (warp == 1) tmem_alloc(&tl->tmem_base, bTmemCols);
   tc_fence_before();
@@ -164,12 +215,12 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
         uint8_t* stage = smem + st * bStageBytes;
         mbar_arrive_expect_tx(&tl->full[st], bStageBytes);
         tma_load_2d(stage, &tmap_w, &tl->full[st], s * (bBK / 2), n0);
-        tma_load_2d(stage + bOpBytes, &tmap_a, &tl->full[st], s * (bBK / 2), m0);
+        tma_load_2d(stage + bABytes, &tmap_a, &tl->full[st], s * (bBK / 2), m0);
         issued = g + 1;
       }
       if (*abort) {     // let every copy already issued land before the CTA moves on
         for (int g = max(0, issued - bStages); g < issued; ++g)
-          mbar_wait(&tl->full[g % bStages], (g / bStages) & 1, bDrainCap, abort, nullptr);
+          mbar_drain(&tl->full[g % bStages], (g / bStages) & 1, bDrainCap);
       }
     }
   } else if (warp == 1) {
@@ -180,9 +231,8 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
       unsigned int ready = 0;
       int g = 0;
       for (int i = 0; i < ntiles && !*abort; ++i) {
-        const int b = i & 1;
-        if (i >= 2) {             // the accumulator is free once the epilogue has read tile i - 2
-          if (!mbar_wait(&tl->acc_empty[b], ((i - 2) >> 1) & 1, p.cap, abort, p.err)) break;
+        if (i >= 1) {             // the accumulator is free once the epilogue has read tile i - 1
+          if (!mbar_wait(&tl->acc_empty, (i - 1) & 1, p.cap, abort, p.err)) break;
           tc_fence_after();
         }
         bool ok = true;
@@ -191,21 +241,20 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
           if (!wait_count(&tl->ready, (unsigned)g, ready, p.cap * 4, abort, p.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t stage = smem_addr(smem + st * bStageBytes);
-          const uint64_t adesc = sw128_kmajor_desc(stage), bdesc = sw128_kmajor_desc(stage + bOpBytes);
+          const uint64_t adesc = sw128_kmajor_desc(stage), bdesc = sw128_kmajor_desc(stage + bABytes);
           const uint32_t sf = tmem + bSfCol0 + (uint32_t)ss * bSfCols;
 #pragma unroll
           for (int j = 0; j < bBK / 64; ++j)      // K = 64 per MMA: 32 packed bytes of each operand row
-            mma_mxf4(tmem + (uint32_t)(b * bTT), adesc + 2 * j, bdesc + 2 * j, idesc,
-                     sf + 8u * j, sf + 8u * j + 4u, (s | j) != 0);
+            mma_mxf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf + 4u * j, sf + 16u + 8u * j, (s | j) != 0);
           tc_commit(&tl->done[g % bDone]);              // frees the stage and the scale-factor slot
           any = true;
         }
         if (!ok) break;
-        tc_commit(&tl->acc_full[b]);
+        tc_commit(&tl->acc_full);
       }
       if (*abort && any) {
         tc_commit(&tl->drain);
-        mbar_wait(&tl->drain, 0, bDrainCap, abort, nullptr);
+        mbar_drain(&tl->drain, 0, bDrainCap);
       }
     }
   } else if (warp == 2) {
@@ -219,88 +268,180 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
     }
   } else if (warp >= bSfWarp0 && warp < bEpiWarp0) {
     // ---------------- scale factors: E8M0 codes -> tensor memory ----------------
-    // The MMA of k-quarter j (64 k: two 32-k blocks) reads the codes of a
-    // 128-row operand from a group of four columns: row 32c + l sits in column
-    // c, lane l, bytes 0 and 1 (scale-factor ID 0); the same words are
-    // written into all four lane quarters.  A's group for MMA j is column 8j
-    // of the slab's slot, B's column 8j + 4, so every address is 4-column
-    // aligned.  Thread (quarter, lane l) loads the slab's 8 codes of rows
-    // l, 32 + l, 64 + l and 96 + l of both operands; the two sets take
-    // alternate slabs (so a slot is always written by the same set) and load
-    // their next slab's codes while storing the current one.
-    const int q = warp & 3, set = (warp - bSfWarp0) >> 2;
+    // The MMA of k-quarter j (64 k: two 32-k blocks) reads an operand's codes
+    // from a group of columns, row 32c + l in column c, lane l, bytes 0 and 1
+    // (scale-factor ID 0), the same words in all four lane quarters: four
+    // columns for the 128 weight rows (A, slot column 4j), eight for the 256
+    // token rows (B, slot column 16 + 8j), so every address is aligned to
+    // its group's width.  Thread (quarter, lane l) stores the slab's 8 codes
+    // of weight rows 32c + l (c < 4) and token rows 32c + l (c < 8).
+    // The codes arrive in chunks of 2 slabs per tile, 384 rows x 16 bytes
+    // (weight rows first) in one of two shared-memory buffers, the next chunk
+    // in flight while the current one is stored: with K % 512 == 0 two TMA
+    // loads issued by one lane (16-byte rows: the row stride is a multiple of
+    // 16), otherwise 8-byte cp.async by all 128 threads.  Each thread reads
+    // its 12 rows 16 bytes at a time (conflict-free).  A slab's slot was last
+    // used 5 slabs earlier, always in an earlier chunk, so the waits never
+    // depend on the chunk being stored.  Rows past the matrix read zero codes
+    // (TMA fill) or the last row's (cp.async): their operand rows are zero
+    // and their results are not stored.
+    const int q = warp & 3, tid = threadIdx.x - bSfWarp0 * 32;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
     const size_t sf_row = (size_t)(p.K / 32);
-    // codes of slab gn (tile index i, slab s of the tile) for this thread's rows;
-    // rows past the matrix take the last row's codes: their operand rows are
-    // zero (TMA fill) and their results are not stored
-    auto load = [&](int i, int s, uint2 (&wv)[4], uint2 (&av)[4]) {
+    uint8_t* sfb = smem + bStages * bStageBytes;
+    const int nch = (nslab + bChunk - 1) / bChunk, nunits = ntiles * nch;
+    const bool issuer = kTmaSf && tid == 0;
+    auto issue = [&](int u) {
+      const int i = u / nch, k = u % nch;
       int m0, n0;
       tile_origin(p, tile_of(i), m0, n0);
+      uint8_t* buf = sfb + (u & 1) * bSfBufBytes;
+      if constexpr (kTmaSf) {
+        mbar_arrive_expect_tx(&tl->sf_tma[u & 1], bSfBufBytes);
+        tma_load_2d(buf, &tmap_wsf, &tl->sf_tma[u & 1], bSfRowBytes * k, n0);
+        tma_load_2d(buf + bTW * bSfRowBytes, &tmap_asf, &tl->sf_tma[u & 1], bSfRowBytes * k, m0);
+      } else {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        wv[c] = __ldg(reinterpret_cast<const uint2*>(p.w_sf + (size_t)min(n0 + 32 * c + lane, p.N - 1) * sf_row + s * 8));
-        av[c] = __ldg(reinterpret_cast<const uint2*>(p.a_sf + (size_t)min(m0 + 32 * c + lane, p.M - 1) * sf_row + s * 8));
+        for (int e = 0; e < bSfRows * bChunk / (bSfWarps * 32); ++e) {
+          const int t = tid + bSfWarps * 32 * e, row = t / bChunk, j = t % bChunk, s = bChunk * k + j;
+          if (s < nslab) {
+            const uint8_t* src = row < bTW ? p.w_sf + (size_t)min(n0 + row, p.N - 1) * sf_row
+                                           : p.a_sf + (size_t)min(m0 + row - bTW, p.M - 1) * sf_row;
+            cp_async8(buf + row * bSfRowBytes + 8 * j, src + 8 * s);
+          }
+        }
+        cp_async_commit();
       }
     };
-    uint2 wv[4], av[4];
-    if (set < total) load(set / nslab, set % nslab, wv, av);
-    for (int g = set; g < total; g += bSfSets) {
-      uint32_t cols[32];
+    bool live = true;            // every warp runs every iteration: the barrier counts stay equal
+    int issued = 0;              // chunks the TMA lane has issued (it stops once its warp gave up)
+    if (nunits > 0 && (issuer || !kTmaSf)) {
+      issue(0);
+      issued = 1;
+    }
+    for (int u = 0; u < nunits; ++u) {
+      if (u + 1 < nunits) {
+        if (!kTmaSf || (issuer && live)) {
+          issue(u + 1);
+          issued = u + 2;
+        }
+      } else if (!kTmaSf) {
+        cp_async_commit();
+      }
+      if constexpr (kTmaSf) {
+        if (live) live = mbar_wait_warp(&tl->sf_tma[u & 1], (u >> 1) & 1, p.cap, abort, p.err);
+      } else {
+        cp_async_wait<1>();                                      // this thread's copies of chunk u landed
+        named_bar_sync(1, bSfWarps * 32);
+      }
+      const int i = u / nch, k = u % nch;
+      const uint8_t* buf = sfb + (u & 1) * bSfBufBytes;
+      uint4 wr[4], ar[8];                                        // rows 32c + l: both slabs' codes
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int c = 0; c < 4; ++c) wr[c] = *reinterpret_cast<const uint4*>(buf + (32 * c + lane) * bSfRowBytes);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t w = j < 2 ? wv[c].x : wv[c].y, a = j < 2 ? av[c].x : av[c].y;
-          cols[8 * j + c] = (w >> (16 * (j & 1))) & 0xFFFFu;       // blocks 2j, 2j + 1 of row 32c + l
-          cols[8 * j + 4 + c] = (a >> (16 * (j & 1))) & 0xFFFFu;
+      for (int c = 0; c < 8; ++c) ar[c] = *reinterpret_cast<const uint4*>(buf + (bTW + 32 * c + lane) * bSfRowBytes);
+      // Both slabs of the chunk go out after one wait: the MMAs complete in
+      // order, so the chunk's last slab's slot being free (slab g1 - 5 done)
+      // frees the others; one wait::st then covers all the stores.
+      const int s0 = bChunk * k, ns = min(bChunk, nslab - s0), g0 = i * nslab + s0, g1 = g0 + ns - 1;
+      const int gp = g1 - bSfSlots;
+      if (live && gp >= 0) {
+        live = mbar_wait_warp(&tl->done[gp % bDone], (gp / bDone) & 1, p.cap, abort, p.err);
+        if (live) tc_fence_after();
+      }
+#pragma unroll
+      for (int j = 0; j < bChunk; ++j) {
+        if (j >= ns) break;
+        uint32_t cols[bSfUsed];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int half = jj >> 1, sh = 16 * (jj & 1);          // word of the slab's 8 codes, byte pair
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {                          // blocks 2jj, 2jj + 1 of weight row 32c + l
+            const uint32_t w = j == 0 ? (half ? wr[c].y : wr[c].x) : (half ? wr[c].w : wr[c].z);
+            cols[4 * jj + c] = (w >> sh) & 0xFFFFu;
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {                          // blocks 2jj, 2jj + 1 of token row 32c + l
+            const uint32_t a = j == 0 ? (half ? ar[c].y : ar[c].x) : (half ? ar[c].w : ar[c].z);
+            cols[16 + 8 * jj + c] = (a >> sh) & 0xFFFFu;
+          }
+        }
+        if (live) {
+          const uint32_t at = tmem + lane_addr + bSfCol0 + (uint32_t)((g0 + j) % bSfSlots) * bSfCols;
+#pragma unroll
+          for (int h = 0; h < (int)bSfUsed / 16; ++h)
+            tmem_st16(at + 16u * h, *reinterpret_cast<const uint32_t(*)[16]>(&cols[16 * h]));
         }
       }
-      const int gn = g + bSfSets;                                // this set's next slab: load it now
-      if (gn < total) load(gn / nslab, gn % nslab, wv, av);
-      const int ss = g % bSfSlots, gp = g - bSfSlots;            // the slot last held slab gp
-      if (gp >= 0) {
-        if (!mbar_wait_warp(&tl->done[gp % bDone], (gp / bDone) & 1, p.cap, abort, p.err)) break;
-        tc_fence_after();
+      if (live) {
+        tmem_wait_st();
+        tc_fence_before();
+        for (int j = 0; j < ns; ++j) mbar_arrive_warp(&tl->sf_full[(g0 + j) % bSfSlots]);
       }
-      {
-        const uint32_t (&c0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&cols[0]);
-        const uint32_t (&c1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&cols[16]);
-        const uint32_t at = tmem + lane_addr + bSfCol0 + (uint32_t)ss * bSfCols;
-        tmem_st16(at, c0);
-        tmem_st16(at + 16, c1);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive_warp(&tl->sf_full[ss]);
+      named_bar_sync(1, bSfWarps * 32);                          // buffer u & 1 is refilled by chunk u + 2
+    }
+    if constexpr (kTmaSf) {
+      if (issuer && *abort)      // let the chunks still in flight land before the CTA moves on
+        for (int u = max(0, issued - 2); u < issued; ++u) mbar_drain(&tl->sf_tma[u & 1], (u >> 1) & 1, bDrainCap);
+    } else {
+      cp_async_wait<0>();
     }
   } else {
     // ---------------- epilogue: TMEM -> bf16 -> Y ----------------
-    const int q = warp & 3, row = 32 * q + lane;
+    // Eight warps: lane quarter warp % 4 (channel rows 32q .. 32q + 31), token
+    // half h (accumulator columns 128h .. 128h + 127).  A thread packs its
+    // 128 results to bf16 in registers and releases the accumulator; the
+    // half then writes 16 tokens at a time into one of two staging buffers
+    // ([token][128 channels], 32 consecutive channels per warp store) and one
+    // lane issues the TMA tile store, which clips rows and channels past the
+    // matrix.  (Per-thread global stores, 64 bytes per warp instruction,
+    // held the tensor pipe back by about a sixth.)
+    const int q = warp & 3, h = (warp - bEpiWarp0) >> 2, row = 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
+    uint8_t* stg = smem + bStages * bStageBytes + bXchBytes + h * 2 * bPieceBytes;
+    const bool leader = warp == bEpiWarp0 + 4 * h && lane == 0;
+    int piece = 0;
     for (int i = 0; i < ntiles; ++i) {
-      const int b = i & 1;
-      if (!mbar_wait_warp(&tl->acc_full[b], (i >> 1) & 1, p.cap, abort, p.err)) break;
+      if (!mbar_wait_warp(&tl->acc_full, i & 1, p.cap, abort, p.err)) break;
       tc_fence_after();
+      uint32_t pk[64];
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_addr + (uint32_t)(128 * h + c0), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 16; c += 2)
+          pk[(c0 + c) / 2] = f32_to_bf16_bits(__uint_as_float(v[c])) |
+                             ((uint32_t)f32_to_bf16_bits(__uint_as_float(v[c + 1])) << 16);
+      }
+      tc_fence_before();
+      mbar_arrive_warp(&tl->acc_empty);                  // the MMAs of tile i + 1 may overwrite it
       int m0, n0;
       tile_origin(p, tile_of(i), m0, n0);
-      const int nn = n0 + row;
-#pragma unroll 1
-      for (int c0 = 0; c0 < bTT; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_addr + (uint32_t)(b * bTT + c0), v);
-        tmem_wait_ld();
-        if (c0 + 32 == bTT) {
-          tc_fence_before();
-          mbar_arrive_warp(&tl->acc_empty[b]);           // the MMAs of tile i + 2 may overwrite it
-        }
-        if (nn < p.N) {
+      const int t0 = m0 + 128 * h;
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (m0 + c0 + c < p.M) p.y[(size_t)(m0 + c0 + c) * p.N + nn] = f32_to_bf16_bits(__uint_as_float(v[c]));
+      for (int pc = 0; pc < 128 / bPieceTok; ++pc) {
+        const int tp = t0 + bPieceTok * pc;
+        if (tp >= p.M) break;                          // the remaining pieces lie past the matrix too
+        uint16_t* buf = reinterpret_cast<uint16_t*>(stg + (piece & 1) * bPieceBytes);
+        if (leader) bulk_wait_read<1>();               // the store issued from this buffer has read it
+        named_bar_sync(2 + h, 128);
+#pragma unroll
+        for (int c = 0; c < bPieceTok; ++c)
+          buf[c * bTW + row] = (uint16_t)(pk[(bPieceTok * pc + c) / 2] >> (16 * (c & 1)));
+        fence_proxy_async_smem();
+        named_bar_sync(2 + h, 128);
+        if (leader) {
+          tma_store_2d(&tmap_y, buf, 2 * n0, tp);
+          bulk_commit();
         }
+        ++piece;
       }
     }
+    if (leader) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -322,11 +463,24 @@ qg_status w4a4_mxfp4_bs(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint
   if (K % bBK != 0 || (reinterpret_cast<uintptr_t>(w_e8m0) & 7) || (reinterpret_cast<uintptr_t>(a_e8m0) & 7))
     return QG_OK;
   *handled = true;
-  CUtensorMap tmap_w, tmap_a;
+  CUtensorMap tmap_w, tmap_a, tmap_y, tmap_wsf, tmap_asf;
   if (!make_u8_tmap_swizzled(&tmap_w, w_e2m1, N, K / 2, bTW, bBK / 2))
     return set_error(QG_ERR_CUDA, "qgemm_w4a4_mxfp4: cannot encode the weight tensor map");
   if (!make_u8_tmap_swizzled(&tmap_a, a_e2m1, M, K / 2, bTT, bBK / 2))
     return set_error(QG_ERR_CUDA, "qgemm_w4a4_mxfp4: cannot encode the activation tensor map");
+  // Y as bytes [M][2N] (16-byte aligned, N % 8 == 0: checked by the caller):
+  // a box of 128 channels x 16 tokens per store
+  if (!make_u8_tmap(&tmap_y, y, M, 2 * N, bPieceTok, 2 * bTW))
+    return set_error(QG_ERR_CUDA, "qgemm_w4a4_mxfp4: cannot encode the output tensor map");
+  // Scale-factor codes by TMA: rows of K/32 bytes need a 16-byte multiple
+  const bool tma_sf = K % 512 == 0 && (reinterpret_cast<uintptr_t>(w_e8m0) & 15) == 0 &&
+                      (reinterpret_cast<uintptr_t>(a_e8m0) & 15) == 0 &&
+                      make_u8_tmap(&tmap_wsf, w_e8m0, N, K / 32, bTW, bSfRowBytes) &&
+                      make_u8_tmap(&tmap_asf, a_e8m0, M, K / 32, bTT, bSfRowBytes);
+  if (!tma_sf) {
+    memset(&tmap_wsf, 0, sizeof(tmap_wsf));
+    memset(&tmap_asf, 0, sizeof(tmap_asf));
+  }
   unsigned int* err = device_error_word();
   if (!err) return set_error(QG_ERR_CUDA, "qgemm_w4a4_mxfp4: no device error word");
   Fp4Args a{};
@@ -335,11 +489,12 @@ qg_status w4a4_mxfp4_bs(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint
   a.tiles_w = (N + bTW - 1) / bTW;
   a.err = err;
   a.cap = wait_limit();
-  const int smem = bStages * bStageBytes + (int)sizeof(Fp4Tail) + 1024;
-  if (!ensure_smem(w4a4_bs_kernel, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a4_mxfp4: smem attribute");
+  const int smem = bStages * bStageBytes + bXchBytes + bStgBytes + (int)sizeof(Fp4Tail) + 1024;
+  auto kern = tma_sf ? w4a4_bs_kernel<true> : w4a4_bs_kernel<false>;
+  if (!ensure_smem(kern, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a4_mxfp4: smem attribute");
   const long long tiles = (long long)a.tiles_t * a.tiles_w;
   const int grid = (int)std::min<long long>(tiles, (long long)sm_count());   // persistent: one CTA per SM
-  w4a4_bs_kernel<<<grid, bThreads, smem, st>>>(tmap_w, tmap_a, a);
+  kern<<<grid, bThreads, smem, st>>>(tmap_w, tmap_a, tmap_y, tmap_wsf, tmap_asf, a);
   return check_launch("qgemm_w4a4_mxfp4 (block-scaled)");
 }
 

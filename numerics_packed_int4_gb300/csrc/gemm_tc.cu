@@ -183,7 +183,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       }
       if (*abort) {     // let every copy already issued land before the CTA exits
         for (int g = max(0, issued - kSt); g < issued; ++g)
-          mbar_wait(&tl->x_full[g % kSt], (g / kSt) & 1, kDrainCap, abort, nullptr);
+          mbar_drain(&tl->x_full[g % kSt], (g / kSt) & 1, kDrainCap);
       }
     }
   } else if (warp == 2) {
@@ -201,7 +201,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       }
       if (*abort) {
         for (int g = max(0, issued - kASlots); g < issued; ++g)
-          mbar_wait(&tl->w_full[g % kASlots], (g / kASlots) & 1, kDrainCap, abort, nullptr);
+          mbar_drain(&tl->w_full[g % kASlots], (g / kASlots) & 1, kDrainCap);
       }
     }
   } else if (warp == 1) {
@@ -234,7 +234,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       }
       if (*abort && any) {
         tc_commit(&tl->drain);                         // every MMA issued so far completes
-        mbar_wait(&tl->drain, 0, kDrainCap, abort, nullptr);
+        mbar_drain(&tl->drain, 0, kDrainCap);
       }
     }
   } else if (warp == kSchedWarp) {

@@ -197,7 +197,7 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       }
       if (*abort) {
         for (int g = max(0, issued - hSlots); g < issued; ++g)
-          mbar_wait(&tl->w_full[g % hSlots], (g / hSlots) & 1, hDrainCap, abort, nullptr);
+          mbar_drain(&tl->w_full[g % hSlots], (g / hSlots) & 1, hDrainCap);
       }
     }
   } else if (warp == 2) {
@@ -215,7 +215,7 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       }
       if (*abort) {
         for (int g = max(0, issued - hXStages); g < issued; ++g)
-          mbar_wait(&tl->x_full[g % hXStages], (g / hXStages) & 1, hDrainCap, abort, nullptr);
+          mbar_drain(&tl->x_full[g % hXStages], (g / hXStages) & 1, hDrainCap);
       }
     }
   } else if (warp == 1) {
@@ -247,7 +247,7 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       }
       if (*abort && any) {
         tc_commit(&tl->drain);
-        mbar_wait(&tl->drain, 0, hDrainCap, abort, nullptr);
+        mbar_drain(&tl->drain, 0, hDrainCap);
       }
     }
   } else if (warp == hSchedWarp) {

@@ -241,7 +241,7 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
       }
       if (*abort) {
         for (int g = max(0, issued - pWStages); g < issued; ++g)
-          mbar_wait(&tl->w_full[g % pWStages], (g / pWStages) & 1, pDrainCap, abort, nullptr);
+          mbar_drain(&tl->w_full[g % pWStages], (g / pWStages) & 1, pDrainCap);
       }
     }
   } else if (warp == 2) {
@@ -260,7 +260,7 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
       }
       if (*abort) {
         for (int g = max(0, issued - pXStages); g < issued; ++g)
-          mbar_wait(&tl->x_full[g % pXStages], (g / pXStages) & 1, pDrainCap, abort, nullptr);
+          mbar_drain(&tl->x_full[g % pXStages], (g / pXStages) & 1, pDrainCap);
       }
     }
   } else if (warp == 1) {
@@ -291,7 +291,7 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
       }
       if (*abort && any) {
         tc_commit(&tl->drain);
-        mbar_wait(&tl->drain, 0, pDrainCap, abort, nullptr);
+        mbar_drain(&tl->drain, 0, pDrainCap);
       }
     }
   } else if (warp == pSchedWarp) {

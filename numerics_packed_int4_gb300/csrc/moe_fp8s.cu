@@ -227,7 +227,7 @@ moe_fp8s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
       }
       if (*abort) {
         for (int g = max(0, issued - fSlots); g < issued; ++g)
-          mbar_wait(&tl->w_full[g % fSlots], (g / fSlots) & 1, fDrainCap, abort, nullptr);
+          mbar_drain(&tl->w_full[g % fSlots], (g / fSlots) & 1, fDrainCap);
       }
     }
   } else if (warp == 2) {
@@ -245,7 +245,7 @@ moe_fp8s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
       }
       if (*abort) {
         for (int g = max(0, issued - fXStages); g < issued; ++g)
-          mbar_wait(&tl->x_full[g % fXStages], (g / fXStages) & 1, fDrainCap, abort, nullptr);
+          mbar_drain(&tl->x_full[g % fXStages], (g / fXStages) & 1, fDrainCap);
       }
     }
   } else if (warp == 1) {
@@ -283,7 +283,7 @@ moe_fp8s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
       }
       if (*abort && any) {
         tc_commit(&tl->drain);
-        mbar_wait(&tl->drain, 0, fDrainCap, abort, nullptr);
+        mbar_drain(&tl->drain, 0, fDrainCap);
       }
     }
   } else if (warp == fSchedWarp) {

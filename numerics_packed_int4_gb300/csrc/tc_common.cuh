@@ -53,6 +53,15 @@ QG_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t cap, volatile 
   return false;
 }
 
+// Bounded wait that ignores 'abort': once a role has given up, the copies and
+// MMAs the CTA already issued must still land before it releases its shared
+// and tensor memory.  Gives up after 'cap' polls and returns false.
+QG_DEVICE bool mbar_drain(uint64_t* bar, uint32_t parity, uint32_t cap) {
+  for (uint32_t i = 0; i < cap; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
 // Warp-collective bounded wait: every lane polls, the warp leaves together
 // (needed before warp-collective tcgen05.st / tcgen05.ld).
 QG_DEVICE bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t cap, volatile int* abort,

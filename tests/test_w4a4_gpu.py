@@ -3,8 +3,8 @@ activation quantizer's codes and the GEMM against the fp64 oracle, which
 quantizes the same bf16 activations by the exponent-first 0.75-threshold rule
 and multiplies the exact values.  For M > 16 with K a multiple of 256 the
 product runs on the block-scaled FP4 tensor cores (scales applied inside the
-MMA); otherwise the activations are expanded exactly to bf16 in the work
-buffer, which is then checked too."""
+MMA, the output written by TMA tile stores); otherwise the activations are expanded
+exactly to bf16 in the work buffer, which is then checked too."""
 
 import numpy as np
 import pytest
@@ -118,3 +118,4 @@ def test_w4a4_block_scaled_matches_the_expansion_path(qg):
     _, _, _, y = run(qg, x, wq, wse, M, N, K)
     parts = [run(qg, x[i:i + 16], wq, wse, 16, N, K)[3] for i in range(0, M, 16)]
     check_gemm(y, np.concatenate(parts), "block-scaled vs expansion")
+
