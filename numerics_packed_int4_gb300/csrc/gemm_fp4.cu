@@ -17,12 +17,14 @@
 //               layout;
 //   B operand = packed E2M1 activations, 256 tokens x 256 k, the same way;
 //   scale factors = E8M0 codes in tensor memory, written from registers
-//               (tcgen05.st) by four warps: for the MMA of k-quarter j (64 k,
-//               two 32-k blocks) an operand's codes fill a group of columns,
-//               row 32c + l in column c, lane l (all four lane quarters hold
-//               the same words), bytes 0 and 1 (scale-factor ID 0): four
-//               columns for the 128 weight rows at slot column 4j, eight for
-//               the 256 token rows at slot column 16 + 8j;
+//               (tcgen05.st) by four warps: an operand's codes fill a group of
+//               columns, row 32c + l in column c, lane l (all four lane
+//               quarters hold the same words), one 32-bit word = a row's codes
+//               of 4 consecutive 32-k blocks; the MMA of k-quarter j (64 k)
+//               reads bytes 0-1 (scale-factor ID 0, j even) or 2-3 (ID 2, j
+//               odd) of the group for pair p = j / 2: four columns for the 128
+//               weight rows at slot column 4p, eight for the 256 token rows at
+//               slot column 8 + 8p (24 of a slot's 32 columns per 256-k slab);
 //   D         = fp32, one 128 x 256 accumulator (256 columns): the epilogue
 //               packs it to bf16 in registers and releases it before storing.
 // One MMA instruction covers 128 x 256 x 64: an issue costs about the same
@@ -58,8 +60,8 @@ constexpr int bTW = 128;                 // channels per tile (MMA M)
 constexpr int bTT = 256;                 // tokens per tile (MMA N)
 constexpr int bBK = 256;                 // k per slab: 128 packed bytes per row
 constexpr int bStages = 4;               // operand stages (A + B)
-constexpr int bSfSlots = 5;              // scale-factor slots in tensor memory
-constexpr int bDone = 8;                 // slab-completion barriers
+constexpr int bSfSlots = 8;              // scale-factor slots in tensor memory
+constexpr int bDone = 16;                // slab-completion barriers
 constexpr int bABytes = bTW * bBK / 2;   // 16 KB of weights per stage
 constexpr int bBBytes = bTT * bBK / 2;   // 32 KB of activations per stage
 constexpr int bStageBytes = bABytes + bBBytes;
@@ -67,9 +69,9 @@ constexpr int bSfWarp0 = 3, bSfWarps = 4, bEpiWarp0 = bSfWarp0 + bSfWarps, bEpiW
 constexpr int bThreads = (bEpiWarp0 + bEpiWarps) * 32;
 constexpr uint32_t bTmemCols = 512;
 constexpr uint32_t bSfCol0 = bTT;        // scale-factor slots follow the accumulator
-constexpr uint32_t bSfCols = 48;         // per slot: MMA j reads A at +4j (4 columns), B at +16+8j (8 columns)
-constexpr uint32_t bSfUsed = 48;         // columns a slot's codes fill
-static_assert(bSfCol0 % 8 == 0 && bSfCols % 8 == 0, "every 8-column group of token codes is 8-column aligned");
+constexpr uint32_t bSfCols = 32;         // per slot: MMAs 2p, 2p + 1 read A at +4p (4 columns), B at +8 + 8p (8);
+                                         // 24 used, each store aligned to its width
+static_assert(bSfCol0 % 32 == 0 && bSfCols % 32 == 0, "slots 32-column aligned: every store and code group aligned to its width");
 constexpr int bChunk = 2;                // slabs of codes per shared-memory chunk (16 bytes per row)
 constexpr int bSfRows = bTW + bTT;       // code rows per chunk: weights, then tokens
 constexpr int bSfRowBytes = 8 * bChunk;
@@ -80,7 +82,7 @@ constexpr int bPieceBytes = bPieceTok * bTW * 2;
 constexpr int bStgBytes = 2 * 2 * bPieceBytes;               // per token half, two pieces in flight
 static_assert(bSfRows * bChunk % (bSfWarps * 32) == 0, "chunk copy divides over the scale-factor threads");
 constexpr uint32_t bDrainCap = 1u << 21;
-static_assert(bDone >= bStages && bDone >= bSfSlots, "slab-completion ring covers every reuse distance");
+static_assert(bDone >= bStages && bDone > bSfSlots, "slab-completion ring covers every reuse distance");
 static_assert(bSfCol0 + bSfSlots * bSfCols <= bTmemCols, "tensor memory budget");
 static_assert(bEpiWarps * 32 * 128 == bTW * bTT, "each epilogue thread owns 128 outputs");
 
@@ -157,6 +159,12 @@ QG_DEVICE void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0
 QG_DEVICE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 QG_DEVICE void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+QG_DEVICE void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 QG_DEVICE void tile_origin(const Fp4Args& p, int tile, int& m0, int& n0) {
   m0 = (tile / p.tiles_w) * bTT;         // every channel tile of a token tile in turn
   n0 = (tile % p.tiles_w) * bTW;
@@ -226,7 +234,7 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_mxf4(bTW, bTT, 0);
+      const uint32_t idesc[2] = {idesc_mxf4(bTW, bTT, 0), idesc_mxf4(bTW, bTT, 2)};   // bytes 0-1, bytes 2-3
       bool any = false;
       unsigned int ready = 0;
       int g = 0;
@@ -245,7 +253,8 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
           const uint32_t sf = tmem + bSfCol0 + (uint32_t)ss * bSfCols;
 #pragma unroll
           for (int j = 0; j < bBK / 64; ++j)      // K = 64 per MMA: 32 packed bytes of each operand row
-            mma_mxf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf + 4u * j, sf + 16u + 8u * j, (s | j) != 0);
+            mma_mxf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc[j & 1], sf + 4u * (j >> 1), sf + 8u + 8u * (j >> 1),
+                     (s | j) != 0);
           tc_commit(&tl->done[g % bDone]);              // frees the stage and the scale-factor slot
           any = true;
         }
@@ -268,20 +277,21 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
     }
   } else if (warp >= bSfWarp0 && warp < bEpiWarp0) {
     // ---------------- scale factors: E8M0 codes -> tensor memory ----------------
-    // The MMA of k-quarter j (64 k: two 32-k blocks) reads an operand's codes
-    // from a group of columns, row 32c + l in column c, lane l, bytes 0 and 1
-    // (scale-factor ID 0), the same words in all four lane quarters: four
-    // columns for the 128 weight rows (A, slot column 4j), eight for the 256
-    // token rows (B, slot column 16 + 8j), so every address is aligned to
-    // its group's width.  Thread (quarter, lane l) stores the slab's 8 codes
-    // of weight rows 32c + l (c < 4) and token rows 32c + l (c < 8).
+    // The MMAs of k-quarters 2p and 2p + 1 read an operand's codes from a
+    // group of columns, row 32c + l in column c, lane l, the same words in
+    // all four lane quarters, bytes 0-1 and 2-3 of a word that holds the
+    // row's codes of 4 consecutive 32-k blocks: four columns for the 128
+    // weight rows (A, slot column 4p), eight for the 256 token rows (B, slot
+    // column 8 + 8p), so every address is aligned to its group's width.
+    // Thread (quarter, lane l) stores the slab's 8 codes of weight rows
+    // 32c + l (c < 4) and token rows 32c + l (c < 8) as they are in memory.
     // The codes arrive in chunks of 2 slabs per tile, 384 rows x 16 bytes
     // (weight rows first) in one of two shared-memory buffers, the next chunk
     // in flight while the current one is stored: with K % 512 == 0 two TMA
     // loads issued by one lane (16-byte rows: the row stride is a multiple of
     // 16), otherwise 8-byte cp.async by all 128 threads.  Each thread reads
     // its 12 rows 16 bytes at a time (conflict-free).  A slab's slot was last
-    // used 5 slabs earlier, always in an earlier chunk, so the waits never
+    // used 8 slabs earlier, always in an earlier chunk, so the waits never
     // depend on the chunk being stored.  Rows past the matrix read zero codes
     // (TMA fill) or the last row's (cp.async): their operand rows are zero
     // and their results are not stored.
@@ -342,7 +352,7 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
 #pragma unroll
       for (int c = 0; c < 8; ++c) ar[c] = *reinterpret_cast<const uint4*>(buf + (bTW + 32 * c + lane) * bSfRowBytes);
       // Both slabs of the chunk go out after one wait: the MMAs complete in
-      // order, so the chunk's last slab's slot being free (slab g1 - 5 done)
+      // order, so the chunk's last slab's slot being free (slab g1 - 8 done)
       // frees the others; one wait::st then covers all the stores.
       const int s0 = bChunk * k, ns = min(bChunk, nslab - s0), g0 = i * nslab + s0, g1 = g0 + ns - 1;
       const int gp = g1 - bSfSlots;
@@ -353,26 +363,23 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
 #pragma unroll
       for (int j = 0; j < bChunk; ++j) {
         if (j >= ns) break;
-        uint32_t cols[bSfUsed];
+        // one 32-bit word = a row's codes of 4 consecutive 32-k blocks: the
+        // MMAs of k-quarters 2p and 2p + 1 read its bytes 0-1 and 2-3
+        uint32_t cols[24];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int half = jj >> 1, sh = 16 * (jj & 1);          // word of the slab's 8 codes, byte pair
+        for (int c = 0; c < 4; ++c) {
+          cols[c] = j == 0 ? wr[c].x : wr[c].z;
+          cols[4 + c] = j == 0 ? wr[c].y : wr[c].w;
+        }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {                          // blocks 2jj, 2jj + 1 of weight row 32c + l
-            const uint32_t w = j == 0 ? (half ? wr[c].y : wr[c].x) : (half ? wr[c].w : wr[c].z);
-            cols[4 * jj + c] = (w >> sh) & 0xFFFFu;
-          }
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {                          // blocks 2jj, 2jj + 1 of token row 32c + l
-            const uint32_t a = j == 0 ? (half ? ar[c].y : ar[c].x) : (half ? ar[c].w : ar[c].z);
-            cols[16 + 8 * jj + c] = (a >> sh) & 0xFFFFu;
-          }
+        for (int c = 0; c < 8; ++c) {
+          cols[8 + c] = j == 0 ? ar[c].x : ar[c].z;
+          cols[16 + c] = j == 0 ? ar[c].y : ar[c].w;
         }
         if (live) {
           const uint32_t at = tmem + lane_addr + bSfCol0 + (uint32_t)((g0 + j) % bSfSlots) * bSfCols;
-#pragma unroll
-          for (int h = 0; h < (int)bSfUsed / 16; ++h)
-            tmem_st16(at + 16u * h, *reinterpret_cast<const uint32_t(*)[16]>(&cols[16 * h]));
+          tmem_st16(at, *reinterpret_cast<const uint32_t(*)[16]>(&cols[0]));
+          tmem_st8(at + 16u, *reinterpret_cast<const uint32_t(*)[8]>(&cols[16]));
         }
       }
       if (live) {
