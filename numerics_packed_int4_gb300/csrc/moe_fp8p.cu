@@ -366,34 +366,39 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
     int ti = 0, s = 0;                                   // tile index and slab of the group promoted next
     PTile t = tile_of(0);
     const uint16_t* srow = p.ws + ((size_t)t.e * p.N + min(t.n0 + row, p.N - 1)) * ng;
-    float sc = bf16_bits_to_f32(__ldg(srow));
+    // The next group's scale is fetched one group ahead and kept raw: it is
+    // widened only after that group's wait, so no group stalls on its load.
+    uint32_t raw = __ldg(srow);
     for (int g = 0; g < total; ++g) {
       // next group's scale (the next tile's first when this group ends the tile)
-      float sc_next = 0.f;
+      uint32_t raw_next = 0;
       PTile t_next = t;
       const uint16_t* srow_next = srow;
       if (s + 1 < nslab) {
-        sc_next = bf16_bits_to_f32(__ldg(srow + s + 1));
+        raw_next = __ldg(srow + s + 1);
       } else if (ti + 1 < ntiles) {
         t_next = tile_of(ti + 1);
         srow_next = p.ws + ((size_t)t_next.e * p.N + min(t_next.n0 + row, p.N - 1)) * ng;
-        sc_next = bf16_bits_to_f32(__ldg(srow_next));
+        raw_next = __ldg(srow_next);
       }
       const int b = g % pBufs;
       if (!mbar_wait_warp(&tl->done[g % pDone], (g / pDone) & 1, p.cap, abort, p.err)) break;
       tc_fence_after();
+      const float sc = __uint_as_float(raw << 16);
 #pragma unroll
       for (int h = 0; h < pProCols / 16; ++h) {
         uint32_t v[16];
         tmem_ld16(tmem + lane_addr + (uint32_t)(b * pTT + pProCols * cq + 16 * h), v);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 16; ++c) sum[16 * h + c] = __fmaf_rn(sc, __uint_as_float(v[c]), sum[16 * h + c]);
+        for (int c = 0; c < 16; c += 2)                  // two fused multiply-adds per packed op
+          ffma2(sum[16 * h + c], sum[16 * h + c + 1], sc, sc, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                sum[16 * h + c], sum[16 * h + c + 1]);
       }
       tc_fence_before();
       mbar_arrive_warp(&tl->g_empty[b]);                 // the accumulator may take group g + 3
       if (s + 1 == nslab) {
-        // tile done: token scale, one bf16 rounding, store; lane l fetches the
+        // tile done: token scale, one bf16 rounding, store; lane l holds the
         // token scales of rows pProCols * cq + l (+ 32), the others come by shuffle
         const int mb = t.r0 + pProCols * cq;
         const int nn = t.n0 + row;
@@ -413,7 +418,7 @@ moe_fp8p_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
       } else {
         ++s;
       }
-      sc = sc_next;
+      raw = raw_next;
     }
   }
 

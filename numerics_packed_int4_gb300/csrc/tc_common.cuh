@@ -262,6 +262,12 @@ QG_DEVICE void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b
       " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
       : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
+// (a0, a1) * (b0, b1) + (c0, c1), two IEEE fused multiply-adds in one packed op
+QG_DEVICE void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
 // two fp32 -> bf16x2 (lo in the low half), round to nearest even
 QG_DEVICE uint32_t f32x2_to_bf16x2(float lo, float hi) {
   uint32_t d;
