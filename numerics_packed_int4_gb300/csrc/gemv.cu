@@ -114,29 +114,45 @@ QG_DEVICE const uint8_t* zero_row(const GemvArgs& p, int n) {
 }
 
 // G1: INT4 with g == 128, one group per segment: the group index is the
-// segment index.  FOLD: the GEMV's folded FP4 factors in s.b (MXFP4; 0 when
-// the code is above 128) and s.a (NVFP4, both codes of the segment); without
-// FOLD the raw codes (the canonical dequant export).
-template <int FMT, bool G1, bool FOLD = false>
+// segment index.  load_scale fetches the raw scale (and zero-point) codes of
+// a segment; finish_scale turns them into the decode's operands.  The GEMV
+// prefetches raw codes a few segments ahead and finishes them only when the
+// segment is decoded, so no warp waits on a prefetch.  FOLD: the GEMV's
+// folded FP4 factors in s.b (MXFP4; 0 when the code is above 128) and s.a
+// (NVFP4, both codes of the segment); without FOLD the raw codes (the
+// canonical dequant export).
+template <int FMT, bool G1>
 QG_DEVICE Scale load_scale(const GemvArgs& p, const uint8_t* srow, const uint8_t* zrow, int seg, int t) {
   Scale s{0u, 0u};
   if constexpr (G1 && FMT == F_INT4) {
-    s.a = bf16x2_splat(__ldg(reinterpret_cast<const uint16_t*>(srow) + seg));
+    s.a = __ldg(reinterpret_cast<const uint16_t*>(srow) + seg);
   } else if constexpr (G1 && FMT == F_INT4Z) {
-    s.a = bf16x2_splat(__ldg(reinterpret_cast<const uint16_t*>(srow) + seg));
-    s.b = bf16x2_zero128(__ldg(zrow + seg));
+    s.a = __ldg(reinterpret_cast<const uint16_t*>(srow) + seg);
+    s.b = __ldg(zrow + seg);
   } else if constexpr (FMT == F_INT4) {
     const int grp = (seg * 128 + 32 * t) >> p.lg;
-    s.a = bf16x2_splat(__ldg(reinterpret_cast<const uint16_t*>(srow) + grp));
+    s.a = __ldg(reinterpret_cast<const uint16_t*>(srow) + grp);
   } else if constexpr (FMT == F_INT4Z) {
     const int grp = (seg * 128 + 32 * t) >> p.lg;
-    s.a = bf16x2_splat(__ldg(reinterpret_cast<const uint16_t*>(srow) + grp));
-    s.b = bf16x2_zero128(__ldg(zrow + grp));
+    s.a = __ldg(reinterpret_cast<const uint16_t*>(srow) + grp);
+    s.b = __ldg(zrow + grp);
   } else if constexpr (FMT == F_MXFP4) {
     s.a = __ldg(srow + seg * 4 + t);
-    if constexpr (FOLD) s.b = mxfp4_fold(s.a);
   } else if constexpr (FMT == F_NVFP4) {
     s.a = __ldg(reinterpret_cast<const uint16_t*>(srow + seg * 8 + 2 * t));
+  }
+  return s;
+}
+template <int FMT, bool FOLD = false>
+QG_DEVICE Scale finish_scale(Scale s) {
+  if constexpr (FMT == F_INT4) {
+    s.a = bf16x2_splat(s.a);
+  } else if constexpr (FMT == F_INT4Z) {
+    s.a = bf16x2_splat(s.a);
+    s.b = bf16x2_zero128(s.b);
+  } else if constexpr (FMT == F_MXFP4) {
+    if constexpr (FOLD) s.b = mxfp4_fold(s.a);
+  } else if constexpr (FMT == F_NVFP4) {
     if constexpr (FOLD) s.a = nvfp4_fold_x2(s.a);
   }
   return s;
@@ -277,8 +293,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
 #pragma unroll
   for (int u = 0; u < kPFS; ++u) {
     if (u < nseg) {
-      sa[u] = load_scale<FMT, G1, true>(p, sr0, zr0, seg_lo + s_lo + u, t);
-      sb[u] = load_scale<FMT, G1, true>(p, sr1, zr1, seg_lo + s_lo + u, t);
+      sa[u] = load_scale<FMT, G1>(p, sr0, zr0, seg_lo + s_lo + u, t);
+      sb[u] = load_scale<FMT, G1>(p, sr1, zr1, seg_lo + s_lo + u, t);
     }
   }
 
@@ -366,10 +382,10 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvArgs p) {
         }
         cp_async_commit();
         const int us = u % kPFS;
-        const Scale s_a = sa[us], s_b = sb[us];
+        const Scale s_a = finish_scale<FMT, true>(sa[us]), s_b = finish_scale<FMT, true>(sb[us]);
         if (s + kPFS < nseg) {
-          sa[us] = load_scale<FMT, G1, true>(p, sr0, zr0, seg_lo + s_lo + s + kPFS, t);
-          sb[us] = load_scale<FMT, G1, true>(p, sr1, zr1, seg_lo + s_lo + s + kPFS, t);
+          sa[us] = load_scale<FMT, G1>(p, sr0, zr0, seg_lo + s_lo + s + kPFS, t);
+          sb[us] = load_scale<FMT, G1>(p, sr1, zr1, seg_lo + s_lo + s + kPFS, t);
         }
         const uint4* xs0 = xq0 + s * kPadSeg;
         const uint4* xs1 = xq1 + s * kPadSeg;
@@ -484,7 +500,7 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ w, const void* __rest
   const uint4 wv = *reinterpret_cast<const uint4*>(w + (size_t)n * row_bytes + seg * 64 + 16 * t);
   GemvArgs p{};
   p.scales = scales; p.zeros = zeros; p.K = K; p.g = g; p.lg = 31 - __clz(g);
-  const Scale s = load_scale<FMT, false>(p, scale_row<FMT>(p, n), zero_row<FMT>(p, n), seg, t);
+  const Scale s = finish_scale<FMT>(load_scale<FMT, false>(p, scale_row<FMT>(p, n), zero_row<FMT>(p, n), seg, t));
   uint16_t* o = out + (size_t)n * K + (size_t)seg * Tr::KSEG + t * Tr::CPL * 8;
 #pragma unroll
   for (int j = 0; j < Tr::CPL; ++j) {
