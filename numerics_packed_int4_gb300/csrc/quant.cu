@@ -72,34 +72,57 @@ QG_DEVICE uint32_t e2m1_codes8(const float (&v)[8], float mul) {
 // ===========================================================================
 // block size <= 256: GT = g/8 lanes per block, shuffles only
 // ===========================================================================
-template <typename Tin, int GT>
+// g <= 256: GT = g/8 consecutive lanes per block.  A CTA takes CPT slices of
+// kThreads consecutive chunks; every thread loads its CPT chunks before any
+// is quantized, so each thread keeps CPT 16-byte loads in flight (with one
+// chunk per thread the divisions held the threads and too few bytes were in
+// flight to cover the memory latency).
+template <typename Tin, int GT, int CPT>
 __global__ void __launch_bounds__(kThreads) fp8_block_small_kernel(
     const Tin* __restrict__ x, uint8_t* __restrict__ q, float* __restrict__ s,
     long long nchunks, int K) {
-  const long long c = blockIdx.x * (long long)kThreads + threadIdx.x;
-  const bool live = c < nchunks;
-  float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  if (live) Load8<Tin>::run(x + c * 8, v);
-  const float amax = group_max<GT>(absmax8(v));
-  const float sc = fp8_scale(amax);
-  if (!live) return;
-  *reinterpret_cast<uint2*>(q + c * 8) = fp8_codes8(v, sc);
-  if ((c % GT) == 0) s[c / GT] = sc;
+  float v[CPT][8];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const long long c = ((long long)blockIdx.x * CPT + j) * kThreads + threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
+    if (c < nchunks) Load8<Tin>::run(x + c * 8, v[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const long long c = ((long long)blockIdx.x * CPT + j) * kThreads + threadIdx.x;
+    const float amax = group_max<GT>(absmax8(v[j]));
+    const float sc = fp8_scale(amax);
+    if (c < nchunks) {
+      *reinterpret_cast<uint2*>(q + c * 8) = fp8_codes8(v[j], sc);
+      if ((c % GT) == 0) s[c / GT] = sc;
+    }
+  }
 }
 
-template <typename Tin, int GT>
+template <typename Tin, int GT, int CPT>
 __global__ void __launch_bounds__(kThreads) mxfp4_kernel(
     const Tin* __restrict__ x, uint8_t* __restrict__ q, uint8_t* __restrict__ se_out,
     long long nchunks) {
-  const long long c = blockIdx.x * (long long)kThreads + threadIdx.x;
-  const bool live = c < nchunks;
-  float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  if (live) Load8<Tin>::run(x + c * 8, v);
-  const float vecMax = group_max<GT>(absmax8(v));
-  const uint32_t se = e8m0_scale_exp(vecMax);
-  if (!live) return;
-  *reinterpret_cast<uint32_t*>(q + c * 4) = e2m1_codes8(v, pow2_127_minus(se));
-  if ((c % GT) == 0) se_out[c / GT] = uint8_t(se);
+  float v[CPT][8];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {          // every load in flight before any block is quantized
+    const long long c = ((long long)blockIdx.x * CPT + j) * kThreads + threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
+    if (c < nchunks) Load8<Tin>::run(x + c * 8, v[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const long long c = ((long long)blockIdx.x * CPT + j) * kThreads + threadIdx.x;
+    const float vecMax = group_max<GT>(absmax8(v[j]));
+    const uint32_t se = e8m0_scale_exp(vecMax);
+    if (c < nchunks) {
+      *reinterpret_cast<uint32_t*>(q + c * 4) = e2m1_codes8(v[j], pow2_127_minus(se));
+      if ((c % GT) == 0) se_out[c / GT] = uint8_t(se);
+    }
+  }
 }
 
 template <int GT>
@@ -469,6 +492,11 @@ __global__ void __launch_bounds__(kThreads) w4a8_fp8_scales_kernel(
 
 // ---- launch helpers ----------------------------------------------------------
 inline unsigned grid_for(long long nchunks) { return unsigned((nchunks + kThreads - 1) / kThreads); }
+constexpr int kFp8Cpt = 2;             // chunks per thread of the small-block FP8 quantizer
+constexpr int kMxCpt = 2;              // and of the MXFP4 quantizer
+inline unsigned grid_cpt(long long nchunks, int cpt) {
+  return unsigned((nchunks + (long long)kThreads * cpt - 1) / ((long long)kThreads * cpt));
+}
 
 template <typename Tin>
 qg_status launch_fp8_block(const Tin* x, uint8_t* q, float* s, int g, long long rows, int K,
@@ -477,12 +505,12 @@ qg_status launch_fp8_block(const Tin* x, uint8_t* q, float* s, int g, long long 
   if (nchunks == 0) return QG_OK;
   const long long nblocks = rows * (long long)(K / g);
   switch (g) {
-    case 8:   fp8_block_small_kernel<Tin, 1><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
-    case 16:  fp8_block_small_kernel<Tin, 2><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
-    case 32:  fp8_block_small_kernel<Tin, 4><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
-    case 64:  fp8_block_small_kernel<Tin, 8><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
-    case 128: fp8_block_small_kernel<Tin, 16><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
-    case 256: fp8_block_small_kernel<Tin, 32><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 8:   fp8_block_small_kernel<Tin, 1, kFp8Cpt><<<grid_cpt(nchunks, kFp8Cpt), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 16:  fp8_block_small_kernel<Tin, 2, kFp8Cpt><<<grid_cpt(nchunks, kFp8Cpt), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 32:  fp8_block_small_kernel<Tin, 4, kFp8Cpt><<<grid_cpt(nchunks, kFp8Cpt), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 64:  fp8_block_small_kernel<Tin, 8, kFp8Cpt><<<grid_cpt(nchunks, kFp8Cpt), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 128: fp8_block_small_kernel<Tin, 16, kFp8Cpt><<<grid_cpt(nchunks, kFp8Cpt), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
+    case 256: fp8_block_small_kernel<Tin, 32, kFp8Cpt><<<grid_cpt(nchunks, kFp8Cpt), kThreads, 0, st>>>(x, q, s, nchunks, K); break;
     default: {
       if (nblocks > 0x7FFFFFFFLL) return set_error(QG_ERR_UNSUPPORTED_SHAPE, "%s: too many blocks", name);
       const int cpt = (g / 8 + kThreads - 1) / kThreads;      // chunks of 8 per thread
@@ -501,8 +529,8 @@ qg_status launch_mxfp4(const Tin* x, uint8_t* q, uint8_t* se, int g, long long r
                        cudaStream_t st, const char* name) {
   const long long nchunks = rows * (long long)K / 8;
   if (nchunks == 0) return QG_OK;
-  if (g == 16) mxfp4_kernel<Tin, 2><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, se, nchunks);
-  else         mxfp4_kernel<Tin, 4><<<grid_for(nchunks), kThreads, 0, st>>>(x, q, se, nchunks);
+  if (g == 16) mxfp4_kernel<Tin, 2, kMxCpt><<<grid_cpt(nchunks, kMxCpt), kThreads, 0, st>>>(x, q, se, nchunks);
+  else         mxfp4_kernel<Tin, 4, kMxCpt><<<grid_cpt(nchunks, kMxCpt), kThreads, 0, st>>>(x, q, se, nchunks);
   return check_launch(name);
 }
 
