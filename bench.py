@@ -24,8 +24,10 @@ the step's dominant kernel -- are timed on their own); CUDA events between
 the graphs time every row inside the timed region.  Measured beside the step,
 outside the timed region: the M = 1 row's single-launch read ceiling (a plain
 streaming read of the same 12 weight matrices, one launch each), the dense
-FP8 rate of this GPU (the FP8 rows' roofline denominator), a bf16 dense GEMM
-(cuBLAS) on the prefill's own data, the 1 x 1024 x 1024 GEMV as latency, the
+FP8 rate of this GPU (the FP8 rows' roofline denominator; three times it, the
+nominal FP4/FP8 ratio, for the FP4 row), the library's block-scaled FP4 GEMM
+(a comparator for the W4A4 row), a bf16 dense GEMM (cuBLAS) on the prefill's
+own data, the 1 x 1024 x 1024 GEMV as latency, the
 pinned host link, and the oracle on the host cores.  The first output line
 holds every row in full; the last is the contract line.  The headline value is the metric's first quantity:
 effective HBM GB/s of the M = 1 GEMVs (algorithmic bytes / time); the
@@ -85,7 +87,7 @@ MAIN_KERNEL = {"moe": "moe_f16_kernel (gate/up + down launches)",
                "moe_e4m3": "moe_fp8p_kernel (gate/up + down launches)"}
 MOE_ROWS = ("moe", "moe_fp8s", "moe_e4m3")
 FP8_ROWS = ("moe_fp8s", "moe_e4m3")          # FP8 tensor-core contractions: roofline against the FP8 peak
-FP4_ROWS = ("prefill_w4a4",)                  # block-scaled FP4 contractions: 2 x the FP8 peak (nominal ratio)
+FP4_ROWS = ("prefill_w4a4",)                  # block-scaled FP4 contractions: 3 x the FP8 peak (nominal 13.5 / 4.5)
 
 
 def gemv_bytes(fmt, M, N, K):
@@ -761,6 +763,10 @@ def run_ours(args):
     else:
         peaks["fp8_src"] = "measured bf16 x 2 (nominal fp8/bf16 ratio)"
     side = {}
+    fp4_lib = measure_fp4_cublas(torch, dev) if any(r in FP4_ROWS for r in rows) else None
+    if fp4_lib is not None:
+        side["fp4_library"] = {"TFLOP/s": fp4_lib,
+                               "what": "torch._scaled_mm E2M1 x E2M1, E4M3 scales per 16, 8192^3, best of 10"}
     if "prefill" in rows:
         side["prefill_vs_bf16"] = bf16_comparator(torch, qg, wl, dev)
     side["gemv_1x1024x1024"] = gemv_1k_latency(torch, qg, dev)
@@ -778,14 +784,17 @@ def run_ours(args):
         else:
             tf = wl.flops[r] / (ms * 1e-3) / 1e12
             fp8 = r in FP8_ROWS
-            peak = 2.0 * peaks["fp8"] if r in FP4_ROWS else (peaks["fp8"] if fp8 else peaks["bf16"])
+            peak = 3.0 * peaks["fp8"] if r in FP4_ROWS else (peaks["fp8"] if fp8 else peaks["bf16"])
             row_out[r] = {"ms": ms, "TFLOP/s": tf, "launches": wl.launches[r],
                           "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                                        "frac": tf / peak, "traffic": traffic_of(r), **traffic_info(r)}}
             if fp8:
                 row_out[r]["roofline"]["peak_kind"] = "fp8 dense: " + peaks["fp8_src"]
             if r in FP4_ROWS:
-                row_out[r]["roofline"]["peak_kind"] = "fp4 dense: 2 x the fp8 peak (" + peaks["fp8_src"] + ")"
+                row_out[r]["roofline"]["peak_kind"] = ("fp4 dense: 3 x the fp8 peak, the nominal 13.5 / 4.5 ratio ("
+                                                       + peaks["fp8_src"] + ")")
+                if fp4_lib is not None:
+                    row_out[r]["vs_fp4_library"] = tf / fp4_lib
             if r in kern_ms:
                 kms, nl = kern_ms[r]
                 ktf = wl.flops[r] / (kms * 1e-3) / 1e12
@@ -860,6 +869,8 @@ def run_ours(args):
     line["gemv_1x1024x1024"] = {"us": g1["graph_us_per_launch"], "GB/s": g1["graph_GB/s"],
                                 "single_call_us": g1["single_call_us_median"]}
     line["peaks"] = {"hbm": peaks["hbm"], "bf16": peaks["bf16"], "fp8": peaks["fp8"], "src": peaks["src"]}
+    if "fp4_library" in side:
+        line["peaks"]["fp4_library"] = side["fp4_library"]["TFLOP/s"]
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
@@ -935,6 +946,31 @@ def measure_fp8_peak(torch, dev, n=8192, reps=10):
 
         def f():
             torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16, out=out)
+
+        _, best = _time_graph(torch, dev, f, reps=reps)
+        del a, b, out
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:
+        return None
+
+
+def measure_fp4_cublas(torch, dev, n=8192, reps=10):
+    """The vendor library's block-scaled FP4 GEMM on this GPU: torch._scaled_mm
+    with E2M1 operands and E4M3 scales per 16 elements (the FP4 form this
+    PyTorch exposes), 8192^3, best of `reps`.  Reported beside the W4A4 row as a
+    comparator (the row's roofline uses the nominal FP4/FP8 ratio on the
+    measured FP8 peak).  A measurement of the library, not part of the path.
+    None if unavailable."""
+    try:
+        a = torch.randint(0, 256, (n, n // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+        b = torch.randint(0, 256, (n, n // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+        ns = ((n + 127) // 128 * 128) * ((n // 16 + 3) // 4 * 4)
+        sa = torch.full((ns,), 0x38, dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)   # 1.0
+        sb = torch.full((ns,), 0x38, dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+        out = torch.empty((n, n), device=dev, dtype=torch.bfloat16)
+
+        def f():
+            torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16, out=out)
 
         _, best = _time_graph(torch, dev, f, reps=reps)
         del a, b, out
