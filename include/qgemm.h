@@ -160,6 +160,23 @@ QG_API qg_status qgemm_w4a4_mxfp4(const uint8_t* w_e2m1, const uint8_t* w_e8m0,
                            uint16_t* a_work, uint16_t* y, int M, int N, int K,
                            qg_stream_t stream);
 
+/* qgemm_w4a4_mxfp4 with the activations' block size as an argument: g_act =
+ * 32 (exactly qgemm_w4a4_mxfp4) or 16 -- the block size of the fixed MXFP4
+ * W4A4 MoE kernel in vLLM PR #43557 and of the configured MXFP4 activation
+ * quantizer -- with a_e8m0 [M][K/g_act]:
+ * y[m,n] = sum_k (e2m1(a[m,k]) * 2^(sa[m,k/g_act]-127)) * (e2m1(w[n,k]) *
+ * 2^(sw[n,k/32]-127)), fp32 accumulation, one bf16 rounding.
+ * For M > 16 with K % 256 == 0 and both scale arrays 8-byte aligned, g_act =
+ * 16 runs on the block-scaled tensor cores with four scale factors per 64-k
+ * step (tcgen05 kind::mxf4nvf4, scale_vec::4X, E8M0: each 32-element weight
+ * code stands for two 16-element blocks); otherwise the activations are
+ * expanded exactly to bf16 into a_work as for qgemm_w4a4_mxfp4.  Rules as
+ * qgemm_w4a4_mxfp4; any other g_act returns QG_ERR_UNSUPPORTED_SHAPE.       */
+QG_API qg_status qgemm_w4a4_mxfp4_g(const uint8_t* w_e2m1, const uint8_t* w_e8m0,
+                             const uint8_t* a_e2m1, const uint8_t* a_e8m0, int g_act,
+                             uint16_t* a_work, uint16_t* y, int M, int N, int K,
+                             qg_stream_t stream);
+
 /* qgemm_w4a4_mxfp4 for callers that cannot allocate device memory; the pages
  * have no counterpart of this entry point.  Plugin-style host interfaces that
  * hand an op only its inputs and outputs, and runtimes that committed all

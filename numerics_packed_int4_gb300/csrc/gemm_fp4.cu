@@ -60,7 +60,7 @@ constexpr int bTW = 128;                 // channels per tile (MMA M)
 constexpr int bTT = 256;                 // tokens per tile (MMA N)
 constexpr int bBK = 256;                 // k per slab: 128 packed bytes per row
 constexpr int bStages = 4;               // operand stages (A + B)
-constexpr int bSfSlots = 8;              // scale-factor slots in tensor memory
+constexpr int bSfSlots = 8;              // scale-factor slots in tensor memory (at most)
 constexpr int bDone = 16;                // slab-completion barriers
 constexpr int bABytes = bTW * bBK / 2;   // 16 KB of weights per stage
 constexpr int bBBytes = bTT * bBK / 2;   // 32 KB of activations per stage
@@ -69,26 +69,34 @@ constexpr int bSfWarp0 = 3, bSfWarps = 4, bEpiWarp0 = bSfWarp0 + bSfWarps, bEpiW
 constexpr int bThreads = (bEpiWarp0 + bEpiWarps) * 32;
 constexpr uint32_t bTmemCols = 512;
 constexpr uint32_t bSfCol0 = bTT;        // scale-factor slots follow the accumulator
-constexpr uint32_t bSfCols = 32;         // per slot: MMAs 2p, 2p + 1 read A at +4p (4 columns), B at +8 + 8p (8);
-                                         // 24 used, each store aligned to its width
-static_assert(bSfCol0 % 32 == 0 && bSfCols % 32 == 0, "slots 32-column aligned: every store and code group aligned to its width");
-constexpr int bChunk = 2;                // slabs of codes per shared-memory chunk (16 bytes per row)
-constexpr int bSfRows = bTW + bTT;       // code rows per chunk: weights, then tokens
-constexpr int bSfRowBytes = 8 * bChunk;
-constexpr int bSfBufBytes = bSfRows * bSfRowBytes;
-constexpr int bXchBytes = 2 * bSfBufBytes;                   // two chunk buffers
+static_assert(bSfCol0 % 32 == 0, "slots aligned: every store and code group aligned to its width");
+constexpr int bChunk = 2;                // slabs of codes per shared-memory chunk
+constexpr int bSfRowBytes = 8 * bChunk;  // weight codes per row of a chunk (32-element blocks): 16 bytes
 constexpr int bPieceTok = 16;            // tokens per staged output piece (TMA store box: 128 channels x 16 tokens)
 constexpr int bPieceBytes = bPieceTok * bTW * 2;
-constexpr int bStgBytes = 2 * 2 * bPieceBytes;               // per token half, two pieces in flight
-static_assert(bSfRows * bChunk % (bSfWarps * 32) == 0, "chunk copy divides over the scale-factor threads");
+
+// What depends on the activations' block size (32, or 16 with kA16):
+template <bool kA16> struct Fp4Cfg {
+  static constexpr int kAScB = kA16 ? 16 : 8;                  // activation codes per row and slab
+  static constexpr int kARowB = kAScB * bChunk;                // activation code bytes per row of a chunk
+  static constexpr uint32_t kSlotCols = kA16 ? 48 : 32;        // tensor-memory columns per slab
+  static constexpr int kSlots = kA16 ? 5 : 8;                  // slots in the ring
+  static constexpr int kBufBytes = bTW * bSfRowBytes + bTT * kARowB;   // one chunk of codes
+  static constexpr int kXchBytes = 2 * kBufBytes;              // two chunk buffers
+  static constexpr int kPieces = kBufBytes / 8;                // 8-byte cp.async pieces per chunk
+  static constexpr int kStgBufs = kA16 ? 1 : 2;                // staged output pieces in flight per token half
+  static constexpr int kStgBytes = 2 * kStgBufs * bPieceBytes;
+  static_assert(kPieces % (bSfWarps * 32) == 0, "chunk copy divides over the scale-factor threads");
+  static_assert(kSlots <= bSfSlots && bDone > kSlots, "slab-completion ring covers every reuse distance");
+  static_assert(bSfCol0 + kSlots * kSlotCols <= bTmemCols && kSlotCols % 16 == 0, "tensor memory budget");
+};
 constexpr uint32_t bDrainCap = 1u << 21;
-static_assert(bDone >= bStages && bDone > bSfSlots, "slab-completion ring covers every reuse distance");
-static_assert(bSfCol0 + bSfSlots * bSfCols <= bTmemCols, "tensor memory budget");
+static_assert(bDone >= bStages, "slab-completion ring covers every reuse distance");
 static_assert(bEpiWarps * 32 * 128 == bTW * bTT, "each epilogue thread owns 128 outputs");
 
 struct Fp4Args {
   const uint8_t* w_sf;                   // [N][K/32] E8M0
-  const uint8_t* a_sf;                   // [M][K/32] E8M0
+  const uint8_t* a_sf;                   // [M][K/32] E8M0 ([M][K/16] with 16-element activation blocks)
   uint16_t* y;                           // [M][N] bf16
   int M, N, K;
   int tiles_t, tiles_w;
@@ -165,19 +173,31 @@ QG_DEVICE void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
                : "memory");
 }
 
+// The same with four scale factors per row and MMA (16-element blocks), one
+// 32-bit word of codes at scale-factor ID 0.
+QG_DEVICE void mma_mxf4nvf4_4x(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa,
+                               uint32_t sfb, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
 QG_DEVICE void tile_origin(const Fp4Args& p, int tile, int& m0, int& n0) {
   m0 = (tile / p.tiles_w) * bTT;         // every channel tile of a token tile in turn
   n0 = (tile % p.tiles_w) * bTW;
 }
 
-template <bool kTmaSf>
+template <bool kTmaSf, bool kA16>
 __global__ void __launch_bounds__(bThreads, 1)
 w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                const __grid_constant__ CUtensorMap tmap_y, const __grid_constant__ CUtensorMap tmap_wsf,
                const __grid_constant__ CUtensorMap tmap_asf, const Fp4Args p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Fp4Tail* tl = reinterpret_cast<Fp4Tail*>(smem + bStages * bStageBytes + bXchBytes + bStgBytes);
+  using Cfg = Fp4Cfg<kA16>;
+  Fp4Tail* tl = reinterpret_cast<Fp4Tail*>(smem + bStages * bStageBytes + Cfg::kXchBytes + Cfg::kStgBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int nslab = p.K / bBK;
@@ -245,16 +265,21 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
         }
         bool ok = true;
         for (int s = 0; s < nslab; ++s, ++g) {
-          const int st = g % bStages, ss = g % bSfSlots;
+          const int st = g % bStages, ss = g % Cfg::kSlots;
           if (!wait_count(&tl->ready, (unsigned)g, ready, p.cap * 4, abort, p.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t stage = smem_addr(smem + st * bStageBytes);
           const uint64_t adesc = sw128_kmajor_desc(stage), bdesc = sw128_kmajor_desc(stage + bABytes);
-          const uint32_t sf = tmem + bSfCol0 + (uint32_t)ss * bSfCols;
+          const uint32_t sf = tmem + bSfCol0 + (uint32_t)ss * Cfg::kSlotCols;
 #pragma unroll
-          for (int j = 0; j < bBK / 64; ++j)      // K = 64 per MMA: 32 packed bytes of each operand row
-            mma_mxf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc[j & 1], sf + 4u * (j >> 1), sf + 8u + 8u * (j >> 1),
-                     (s | j) != 0);
+          for (int j = 0; j < bBK / 64; ++j) {    // K = 64 per MMA: 32 packed bytes of each operand row
+            if constexpr (kA16)                   // one word of four 16-element codes per row and MMA
+              mma_mxf4nvf4_4x(tmem, adesc + 2 * j, bdesc + 2 * j, idesc[0], sf + 4u * j, sf + 16u + 8u * j,
+                              (s | j) != 0);
+            else
+              mma_mxf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc[j & 1], sf + 4u * (j >> 1), sf + 8u + 8u * (j >> 1),
+                       (s | j) != 0);
+          }
           tc_commit(&tl->done[g % bDone]);              // frees the stage and the scale-factor slot
           any = true;
         }
@@ -271,7 +296,7 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
     if (lane == 0) {
       for (int g = 0; g < total; ++g) {
         if (!mbar_wait(&tl->full[g % bStages], (g / bStages) & 1, p.cap, abort, p.err)) break;
-        if (!mbar_wait(&tl->sf_full[g % bSfSlots], (g / bSfSlots) & 1, p.cap, abort, p.err)) break;
+        if (!mbar_wait(&tl->sf_full[g % Cfg::kSlots], (g / Cfg::kSlots) & 1, p.cap, abort, p.err)) break;
         publish_count(&tl->ready, (unsigned)(g + 1));
       }
     }
@@ -297,7 +322,7 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
     // and their results are not stored.
     const int q = warp & 3, tid = threadIdx.x - bSfWarp0 * 32;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-    const size_t sf_row = (size_t)(p.K / 32);
+    const size_t sf_row = (size_t)(p.K / 32), sf_row_a = (size_t)(p.K / (kA16 ? 16 : 32));
     uint8_t* sfb = smem + bStages * bStageBytes;
     const int nch = (nslab + bChunk - 1) / bChunk, nunits = ntiles * nch;
     const bool issuer = kTmaSf && tid == 0;
@@ -305,19 +330,26 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
       const int i = u / nch, k = u % nch;
       int m0, n0;
       tile_origin(p, tile_of(i), m0, n0);
-      uint8_t* buf = sfb + (u & 1) * bSfBufBytes;
+      uint8_t* buf = sfb + (u & 1) * Cfg::kBufBytes;
       if constexpr (kTmaSf) {
-        mbar_arrive_expect_tx(&tl->sf_tma[u & 1], bSfBufBytes);
+        mbar_arrive_expect_tx(&tl->sf_tma[u & 1], Cfg::kBufBytes);
         tma_load_2d(buf, &tmap_wsf, &tl->sf_tma[u & 1], bSfRowBytes * k, n0);
-        tma_load_2d(buf + bTW * bSfRowBytes, &tmap_asf, &tl->sf_tma[u & 1], bSfRowBytes * k, m0);
+        tma_load_2d(buf + bTW * bSfRowBytes, &tmap_asf, &tl->sf_tma[u & 1], Cfg::kARowB * k, m0);
       } else {
 #pragma unroll
-        for (int e = 0; e < bSfRows * bChunk / (bSfWarps * 32); ++e) {
-          const int t = tid + bSfWarps * 32 * e, row = t / bChunk, j = t % bChunk, s = bChunk * k + j;
-          if (s < nslab) {
-            const uint8_t* src = row < bTW ? p.w_sf + (size_t)min(n0 + row, p.N - 1) * sf_row
-                                           : p.a_sf + (size_t)min(m0 + row - bTW, p.M - 1) * sf_row;
-            cp_async8(buf + row * bSfRowBytes + 8 * j, src + 8 * s);
+        for (int e = 0; e < Cfg::kPieces / (bSfWarps * 32); ++e) {
+          // pieces 0 .. 2 * bTW - 1: weight rows, two per row; then the token
+          // rows, kARowB / 8 per row; a piece whose slab lies past the row is
+          // skipped (its codes are never read)
+          const int t = tid + bSfWarps * 32 * e;
+          const bool wpiece = t < 2 * bTW;
+          const int tt = wpiece ? t : t - 2 * bTW, per = wpiece ? 2 : Cfg::kARowB / 8;
+          const int row = tt / per, j = tt % per, rb = wpiece ? 8 : Cfg::kAScB;
+          if (bChunk * k + 8 * j / rb < nslab) {
+            const uint8_t* src = wpiece ? p.w_sf + (size_t)min(n0 + row, p.N - 1) * sf_row + bSfRowBytes * k
+                                        : p.a_sf + (size_t)min(m0 + row, p.M - 1) * sf_row_a + Cfg::kARowB * k;
+            uint8_t* dst = wpiece ? buf + row * bSfRowBytes : buf + bTW * bSfRowBytes + row * Cfg::kARowB;
+            cp_async8(dst + 8 * j, src + 8 * j);
           }
         }
         cp_async_commit();
@@ -345,17 +377,20 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
         named_bar_sync(1, bSfWarps * 32);
       }
       const int i = u / nch, k = u % nch;
-      const uint8_t* buf = sfb + (u & 1) * bSfBufBytes;
-      uint4 wr[4], ar[8];                                        // rows 32c + l: both slabs' codes
+      const uint8_t* buf = sfb + (u & 1) * Cfg::kBufBytes;
+      const uint8_t* abuf = buf + bTW * bSfRowBytes;             // token rows, kARowB bytes each
+      uint4 wr[4], ar[8];                                        // rows 32c + l: both slabs' weight codes
 #pragma unroll
       for (int c = 0; c < 4; ++c) wr[c] = *reinterpret_cast<const uint4*>(buf + (32 * c + lane) * bSfRowBytes);
+      if constexpr (!kA16) {                                     // both slabs' token codes
 #pragma unroll
-      for (int c = 0; c < 8; ++c) ar[c] = *reinterpret_cast<const uint4*>(buf + (bTW + 32 * c + lane) * bSfRowBytes);
+        for (int c = 0; c < 8; ++c) ar[c] = *reinterpret_cast<const uint4*>(abuf + (32 * c + lane) * Cfg::kARowB);
+      }
       // Both slabs of the chunk go out after one wait: the MMAs complete in
       // order, so the chunk's last slab's slot being free (slab g1 - 8 done)
       // frees the others; one wait::st then covers all the stores.
       const int s0 = bChunk * k, ns = min(bChunk, nslab - s0), g0 = i * nslab + s0, g1 = g0 + ns - 1;
-      const int gp = g1 - bSfSlots;
+      const int gp = g1 - Cfg::kSlots;
       if (live && gp >= 0) {
         live = mbar_wait_warp(&tl->done[gp % bDone], (gp / bDone) & 1, p.cap, abort, p.err);
         if (live) tc_fence_after();
@@ -363,29 +398,56 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
 #pragma unroll
       for (int j = 0; j < bChunk; ++j) {
         if (j >= ns) break;
-        // one 32-bit word = a row's codes of 4 consecutive 32-k blocks: the
-        // MMAs of k-quarters 2p and 2p + 1 read its bytes 0-1 and 2-3
-        uint32_t cols[24];
+        const uint32_t at = tmem + lane_addr + bSfCol0 + (uint32_t)((g0 + j) % Cfg::kSlots) * Cfg::kSlotCols;
+        if constexpr (!kA16) {
+          // one 32-bit word = a row's codes of 4 consecutive 32-k blocks: the
+          // MMAs of k-quarters 2p and 2p + 1 read its bytes 0-1 and 2-3
+          uint32_t cols[24];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          cols[c] = j == 0 ? wr[c].x : wr[c].z;
-          cols[4 + c] = j == 0 ? wr[c].y : wr[c].w;
-        }
+          for (int c = 0; c < 4; ++c) {
+            cols[c] = j == 0 ? wr[c].x : wr[c].z;
+            cols[4 + c] = j == 0 ? wr[c].y : wr[c].w;
+          }
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          cols[8 + c] = j == 0 ? ar[c].x : ar[c].z;
-          cols[16 + c] = j == 0 ? ar[c].y : ar[c].w;
-        }
-        if (live) {
-          const uint32_t at = tmem + lane_addr + bSfCol0 + (uint32_t)((g0 + j) % bSfSlots) * bSfCols;
-          tmem_st16(at, *reinterpret_cast<const uint32_t(*)[16]>(&cols[0]));
-          tmem_st8(at + 16u, *reinterpret_cast<const uint32_t(*)[8]>(&cols[16]));
+          for (int c = 0; c < 8; ++c) {
+            cols[8 + c] = j == 0 ? ar[c].x : ar[c].z;
+            cols[16 + c] = j == 0 ? ar[c].y : ar[c].w;
+          }
+          if (live) {
+            tmem_st16(at, *reinterpret_cast<const uint32_t(*)[16]>(&cols[0]));
+            tmem_st8(at + 16u, *reinterpret_cast<const uint32_t(*)[8]>(&cols[16]));
+          }
+        } else {
+          // one word per row and MMA, four codes of 16-element blocks: the
+          // token codes as they are in memory; each weight code (a 32-element
+          // block) covers two of them, so it is written twice
+          uint32_t cols[48];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t lo = j == 0 ? wr[c].x : wr[c].z, hi = j == 0 ? wr[c].y : wr[c].w;
+            cols[c] = prmt(lo, 0u, 0x1100u);
+            cols[4 + c] = prmt(lo, 0u, 0x3322u);
+            cols[8 + c] = prmt(hi, 0u, 0x1100u);
+            cols[12 + c] = prmt(hi, 0u, 0x3322u);
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 a = *reinterpret_cast<const uint4*>(abuf + (32 * c + lane) * Cfg::kARowB + Cfg::kAScB * j);
+            cols[16 + c] = a.x;
+            cols[24 + c] = a.y;
+            cols[32 + c] = a.z;
+            cols[40 + c] = a.w;
+          }
+          if (live) {
+#pragma unroll
+            for (int h = 0; h < 3; ++h) tmem_st16(at + 16u * h, *reinterpret_cast<const uint32_t(*)[16]>(&cols[16 * h]));
+          }
         }
       }
       if (live) {
         tmem_wait_st();
         tc_fence_before();
-        for (int j = 0; j < ns; ++j) mbar_arrive_warp(&tl->sf_full[(g0 + j) % bSfSlots]);
+        for (int j = 0; j < ns; ++j) mbar_arrive_warp(&tl->sf_full[(g0 + j) % Cfg::kSlots]);
       }
       named_bar_sync(1, bSfWarps * 32);                          // buffer u & 1 is refilled by chunk u + 2
     }
@@ -407,7 +469,7 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
     // held the tensor pipe back by about a sixth.)
     const int q = warp & 3, h = (warp - bEpiWarp0) >> 2, row = 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-    uint8_t* stg = smem + bStages * bStageBytes + bXchBytes + h * 2 * bPieceBytes;
+    uint8_t* stg = smem + bStages * bStageBytes + Cfg::kXchBytes + h * Cfg::kStgBufs * bPieceBytes;
     const bool leader = warp == bEpiWarp0 + 4 * h && lane == 0;
     int piece = 0;
     for (int i = 0; i < ntiles; ++i) {
@@ -433,8 +495,8 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
       for (int pc = 0; pc < 128 / bPieceTok; ++pc) {
         const int tp = t0 + bPieceTok * pc;
         if (tp >= p.M) break;                          // the remaining pieces lie past the matrix too
-        uint16_t* buf = reinterpret_cast<uint16_t*>(stg + (piece & 1) * bPieceBytes);
-        if (leader) bulk_wait_read<1>();               // the store issued from this buffer has read it
+        uint16_t* buf = reinterpret_cast<uint16_t*>(stg + (piece % Cfg::kStgBufs) * bPieceBytes);
+        if (leader) bulk_wait_read<Cfg::kStgBufs - 1>();   // the store issued from this buffer has read it
         named_bar_sync(2 + h, 128);
 #pragma unroll
         for (int c = 0; c < bPieceTok; ++c)
@@ -461,15 +523,19 @@ w4a4_bs_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant
 
 }  // namespace
 
-// The W4A4 block-scaled launch (qgemm_w4a4_mxfp4 for M > 16 and K % 256 == 0;
-// arguments validated by the caller).  Declines (handled = false) when a
-// scale array is not 8-byte aligned.
+// The W4A4 block-scaled launch (qgemm_w4a4_mxfp4 / _g for M > 16 and K % 256
+// == 0; arguments validated by the caller).  g_act: the activations' block
+// size, 32 or 16.  Declines (handled = false) when a scale array is not
+// 8-byte aligned.
 qg_status w4a4_mxfp4_bs(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint8_t* a_e2m1,
-                        const uint8_t* a_e8m0, uint16_t* y, int M, int N, int K, cudaStream_t st, bool* handled) {
+                        const uint8_t* a_e8m0, int g_act, uint16_t* y, int M, int N, int K, cudaStream_t st,
+                        bool* handled) {
   *handled = false;
-  if (K % bBK != 0 || (reinterpret_cast<uintptr_t>(w_e8m0) & 7) || (reinterpret_cast<uintptr_t>(a_e8m0) & 7))
+  if (K % bBK != 0 || (g_act != 16 && g_act != 32) || (reinterpret_cast<uintptr_t>(w_e8m0) & 7) ||
+      (reinterpret_cast<uintptr_t>(a_e8m0) & 7))
     return QG_OK;
   *handled = true;
+  const bool a16 = g_act == 16;
   CUtensorMap tmap_w, tmap_a, tmap_y, tmap_wsf, tmap_asf;
   if (!make_u8_tmap_swizzled(&tmap_w, w_e2m1, N, K / 2, bTW, bBK / 2))
     return set_error(QG_ERR_CUDA, "qgemm_w4a4_mxfp4: cannot encode the weight tensor map");
@@ -479,11 +545,12 @@ qg_status w4a4_mxfp4_bs(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint
   // a box of 128 channels x 16 tokens per store
   if (!make_u8_tmap(&tmap_y, y, M, 2 * N, bPieceTok, 2 * bTW))
     return set_error(QG_ERR_CUDA, "qgemm_w4a4_mxfp4: cannot encode the output tensor map");
-  // Scale-factor codes by TMA: rows of K/32 bytes need a 16-byte multiple
+  // Scale-factor codes by TMA: rows of K/32 (K/g_act) bytes need a 16-byte multiple
+  const int arow = a16 ? Fp4Cfg<true>::kARowB : Fp4Cfg<false>::kARowB;
   const bool tma_sf = K % 512 == 0 && (reinterpret_cast<uintptr_t>(w_e8m0) & 15) == 0 &&
                       (reinterpret_cast<uintptr_t>(a_e8m0) & 15) == 0 &&
                       make_u8_tmap(&tmap_wsf, w_e8m0, N, K / 32, bTW, bSfRowBytes) &&
-                      make_u8_tmap(&tmap_asf, a_e8m0, M, K / 32, bTT, bSfRowBytes);
+                      make_u8_tmap(&tmap_asf, a_e8m0, M, K / g_act, bTT, arow);
   if (!tma_sf) {
     memset(&tmap_wsf, 0, sizeof(tmap_wsf));
     memset(&tmap_asf, 0, sizeof(tmap_asf));
@@ -496,8 +563,11 @@ qg_status w4a4_mxfp4_bs(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint
   a.tiles_w = (N + bTW - 1) / bTW;
   a.err = err;
   a.cap = wait_limit();
-  const int smem = bStages * bStageBytes + bXchBytes + bStgBytes + (int)sizeof(Fp4Tail) + 1024;
-  auto kern = tma_sf ? w4a4_bs_kernel<true> : w4a4_bs_kernel<false>;
+  const int xch = a16 ? Fp4Cfg<true>::kXchBytes + Fp4Cfg<true>::kStgBytes
+                      : Fp4Cfg<false>::kXchBytes + Fp4Cfg<false>::kStgBytes;
+  const int smem = bStages * bStageBytes + xch + (int)sizeof(Fp4Tail) + 1024;
+  auto kern = a16 ? (tma_sf ? w4a4_bs_kernel<true, true> : w4a4_bs_kernel<false, true>)
+                  : (tma_sf ? w4a4_bs_kernel<true, false> : w4a4_bs_kernel<false, false>);
   if (!ensure_smem(kern, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a4_mxfp4: smem attribute");
   const long long tiles = (long long)a.tiles_t * a.tiles_w;
   const int grid = (int)std::min<long long>(tiles, (long long)sm_count());   // persistent: one CTA per SM

@@ -616,11 +616,39 @@ qg_status check_common(const void* w, const void* x, const void* y, int M, int N
   return QG_OK;
 }
 
+// MXFP4 codes with one E8M0 code per 16 elements -> their exact bf16 values,
+// natural k order (the W4A4 expansion for 16-element activation blocks): a
+// thread takes 8 codes (half a block); each value is the E2M1 value times
+// 2^(se - 127), exact in fp32 (2^-127 is the subnormal 2^-127 for se = 0) and
+// exact in bf16 (at most two significant bits, at least 2^-128).
+__global__ void mxfp4_expand16_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ se,
+                                      uint16_t* __restrict__ out, long long n8) {
+  const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(q) + i);
+  const uint32_t c = __ldg(se + (i >> 1));
+  const float f = __uint_as_float(c ? c << 23 : 0x00400000u);
+  uint32_t o[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    uint32_t h[2];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {                 // element 2b + n: the low nibble first
+      const uint32_t x = (w >> (8 * b + 4 * n)) & 0xFu, m = x & 7u, e = m >> 1, man = m & 1u;
+      const uint32_t bits = e ? ((e + 126u) << 23) | (man << 22) : (man ? 0x3F000000u : 0u);
+      h[n] = f32_to_bf16_bits(__uint_as_float(bits | ((x & 8u) << 28)) * f);
+    }
+    o[b] = h[0] | (h[1] << 16);
+  }
+  reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 }  // namespace
 
 // block-scaled FP4 W4A4 (gemm_fp4.cu)
 qg_status w4a4_mxfp4_bs(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint8_t* a_e2m1,
-                        const uint8_t* a_e8m0, uint16_t* y, int M, int N, int K, cudaStream_t st, bool* handled);
+                        const uint8_t* a_e8m0, int g_act, uint16_t* y, int M, int N, int K, cudaStream_t st,
+                        bool* handled);
 
 // entry for the prefill path (gemm_tc.cu) when it declines a shape; w_z
 // (zero points) selects the asymmetric format
@@ -747,27 +775,50 @@ qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt
   return qg::set_error(QG_ERR_INVALID_ARG, "qgemm_fp4a16: unknown scale format %d", scale_fmt);
 }
 
+namespace qg {
+namespace {
 // W4A4: for M > 16 the block-scaled FP4 tensor cores (gemm_fp4.cu), when K
 // is a multiple of 256 and both scale arrays are 8-byte aligned; otherwise
-// the MXFP4 activations are expanded to bf16 (exact) into a_work and the
-// MXFP4-weight GEMM runs on them.
+// the MXFP4 activations (blocks of g_act) are expanded to bf16 (exact) into
+// a_work and the MXFP4-weight GEMM runs on them.
+qg_status w4a4_impl(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint8_t* a_e2m1, const uint8_t* a_e8m0,
+                    int g_act, uint16_t* a_work, uint16_t* y, int M, int N, int K, qg_stream_t stream,
+                    const char* name) {
+  QG_REQUIRE(a_e2m1 && a_e8m0 && a_work && w_e8m0, QG_ERR_INVALID_ARG, "%s: NULL pointer", name);
+  qg_status r = check_common(w_e2m1, a_work, y, M, N, K, name);
+  if (r != QG_OK) return r;
+  QG_REQUIRE(aligned16(a_e2m1), QG_ERR_MISALIGNED, "%s: misaligned activation codes", name);
+  if (M == 0) return QG_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (M > 16) {
+    bool handled = false;
+    r = w4a4_mxfp4_bs(w_e2m1, w_e8m0, a_e2m1, a_e8m0, g_act, y, M, N, K, st, &handled);
+    if (handled) return r;
+  }
+  if (g_act == 32) {
+    r = qg_dequant_weights(QG_FMT_MXFP4, a_e2m1, a_e8m0, 32, a_work, M, K, stream);
+  } else {
+    const long long n8 = (long long)M * K / 8;
+    mxfp4_expand16_kernel<<<unsigned((n8 + 255) / 256), 256, 0, st>>>(a_e2m1, a_e8m0, a_work, n8);
+    r = check_launch(name);
+  }
+  if (r != QG_OK) return r;
+  return qgemm_fp4a16(w_e2m1, w_e8m0, QG_SCALE_E8M0, 32, nullptr, a_work, y, M, N, K, stream);
+}
+}  // namespace
+}  // namespace qg
+
 qg_status qgemm_w4a4_mxfp4(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint8_t* a_e2m1,
                            const uint8_t* a_e8m0, uint16_t* a_work, uint16_t* y, int M, int N, int K,
                            qg_stream_t stream) {
-  QG_REQUIRE(a_e2m1 && a_e8m0 && a_work && w_e8m0, QG_ERR_INVALID_ARG, "qgemm_w4a4_mxfp4: NULL pointer");
-  qg_status r = qg::check_common(w_e2m1, a_work, y, M, N, K, "qgemm_w4a4_mxfp4");
-  if (r != QG_OK) return r;
-  QG_REQUIRE(aligned16(a_e2m1), QG_ERR_MISALIGNED, "qgemm_w4a4_mxfp4: misaligned activation codes");
-  if (M == 0) return QG_OK;
-  if (M > 16) {
-    bool handled = false;
-    r = qg::w4a4_mxfp4_bs(w_e2m1, w_e8m0, a_e2m1, a_e8m0, y, M, N, K, reinterpret_cast<cudaStream_t>(stream),
-                          &handled);
-    if (handled) return r;
-  }
-  r = qg_dequant_weights(QG_FMT_MXFP4, a_e2m1, a_e8m0, 32, a_work, M, K, stream);
-  if (r != QG_OK) return r;
-  return qgemm_fp4a16(w_e2m1, w_e8m0, QG_SCALE_E8M0, 32, nullptr, a_work, y, M, N, K, stream);
+  return qg::w4a4_impl(w_e2m1, w_e8m0, a_e2m1, a_e8m0, 32, a_work, y, M, N, K, stream, "qgemm_w4a4_mxfp4");
+}
+
+qg_status qgemm_w4a4_mxfp4_g(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint8_t* a_e2m1,
+                             const uint8_t* a_e8m0, int g_act, uint16_t* a_work, uint16_t* y, int M, int N,
+                             int K, qg_stream_t stream) {
+  QG_REQUIRE(g_act == 16 || g_act == 32, QG_ERR_UNSUPPORTED_SHAPE, "qgemm_w4a4_mxfp4_g: g_act must be 16 or 32");
+  return qg::w4a4_impl(w_e2m1, w_e8m0, a_e2m1, a_e8m0, g_act, a_work, y, M, N, K, stream, "qgemm_w4a4_mxfp4_g");
 }
 
 qg_status qg_dequant_weights(int fmt, const uint8_t* w, const void* scales, int g, uint16_t* w_out,

@@ -29,6 +29,7 @@ SIGNATURES = {
     "qgemm_fp4a16": [P, P, I, I, P, P, P, I, I, I, P],
     "qgemm_w4a4_mxfp4": [P, P, P, P, P, P, I, I, I, P],
     "qgemm_w4a4_mxfp4_noalloc": [P, P, P, P, P, I, I, I, P],
+    "qgemm_w4a4_mxfp4_g": [P, P, P, P, I, P, P, I, I, I, P],
     "qg_stream_read": [P, I64, P, P],
     "quant_act_mxfp4": [P, P, P, I, I, I, P],
     "quant_act_fp8_block": [P, P, P, I, I, I, P],
@@ -140,6 +141,11 @@ def qg_stream_read(p, nbytes, sink, stream=None):
 def qgemm_w4a4_mxfp4(w_e2m1, w_e8m0, a_e2m1, a_e8m0, a_work, y, M, N, K, stream=None):
     return _call("qgemm_w4a4_mxfp4", _ptr(w_e2m1), _ptr(w_e8m0), _ptr(a_e2m1), _ptr(a_e8m0), _ptr(a_work),
                  _ptr(y), M, N, K, stream=stream)
+
+
+def qgemm_w4a4_mxfp4_g(w_e2m1, w_e8m0, a_e2m1, a_e8m0, g_act, a_work, y, M, N, K, stream=None):
+    return _call("qgemm_w4a4_mxfp4_g", _ptr(w_e2m1), _ptr(w_e8m0), _ptr(a_e2m1), _ptr(a_e8m0), g_act,
+                 _ptr(a_work), _ptr(y), M, N, K, stream=stream)
 
 
 def qgemm_w4a4_mxfp4_noalloc(w_e2m1, w_e8m0, a_e2m1, a_e8m0, y, M, N, K, stream=None):

@@ -220,3 +220,14 @@ def test_w4a4_noalloc_argument_validation(lib):
     assert _rc(lib, "qgemm_w4a4_mxfp4_noalloc", FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 0) == 1
     assert _rc(lib, "qgemm_w4a4_mxfp4_noalloc", FAKE, FAKE, FAKE, FAKE, FAKE, 4097, 128, 2048) == 2
     assert "static work area" in lib.qg_last_error_string().decode()
+
+
+def test_w4a4_g_argument_validation(lib):
+    # (w_e2m1, w_e8m0, a_e2m1, a_e8m0, g_act, a_work, y, M, N, K, stream)
+    for g in (8, 24, 64):
+        assert _rc(lib, "qgemm_w4a4_mxfp4_g", FAKE, FAKE, FAKE, FAKE, g, FAKE, FAKE, 1, 128, 128) == 2
+    assert "g_act" in lib.qg_last_error_string().decode()
+    assert _rc(lib, "qgemm_w4a4_mxfp4_g", FAKE, FAKE, None, FAKE, 16, FAKE, FAKE, 1, 128, 128) == 1
+    assert _rc(lib, "qgemm_w4a4_mxfp4_g", FAKE, FAKE, FAKE, FAKE, 16, FAKE, FAKE, 1, 12, 128) == 2   # N % 8
+    assert _rc(lib, "qgemm_w4a4_mxfp4_g", FAKE, FAKE, FAKE_MIS, FAKE, 16, FAKE, FAKE, 1, 128, 128) == 3
+    assert _rc(lib, "qgemm_w4a4_mxfp4_g", FAKE, FAKE, FAKE, FAKE, 16, FAKE, FAKE, 0, 128, 128) == 0  # M = 0
