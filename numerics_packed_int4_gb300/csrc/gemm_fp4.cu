@@ -24,7 +24,13 @@
 //               reads bytes 0-1 (scale-factor ID 0, j even) or 2-3 (ID 2, j
 //               odd) of the group for pair p = j / 2: four columns for the 128
 //               weight rows at slot column 4p, eight for the 256 token rows at
-//               slot column 8 + 8p (24 of a slot's 32 columns per 256-k slab);
+//               slot column 8 + 8p (24 of a slot's 32 columns per 256-k slab).
+//               With 16-element activation blocks (kA16) the same kernel runs
+//               kind::mxf4nvf4.block_scale.scale_vec::4X: one word of four
+//               16-element codes per row and MMA at ID 0 -- the token codes as
+//               they are in memory, each 32-element weight code written twice
+//               -- four columns per MMA for the weights (slot column 4j),
+//               eight for the tokens (16 + 8j), 48 per slab;
 //   D         = fp32, one 128 x 256 accumulator (256 columns): the epilogue
 //               packs it to bf16 in registers and releases it before storing.
 // One MMA instruction covers 128 x 256 x 64: an issue costs about the same
@@ -37,12 +43,15 @@
 //   warp 1      TMEM allocation and MMA issuer (one lane)
 //   warp 2      scheduler: waits for each slab's operands and scale factors,
 //               publishes the ready count the issuer polls
-//   warps 3-6   scale factors (lane quarter = warp % 4): copy the codes of 2
-//               slabs at a time into shared memory with cp.async, 16
-//               contiguous bytes per row (one row per lane straight from
-//               global memory would cost a wavefront per row), and store each
-//               slab's words into their lane quarter
-//   warps 7-14  epilogue: lane quarter = warp % 4, token half = (warp - 7) / 4
+//   warps 3-6   scale factors (lane quarter = warp % 4): bring the codes of
+//               2 slabs at a time into shared memory (two TMA loads, or
+//               8-byte cp.async when a code row's stride is not a multiple of
+//               16 bytes; one row per lane straight from global memory would
+//               cost a wavefront per row), and store each slab's words into
+//               their lane quarter
+//   warps 7-14  epilogue: lane quarter = warp % 4, token half = (warp - 7) / 4;
+//               bf16 in registers, then 16-token pieces staged in shared
+//               memory and written by TMA tile stores
 // Every wait is bounded; on expiry the CTA records a timeout in the device
 // error word, drains what it issued, frees its tensor memory and returns.
 #include <algorithm>
