@@ -62,7 +62,12 @@ enum { QG_FMT_INT4 = 0, QG_FMT_FP8 = 1, QG_FMT_MXFP4 = 2, QG_FMT_NVFP4 = 3 };
 /* ------------------------------------------------------------------------ *
  * Weight-only GEMM/GEMV (W x A16): Y = X . dequant(W)^T, fp32 accumulate.
  * M <= 16 runs the HBM-streaming decode kernel; larger M the prefill kernel.
- * Shape rules: M >= 1, N >= 1, N % 8 == 0, K % 128 == 0.
+ * Shape rules: M >= 0 (M = 0 launches nothing), N >= 1, N % 8 == 0,
+ * K % 32 == 0 and K % g == 0.  The decode and prefill kernels walk K in
+ * 128-element segments; a K that is not a multiple of 128 runs instead on a
+ * general kernel (one thread per output, the same canonical weights, fp32
+ * accumulation in k order, the same epilogue), correct at any such shape
+ * but not tuned: it is for odd layer widths, not for the hot path.
  * Stream overlap: the decode kernel (M <= 16) is launched with programmatic
  * dependent launch.  It may start while kernels enqueued before it on the
  * stream are still running or have not yet made their writes visible, and it
@@ -99,7 +104,7 @@ QG_API qg_status qgemm_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g,
  * rounding.  Same kernels as qgemm_w4a16 (GEMV for M <= 16, tcgen05 above).
  *   w_q [N][K/2] unsigned nibbles (even k low)   w_s [N][K/g] bf16
  *   w_z [N][K/g] uint8 zero points in [0, 15]    x [M][K] bf16  y [M][N] bf16
- * Rules as qgemm_w4a16 (g a power of two >= 32 dividing K, K % 128 == 0,
+ * Rules as qgemm_w4a16 (g a power of two >= 32 dividing K, K % 32 == 0,
  * N % 8 == 0); w_z needs no alignment.                                      */
 QG_API qg_status qgemm_w4a16_zp(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g,
                          const uint16_t* x, uint16_t* y, int M, int N, int K,
@@ -231,7 +236,11 @@ QG_API qg_status quant_act_fp8_block(const uint16_t* x, uint8_t* q, float* s, in
  *   a_e4m3 [R][K] E4M3   a_s [R] fp32   expert_off [E+1] int32 (DEVICE,
  *   non-decreasing, expert_off[0] == 0, expert_off[E] == R)
  *   w_q [E][N][K/2] packed INT4   w_s [E][N][K/g] bf16   y [R][N] bf16.
- * Rules: g == 128, K % 128 == 0, N % 16 == 0, R >= 0, E >= 1.               */
+ * Rules: g a power of two >= 32, K % g == 0, K % 32 == 0, N % 8 == 0,
+ * R >= 0, E >= 1.  g == 128 with K % 128 == 0 and N % 16 == 0 (the W4A8
+ * configuration) runs on the tiled kernels (FP8 tensor cores from 256 rows);
+ * every other shape on a general kernel with the same arithmetic (per-group
+ * fp32 partial sums, scaled in fp32), correct but not tuned.                */
 QG_API qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,
                              const int32_t* expert_off, const uint8_t* w_q,
                              const uint16_t* w_s, int g, uint16_t* y, int R,

@@ -616,30 +616,101 @@ qg_status check_common(const void* w, const void* x, const void* y, int M, int N
   return QG_OK;
 }
 
-// MXFP4 codes with one E8M0 code per 16 elements -> their exact bf16 values,
-// natural k order (the W4A4 expansion for 16-element activation blocks): a
-// thread takes 8 codes (half a block); each value is the E2M1 value times
-// 2^(se - 127), exact in fp32 (2^-127 is the subnormal 2^-127 for se = 0) and
-// exact in bf16 (at most two significant bits, at least 2^-128).
-__global__ void mxfp4_expand16_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ se,
-                                      uint16_t* __restrict__ out, long long n8) {
+// The dense entries (W4A16, W4A16 with zero points, W8A16, FP4A16, W4A4)
+// take any K that is a multiple of 32 (and of g); K % 128 == 0 runs on the
+// fast kernels, anything else on gemm_any_k_kernel.
+qg_status check_common_k32(const void* w, const void* x, const void* y, int M, int N, int K, const char* name) {
+  QG_REQUIRE(w && x && y, QG_ERR_INVALID_ARG, "%s: NULL pointer", name);
+  QG_REQUIRE(M >= 0 && N > 0 && K > 0, QG_ERR_INVALID_ARG, "%s: bad sizes M=%d N=%d K=%d", name, M, N, K);
+  QG_REQUIRE(N % 8 == 0 && K % 32 == 0, QG_ERR_UNSUPPORTED_SHAPE,
+             "%s: need N %% 8 == 0 and K %% 32 == 0 (N=%d K=%d)", name, N, K);
+  QG_REQUIRE(aligned16(w) && aligned16(x) && aligned16(y), QG_ERR_MISALIGNED, "%s: misaligned pointer", name);
+  return QG_OK;
+}
+
+// E2M1 code (4 bits) -> its value: sign, then 0, 0.5 or 2^(e-1) * (1 + m/2)
+QG_DEVICE float e2m1_value(uint32_t x) {
+  const uint32_t m = x & 7u, e = m >> 1, man = m & 1u;
+  const uint32_t bits = e ? ((e + 126u) << 23) | (man << 22) : (man ? 0x3F000000u : 0u);
+  return __uint_as_float(bits | ((x & 8u) << 28));
+}
+// 2^(se - 127) exactly (se = 0 gives the fp32 subnormal 2^-127)
+QG_DEVICE float e8m0_value(uint32_t se) { return __uint_as_float(se ? se << 23 : 0x00400000u); }
+
+// The general path for K % 128 != 0: one thread per output, the canonical
+// dequantized weight of every k (INT4: bf16_RNE(q * s), exact fp32 product;
+// zero points: bf16_RNE((u - z) * s); FP8, MXFP4, NVFP4: the exact values),
+// fp32 accumulation in k order, the format's epilogue scale (FP8 channel,
+// NVFP4 global), one bf16 rounding.  It is there for the shapes the fast
+// kernels' 128-k segments do not cover, not for speed.
+struct AnyK {
+  const uint8_t* w;                      // packed codes, rows of K (FP8) or K/2 bytes
+  const void* s;                         // bf16 [N][K/g] (INT4), E8M0 / E4M3 bytes [N][K/g] (FP4)
+  const uint8_t* z;                      // zero points [N][K/g] (INT4 with zero points)
+  const float* cs;                       // FP8 channel scales [N]
+  const float* gs;                       // NVFP4 global scale
+  const uint16_t* x;
+  uint16_t* y;
+  int M, N, K, g;
+};
+template <int FMT>
+__global__ void gemm_any_k_kernel(const AnyK p) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x, m = blockIdx.y;
+  if (n >= p.N) return;
+  const uint16_t* xr = p.x + (size_t)m * p.K;
+  const size_t sg = (size_t)n * (p.K / p.g);
+  float acc = 0.f;
+  for (int k = 0; k < p.K; ++k) {
+    float w;
+    if constexpr (FMT == F_FP8) {
+      w = e4m3_to_f32(__ldg(p.w + (size_t)n * p.K + k));
+    } else {
+      const uint32_t b = __ldg(p.w + (size_t)n * (p.K / 2) + k / 2), u = (k & 1) ? b >> 4 : b & 15u;
+      if constexpr (FMT == F_INT4 || FMT == F_INT4Z) {
+        const float sc = bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(p.s) + sg + k / p.g));
+        const int q = FMT == F_INT4 ? (u >= 8u ? (int)u - 16 : (int)u) : (int)u - (int)__ldg(p.z + sg + k / p.g);
+        w = bf16_bits_to_f32(f32_to_bf16_bits((float)q * sc));
+      } else {
+        const uint32_t c = __ldg(reinterpret_cast<const uint8_t*>(p.s) + sg + k / p.g);
+        w = e2m1_value(u) * (FMT == F_MXFP4 ? e8m0_value(c) : e4m3_to_f32(c));
+      }
+    }
+    acc = fmaf(bf16_bits_to_f32(__ldg(xr + k)), w, acc);
+  }
+  if constexpr (FMT == F_FP8) acc = __fmul_rn(acc, __ldg(p.cs + n));
+  if constexpr (FMT == F_NVFP4) acc = __fmul_rn(acc, __ldg(p.gs));
+  p.y[(size_t)m * p.N + n] = f32_to_bf16_bits(acc);
+}
+template <int FMT>
+qg_status run_any_k(const AnyK& a, cudaStream_t st, const char* name) {
+  for (int m0 = 0; m0 < a.M; m0 += 65535) {          // the grid's y extent is at most 65535 rows
+    AnyK s = a;
+    s.M = std::min(65535, a.M - m0);
+    s.x = a.x + (size_t)m0 * a.K;
+    s.y = a.y + (size_t)m0 * a.N;
+    gemm_any_k_kernel<FMT><<<dim3((s.N + 127) / 128, s.M), 128, 0, st>>>(s);
+    const qg_status r = check_launch(name);
+    if (r != QG_OK) return r;
+  }
+  return QG_OK;
+}
+
+// MXFP4 codes with one E8M0 code per G elements (G = 16 or 32) -> their exact
+// bf16 values, natural k order (the W4A4 expansion): a thread takes 8 codes
+// (within one block); each value is the E2M1 value times 2^(se - 127), exact
+// in fp32 and in bf16 (at most two significant bits, at least 2^-128).
+template <int G>
+__global__ void mxfp4_expand_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ se,
+                                    uint16_t* __restrict__ out, long long n8) {
   const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (i >= n8) return;
   const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(q) + i);
-  const uint32_t c = __ldg(se + (i >> 1));
-  const float f = __uint_as_float(c ? c << 23 : 0x00400000u);
+  const float f = e8m0_value(__ldg(se + i / (G / 8)));
   uint32_t o[4];
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    uint32_t h[2];
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {                 // element 2b + n: the low nibble first
-      const uint32_t x = (w >> (8 * b + 4 * n)) & 0xFu, m = x & 7u, e = m >> 1, man = m & 1u;
-      const uint32_t bits = e ? ((e + 126u) << 23) | (man << 22) : (man ? 0x3F000000u : 0u);
-      h[n] = f32_to_bf16_bits(__uint_as_float(bits | ((x & 8u) << 28)) * f);
-    }
-    o[b] = h[0] | (h[1] << 16);
-  }
+  for (int b = 0; b < 4; ++b)                     // elements 2b, 2b + 1: the low nibble first
+    o[b] = (uint32_t)f32_to_bf16_bits(e2m1_value((w >> (8 * b)) & 0xFu) * f) |
+           ((uint32_t)f32_to_bf16_bits(e2m1_value((w >> (8 * b + 4)) & 0xFu) * f) << 16);
   reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
@@ -677,12 +748,15 @@ extern "C" {
 
 qg_status qgemm_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint16_t* x, uint16_t* y,
                       int M, int N, int K, qg_stream_t stream) {
-  qg_status r = qg::check_common(w_q, x, y, M, N, K, "qgemm_w4a16");
+  qg_status r = qg::check_common_k32(w_q, x, y, M, N, K, "qgemm_w4a16");
   if (r != QG_OK) return r;
   QG_REQUIRE(w_s, QG_ERR_INVALID_ARG, "qgemm_w4a16: NULL scales");
   QG_REQUIRE(g >= 32 && (g & (g - 1)) == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
              "qgemm_w4a16: need g a power of two >= 32 dividing K (g=%d)", g);
   if (M == 0) return QG_OK;
+  if (K % 128 != 0)
+    return qg::run_any_k<qg::F_INT4>({w_q, w_s, nullptr, nullptr, nullptr, x, y, M, N, K, g},
+                                     reinterpret_cast<cudaStream_t>(stream), "qgemm_w4a16");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (M > 16) {
     bool handled = false;
@@ -694,12 +768,15 @@ qg_status qgemm_w4a16(const uint8_t* w_q, const uint16_t* w_s, int g, const uint
 
 qg_status qgemm_w4a16_zp(const uint8_t* w_q, const uint16_t* w_s, const uint8_t* w_z, int g,
                          const uint16_t* x, uint16_t* y, int M, int N, int K, qg_stream_t stream) {
-  qg_status r = qg::check_common(w_q, x, y, M, N, K, "qgemm_w4a16_zp");
+  qg_status r = qg::check_common_k32(w_q, x, y, M, N, K, "qgemm_w4a16_zp");
   if (r != QG_OK) return r;
   QG_REQUIRE(w_s && w_z, QG_ERR_INVALID_ARG, "qgemm_w4a16_zp: NULL scales or zero points");
   QG_REQUIRE(g >= 32 && (g & (g - 1)) == 0 && K % g == 0, QG_ERR_UNSUPPORTED_SHAPE,
              "qgemm_w4a16_zp: need g a power of two >= 32 dividing K (g=%d)", g);
   if (M == 0) return QG_OK;
+  if (K % 128 != 0)
+    return qg::run_any_k<qg::F_INT4Z>({w_q, w_s, w_z, nullptr, nullptr, x, y, M, N, K, g},
+                                      reinterpret_cast<cudaStream_t>(stream), "qgemm_w4a16_zp");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (M > 16) {
     bool handled = false;
@@ -711,10 +788,13 @@ qg_status qgemm_w4a16_zp(const uint8_t* w_q, const uint16_t* w_s, const uint8_t*
 
 qg_status qgemm_w8a16(const uint8_t* w_e4m3, const float* w_cs, const uint16_t* x, uint16_t* y,
                       int M, int N, int K, qg_stream_t stream) {
-  qg_status r = qg::check_common(w_e4m3, x, y, M, N, K, "qgemm_w8a16");
+  qg_status r = qg::check_common_k32(w_e4m3, x, y, M, N, K, "qgemm_w8a16");
   if (r != QG_OK) return r;
   QG_REQUIRE(w_cs, QG_ERR_INVALID_ARG, "qgemm_w8a16: NULL channel scales");
   if (M == 0) return QG_OK;
+  if (K % 128 != 0)
+    return qg::run_any_k<qg::F_FP8>({w_e4m3, nullptr, nullptr, w_cs, nullptr, x, y, M, N, K, 1},
+                                    reinterpret_cast<cudaStream_t>(stream), "qgemm_w8a16");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (M > 16) {
     bool handled = false;
@@ -740,7 +820,7 @@ qg_status qgemm_w8a8(const uint8_t* w_e4m3, const float* w_cs, const uint16_t* x
 qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt, int g,
                        const float* global_scale, const uint16_t* x, uint16_t* y, int M, int N, int K,
                        qg_stream_t stream) {
-  qg_status r = qg::check_common(w_e2m1, x, y, M, N, K, "qgemm_fp4a16");
+  qg_status r = qg::check_common_k32(w_e2m1, x, y, M, N, K, "qgemm_fp4a16");
   if (r != QG_OK) return r;
   QG_REQUIRE(w_bs, QG_ERR_INVALID_ARG, "qgemm_fp4a16: NULL block scales");
   qg::GemvArgs a{};
@@ -750,6 +830,9 @@ qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt
     QG_REQUIRE(g == 32, QG_ERR_UNSUPPORTED_SHAPE, "qgemm_fp4a16: MXFP4 needs g == 32");
     QG_REQUIRE(global_scale == nullptr, QG_ERR_INVALID_ARG, "qgemm_fp4a16: MXFP4 takes no global scale");
     if (M == 0) return QG_OK;
+    if (K % 128 != 0)
+      return qg::run_any_k<qg::F_MXFP4>({w_e2m1, w_bs, nullptr, nullptr, nullptr, x, y, M, N, K, 32}, st,
+                                        "qgemm_fp4a16");
     if (M > 16) {
       bool handled = false;
       r = qg::prefill_tc(3, w_e2m1, w_bs, nullptr, nullptr, nullptr, g, x, y, M, N, K, st, &handled, "qgemm_fp4a16");
@@ -764,6 +847,9 @@ qg_status qgemm_fp4a16(const uint8_t* w_e2m1, const uint8_t* w_bs, int scale_fmt
                "qgemm_fp4a16: misaligned global scale");
     a.gscale = global_scale;
     if (M == 0) return QG_OK;
+    if (K % 128 != 0)
+      return qg::run_any_k<qg::F_NVFP4>({w_e2m1, w_bs, nullptr, nullptr, global_scale, x, y, M, N, K, 16}, st,
+                                        "qgemm_fp4a16");
     if (M > 16) {
       bool handled = false;
       r = qg::prefill_tc(4, w_e2m1, w_bs, nullptr, nullptr, global_scale, g, x, y, M, N, K, st, &handled,
@@ -780,12 +866,12 @@ namespace {
 // W4A4: for M > 16 the block-scaled FP4 tensor cores (gemm_fp4.cu), when K
 // is a multiple of 256 and both scale arrays are 8-byte aligned; otherwise
 // the MXFP4 activations (blocks of g_act) are expanded to bf16 (exact) into
-// a_work and the MXFP4-weight GEMM runs on them.
+// a_work and the MXFP4-weight GEMM (qgemm_fp4a16) runs on them.
 qg_status w4a4_impl(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint8_t* a_e2m1, const uint8_t* a_e8m0,
                     int g_act, uint16_t* a_work, uint16_t* y, int M, int N, int K, qg_stream_t stream,
                     const char* name) {
   QG_REQUIRE(a_e2m1 && a_e8m0 && a_work && w_e8m0, QG_ERR_INVALID_ARG, "%s: NULL pointer", name);
-  qg_status r = check_common(w_e2m1, a_work, y, M, N, K, name);
+  qg_status r = check_common_k32(w_e2m1, a_work, y, M, N, K, name);
   if (r != QG_OK) return r;
   QG_REQUIRE(aligned16(a_e2m1), QG_ERR_MISALIGNED, "%s: misaligned activation codes", name);
   if (M == 0) return QG_OK;
@@ -795,13 +881,12 @@ qg_status w4a4_impl(const uint8_t* w_e2m1, const uint8_t* w_e8m0, const uint8_t*
     r = w4a4_mxfp4_bs(w_e2m1, w_e8m0, a_e2m1, a_e8m0, g_act, y, M, N, K, st, &handled);
     if (handled) return r;
   }
-  if (g_act == 32) {
-    r = qg_dequant_weights(QG_FMT_MXFP4, a_e2m1, a_e8m0, 32, a_work, M, K, stream);
-  } else {
-    const long long n8 = (long long)M * K / 8;
-    mxfp4_expand16_kernel<<<unsigned((n8 + 255) / 256), 256, 0, st>>>(a_e2m1, a_e8m0, a_work, n8);
-    r = check_launch(name);
-  }
+  const long long n8 = (long long)M * K / 8;
+  if (g_act == 32)
+    mxfp4_expand_kernel<32><<<unsigned((n8 + 255) / 256), 256, 0, st>>>(a_e2m1, a_e8m0, a_work, n8);
+  else
+    mxfp4_expand_kernel<16><<<unsigned((n8 + 255) / 256), 256, 0, st>>>(a_e2m1, a_e8m0, a_work, n8);
+  r = check_launch(name);
   if (r != QG_OK) return r;
   return qgemm_fp4a16(w_e2m1, w_e8m0, QG_SCALE_E8M0, 32, nullptr, a_work, y, M, N, K, stream);
 }

@@ -212,6 +212,37 @@ __global__ void __launch_bounds__(kThreadsMoe) moe_w4a8_kernel(const MoeArgs p) 
   }
 }
 
+// The general path for shapes outside the tiled kernels' (g == 128,
+// K % 128 == 0, N % 16 == 0): one thread per output y[r, n].  The row's
+// expert is found by binary search in expert_off; each group's partial sum of
+// the exact products e4m3(a) * q accumulates in fp32 in k order, the group
+// scale is applied to it in fp32, the row scale to the total, then one bf16
+// rounding -- the tiled kernels' arithmetic, without their tiling.  It is
+// there for odd widths and group sizes, not for speed.
+__global__ void moe_w4a8_any_kernel(const MoeArgs p, int g, int r0) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x, r = r0 + (int)blockIdx.y;
+  if (n >= p.N || r < __ldg(p.off) || r >= __ldg(p.off + p.E)) return;
+  int lo = 0, hi = p.E;                               // off[lo] <= r < off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.off + mid) <= r) lo = mid; else hi = mid;
+  }
+  const size_t wrow = (size_t)lo * p.N + n;
+  const uint8_t* wq = p.wq + wrow * (p.K / 2);
+  const uint16_t* ws = p.ws + wrow * (p.K / g);
+  const uint8_t* a = p.a + (size_t)r * p.K;
+  float acc = 0.f;
+  for (int k0 = 0; k0 < p.K; k0 += g) {
+    float part = 0.f;
+    for (int k = k0; k < k0 + g; ++k) {
+      const uint32_t b = __ldg(wq + k / 2), u = (k & 1) ? b >> 4 : b & 15u;
+      part = fmaf(e4m3_to_f32(__ldg(a + k)), (float)(u >= 8u ? (int)u - 16 : (int)u), part);
+    }
+    acc = fmaf(bf16_bits_to_f32(__ldg(ws + k0 / g)), part, acc);
+  }
+  p.y[(size_t)r * p.N + n] = f32_to_bf16_bits(acc * __ldg(p.a_s + r));
+}
+
 }  // namespace
 }  // namespace qg
 
@@ -229,11 +260,22 @@ extern "C" qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,
   QG_REQUIRE(a_e4m3 && a_s && expert_off && w_q && w_s && y, QG_ERR_INVALID_ARG,
              "qgemm_w4a8_grouped: NULL pointer");
   QG_REQUIRE(R >= 0 && E >= 1 && N > 0 && K > 0, QG_ERR_INVALID_ARG, "qgemm_w4a8_grouped: bad sizes");
-  QG_REQUIRE(g == 128 && K % 128 == 0 && N % 16 == 0, QG_ERR_UNSUPPORTED_SHAPE,
-             "qgemm_w4a8_grouped: need g == 128, K %% 128 == 0, N %% 16 == 0");
+  QG_REQUIRE(g >= 32 && (g & (g - 1)) == 0 && K % g == 0 && K % 32 == 0 && N % 8 == 0,
+             QG_ERR_UNSUPPORTED_SHAPE,
+             "qgemm_w4a8_grouped: need g a power of two >= 32 dividing K, K %% 32 == 0, N %% 8 == 0");
   QG_REQUIRE(qg::aligned16(a_e4m3) && qg::aligned16(w_q) && qg::aligned16(y) && qg::aligned16(w_s),
              QG_ERR_MISALIGNED, "qgemm_w4a8_grouped: misaligned pointer");
   if (R == 0) return QG_OK;
+  if (!(g == 128 && K % 128 == 0 && N % 16 == 0)) {
+    const qg::MoeArgs p{a_e4m3, a_s, expert_off, w_q, w_s, y, R, E, N, K};
+    for (int r0 = 0; r0 < R; r0 += 65535) {           // the grid's y extent is at most 65535 rows
+      qg::moe_w4a8_any_kernel<<<dim3((N + 127) / 128, std::min(65535, R - r0)), 128, 0,
+                                reinterpret_cast<cudaStream_t>(stream)>>>(p, g, r0);
+      const qg_status r = qg::check_launch("qgemm_w4a8_grouped");
+      if (r != QG_OK) return r;
+    }
+    return QG_OK;
+  }
   if (R >= qg::kFp8pMinRows)
     return qg::moe_w4a8_fp8p(a_e4m3, a_s, expert_off, w_q, w_s, y, R, E, N, K,
                              reinterpret_cast<cudaStream_t>(stream));

@@ -66,7 +66,10 @@ def test_null_pointers_are_invalid_args(lib):
 
 
 def test_shape_rules(lib):
-    assert _rc(lib, "qgemm_w4a16", FAKE, FAKE, 128, FAKE, FAKE, 1, 128, 100) == 2    # K % 128
+    assert _rc(lib, "qgemm_w4a16", FAKE, FAKE, 128, FAKE, FAKE, 1, 128, 100) == 2    # K % 32
+    assert _rc(lib, "qgemm_w4a16", FAKE, FAKE, 128, FAKE, FAKE, 1, 128, 160) == 2    # K % g
+    assert _rc(lib, "qgemm_w8a16", FAKE, FAKE, FAKE, FAKE, 1, 128, 112) == 2         # K % 32
+    assert _rc(lib, "qgemm_w8a8", FAKE, FAKE, FAKE, FAKE, 1, 128, 160) == 2          # K % 128 (1 x 128 blocks)
     assert _rc(lib, "qgemm_w4a16", FAKE, FAKE, 48, FAKE, FAKE, 1, 128, 384) == 2     # g % 32
     assert _rc(lib, "qgemm_w8a16", FAKE, FAKE, FAKE, FAKE, 1, 12, 128) == 2          # N % 8
     assert _rc(lib, "qgemm_fp4a16", FAKE, FAKE, 0, 16, None, FAKE, FAKE, 1, 128, 128) == 2
@@ -74,7 +77,10 @@ def test_shape_rules(lib):
     assert _rc(lib, "qgemm_fp4a16", FAKE, FAKE, 7, 16, FAKE, FAKE, FAKE, 1, 128, 128) == 1
     assert _rc(lib, "quant_act_mxfp4", FAKE, FAKE, FAKE, 8, 1, 128) == 2
     assert _rc(lib, "quant_act_fp8_block", FAKE, FAKE, FAKE, 12, 1, 96) == 2
-    assert _rc(lib, "qgemm_w4a8_grouped", FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, 1, 1, 16, 128) == 2
+    assert _rc(lib, "qgemm_w4a8_grouped", FAKE, FAKE, FAKE, FAKE, FAKE, 48, FAKE, 1, 1, 16, 384) == 2  # g
+    assert _rc(lib, "qgemm_w4a8_grouped", FAKE, FAKE, FAKE, FAKE, FAKE, 32, FAKE, 1, 1, 12, 128) == 2  # N % 8
+    assert _rc(lib, "qgemm_w4a8_grouped", FAKE, FAKE, FAKE, FAKE, FAKE, 128, FAKE, 1, 1, 16, 160) == 2  # K % g
+    assert _rc(lib, "qgemm_w4a8_grouped", FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, 0, 1, 8, 96) == 2  # K % g
     assert _rc(lib, "qg_dequant_weights", 9, FAKE, FAKE, 128, FAKE, 8, 128) == 1
 
 
@@ -142,7 +148,7 @@ def test_w4a4_argument_validation(lib):
     assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, None, FAKE, FAKE, FAKE, 1, 128, 128) == 1
     assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, None, FAKE, FAKE, FAKE, FAKE, 1, 128, 128) == 1
     assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 12, 128) == 2     # N % 8
-    assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 96) == 2     # K % 128
+    assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 80) == 2     # K % 32
     assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE_MIS, FAKE, FAKE, FAKE, 1, 128, 128) == 3
     assert _rc(lib, "qgemm_w4a4_mxfp4", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 128, 128) == 0    # M = 0
 
