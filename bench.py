@@ -10,7 +10,8 @@ One step = one pass over every row of the hot path at its workload size:
   MoE, FP8 scales  the same layer on the FP8-group-scale recipe (E4M3 x E4M3
                  tensor-core GEMMs; roofline against the FP8 dense peak)
   MoE, E4M3 entry  the same layer through qgemm_w4a8_grouped (E4M3 activations
-                 handed over as codes, exact bf16 group scales)
+                 handed over as codes, converted to fp16 inside the GEMM, exact
+                 bf16 group scales; fp16 tensor cores, roofline against bf16)
   zero points    asymmetric INT4 (zero point per group of 64): M = 1 GEMVs and
                  M = 8192 prefill over the same three (N, K)
   W8A8 GEMV      FP8 weights, activations quantized per 1 x 128 block inside the
@@ -74,8 +75,7 @@ PROFILED_TRAFFIC = {
             "algorithmic_bytes": 1021.4e6, "profile": "profiles/moe_w4a8_f16act_t4096_e8.md"},
     "moe_fp8s": {"bytes": 940.7e6, "launch": "moe_fp8s_kernel gate/up R=8192 N=28672 K=4096",
                  "algorithmic_bytes": 981.4e6, "profile": "profiles/moe_fp8s_t4096_e8.md"},
-    "moe_e4m3": {"bytes": 950.95e6, "launch": "moe_fp8p_kernel gate/up R=8192 N=28672 K=4096",
-                 "algorithmic_bytes": 987.8e6, "profile": "profiles/moe_w4a8_e4m3_fp8p_t4096_e8.md"},
+    "moe_e4m3": None,
     "prefill_w4a4": {"bytes": 245.8e6, "launch": "w4a4_bs_kernel<true> M=8192 N=14336 K=4096",
                      "algorithmic_bytes": 283.9e6, "profile": "profiles/w4a4_bs_m8192.md"},
 }
@@ -84,9 +84,9 @@ PROFILED_TRAFFIC = {
 # the main kernel of rows timed in parts
 MAIN_KERNEL = {"moe": "moe_f16_kernel (gate/up + down launches)",
                "moe_fp8s": "moe_fp8s_kernel (gate/up + down launches)",
-               "moe_e4m3": "moe_fp8p_kernel (gate/up + down launches)"}
+               "moe_e4m3": "moe_f16_kernel<true> (gate/up + down launches)"}
 MOE_ROWS = ("moe", "moe_fp8s", "moe_e4m3")
-FP8_ROWS = ("moe_fp8s", "moe_e4m3")          # FP8 tensor-core contractions: roofline against the FP8 peak
+FP8_ROWS = ("moe_fp8s",)                     # FP8 tensor-core contractions: roofline against the FP8 peak
 FP4_ROWS = ("prefill_w4a4",)                  # block-scaled FP4 contractions: 3 x the FP8 peak (nominal 13.5 / 4.5)
 
 

@@ -247,11 +247,11 @@ __global__ void moe_w4a8_any_kernel(const MoeArgs p, int g, int r0) {
 }  // namespace qg
 
 namespace qg {
-qg_status moe_w4a8_fp8p(const uint8_t* a_e4m3, const float* a_s, const int32_t* expert_off, const uint8_t* w_q,
-                        const uint16_t* w_s, uint16_t* y, int R, int E, int N, int K, cudaStream_t st);
-// rows from which the FP8 tensor-core kernel (128-row tiles, per-group
-// promotion) takes over from the 64-row mma.sync tiles
-constexpr int kFp8pMinRows = 256;
+qg_status moe_w4a8_e4m3_f16(const uint8_t* a_e4m3, const float* a_s, const int32_t* expert_off, const uint8_t* w_q,
+                            const uint16_t* w_s, uint16_t* y, int R, int E, int N, int K, cudaStream_t st);
+// rows from which the tcgen05 kernel (256-row tiles, codes converted to fp16
+// in shared memory) takes over from the 64-row mma.sync tiles
+constexpr int kTcMinRows = 256;
 }  // namespace qg
 
 extern "C" qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s, const int32_t* expert_off,
@@ -276,9 +276,9 @@ extern "C" qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,
     }
     return QG_OK;
   }
-  if (R >= qg::kFp8pMinRows)
-    return qg::moe_w4a8_fp8p(a_e4m3, a_s, expert_off, w_q, w_s, y, R, E, N, K,
-                             reinterpret_cast<cudaStream_t>(stream));
+  if (R >= qg::kTcMinRows)
+    return qg::moe_w4a8_e4m3_f16(a_e4m3, a_s, expert_off, w_q, w_s, y, R, E, N, K,
+                                 reinterpret_cast<cudaStream_t>(stream));
   qg::MoeArgs p{a_e4m3, a_s, expert_off, w_q, w_s, y, R, E, N, K};
   const size_t smem = (size_t)(2 * qg::BM + 2 * qg::BN) * qg::LDS * 2;
   if (!qg::ensure_smem(qg::moe_w4a8_kernel, (int)smem))

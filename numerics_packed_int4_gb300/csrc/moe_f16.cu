@@ -38,6 +38,7 @@ namespace qg {
 
 bool make_u8_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols);
 bool make_bf16_tmap(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols);
+bool make_u8_tmap_swizzled(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_cols);
 
 namespace {
 
@@ -45,7 +46,10 @@ constexpr int hTW = 128;                 // weight rows per tile (MMA M)
 constexpr int hTT = 256;                 // activation rows per tile (MMA N)
 constexpr int hBK = 64;                  // k per slab: one 128-byte row of fp16
 constexpr int hXStages = 6;              // activation stages (<= hSlots: released through a_empty)
-constexpr int hSlots = 8;                // TMEM A slots and packed-weight stages
+constexpr int hXStagesE = 4;             // fp16 stages written by the dequant sets (E4M3 input)
+constexpr int hEStages = 4;              // E4M3 staging stages (E4M3 input)
+constexpr int hSlots = 8;                // TMEM A slots (and packed-weight stages, fp16 input)
+constexpr int hWStagesE = 4;             // packed-weight stages, E4M3 input
 constexpr int hDeqWarps = 16;            // four sets of 4 (one per TMEM lane quarter)
 constexpr int hDeqSet = 4;
 constexpr int hDeqSets = hDeqWarps / hDeqSet;
@@ -54,11 +58,20 @@ constexpr int hSchedWarp = hDeq0 + hDeqWarps;
 constexpr int hThreads = (hSchedWarp + 1) * 32;
 constexpr int hXStage = hTT * hBK * 2;   // 32 KB fp16 activations
 constexpr int hWStage = hTW * hBK / 2;   // 4 KB packed INT4
+constexpr int hEStage = hTT * hBK;       // 16 KB E4M3 activations (64-byte swizzled rows)
 constexpr uint32_t hTmemCols = 512;
 constexpr uint32_t hACol0 = 256;
 constexpr uint32_t hACols = hBK / 2;     // 32 columns: 64 fp16 per lane
 constexpr uint32_t hDrainCap = 1u << 21;
-static_assert(hXStages <= hSlots, "activation stages are released through the A-slot barriers");
+static_assert(hXStages <= hSlots && hXStagesE <= hSlots, "activation stages are released through the A-slot barriers");
+// E4M3 input: the set converting slab g waits on staging stage g % hEStages
+// for the phase of slab g.  A parity wait is only sound if the stage's
+// previous phase (slab g - hEStages) has completed, and that is guaranteed
+// only when the same set converted slab g - hEStages: with 4 sets and 3
+// staging stages a set can pass the wait on the previous phase's parity and
+// the phases of the barrier pair mix (a build with 3 stages faulted).
+static_assert(hEStages % hDeqSets == 0, "E4M3 staging ring: a multiple of the dequant sets");
+static_assert(hWStagesE % hDeqSets == 0 && hSlots % hDeqSets == 0, "packed-weight ring: the same rule");
 
 struct F16Args {
   const float* a_s;
@@ -74,10 +87,12 @@ struct F16Args {
 
 struct __align__(8) F16Tail {
   uint64_t x_full[hXStages];
-  uint64_t w_full[hSlots];
+  uint64_t w_full[hSlots];                // the first nW used
   uint64_t w_empty[hSlots];
   uint64_t a_full[hSlots];
   uint64_t a_empty[hSlots];
+  uint64_t e_full[hEStages];             // E4M3 input: staging stage loaded
+  uint64_t e_empty[hEStages];            // E4M3 input: staging stage converted
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
@@ -140,9 +155,21 @@ QG_DEVICE int row_exponent(const uint16_t* srow, int ng) {
   return min(max(12 - e2, -100), 100);
 }
 
+// kE8: the activations arrive as E4M3 codes.  warp 2 then TMA-loads them
+// into a 64-byte swizzled staging ring, and the dequant set that writes slab
+// g's A slot also converts slab g's codes to fp16 (exact) into the 128-byte
+// swizzled B layout, once slab g - hXStagesE's MMAs have released the stage;
+// its A-slot arrival then covers both operands.
+template <bool kE8>
 __global__ void __launch_bounds__(hThreads, 1)
 moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                const F16Args p) {
+  constexpr int nX = kE8 ? hXStagesE : hXStages;
+  // how far a dequant set may produce into tile e + 1 before the epilogue of
+  // tile e: its waits reach back hSlots slabs (A slot), with E4M3 input nX
+  // (fp16 stage), and must not wait on MMAs of tile e + 1
+  constexpr int kRun = kE8 ? nX : hSlots;
+  constexpr int nW = kE8 ? hWStagesE : hSlots;           // packed-weight stages
   const int ntiles_total = tile_count(p);
   const int ntiles = ((int)blockIdx.x < ntiles_total)
                          ? (ntiles_total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
@@ -153,13 +180,18 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* xs = smem;                                    // [hXStages][32 KB] fp16, swizzled
-  uint8_t* wsm = xs + hXStages * hXStage;                // [hSlots][4 KB] INT4
-  F16Tail* tl = reinterpret_cast<F16Tail*>(wsm + hSlots * hWStage);
+  uint8_t* xs = smem;                                    // [nX][32 KB] fp16, swizzled
+  uint8_t* es = xs + nX * hXStage;                       // E4M3 input: [hEStages][16 KB]
+  uint8_t* wsm = es + (kE8 ? hEStages * hEStage : 0);    // [nW][4 KB] INT4
+  F16Tail* tl = reinterpret_cast<F16Tail*>(wsm + nW * hWStage);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < hXStages; ++s) mbar_init(&tl->x_full[s], 1);
+    for (int s = 0; s < hEStages; ++s) {
+      mbar_init(&tl->e_full[s], 1);
+      mbar_init(&tl->e_empty[s], hDeqSet);
+    }
     for (int s = 0; s < hSlots; ++s) {
       mbar_init(&tl->w_full[s], 1);
       mbar_init(&tl->w_empty[s], hDeqSet);
@@ -189,15 +221,33 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       HTile t = tile_of(0);
       for (int g = 0; g < total; ++g, ++s) {
         if (s == nslab) { s = 0; t = tile_of(++i); }
-        const int st = g % hSlots, r = g / hSlots;
+        const int st = g % nW, r = g / nW;
         if (r > 0 && !mbar_wait(&tl->w_empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
         mbar_arrive_expect_tx(&tl->w_full[st], hWStage);
         tma_load_2d(wsm + st * hWStage, &tmap_w, &tl->w_full[st], s * (hBK / 2), t.e * p.N + t.n0);
         issued = g + 1;
       }
       if (*abort) {
-        for (int g = max(0, issued - hSlots); g < issued; ++g)
-          mbar_drain(&tl->w_full[g % hSlots], (g / hSlots) & 1, hDrainCap);
+        for (int g = max(0, issued - nW); g < issued; ++g)
+          mbar_drain(&tl->w_full[g % nW], (g / nW) & 1, hDrainCap);
+      }
+    }
+  } else if (warp == 2 && kE8) {
+    // ---------------- TMA producer: E4M3 activations ----------------
+    if (lane == 0) {
+      int issued = 0, s = 0, i = 0;
+      HTile t = tile_of(0);
+      for (int g = 0; g < total; ++g, ++s) {
+        if (s == nslab) { s = 0; t = tile_of(++i); }
+        const int st = g % hEStages, r = g / hEStages;
+        if (r > 0 && !mbar_wait(&tl->e_empty[st], (r - 1) & 1, p.cap, abort, p.err)) break;
+        mbar_arrive_expect_tx(&tl->e_full[st], hEStage);
+        tma_load_2d(es + st * hEStage, &tmap_a, &tl->e_full[st], s * hBK, t.r0);
+        issued = g + 1;
+      }
+      if (*abort) {
+        for (int g = max(0, issued - hEStages); g < issued; ++g)
+          mbar_drain(&tl->e_full[g % hEStages], (g / hEStages) & 1, hDrainCap);
       }
     }
   } else if (warp == 2) {
@@ -232,7 +282,7 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         }
         bool ok = true;
         for (int s = 0; s < nslab; ++s, ++g) {
-          const int st = g % hXStages, sa = g % hSlots;
+          const int st = g % nX, sa = g % hSlots;
           if (!wait_count(&tl->ready, (unsigned)g, ready, p.cap * 4, abort, p.err)) { ok = false; break; }
           tc_fence_after();
           const uint64_t bdesc = sw128_kmajor_desc(smem_addr(xs + st * hXStage));
@@ -255,7 +305,7 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     if (lane == 0) {
       for (int g = 0; g < total; ++g) {
         if (!mbar_wait(&tl->a_full[g % hSlots], (g / hSlots) & 1, p.cap, abort, p.err)) break;
-        if (!mbar_wait(&tl->x_full[g % hXStages], (g / hXStages) & 1, p.cap, abort, p.err)) break;
+        if (!kE8 && !mbar_wait(&tl->x_full[g % hXStages], (g / hXStages) & 1, p.cap, abort, p.err)) break;
         publish_count(&tl->ready, (unsigned)(g + 1));
       }
     }
@@ -337,19 +387,19 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     advance(pf, hDeqSets);
     uint32_t sc_nxt = scale_of(pf);
     for (int g = set; g < total; g += hDeqSets) {
-      while (e_next < ntiles - 1 && g >= (e_next + 1) * nslab + hSlots) {
+      while (e_next < ntiles - 1 && g >= (e_next + 1) * nslab + kRun) {
         if (!(ok = epilogue(e_next))) break;
         ++e_next;
       }
       if (!ok) break;
-      const int sa = g % hSlots, ra = g / hSlots;
+      const int sa = g % hSlots, ra = g / hSlots, sw = g % nW;
       const uint32_t s2 = sc_cur;
       sc_cur = sc_nxt;
       advance(pf, hDeqSets);                         // pf now at this set's slab after the next
       sc_nxt = scale_of(pf);
-      if (!mbar_wait_warp(&tl->w_full[sa], ra & 1, p.cap, abort, p.err)) { ok = false; break; }
-      const uint4 wa = *reinterpret_cast<const uint4*>(wsm + sa * hWStage + row * (hBK / 2));
-      const uint4 wb = *reinterpret_cast<const uint4*>(wsm + sa * hWStage + row * (hBK / 2) + 16);
+      if (!mbar_wait_warp(&tl->w_full[sw], (g / nW) & 1, p.cap, abort, p.err)) { ok = false; break; }
+      const uint4 wa = *reinterpret_cast<const uint4*>(wsm + sw * hWStage + row * (hBK / 2));
+      const uint4 wb = *reinterpret_cast<const uint4*>(wsm + sw * hWStage + row * (hBK / 2) + 16);
       const uint32_t v[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
       uint32_t out[32];
 #pragma unroll
@@ -359,8 +409,16 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         out[4 * j + 0] = nat[0]; out[4 * j + 1] = nat[1];
         out[4 * j + 2] = nat[2]; out[4 * j + 3] = nat[3];
       }
-      mbar_arrive_warp(&tl->w_empty[sa]);            // packed slab decoded: its stage may be refilled
-      if (ra > 0) {
+      mbar_arrive_warp(&tl->w_empty[sw]);            // packed slab decoded: its stage may be refilled
+      if (kE8) {
+        // slab g - nX's MMAs complete (and with them slab g - hSlots's): the
+        // fp16 stage and the A slot are both free
+        if (g >= nX) {
+          const int gp = g - nX;
+          if (!mbar_wait_warp(&tl->a_empty[gp % hSlots], (gp / hSlots) & 1, p.cap, abort, p.err)) { ok = false; break; }
+          tc_fence_after();
+        }
+      } else if (ra > 0) {
         if (!mbar_wait_warp(&tl->a_empty[sa], (ra - 1) & 1, p.cap, abort, p.err)) { ok = false; break; }
         tc_fence_after();
       }
@@ -369,6 +427,34 @@ moe_f16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         const uint32_t (&o1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&out[16]);
         tmem_st16(lane_base + sa * hACols, o0);
         tmem_st16(lane_base + sa * hACols + 16, o1);
+      }
+      if (kE8) {
+        // slab g's E4M3 codes -> fp16 B stage.  Task (row r, 16 codes j): the
+        // codes are chunk j of r's 64-byte staging row (64-byte swizzle: at
+        // chunk j ^ ((r >> 1) & 3)); their fp16 values are chunks 2j, 2j + 1
+        // of r's 128-byte B row (128-byte swizzle: chunk c at c ^ (r & 7)).
+        // Eight consecutive lanes take eight consecutive rows: conflict-free.
+        const int se = g % hEStages;
+        if (!mbar_wait_warp(&tl->e_full[se], (g / hEStages) & 1, p.cap, abort, p.err)) {
+          tmem_wait_st();
+          ok = false;
+          break;
+        }
+        const uint8_t* eb = es + se * hEStage;
+        uint8_t* xb = xs + (g % nX) * hXStage;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int j = i & 3, r = 128 * (i >> 2) + row;
+          const uint4 c = *reinterpret_cast<const uint4*>(eb + r * hBK + 16 * (j ^ ((r >> 1) & 3)));
+          const uint4 lo = make_uint4(e4m3x2_to_f16x2(c.x), e4m3x2_to_f16x2(c.x >> 16),
+                                      e4m3x2_to_f16x2(c.y), e4m3x2_to_f16x2(c.y >> 16));
+          const uint4 hi = make_uint4(e4m3x2_to_f16x2(c.z), e4m3x2_to_f16x2(c.z >> 16),
+                                      e4m3x2_to_f16x2(c.w), e4m3x2_to_f16x2(c.w >> 16));
+          *reinterpret_cast<uint4*>(xb + r * 2 * hBK + 16 * ((2 * j) ^ (r & 7))) = lo;
+          *reinterpret_cast<uint4*>(xb + r * 2 * hBK + 16 * ((2 * j + 1) ^ (r & 7))) = hi;
+        }
+        fence_proxy_async_smem();                    // the tensor core reads the stage through the async proxy
+        mbar_arrive_warp(&tl->e_empty[se]);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -450,12 +536,42 @@ extern "C" qg_status qgemm_w4a8_grouped_f16act(const uint16_t* a_f16, const floa
   a.err = err;
   a.cap = wait_limit();
   const int smem = hXStages * hXStage + hSlots * hWStage + (int)sizeof(F16Tail) + 1024;
-  if (!ensure_smem(moe_f16_kernel, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped_f16act: smem attribute");
+  if (!ensure_smem(moe_f16_kernel<false>, smem))
+    return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped_f16act: smem attribute");
   const long long bound = ((long long)(R + hTT - 1) / hTT + E) * a.tiles_w;
   const int grid = (int)std::min<long long>(bound, (long long)sm_count());
-  moe_f16_kernel<<<grid, hThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tmap_a, tmap_w, a);
+  moe_f16_kernel<false><<<grid, hThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tmap_a, tmap_w, a);
   return check_launch("qgemm_w4a8_grouped_f16act");
 }
+
+namespace qg {
+// The E4M3-activation entry qgemm_w4a8_grouped on the same kernel, converting
+// the codes to fp16 in shared memory (arguments validated by the caller:
+// g == 128, K % 128 == 0, N % 16 == 0, 16-byte aligned pointers).  The
+// result is bit-identical to qgemm_w4a8_grouped_f16act on the fp16 copy.
+qg_status moe_w4a8_e4m3_f16(const uint8_t* a_e4m3, const float* a_s, const int32_t* expert_off, const uint8_t* w_q,
+                            const uint16_t* w_s, uint16_t* y, int R, int E, int N, int K, cudaStream_t st) {
+  CUtensorMap tmap_a, tmap_w;
+  if (!make_u8_tmap_swizzled(&tmap_a, a_e4m3, R, K, hTT, hBK))      // 64-byte rows: 64-byte swizzle
+    return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped: cannot encode the activation tensor map");
+  if (!make_u8_tmap(&tmap_w, w_q, E * N, K / 2, hTW, hBK / 2))
+    return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped: cannot encode the weight tensor map");
+  unsigned int* err = device_error_word();
+  if (!err) return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped: no device error word");
+  F16Args a{};
+  a.a_s = a_s; a.off = expert_off; a.ws = w_s; a.we = nullptr; a.y = y;
+  a.R = R; a.E = E; a.N = N; a.K = K;
+  a.tiles_w = (N + hTW - 1) / hTW;
+  a.err = err;
+  a.cap = wait_limit();
+  const int smem = hXStagesE * hXStage + hEStages * hEStage + hWStagesE * hWStage + (int)sizeof(F16Tail) + 1024;
+  if (!ensure_smem(moe_f16_kernel<true>, smem)) return set_error(QG_ERR_CUDA, "qgemm_w4a8_grouped: smem attribute");
+  const long long bound = ((long long)(R + hTT - 1) / hTT + E) * a.tiles_w;
+  const int grid = (int)std::min<long long>(bound, (long long)sm_count());
+  moe_f16_kernel<true><<<grid, hThreads, smem, st>>>(tmap_a, tmap_w, a);
+  return check_launch("qgemm_w4a8_grouped (tcgen05, E4M3 converted in shared memory)");
+}
+}  // namespace qg
 
 extern "C" qg_status qg_w4a8_row_shifts(const uint16_t* w_s, int8_t* w_e, int rows, int G, qg_stream_t stream) {
   using namespace qg;

@@ -130,6 +130,9 @@ QG_DEVICE void tmem_dealloc(uint32_t taddr, uint32_t ncols) {   // whole warp
 }
 QG_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 QG_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// generic-proxy shared-memory writes made visible to the async proxy (TMA
+// stores, tensor-core operand reads) that a later barrier hands them to
+QG_DEVICE void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // D[tmem] (+)= A[tmem] x B[smem desc]; kind::f16 (bf16 inputs, fp32 accumulate)
 QG_DEVICE void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, bool accumulate) {
