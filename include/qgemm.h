@@ -238,7 +238,9 @@ QG_API qg_status quant_act_fp8_block(const uint16_t* x, uint8_t* q, float* s, in
  *   w_q [E][N][K/2] packed INT4   w_s [E][N][K/g] bf16   y [R][N] bf16.
  * Rules: g a power of two >= 32, K % g == 0, K % 32 == 0, N % 8 == 0,
  * R >= 0, E >= 1.  g == 128 with K % 128 == 0 and N % 16 == 0 (the W4A8
- * configuration) runs on the tiled kernels (FP8 tensor cores from 256 rows);
+ * configuration) runs on the tiled kernels (from 256 rows tcgen05 with the
+ * codes converted to fp16 in shared memory, bit-identical to
+ * qgemm_w4a8_grouped_f16act);
  * every other shape on a general kernel with the same arithmetic (per-group
  * fp32 partial sums, scaled in fp32), correct but not tuned.                */
 QG_API qg_status qgemm_w4a8_grouped(const uint8_t* a_e4m3, const float* a_s,

@@ -1,34 +1,36 @@
-// W4A8 grouped (MoE) GEMM with exact bf16 group scales, for activations
-// handed over as fp16 re-encodings of their E4M3 codes.
+// W4A8 grouped (MoE) GEMM with exact bf16 group scales on the fp16 tensor
+// cores, for both forms of the activations: E4M3 codes (qgemm_w4a8_grouped,
+// from 256 rows) and fp16 re-encodings of those codes handed over by the
+// caller (qgemm_w4a8_grouped_f16act).
 //
 // Semantics (Production-Ready W4A8): y[r,n] = a_s[r] * sum_k e4m3(a[r,k]) *
 // q[n,k] * s[n,k/128], every product exact, fp32 accumulation, one bf16
-// rounding at the store -- the same result as qgemm_w4a8_grouped.  Every
-// E4M3 value is exact in fp16, so an fp16 copy of the E4M3 activations is a
-// lossless encoding; with it in HBM the activations go by TMA straight into
-// the MMA's B layout, and the kernel needs none of the shared-memory
-// restaging (E4M3 -> fp16 converter warps) that bounds the E4M3-input kernel,
-// nor that kernel's CTA pairs.  The weights are formed as fp16(q * s * 2^e_n)
-// -- exact: q * s has at most 11 significant bits, and the per-row power of
-// two e_n puts the row's largest scale in [2^11, 2^12) -- and the epilogue
-// multiplies by 2^-e_n and the token scale.
+// rounding at the store.  Every E4M3 value is exact in fp16, so the fp16
+// form of the activations is a lossless encoding and both forms give the
+// same bits.  The weights are formed as fp16(q * s * 2^e_n) -- exact: q * s
+// has at most 11 significant bits, and the per-row power of two e_n puts the
+// row's largest scale in [2^11, 2^12) -- and the epilogue multiplies by
+// 2^-e_n and the token scale.  No per-group promotion is needed.
 //
 // tcgen05.mma.cta_group::1.kind::f16 (fp16 A and B), M = 128 channels,
 // N = 256 activation rows, K = 16:
 //   A operand  = the fp16 weights, written by 16 dequant warps into 8 slots
 //                of tensor memory (64 k = 32 columns per slot);
-//   B operand  = the fp16 activations, TMA-loaded in the 128-byte swizzled
-//                K-major layout (64 k per 128-byte row, 32 KB per stage);
+//   B operand  = the fp16 activations in the 128-byte swizzled K-major
+//                layout (64 k per 128-byte row, 32 KB per stage): TMA-loaded
+//                as they are (fp16 input, 6 stages), or converted from the
+//                E4M3 codes by the dequant sets (E4M3 input, 4 stages, the
+//                codes TMA-loaded into a 4-stage staging ring);
 //   D          = fp32 accumulator in TMEM columns 0-255.
 // Persistent, one CTA per SM over the (expert, 128-channel block, 256-row
 // block) tile list with row blocks inner, the rings running on across tiles
 // and the epilogue of a tile overlapping the next tile's MMAs.  Roles: warp 0
-// TMA for the packed weights (8 stages), warp 1 TMEM + MMA issuer, warp 2 TMA
-// for the activations (6 stages), warps 3-18 dequant (four sets of four, one
-// warp per TMEM lane quarter, a thread decoding its row's 64-k slab, each set
-// taking every fourth slab) and the epilogue, warp 19 scheduler (waits for
-// each slab's operands and publishes the ready count the issuer polls).
-// Every wait is bounded.
+// TMA for the packed weights, warp 1 TMEM + MMA issuer, warp 2 TMA for the
+// activations, warps 3-18 dequant (four sets of four, one warp per TMEM lane
+// quarter, a thread decoding its row's 64-k slab, each set taking every
+// fourth slab; with E4M3 input the set also converts its slab's codes) and
+// the epilogue, warp 19 scheduler (waits for each slab's operands and
+// publishes the ready count the issuer polls).  Every wait is bounded.
 #include <algorithm>
 
 #include "dequant.cuh"
