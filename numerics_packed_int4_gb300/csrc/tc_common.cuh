@@ -105,7 +105,6 @@ QG_DEVICE bool wait_count(unsigned int* ctr, unsigned int idx, unsigned int& cac
   return false;
 }
 
-QG_DEVICE bool warp_aborted(volatile int* abort) { return __any_sync(0xffffffffu, *abort != 0); }
 
 // ---- TMA ------------------------------------------------------------------
 QG_DEVICE void tma_prefetch_desc(const CUtensorMap* m) {
@@ -176,78 +175,6 @@ QG_DEVICE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 QG_DEVICE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// ---- CTA pairs (cta_group::2) ----------------------------------------------------
-QG_DEVICE uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// all threads of both CTAs of the cluster
-QG_DEVICE void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// arrive on the mbarrier at the same shared-memory offset in CTA 'rank' of the cluster
-QG_DEVICE void mbar_arrive_remote(uint64_t* bar, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(bar)), "r"(rank));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(remote) : "memory");
-}
-QG_DEVICE bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(1000u) : "memory");
-  return ok != 0;
-}
-// bounded wait with cluster-scope acquire (the arrivals come from the peer CTA)
-QG_DEVICE bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t cap, volatile int* abort,
-                                 unsigned int* err) {
-  for (uint32_t i = 0; i < cap; ++i) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 31u) == 31u && *abort) return false;
-  }
-  *abort = 1;
-  if (err) atomicExch(err, DEV_ERR_TIMEOUT);
-  return false;
-}
-// TMEM of both CTAs of the pair: one warp of each CTA executes these together
-QG_DEVICE void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
-               :: "r"(smem_addr(dst_smem)), "r"(ncols) : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-QG_DEVICE void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
-}
-// M = 256 over the pair: A rows 0-127 from the even CTA's TMEM, 128-255 from
-// the odd CTA's (same address); B columns split the same way between the two
-// CTAs' shared memory (same offset); each CTA's D holds its 128 rows.
-QG_DEVICE void tc_mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}"
-      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u) : "memory");
-}
-// TMA load into this CTA's shared memory whose completion is signalled on
-// the mbarrier at the same offset in CTA 'bar_rank' of the pair.
-QG_DEVICE void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint64_t* bar, uint32_t bar_rank, int x, int y) {
-  uint32_t rbar;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(smem_addr(bar)), "r"(bar_rank));
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%3, %4}], [%2];"
-      :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(rbar), "r"(x), "r"(y)
-      : "memory");
-}
-// arrive on the mbarrier at this offset in every CTA of 'mask' once the
-// pair's tcgen05 operations issued so far complete
-QG_DEVICE void tc_commit_pair(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               :: "r"(smem_addr(bar)), "h"(mask) : "memory");
-}
-
 // ---- descriptors ---------------------------------------------------------------
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
 // layout written by TMA (rows of 128 B, 8-row atoms of 1024 B): start address,
@@ -264,12 +191,6 @@ QG_DEVICE void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
       " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
       : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-// (a0, a1) * (b0, b1) + (c0, c1), two IEEE fused multiply-adds in one packed op
-QG_DEVICE void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
-  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
-      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
-      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 // two fp32 -> bf16x2 (lo in the low half), round to nearest even
 QG_DEVICE uint32_t f32x2_to_bf16x2(float lo, float hi) {
