@@ -71,7 +71,7 @@ PROFILED_TRAFFIC = {
                   "algorithmic_bytes": 30.30e6, "profile": "profiles/gemv_int4_m1_n14336_k4096.md"},
     "prefill": {"bytes": 309.86e6, "launch": "w4a16_tc_kernel<0> M=8192 N=14336 K=4096",
                 "algorithmic_bytes": 332.3e6, "profile": "profiles/prefill_w4a16_tc_m8192_n14336_k4096.md"},
-    "moe": {"bytes": 985.3e6, "launch": "moe_f16_kernel gate/up R=8192 N=28672 K=4096",
+    "moe": {"bytes": 985.5e6, "launch": "moe_f16_kernel<false> gate/up R=8192 N=28672 K=4096",
             "algorithmic_bytes": 1021.4e6, "profile": "profiles/moe_w4a8_f16act_t4096_e8.md"},
     "moe_fp8s": {"bytes": 940.7e6, "launch": "moe_fp8s_kernel gate/up R=8192 N=28672 K=4096",
                  "algorithmic_bytes": 981.4e6, "profile": "profiles/moe_fp8s_t4096_e8.md"},
@@ -83,7 +83,7 @@ PROFILED_TRAFFIC = {
 
 
 # the main kernel of rows timed in parts
-MAIN_KERNEL = {"moe": "moe_f16_kernel (gate/up + down launches)",
+MAIN_KERNEL = {"moe": "moe_f16_kernel<false> (gate/up + down launches)",
                "moe_fp8s": "moe_fp8s_kernel (gate/up + down launches)",
                "moe_e4m3": "moe_f16_kernel<true> (gate/up + down launches)"}
 MOE_ROWS = ("moe", "moe_fp8s", "moe_e4m3")
