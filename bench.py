@@ -73,11 +73,11 @@ PROFILED_TRAFFIC = {
                 "algorithmic_bytes": 332.3e6, "profile": "profiles/prefill_w4a16_tc_m8192_n14336_k4096.md"},
     "moe": {"bytes": 985.5e6, "launch": "moe_f16_kernel<false> gate/up R=8192 N=28672 K=4096",
             "algorithmic_bytes": 1021.4e6, "profile": "profiles/moe_w4a8_f16act_t4096_e8.md"},
-    "moe_fp8s": {"bytes": 940.7e6, "launch": "moe_fp8s_kernel gate/up R=8192 N=28672 K=4096",
+    "moe_fp8s": {"bytes": 940.19e6, "launch": "moe_fp8s_kernel gate/up R=8192 N=28672 K=4096",
                  "algorithmic_bytes": 981.4e6, "profile": "profiles/moe_fp8s_t4096_e8.md"},
     "moe_e4m3": {"bytes": 949.82e6, "launch": "moe_f16_kernel<true> gate/up R=8192 N=28672 K=4096",
                  "algorithmic_bytes": 987.8e6, "profile": "profiles/moe_w4a8_e4m3_f16conv_t4096_e8.md"},
-    "prefill_w4a4": {"bytes": 245.8e6, "launch": "w4a4_bs_kernel<true> M=8192 N=14336 K=4096",
+    "prefill_w4a4": {"bytes": 246.08e6, "launch": "w4a4_bs_kernel<true, false> M=8192 N=14336 K=4096",
                      "algorithmic_bytes": 283.9e6, "profile": "profiles/w4a4_bs_m8192.md"},
 }
 
